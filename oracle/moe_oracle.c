@@ -1,0 +1,382 @@
+/*
+ * moe_oracle.c -- plain, slow CPU oracle of the MoE layer between DP attention
+ * and expert parallelism.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
+ * this file: only the tests, the smoke check and the CPU-baseline leg of the
+ * bench use it.  It shares no code, header, table or helper with the CUDA
+ * library; both sides only receive the same seeded inputs.
+ *
+ * Arithmetic is done in double precision.  Every loop runs in the order the
+ * definition states (rows ascending, k-slots ascending, reduction index
+ * ascending); nothing is blocked, fused or reordered.  OpenMP is used only to
+ * split independent output rows between threads in the FFN, which changes no
+ * result.
+ *
+ * Sources (pages of the web text this project follows):
+ *   [P1] "SGLang 源码完全拆解(十七): DP Attention 与专家并行" (SGLang source
+ *        walkthrough, chapter 17: DP attention and expert parallelism).
+ *   [P2] "vLLM 源码完全拆解(二十七): Dual Batch Overlap".
+ *   [P4] "DP" (zdszero, data_parallelism): DP vs TP, MLP sync, static bound.
+ *
+ * Parity status of each function is stated in its comment; the pins live in
+ * tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_ERR_ARG 1
+#define ORC_ERR_CAPACITY 2
+#define ORC_ERR_BOUND 3
+#define ORC_ERR_INPUT 4
+
+#define ORC_PAD_SUM 0
+#define ORC_PAD_MAX 1
+#define ORC_PAD_STATIC 2
+
+/* ------------------------------------------------------------------------ */
+/* Layout of the global buffer.                                              */
+/*                                                                          */
+/* [P1] section "本 rank 的切片位置怎么算" (where this rank's slice starts):   */
+/*   replica r starts at the sum of the token counts of replicas 0..r-1     */
+/*   (a cumulative sum, replica 0 at row 0).                                 */
+/* [P1] section "DpPaddingMode: 补齐到最长还是补齐到总和":                    */
+/*   MAX_LEN pads every replica to max(global_num_tokens) so that all        */
+/*   segments have equal length (all_gather layout: replica r at r*max);     */
+/*   SUM_LEN sizes the buffer as the sum of the counts, segments back to     */
+/*   back at the cumulative-sum offsets.                                     */
+/* [P4] section "跳过同步: 用约定代替通信" (static bound B): every rank        */
+/*   assumes every rank holds B requests, offset = rank * B; a rank above B  */
+/*   is an error.  [P4] section "整体流程" states that decode counts are     */
+/*   request counts, multiplied by tokens per request (draft + 1) inside the */
+/*   forward, so the token offset of replica r is r * B * tokens_per_req.    */
+/* Parity: pinned (closed forms, concatenation, golden fixtures).            */
+/* ------------------------------------------------------------------------ */
+int orc_dp_layout(const int32_t *counts, int R, int mode, int static_bound,
+                  int tokens_per_req, int32_t *offsets, int64_t *rows_out) {
+  if (R < 1 || counts == NULL || offsets == NULL || rows_out == NULL) return ORC_ERR_ARG;
+  for (int r = 0; r < R; ++r)
+    if (counts[r] < 0) return ORC_ERR_ARG;
+  int64_t start = 0;
+  if (mode == ORC_PAD_SUM) {
+    for (int r = 0; r < R; ++r) {
+      offsets[r] = (int32_t)start;
+      start += counts[r];
+    }
+  } else if (mode == ORC_PAD_MAX) {
+    int32_t mx = 0;
+    for (int r = 0; r < R; ++r)
+      if (counts[r] > mx) mx = counts[r];
+    for (int r = 0; r < R; ++r) {
+      offsets[r] = (int32_t)start;
+      start += mx;
+    }
+  } else if (mode == ORC_PAD_STATIC) {
+    if (static_bound < 0 || tokens_per_req < 1) return ORC_ERR_ARG;
+    int64_t seg = (int64_t)static_bound * tokens_per_req;
+    for (int r = 0; r < R; ++r)
+      if (counts[r] > seg) return ORC_ERR_BOUND;
+    for (int r = 0; r < R; ++r) {
+      offsets[r] = (int32_t)start;
+      start += seg;
+    }
+  } else {
+    return ORC_ERR_ARG;
+  }
+  if (start > INT32_MAX) return ORC_ERR_ARG;
+  offsets[R] = (int32_t)start;
+  *rows_out = start;
+  return ORC_OK;
+}
+
+/* [P1] section "DpPaddingMode", the get_dp_padding_mode rule, with the two
+ * backend-specific branches (pplx, DeepEP v2) left out because no a2a
+ * backend exists here:
+ *   prefill in the batch and gather width > 1:
+ *       MAX if the idle-aware flag is set and some replica has 0 tokens,
+ *       else SUM;
+ *   otherwise MAX iff 2 * sum >= max * width (the cheaper communication).
+ * Parity: pinned (hand-worked golden table). */
+int orc_dp_padding_mode(const int32_t *counts, int R, int gather_width,
+                        int is_extend_in_batch, int max_len_with_idle) {
+  int64_t sum = 0;
+  int32_t mx = 0, mn = INT32_MAX;
+  for (int r = 0; r < R; ++r) {
+    sum += counts[r];
+    if (counts[r] > mx) mx = counts[r];
+    if (counts[r] < mn) mn = counts[r];
+  }
+  if (is_extend_in_batch && gather_width > 1) {
+    if (max_len_with_idle && R > 0 && mn == 0) return ORC_PAD_MAX;
+    return ORC_PAD_SUM;
+  }
+  if (sum * 2 >= (int64_t)mx * gather_width) return ORC_PAD_MAX;
+  return ORC_PAD_SUM;
+}
+
+/* Row g of the global buffer carries a real token iff it lies in the first
+ * counts[r] rows of the segment that starts at offsets[r]; the remaining rows
+ * of a MAX or static-bound segment are padding.  Pad rows are not routed. */
+void orc_valid_rows(const int32_t *counts, const int32_t *offsets, int R, int64_t rows,
+                    uint8_t *valid) {
+  for (int64_t g = 0; g < rows; ++g) valid[g] = 0;
+  for (int r = 0; r < R; ++r)
+    for (int32_t i = 0; i < counts[r]; ++i) valid[(int64_t)offsets[r] + i] = 1;
+}
+
+/* [P1] section "两种 gather: all_reduce 与 all_gather", path one: the global
+ * buffer is filled with zeros, then each replica's tokens are copied to rows
+ * [start, start + count).  With one device the all-reduce that follows sums
+ * one non-zero contribution per row, so the result is that copy.
+ * Rows are opaque byte strings of row_bytes bytes.  Parity: pinned
+ * (gather then scatter is the identity; SUM equals concatenation). */
+void orc_dp_gather(const void *const *local, const int32_t *counts, const int32_t *offsets,
+                   int R, int64_t rows, int64_t row_bytes, void *global) {
+  memset(global, 0, (size_t)(rows * row_bytes));
+  for (int r = 0; r < R; ++r)
+    for (int32_t i = 0; i < counts[r]; ++i)
+      memcpy((char *)global + ((int64_t)offsets[r] + i) * row_bytes,
+             (const char *)local[r] + (int64_t)i * row_bytes, (size_t)row_bytes);
+}
+
+/* [P1] section "scatter: 把 MoE 的输出还回本副本": the global buffer is cut
+ * back into per-replica pieces by the same global_num_tokens that placed
+ * them.  Parity: pinned (identity with gather). */
+void orc_dp_scatter(const void *global, const int32_t *counts, const int32_t *offsets, int R,
+                    int64_t row_bytes, void *const *local) {
+  for (int r = 0; r < R; ++r)
+    for (int32_t i = 0; i < counts[r]; ++i)
+      memcpy((char *)local[r] + (int64_t)i * row_bytes,
+             (const char *)global + ((int64_t)offsets[r] + i) * row_bytes, (size_t)row_bytes);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Top-k routing.  [P1] (TopKOutput{topk_ids, topk_weights} produced by       */
+/* select_experts, section "normal dispatch 的调用链" and the TBO operation  */
+/* list) names the output but not the scoring.  Reading taken: softmax       */
+/* routing.  The k experts with the largest logits are chosen (largest      */
+/* probability, the same order); equal logits go to the lower expert id;     */
+/* ids are listed best first.  With renormalize the weights are the softmax */
+/* over the k chosen logits, else the full softmax probabilities of the      */
+/* chosen experts.  Pad rows get id -1 and weight 0.                         */
+/* Parity: pinned (brute force over all k-subsets, scipy softmax, k=1, k=E). */
+/* ------------------------------------------------------------------------ */
+int orc_route_topk(const float *logits, int64_t rows, int E, int k, int renormalize,
+                   const uint8_t *valid, int32_t *ids, double *w) {
+  if (E < 1 || k < 1 || k > E) return ORC_ERR_ARG;
+  uint8_t *taken = (uint8_t *)malloc((size_t)E);
+  if (taken == NULL) return ORC_ERR_ARG;
+  for (int64_t g = 0; g < rows; ++g) {
+    const float *l = logits + g * E;
+    if (!valid[g]) {
+      for (int j = 0; j < k; ++j) {
+        ids[g * k + j] = -1;
+        w[g * k + j] = 0.0;
+      }
+      continue;
+    }
+    memset(taken, 0, (size_t)E);
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || l[e] > l[best]) best = e; /* strict: ties keep the lower id */
+      }
+      taken[best] = 1;
+      ids[g * k + j] = best;
+    }
+    double lmax = (double)l[ids[g * k]];
+    double denom = 0.0;
+    if (renormalize) {
+      for (int j = 0; j < k; ++j) denom += exp((double)l[ids[g * k + j]] - lmax);
+    } else {
+      for (int e = 0; e < E; ++e) denom += exp((double)l[e] - lmax);
+    }
+    for (int j = 0; j < k; ++j) w[g * k + j] = exp((double)l[ids[g * k + j]] - lmax) / denom;
+  }
+  free(taken);
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dispatch: sort the routed (row, j) pairs by expert slot into contiguous    */
+/* per-slot buffers.                                                         */
+/* [P1] section "normal dispatch 的调用链": get_dispatch_layout computes the  */
+/*   tokens per expert; expert_alignment=128 rounds each expert's token      */
+/*   count up to a multiple of 128 for the grouped GEMM tiles.               */
+/* [P1] section "逻辑与物理的两套映射": logical_to_all_physical_map[E, X]      */
+/*   with num_valid[E] lists the physical slots that hold a logical expert.  */
+/* [P1] section "推理时怎么选副本": every rank must pick the same physical     */
+/*   replica for a token (rank_invariant) when no a2a backend exists.        */
+/* Reading taken for the replica choice: the occurrences of a logical expert */
+/* are counted in (row, j) order and occurrence p goes to replica            */
+/* p mod num_valid (round robin, the same on every simulated rank).          */
+/* The order inside a slot is by (row, j): a stable sort by (slot, row, j).   */
+/* Align pad positions get perm = -1.                                        */
+/* Parity: pinned (Python sort with a tuple key on tiny inputs, bijection,   */
+/* per-expert conservation, alignment).                                      */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t slot, row, j;
+} orc_key;
+
+static int orc_key_cmp(const void *a, const void *b) {
+  const orc_key *x = (const orc_key *)a, *y = (const orc_key *)b;
+  if (x->slot != y->slot) return x->slot < y->slot ? -1 : 1;
+  if (x->row != y->row) return x->row < y->row ? -1 : 1;
+  if (x->j != y->j) return x->j < y->j ? -1 : 1;
+  return 0;
+}
+
+int orc_dispatch(const int32_t *ids, int64_t rows, int k, int E, int P, const int32_t *l2p,
+                 const int32_t *nrep, int X, int align, int64_t cap, int32_t *counts,
+                 int32_t *offsets, int32_t *perm, int32_t *inv) {
+  if (k < 1 || E < 1 || P < 1 || align < 1) return ORC_ERR_ARG;
+  if (l2p == NULL && P != E) return ORC_ERR_ARG;
+  int64_t n = rows * k;
+  orc_key *keys = (orc_key *)malloc(sizeof(orc_key) * (size_t)(n > 0 ? n : 1));
+  int64_t *seen = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+  if (keys == NULL || seen == NULL) {
+    free(keys);
+    free(seen);
+    return ORC_ERR_ARG;
+  }
+  int64_t m = 0;
+  int status = ORC_OK;
+  for (int s = 0; s < P; ++s) counts[s] = 0;
+  for (int64_t g = 0; g < rows && status == ORC_OK; ++g) {
+    for (int j = 0; j < k; ++j) {
+      int32_t l = ids[g * k + j];
+      inv[g * k + j] = -1;
+      if (l < 0) continue; /* pad row: not routed */
+      if (l >= E) {
+        status = ORC_ERR_INPUT;
+        break;
+      }
+      int32_t slot = l;
+      if (l2p != NULL) {
+        int32_t nv = nrep[l];
+        if (nv < 1 || nv > X) {
+          status = ORC_ERR_INPUT;
+          break;
+        }
+        int64_t p = seen[l]++;
+        slot = l2p[(int64_t)l * X + (int32_t)(p % nv)];
+        if (slot < 0 || slot >= P) {
+          status = ORC_ERR_INPUT;
+          break;
+        }
+      }
+      counts[slot] += 1;
+      keys[m].slot = slot;
+      keys[m].row = (int32_t)g;
+      keys[m].j = j;
+      ++m;
+    }
+  }
+  if (status == ORC_OK) {
+    int64_t acc = 0;
+    for (int s = 0; s < P; ++s) {
+      offsets[s] = (int32_t)acc;
+      acc += ((int64_t)counts[s] + align - 1) / align * align;
+    }
+    offsets[P] = (int32_t)acc;
+    if (acc > cap) status = ORC_ERR_CAPACITY;
+  }
+  if (status == ORC_OK) {
+    qsort(keys, (size_t)m, sizeof(orc_key), orc_key_cmp);
+    for (int64_t d = 0; d < cap; ++d) perm[d] = -1;
+    /* walk the sorted keys; within a slot they occupy consecutive positions
+     * starting at the slot's offset */
+    int64_t i = 0;
+    for (int s = 0; s < P; ++s) {
+      for (int32_t c = 0; c < counts[s]; ++c, ++i) {
+        int64_t d = (int64_t)offsets[s] + c;
+        perm[d] = keys[i].row;
+        inv[(int64_t)keys[i].row * k + keys[i].j] = (int32_t)d;
+      }
+    }
+  }
+  free(keys);
+  free(seen);
+  return status;
+}
+
+/* xs[d] = xg[perm[d]], or a zero row where perm[d] = -1 (align padding).
+ * Rows are opaque byte strings. */
+void orc_permute_rows(const void *xg, const int32_t *perm, int64_t n, int64_t row_bytes,
+                      void *xs) {
+  for (int64_t d = 0; d < n; ++d) {
+    if (perm[d] < 0)
+      memset((char *)xs + d * row_bytes, 0, (size_t)row_bytes);
+    else
+      memcpy((char *)xs + d * row_bytes, (const char *)xg + (int64_t)perm[d] * row_bytes,
+             (size_t)row_bytes);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Expert FFN (SwiGLU) of one expert slot over n rows.                        */
+/* [P1] opening sections: a DeepSeek-V3 expert has gate_proj [2048, 7168],   */
+/*   up_proj of the same size and down_proj [7168, 2048], i.e. weights are   */
+/*   stored [out, in].                                                        */
+/* [P2] figure "MoE 模块化内核的 PrepareAndFinalize 块结构": permute, MM1,     */
+/*   activation, MM2, unpermute.                                             */
+/* SwiGLU: a = silu(x Wg^T) * (x Wu^T), y = a Wd^T, silu(g) = g / (1 + e^-g). */
+/* wgu holds the gate rows 0..I-1 followed by the up rows I..2I-1.           */
+/* Everything in double, sums in index order, no intermediate rounding.     */
+/* Parity: pinned against numpy float64 matmul + scipy expit on small cases. */
+/* ------------------------------------------------------------------------ */
+void orc_expert_ffn(const float *x, int64_t n, int H, int I, const float *wgu, const float *wd,
+                    double *y) {
+#pragma omp parallel
+  {
+    double *a = (double *)malloc(sizeof(double) * (size_t)I);
+#pragma omp for schedule(static)
+    for (int64_t r = 0; r < n; ++r) {
+      const float *xr = x + r * H;
+      for (int i = 0; i < I; ++i) {
+        const float *wg = wgu + (int64_t)i * H;
+        const float *wu = wgu + (int64_t)(I + i) * H;
+        double gsum = 0.0, usum = 0.0;
+        for (int h = 0; h < H; ++h) {
+          gsum += (double)xr[h] * (double)wg[h];
+          usum += (double)xr[h] * (double)wu[h];
+        }
+        a[i] = gsum / (1.0 + exp(-gsum)) * usum;
+      }
+      for (int o = 0; o < H; ++o) {
+        const float *wdo = wd + (int64_t)o * I;
+        double ysum = 0.0;
+        for (int i = 0; i < I; ++i) ysum += a[i] * (double)wdo[i];
+        y[r * H + o] = ysum;
+      }
+    }
+    free(a);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Combine.  [P2] figure "MoE 模块化内核的 PrepareAndFinalize 块结构":        */
+/* finalize applies the top-k weights while un-permuting: token row g        */
+/* receives sum_j w[g, j] * ys[inv[g, j]], j ascending.  Pad rows (inv = -1  */
+/* everywhere) are zero.  Parity: pinned (identity experts with weights      */
+/* summing to 1 give the input back; numpy einsum on random inputs).         */
+/* ------------------------------------------------------------------------ */
+void orc_combine(const double *ys, const int32_t *inv, const double *w, int64_t rows, int k,
+                 int H, double *out) {
+  for (int64_t g = 0; g < rows; ++g) {
+    double *o = out + g * H;
+    for (int h = 0; h < H; ++h) o[h] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      int32_t d = inv[g * k + j];
+      if (d < 0) continue;
+      const double *src = ys + (int64_t)d * H;
+      double wj = w[g * k + j];
+      for (int h = 0; h < H; ++h) o[h] += wj * src[h];
+    }
+  }
+}

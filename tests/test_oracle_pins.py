@@ -1,0 +1,452 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Every check here is independent of the oracle's own code path: numpy
+concatenation / padding, Python's sort with a tuple key, brute force over all
+k-subsets, scipy's softmax, numpy float64 matmul, a dense per-token
+formulation of the layer, and golden values cited from the pages.  The
+"mutant" tests feed deliberately wrong variants to the same checks to show
+that each check catches the mistake it is meant to catch.
+"""
+import itertools
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from conftest import ints, read_golden
+
+MODES = {"sum": 0, "max": 1, "static": 2}
+
+
+# ----------------------------------------------------------------- layout
+@pytest.mark.parametrize("row", read_golden("dp_layout.txt"))
+def test_layout_golden(orc, row):
+    counts, mode, B, tpr, offs, rows = row
+    o, n = orc.dp_layout(ints(counts), MODES[mode], int(B), int(tpr))
+    assert o.tolist() == ints(offs)
+    assert n == int(rows)
+
+
+@pytest.mark.parametrize("row", read_golden("dp_layout_errors.txt"))
+def test_layout_errors_golden(orc, row):
+    counts, mode, B, tpr, err = row
+    with pytest.raises(orc.OracleError) as ei:
+        orc.dp_layout(ints(counts), MODES[mode], int(B), int(tpr))
+    assert ei.value.code == {"bound": 3, "arg": 1}[err]
+
+
+@pytest.mark.parametrize("row", read_golden("dp_padding_mode.txt"))
+def test_padding_mode_golden(orc, row):
+    counts, width, ext, idle, mode = row
+    assert orc.dp_padding_mode(ints(counts), int(width), int(ext), int(idle)) == MODES[mode]
+
+
+def _segments(rng, counts, H, dtype=np.float32):
+    return [rng.standard_normal((c, H)).astype(dtype) for c in counts]
+
+
+def check_sum_is_concatenation(gather, layout, counts, H=5, seed=0):
+    rng = np.random.default_rng(seed)
+    segs = _segments(rng, counts, H)
+    offs, rows = layout(counts, 0)
+    g = gather(segs, counts, offs, rows)
+    return rows == sum(counts) and np.array_equal(g, np.concatenate(segs, axis=0))
+
+
+def check_max_is_padded_stack(gather, layout, counts, H=3, seed=1):
+    rng = np.random.default_rng(seed)
+    segs = _segments(rng, counts, H)
+    offs, rows = layout(counts, 1)
+    mx = max(counts)
+    g = gather(segs, counts, offs, rows)
+    ref = np.stack([np.pad(s, ((0, mx - len(s)), (0, 0))) for s in segs])
+    return rows == len(counts) * mx and np.array_equal(g.reshape(len(counts), mx, H), ref)
+
+
+def test_layout_sum_exhaustive_small(orc):
+    for R in range(1, 4):
+        for counts in itertools.product(range(0, 4), repeat=R):
+            assert check_sum_is_concatenation(orc.dp_gather, orc.dp_layout, list(counts))
+            if max(counts) > 0:
+                assert check_max_is_padded_stack(orc.dp_gather, orc.dp_layout, list(counts))
+
+
+def test_layout_static_blocks(orc):
+    rng = np.random.default_rng(3)
+    for tpr in (1, 4):
+        counts = [int(v) * tpr for v in rng.choice([0, 4, 8, 24], size=16)]
+        offs, rows = orc.dp_layout(counts, 2, 24, tpr)
+        seg = 24 * tpr
+        assert rows == 16 * seg
+        segs = _segments(rng, counts, 4)
+        g = orc.dp_gather(segs, counts, offs, rows).reshape(16, seg, 4)
+        for r in range(16):
+            assert np.array_equal(g[r, : counts[r]], segs[r])
+            assert not g[r, counts[r]:].any()
+
+
+def test_gather_scatter_identity(orc):
+    rng = np.random.default_rng(4)
+    for mode in (0, 1):
+        counts = [int(v) for v in rng.integers(0, 9, size=6)]
+        segs = [rng.integers(0, 2**16, size=(c, 7), dtype=np.uint16) for c in counts]
+        offs, rows = orc.dp_layout(counts, mode)
+        g = orc.dp_gather(segs, counts, offs, rows)
+        back = orc.dp_scatter(g, counts, offs)
+        assert all(np.array_equal(a, b) for a, b in zip(segs, back))
+        valid = orc.valid_rows(counts, offs, rows)
+        assert int(valid.sum()) == sum(counts)
+        assert not g[valid == 0].any()  # pad rows are zero
+
+
+def test_mutant_inclusive_prefix_is_caught(orc):
+    def bad_layout(counts, mode, *a):
+        o, n = orc.dp_layout(counts, mode, *a)
+        o = o.copy()
+        o[:-1] = np.cumsum(counts)  # inclusive instead of exclusive
+        return o, n
+
+    def tolerant_gather(segs, counts, offs, rows):
+        out = np.zeros((rows + max(counts, default=0),) + segs[0].shape[1:], segs[0].dtype)
+        for r, s in enumerate(segs):
+            out[offs[r]: offs[r] + len(s)] = s
+        return out[:rows]
+
+    assert not check_sum_is_concatenation(tolerant_gather, bad_layout, [2, 3, 1])
+
+
+# ----------------------------------------------------------------- top-k routing
+def brute_force_topk(lrow, k):
+    """Best k-subset by total logit; ties by the lexicographically smallest ids."""
+    E = len(lrow)
+    best = None
+    for sub in itertools.combinations(range(E), k):
+        key = (sum(float(lrow[e]) for e in sub), tuple(-e for e in sub))
+        if best is None or key > best[0]:
+            best = (key, sub)
+    sub = best[1]
+    return sorted(sub, key=lambda e: (-float(lrow[e]), e))
+
+
+def check_topk(route, E, k, seed, renorm=True):
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((12, E)).astype(np.float32)
+    valid = np.ones(12, np.uint8)
+    valid[[3, 7]] = 0
+    ids, w = route(logits, k, renorm, valid)
+    for g in range(12):
+        if not valid[g]:
+            if not ((ids[g] == -1).all() and (w[g] == 0).all()):
+                return False
+            continue
+        ref = brute_force_topk(logits[g], k)
+        if ids[g].tolist() != ref:
+            return False
+        sel = logits[g].astype(np.float64)[ref]
+        wref = (scipy.special.softmax(sel) if renorm
+                else scipy.special.softmax(logits[g].astype(np.float64))[ref])
+        if not np.allclose(w[g], wref, rtol=1e-12, atol=0):
+            return False
+    return True
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (6, 3), (5, 1), (5, 5), (9, 4)])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_topk_brute_force(orc, E, k, renorm):
+    assert check_topk(orc.route_topk, E, k, seed=E * 10 + k, renorm=renorm)
+
+
+def test_topk_ties_lower_id_and_special_cases(orc):
+    E = 8
+    logits = np.zeros((3, E), np.float32)
+    logits[1, [2, 5, 6]] = 1.5          # a 3-way tie for the top
+    logits[2] = np.arange(E)[::-1]      # strictly decreasing
+    ids, w = orc.route_topk(logits, 4, True, np.ones(3, np.uint8))
+    assert ids[0].tolist() == [0, 1, 2, 3] and np.all(w[0] == 0.25)
+    assert ids[1].tolist() == [2, 5, 6, 0]
+    assert ids[2].tolist() == [0, 1, 2, 3]
+    ids1, w1 = orc.route_topk(logits, 1, True, np.ones(3, np.uint8))
+    assert np.all(w1 == 1.0)
+    idsE, wE = orc.route_topk(logits, E, True, np.ones(3, np.uint8))
+    assert np.allclose(wE.sum(1), 1.0, rtol=0, atol=1e-15)
+
+
+def test_mutant_tie_to_higher_id_is_caught(orc):
+    def bad_route(logits, k, renorm, valid):
+        # picks among equal logits the higher id
+        rev = np.ascontiguousarray(logits[:, ::-1])
+        ids, w = orc.route_topk(rev, k, renorm, valid)
+        E = logits.shape[1]
+        return np.where(ids >= 0, E - 1 - ids, ids), w
+
+    rng_logits = np.round(np.random.default_rng(5).standard_normal((12, 6)), 0)
+
+    def tied_route(logits, k, renorm, valid):
+        return bad_route(rng_logits.astype(np.float32), k, renorm, valid)
+
+    ok = True
+    valid = np.ones(12, np.uint8)
+    ids, _ = tied_route(None, 3, True, valid)
+    for g in range(12):
+        if ids[g].tolist() != brute_force_topk(rng_logits[g].astype(np.float32), 3):
+            ok = False
+    assert not ok
+
+
+# ----------------------------------------------------------------- dispatch
+def sort_reference(ids, E, P, l2p=None, nrep=None, align=1):
+    """Dispatch by definition: slot choice by round-robin occurrence count, then
+    Python's sort of (slot, row, j) tuples."""
+    rows, k = ids.shape
+    seen = {}
+    keys = []
+    for g in range(rows):
+        for j in range(k):
+            l = int(ids[g, j])
+            if l < 0:
+                continue
+            if l2p is None:
+                slot = l
+            else:
+                p = seen.get(l, 0)
+                seen[l] = p + 1
+                slot = int(l2p[l, p % int(nrep[l])])
+            keys.append((slot, g, j))
+    keys.sort()
+    counts = np.zeros(P, np.int64)
+    for s, _, _ in keys:
+        counts[s] += 1
+    padded = (counts + align - 1) // align * align
+    offsets = np.concatenate([[0], np.cumsum(padded)])
+    perm = np.full(offsets[-1], -1, np.int64)
+    inv = np.full((rows, k), -1, np.int64)
+    i = 0
+    for s in range(P):
+        for c in range(counts[s]):
+            _, g, j = keys[i]
+            perm[offsets[s] + c] = g
+            inv[g, j] = offsets[s] + c
+            i += 1
+    return counts, offsets, perm, inv
+
+
+def _random_ids(rng, rows, k, E, pad_rows=()):
+    ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(rows)]).astype(np.int32)
+    ids[list(pad_rows)] = -1
+    return ids
+
+
+@pytest.mark.parametrize("align", [1, 4, 128])
+def test_dispatch_matches_tuple_sort(orc, align):
+    rng = np.random.default_rng(6)
+    E, k, rows = 8, 3, 37
+    ids = _random_ids(rng, rows, k, E, pad_rows=(0, 5, 36))
+    c, o, perm, inv = orc.dispatch(ids, E, E, align=align)
+    rc, ro, rp, ri = sort_reference(ids, E, E, align=align)
+    assert np.array_equal(c, rc) and np.array_equal(o, ro)
+    assert np.array_equal(perm[: o[-1]], rp) and np.array_equal(inv, ri)
+    assert (perm[o[-1]:] == -1).all()
+    assert int(c.sum()) == (rows - 3) * k
+    assert all(v % align == 0 for v in o)
+
+
+def test_dispatch_with_map_matches_tuple_sort(orc):
+    from combine_dp_gather_gb300 import synth
+    rng = np.random.default_rng(7)
+    E, P, k, rows = 6, 10, 2, 50
+    l2p, nrep, p2l = synth.trivial_map(E, P)
+    ids = _random_ids(rng, rows, k, E, pad_rows=(3,))
+    c, o, perm, inv = orc.dispatch(ids, E, P, l2p, nrep)
+    rc, ro, rp, ri = sort_reference(ids, E, P, l2p, nrep)
+    assert np.array_equal(c, rc) and np.array_equal(perm[: o[-1]], rp)
+    assert np.array_equal(inv, ri)
+    # physical -> logical counts by scatter-add conserve the logical histogram
+    logical = np.zeros(E, np.int64)
+    np.add.at(logical, p2l, c)
+    assert np.array_equal(logical, np.bincount(ids[ids >= 0], minlength=E))
+    # round robin: replicas of one expert differ by at most one, earlier replicas first
+    for e in range(E):
+        rc_e = [int(c[l2p[e, x]]) for x in range(nrep[e])]
+        assert max(rc_e) - min(rc_e) <= 1 and rc_e == sorted(rc_e, reverse=True)
+
+
+def test_dispatch_bijection_and_errors(orc):
+    rng = np.random.default_rng(8)
+    E, k, rows = 16, 4, 200
+    ids = _random_ids(rng, rows, k, E)
+    c, o, perm, inv = orc.dispatch(ids, E, E)
+    flat = inv.reshape(-1)
+    assert sorted(flat.tolist()) == list(range(rows * k))
+    for g in range(rows):
+        for j in range(k):
+            assert perm[inv[g, j]] == g
+    with pytest.raises(orc.OracleError) as ei:
+        orc.dispatch(ids, E, E, cap=rows * k - 1)
+    assert ei.value.code == 2
+    bad = ids.copy()
+    bad[5, 1] = E
+    with pytest.raises(orc.OracleError) as ei:
+        orc.dispatch(bad, E, E)
+    assert ei.value.code == 4
+
+
+def test_mutant_reversed_order_is_caught(orc):
+    rng = np.random.default_rng(9)
+    ids = _random_ids(rng, 20, 2, 4)
+    c, o, perm, inv = orc.dispatch(ids, 4, 4)
+    bad_perm = perm.copy()
+    for s in range(4):
+        bad_perm[o[s]: o[s + 1]] = perm[o[s]: o[s + 1]][::-1]
+    _, _, rp, _ = sort_reference(ids, 4, 4)
+    assert not np.array_equal(bad_perm[: o[-1]], rp)
+
+
+def test_permute_rows(orc):
+    rng = np.random.default_rng(10)
+    xg = rng.integers(0, 2**16, size=(9, 6), dtype=np.uint16)
+    perm = np.array([3, -1, 0, 8, 8, -1], np.int32)
+    xs = orc.permute_rows(xg, perm)
+    for d, p in enumerate(perm):
+        assert np.array_equal(xs[d], xg[p] if p >= 0 else np.zeros(6, np.uint16))
+
+
+# ----------------------------------------------------------------- FFN
+def numpy_swiglu(x, wgu, wd):
+    I = wd.shape[1]
+    x = x.astype(np.float64)
+    g = x @ wgu[:I].astype(np.float64).T
+    u = x @ wgu[I:].astype(np.float64).T
+    a = g * scipy.special.expit(g) * u
+    return a @ wd.astype(np.float64).T
+
+
+@pytest.mark.parametrize("n,H,I", [(5, 16, 8), (3, 64, 32), (1, 7, 3)])
+def test_ffn_matches_numpy(orc, n, H, I):
+    rng = np.random.default_rng(n * H + I)
+    x = rng.standard_normal((n, H)).astype(np.float32)
+    wgu = (0.2 * rng.standard_normal((2 * I, H))).astype(np.float32)
+    wd = (0.2 * rng.standard_normal((H, I))).astype(np.float32)
+    y = orc.expert_ffn(x, wgu, wd)
+    ref = numpy_swiglu(x, wgu, wd)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_ffn_special_cases(orc):
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((4, 16)).astype(np.float32)
+    wgu = rng.standard_normal((16, 16)).astype(np.float32)
+    wd = rng.standard_normal((16, 8)).astype(np.float32)
+    assert not orc.expert_ffn(x, np.zeros_like(wgu), wd).any()
+    up0 = wgu.copy()
+    up0[8:] = 0
+    assert not orc.expert_ffn(x, up0, wd).any()
+    assert not orc.expert_ffn(np.zeros_like(x), wgu, wd).any()
+    # gate and up swapped must change the result: silu is not symmetric
+    swapped = np.concatenate([wgu[8:], wgu[:8]])
+    assert not np.allclose(orc.expert_ffn(x, swapped, wd), orc.expert_ffn(x, wgu, wd))
+
+
+# ----------------------------------------------------------------- combine
+def test_combine_identity_experts_return_input(orc):
+    rng = np.random.default_rng(12)
+    rows, k, E, H = 30, 4, 8, 64
+    xb = orc.f64_to_bf16_bits(rng.standard_normal((rows, H)))
+    x = orc.bf16_bits_to_f32(xb).astype(np.float64)
+    logits = rng.standard_normal((rows, E)).astype(np.float32)
+    valid = np.ones(rows, np.uint8)
+    valid[[2, 9]] = 0
+    ids, w = orc.route_topk(logits, k, True, valid)
+    c, o, perm, inv = orc.dispatch(ids, E, E)
+    xs = orc.permute_rows(x, perm[: o[-1]])
+    out = orc.combine(xs, inv, w)          # identity experts: ys = xs
+    assert np.array_equal(orc.f64_to_bf16_bits(out[valid == 1]), xb[valid == 1])
+    assert not out[valid == 0].any()
+
+
+def test_combine_matches_einsum(orc):
+    rng = np.random.default_rng(13)
+    rows, k, H, cap = 10, 3, 5, 40
+    ys = rng.standard_normal((cap, H))
+    inv = np.stack([rng.choice(cap, size=k, replace=False) for _ in range(rows)]).astype(np.int32)
+    inv[4] = -1
+    w = rng.random((rows, k))
+    out = orc.combine(ys, inv, w)
+    g = np.where(inv[..., None] >= 0, ys[np.maximum(inv, 0)], 0.0)
+    assert np.allclose(out, np.einsum("rk,rkh->rh", w, g), rtol=1e-14, atol=1e-14)
+
+
+def test_mutant_dropped_term_is_caught(orc):
+    rng = np.random.default_rng(14)
+    xb = orc.f64_to_bf16_bits(rng.standard_normal((6, 8)))
+    x = orc.bf16_bits_to_f32(xb).astype(np.float64)
+    ids, w = orc.route_topk(rng.standard_normal((6, 4)).astype(np.float32), 2, True,
+                            np.ones(6, np.uint8))
+    c, o, perm, inv = orc.dispatch(ids, 4, 4)
+    xs = orc.permute_rows(x, perm[: o[-1]])
+    inv_bad = inv.copy()
+    inv_bad[:, -1] = -1                     # last expert's term dropped
+    out = orc.combine(xs, inv_bad, w)
+    assert not np.array_equal(orc.f64_to_bf16_bits(out), xb)
+
+
+# ----------------------------------------------------------------- bf16 helpers
+def test_bf16_rounding_matches_torch_cast(orc):
+    rng = np.random.default_rng(15)
+    x = (rng.standard_normal(100_000) * np.exp(rng.uniform(-20, 20, 100_000))).astype(np.float32)
+    mine = orc.f64_to_bf16_bits(x.astype(np.float64))
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(mine, ref)
+    assert np.array_equal(orc.bf16_bits_to_f32(ref),
+                          torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16).float().numpy())
+
+
+# ----------------------------------------------------------------- whole layer
+def dense_layer(x_tokens, logits_tokens, k, wgu, wd):
+    """Per-token definition with no dispatch: out_t = sum_j w_tj FFN_{e_tj}(x_t)."""
+    out = np.zeros((len(x_tokens), x_tokens.shape[1]))
+    for t in range(len(x_tokens)):
+        lr = logits_tokens[t]
+        sel = brute_force_topk(lr, k) if len(lr) <= 10 else list(
+            np.lexsort((np.arange(len(lr)), -lr.astype(np.float64)))[:k])
+        wts = scipy.special.softmax(lr.astype(np.float64)[sel])
+        for j, e in enumerate(sel):
+            out[t] += wts[j] * numpy_swiglu(x_tokens[t: t + 1], wgu[e], wd[e])[0]
+    return out
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_layer_tiny_matches_dense_definition(orc, mode):
+    from combine_dp_gather_gb300 import synth
+    spec = synth.spec_tiny()
+    xs = [t.numpy() for t in synth.hidden_states(spec)]
+    lg = [t.numpy() for t in synth.router_logits(spec)]
+    wgu, wd = synth.expert_weights(spec)
+    wgu, wd = wgu.numpy(), wd.numpy()
+    offs, rows = orc.dp_layout(spec.counts, mode)
+    logits = orc.dp_gather(lg, spec.counts, offs, rows)
+    res = orc.layer(xs, logits, spec.counts, mode, spec.k, True, wgu, wd, spec.E)
+    dense = dense_layer(np.concatenate(xs), np.concatenate(lg), spec.k, wgu, wd)
+    got = np.concatenate([o for o in res["outs"]])
+    assert np.allclose(got, dense, rtol=1e-10, atol=1e-12)
+
+
+def test_layer_with_replicated_map_equals_without(orc):
+    """rank_invariant reading: replicas hold identical weights, so routing a
+    logical expert to any of its replicas must not change the layer output."""
+    from combine_dp_gather_gb300 import synth
+    spec = synth.spec_tiny()
+    xs = [t.numpy() for t in synth.hidden_states(spec)]
+    lg = [t.numpy() for t in synth.router_logits(spec)]
+    offs, rows = orc.dp_layout(spec.counts, 0)
+    logits = orc.dp_gather(lg, spec.counts, offs, rows)
+    wgu, wd = synth.expert_weights(spec)
+    base = orc.layer(xs, logits, spec.counts, 0, spec.k, True, wgu.numpy(), wd.numpy(), spec.E)
+    P = 12
+    l2p, nrep, p2l = synth.trivial_map(spec.E, P)
+    wgu_p, wd_p = wgu.numpy()[p2l], wd.numpy()[p2l]
+    mapped = orc.layer(xs, logits, spec.counts, 0, spec.k, True, wgu_p, wd_p, spec.E, P=P,
+                       l2p=l2p, nrep=nrep)
+    assert (mapped["counts"][spec.E:] > 0).any()   # replicas really used
+    for a, b in zip(base["outs"], mapped["outs"]):
+        assert np.array_equal(a, b)
