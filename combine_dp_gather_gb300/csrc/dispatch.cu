@@ -1,0 +1,322 @@
+// Dispatch: a deterministic, stable counting sort of the routed (row, j)
+// pairs by physical expert slot, plus the row permute that builds the
+// per-slot contiguous buffers.
+//
+// SGLang chapter 17, section "normal dispatch 的调用链": get_dispatch_layout
+// counts tokens per expert; expert_alignment rounds each expert's count up to
+// a multiple of 128 for the grouped GEMM.  Sections "逻辑与物理的两套映射" and
+// "推理时怎么选副本": a logical expert lives in num_valid physical slots
+// (logical_to_all_physical_map); without an all-to-all every rank must pick
+// the same replica for a token.  The pick here: occurrence p of logical expert
+// l, counted in (row, j) order, goes to replica p mod num_valid[l], at
+// position p / num_valid[l] inside that slot -- the stable (slot, row, j)
+// order needs no second sort.
+//
+// Kernels (all deterministic: integer shared-memory atomics only where the
+// result does not depend on their order):
+//   1. hist   one block per chunk of kChunk pairs: per-chunk logical histogram
+//   2. scan   one block: per-expert exclusive scan over chunks, per-slot
+//             counts from the replica rule, aligned exclusive scan -> offsets
+//   3. rank   one warp per chunk, 32 pairs per step in order: __match_any_sync
+//             groups equal ids, popc of the lower lanes gives the in-step
+//             rank, a shared running count carries it across steps
+//   4. copy   one warp per source row: the row is read once and written to
+//             its k destinations with 16-byte vectors
+//   5. pad    (align > 1) zero the alignment rows and mark them perm = -1
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kChunk = 1024;  // routed pairs per chunk
+
+inline int64_t n_chunks(int64_t pairs) { return (pairs + kChunk - 1) / kChunk; }
+
+__global__ void __launch_bounds__(256)
+    dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t pairs, int E,
+                         int32_t* __restrict__ hist, uint32_t* status) {
+  extern __shared__ int32_t s_h[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_h[e] = 0;
+  __syncthreads();
+  const int64_t base = (int64_t)blockIdx.x * kChunk;
+  for (int t = threadIdx.x; t < kChunk; t += blockDim.x) {
+    int64_t q = base + t;
+    if (q >= pairs) break;
+    int32_t l = ids[q];
+    if (l >= 0 && l < E)
+      atomicAdd(&s_h[l], 1);
+    else if (l != -1)
+      flag(status, MOE_DEV_BAD_EXPERT_ID);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = s_h[e];
+}
+
+// Block-wide exclusive scan of one value per thread (blockDim.x == 1024).
+__device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* s_warp,
+                                                        int32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int32_t x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int32_t y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) s_warp[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int32_t t = s_warp[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int32_t y = __shfl_up_sync(0xffffffffu, t, off);
+      if (lane >= off) t += y;
+    }
+    s_warp[lane] = t;  // inclusive over warps
+  }
+  __syncthreads();
+  int32_t excl = x - v + (wid > 0 ? s_warp[wid - 1] : 0);
+  *total = s_warp[31];
+  return excl;
+}
+
+__global__ void __launch_bounds__(1024)
+    dispatch_scan_kernel(int32_t* __restrict__ hist, int64_t chunks, int E, int P,
+                         const int32_t* __restrict__ l2p, const int32_t* __restrict__ nrep, int X,
+                         int align, int64_t cap, int32_t* __restrict__ counts_P,
+                         int32_t* __restrict__ offsets_P, uint32_t* status) {
+  __shared__ int32_t s_cnt[MOE_MAX_SLOTS];    // per logical expert
+  __shared__ int32_t s_slot[MOE_MAX_SLOTS];   // per physical slot
+  __shared__ int32_t s_claim[MOE_MAX_SLOTS];
+  __shared__ int32_t s_warp[32];
+  // per-expert exclusive scan over chunks (in place: hist becomes chunk bases)
+  for (int l = threadIdx.x; l < E; l += blockDim.x) {
+    int32_t run = 0;
+    for (int64_t c = 0; c < chunks; ++c) {
+      int32_t t = hist[c * E + l];
+      hist[c * E + l] = run;
+      run += t;
+    }
+    s_cnt[l] = run;
+  }
+  for (int s = threadIdx.x; s < P; s += blockDim.x) {
+    s_slot[s] = 0;
+    s_claim[s] = 0;
+  }
+  __syncthreads();
+  if (l2p == nullptr) {
+    for (int s = threadIdx.x; s < P; s += blockDim.x) s_slot[s] = s_cnt[s];
+  } else {
+    for (int l = threadIdx.x; l < E; l += blockDim.x) {
+      int32_t nv = nrep[l];
+      int32_t cl = s_cnt[l];
+      if (nv < 1 || nv > X) {
+        if (cl > 0) flag(status, MOE_DEV_BAD_MAP);
+        continue;
+      }
+      for (int r = 0; r < nv; ++r) {
+        int32_t slot = l2p[(int64_t)l * X + r];
+        if (slot < 0 || slot >= P || atomicAdd(&s_claim[slot], 1) != 0) {
+          flag(status, MOE_DEV_BAD_MAP);
+          continue;
+        }
+        s_slot[slot] = cl > r ? (cl - 1 - r) / nv + 1 : 0;
+      }
+    }
+  }
+  __syncthreads();
+  // aligned exclusive scan over slots (P <= 1024, one slot per thread)
+  const int s = threadIdx.x;
+  int32_t cnt = s < P ? s_slot[s] : 0;
+  int32_t padded = (int32_t)(((int64_t)cnt + align - 1) / align * align);
+  int32_t total = 0;
+  int32_t excl = block_exclusive_scan(padded, s_warp, &total);
+  if (s < P) {
+    counts_P[s] = cnt;
+    offsets_P[s] = excl;
+  }
+  if (s == 0) {
+    offsets_P[P] = total;
+    if ((int64_t)total > cap) flag(status, MOE_DEV_CAPACITY);
+  }
+}
+
+__global__ void __launch_bounds__(32)
+    dispatch_rank_kernel(const int32_t* __restrict__ ids, int64_t pairs, int k, int E,
+                         const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ l2p,
+                         const int32_t* __restrict__ nrep, int X, int P,
+                         const int32_t* __restrict__ offsets_P, int64_t cap,
+                         int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                         uint32_t* status) {
+  extern __shared__ int32_t s_run[];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) s_run[e] = 0;
+  __syncwarp();
+  const int64_t base = (int64_t)blockIdx.x * kChunk;
+  const int32_t* cb = chunk_base + (int64_t)blockIdx.x * E;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int step = 0; step < kChunk; step += 32) {
+    int64_t q = base + step + lane;
+    int32_t l = q < pairs ? ids[q] : -1;
+    bool valid = l >= 0 && l < E;
+    uint32_t mask = __match_any_sync(0xffffffffu, valid ? l : -1);
+    int rank = __popc(mask & lt);
+    int32_t p = 0;
+    if (valid) p = cb[l] + s_run[l] + rank;
+    __syncwarp();
+    if (valid && rank == __popc(mask) - 1) s_run[l] += __popc(mask);
+    __syncwarp();
+    if (q >= pairs) continue;
+    int32_t dest = -1;
+    if (valid) {
+      int32_t slot = l, pos = p;
+      bool ok = true;
+      if (l2p != nullptr) {
+        int32_t nv = nrep[l];
+        if (nv < 1 || nv > X) {
+          ok = false;
+        } else {
+          slot = l2p[(int64_t)l * X + p % nv];
+          pos = p / nv;
+          ok = slot >= 0 && slot < P;
+        }
+      }
+      if (ok) {
+        int64_t d = (int64_t)offsets_P[slot] + pos;
+        if (d < cap && d < offsets_P[slot + 1]) {
+          dest = (int32_t)d;
+          perm[d] = (int32_t)(q / k);
+        } else {
+          flag(status, MOE_DEV_CAPACITY);
+        }
+      }
+    }
+    inv[q] = dest;
+  }
+}
+
+__device__ __forceinline__ uint4 ld_nc(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+constexpr int kCopyWarps = 8;
+constexpr int kCopyUnroll = 4;
+
+__global__ void __launch_bounds__(kCopyWarps * 32)
+    dispatch_copy_kernel(const uint4* __restrict__ xg, const int32_t* __restrict__ inv,
+                         int64_t rows, int k, int vpr, int64_t cap, uint4* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t)blockIdx.x * kCopyWarps + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kCopyWarps;
+  for (int64_t g = warp0; g < rows; g += nwarps) {
+    int32_t my_d = lane < k ? inv[g * k + lane] : -1;
+    if (my_d >= cap) my_d = -1;
+    if (__ballot_sync(0xffffffffu, my_d >= 0) == 0) continue;  // pad row
+    const uint4* src = xg + g * vpr;
+    for (int v0 = lane; v0 < vpr; v0 += 32 * kCopyUnroll) {
+      uint4 t[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        int v = v0 + u * 32;
+        if (v < vpr) t[u] = ld_nc(src + v);
+      }
+      for (int j = 0; j < k; ++j) {
+        int32_t d = __shfl_sync(0xffffffffu, my_d, j);
+        if (d < 0) continue;
+        uint4* dst = xs + (int64_t)d * vpr;
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+          int v = v0 + u * 32;
+          if (v < vpr) dst[v] = t[u];
+        }
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256)
+    dispatch_pad_kernel(const int32_t* __restrict__ counts_P, const int32_t* __restrict__ offsets_P,
+                        int P, int vpr, int64_t cap, int32_t* __restrict__ perm,
+                        uint4* __restrict__ xs) {
+  const int s = blockIdx.x;
+  if (s >= P) return;
+  int64_t a = (int64_t)offsets_P[s] + counts_P[s];
+  int64_t b = offsets_P[s + 1];
+  if (b > cap) b = cap;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int64_t d = a; d < b; ++d) {
+    if (threadIdx.x == 0) perm[d] = -1;
+    if (xs != nullptr)
+      for (int v = threadIdx.x; v < vpr; v += blockDim.x) xs[d * vpr + v] = z;
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_dispatch_ws_bytes(int64_t rows, int k, int E) {
+  if (rows < 0 || k < 1 || E < 1) return 0;
+  int64_t chunks = n_chunks(rows * k);
+  if (chunks < 1) chunks = 1;
+  return (size_t)(chunks * E * (int64_t)sizeof(int32_t));
+}
+
+extern "C" moe_status moe_dispatch(const void* d_global, const int32_t* d_ids, int64_t rows,
+                                   int k, int H, int dtype, int E, int P, const int32_t* d_l2p,
+                                   const int32_t* d_nrep, int X, int align, int64_t cap,
+                                   int32_t* d_counts_P, int32_t* d_offsets_P, int32_t* d_perm,
+                                   int32_t* d_inv, void* d_sorted, void* d_ws, size_t ws_bytes,
+                                   uint32_t* d_status, void* stream) {
+  if (d_counts_P == nullptr || d_offsets_P == nullptr || d_ws == nullptr ||
+      (rows > 0 && (d_ids == nullptr || d_inv == nullptr)) || (cap > 0 && d_perm == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (rows < 0 || k < 1 || k > MOE_MAX_TOPK || E < 1 || P < 1 || P > MOE_MAX_SLOTS ||
+      E > MOE_MAX_SLOTS || align < 1 || cap < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (rows * k > INT32_MAX || cap > INT32_MAX) return MOE_ERR_INVALID_ARG;
+  if ((d_l2p == nullptr) != (d_nrep == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (d_l2p == nullptr && P != E) return MOE_ERR_INVALID_ARG;
+  if (d_l2p != nullptr && X < 1) return MOE_ERR_INVALID_ARG;
+  const bool move_rows = rows > 0 && (d_global != nullptr || d_sorted != nullptr);
+  int vpr = 0;
+  if (move_rows) {
+    if (d_global == nullptr || d_sorted == nullptr || H < 1) return MOE_ERR_INVALID_ARG;
+    int eb = dtype_bytes(dtype);
+    if (eb == 0) return MOE_ERR_UNSUPPORTED;
+    if (((int64_t)H * eb) % 16 != 0 || !aligned16(d_global) || !aligned16(d_sorted))
+      return MOE_ERR_INVALID_ARG;
+    vpr = (int)((int64_t)H * eb / 16);
+  }
+  if (ws_bytes < moe_dispatch_ws_bytes(rows, k, E)) return MOE_ERR_CAPACITY;
+  cudaStream_t s = as_stream(stream);
+  const int64_t pairs = rows * k;
+  const int64_t chunks = n_chunks(pairs);
+  int32_t* hist = static_cast<int32_t*>(d_ws);
+  if (chunks > 0) {
+    dispatch_hist_kernel<<<(unsigned)chunks, 256, E * sizeof(int32_t), s>>>(d_ids, pairs, E, hist,
+                                                                            d_status);
+  }
+  dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, chunks, E, P, d_l2p, d_nrep, X, align, cap,
+                                          d_counts_P, d_offsets_P, d_status);
+  if (chunks > 0) {
+    dispatch_rank_kernel<<<(unsigned)chunks, 32, E * sizeof(int32_t), s>>>(
+        d_ids, pairs, k, E, hist, d_l2p, d_nrep, X, P, d_offsets_P, cap, d_perm, d_inv, d_status);
+  }
+  if (move_rows && rows > 0) {
+    int64_t want = (rows + kCopyWarps - 1) / kCopyWarps;
+    int64_t lim = (int64_t)num_sms() * 16;
+    dispatch_copy_kernel<<<(unsigned)(want < lim ? want : lim), kCopyWarps * 32, 0, s>>>(
+        static_cast<const uint4*>(d_global), d_inv, rows, k, vpr, cap,
+        static_cast<uint4*>(d_sorted));
+  }
+  if (align > 1) {
+    dispatch_pad_kernel<<<P, 256, 0, s>>>(d_counts_P, d_offsets_P, P, vpr, cap, d_perm,
+                                          move_rows ? static_cast<uint4*>(d_sorted) : nullptr);
+  }
+  return launch_status();
+}

@@ -1,0 +1,29 @@
+// Internal launchers of the grouped SwiGLU expert FFN (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_dp.h"
+
+namespace moe {
+
+struct FfnArgs {
+  const void* xs;       // [cap, H] sorted rows
+  const int32_t* offsets;  // [P + 1]
+  int P, slot_lo, slot_hi;
+  int64_t cap;
+  const void* wgu;      // [P, 2I, H]
+  const void* wd;       // [P, H, I]
+  int H, I;
+  void* ys;             // [cap, H]
+  void* h;              // [cap, I] workspace
+  uint32_t* status;
+};
+
+// bf16 operands on the tcgen05 tensor cores (TMA-fed, TMEM accumulators).
+moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s);
+// float32 on the CUDA cores.
+moe_status launch_ffn_simt_f32(const FfnArgs& a, cudaStream_t s);
+
+}  // namespace moe

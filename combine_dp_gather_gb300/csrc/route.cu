@@ -1,0 +1,156 @@
+// Top-k routing: for every real row of the global buffer, the k experts with
+// the largest router logits (equal logits: lower id first), best first, and
+// their softmax weights.
+//
+// SGLang chapter 17 names the result TopKOutput{topk_ids, topk_weights}
+// (sections "normal dispatch 的调用链" and "Two-batch Overlap"); the scoring
+// is softmax routing, renormalised over the k chosen experts unless asked
+// otherwise.  Rows past counts[r] inside replica r's segment are padding:
+// id -1, weight 0.
+//
+// Design: one warp per row.  Lane l holds experts l, l+32, ... (coalesced
+// 128-byte loads); k rounds of a warp arg-max on (logit desc, id asc) pick
+// the experts; lane j keeps the j-th pick; the weights use expf in float32
+// and sum in pick order.
+#include <float.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 8;
+
+template <int EPL>
+__global__ void __launch_bounds__(kWarps * 32)
+    route_topk_kernel(const float* __restrict__ logits, int64_t rows, int E, int k, int renorm,
+                      const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+                      int R, int32_t* __restrict__ ids, float* __restrict__ w, uint32_t* status) {
+  __shared__ int32_t s_off[MOE_MAX_REPLICAS + 1];
+  __shared__ int32_t s_cnt[MOE_MAX_REPLICAS];
+  for (int i = threadIdx.x; i <= R; i += blockDim.x) {
+    s_off[i] = offsets[i];
+    if (i < R) s_cnt[i] = counts[i];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+  for (int64_t g = warp0; g < rows; g += nwarps) {
+    int r = find_segment(s_off, R, g);
+    int64_t i = g - s_off[r];
+    int64_t c = s_cnt[r];
+    int64_t seg = (int64_t)s_off[r + 1] - s_off[r];
+    if (c > seg) {
+      if (i == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
+      c = seg;
+    }
+    if (!(i >= 0 && i < c)) {
+      if (lane < k) {
+        ids[g * k + lane] = -1;
+        w[g * k + lane] = 0.f;
+      }
+      continue;
+    }
+    const float* lr = logits + g * E;
+    float v[EPL];
+#pragma unroll
+    for (int t = 0; t < EPL; ++t) {
+      int e = lane + 32 * t;
+      v[t] = e < E ? lr[e] : -FLT_MAX;
+    }
+    uint32_t taken = 0;
+    float my_val = 0.f;
+    int my_id = -1;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = INT32_MAX;
+#pragma unroll
+      for (int t = 0; t < EPL; ++t) {
+        int e = lane + 32 * t;
+        bool cand = e < E && !((taken >> t) & 1u);
+        if (cand && (v[t] > bv || (v[t] == bv && e < bi))) {
+          bv = v[t];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        my_val = bv;
+        my_id = bi;
+      }
+    }
+    const float top = __shfl_sync(0xffffffffu, my_val, 0);
+    float ex = lane < k ? expf(my_val - top) : 0.f;
+    float denom = 0.f;
+    if (renorm) {
+      for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
+    } else {
+      float part = 0.f;
+#pragma unroll
+      for (int t = 0; t < EPL; ++t) {
+        int e = lane + 32 * t;
+        if (e < E) part += expf(v[t] - top);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+      denom = part;
+    }
+    if (lane < k) {
+      ids[g * k + lane] = my_id;
+      w[g * k + lane] = ex / denom;
+    }
+  }
+}
+
+template <int EPL>
+void launch_route(const float* logits, int64_t rows, int E, int k, int renorm,
+                  const int32_t* counts, const int32_t* offsets, int R, int32_t* ids, float* w,
+                  uint32_t* status, cudaStream_t s) {
+  int64_t want = (rows + kWarps - 1) / kWarps;
+  int64_t cap = (int64_t)num_sms() * 8;
+  int grid = (int)(want < cap ? want : cap);
+  route_topk_kernel<EPL><<<grid, kWarps * 32, 0, s>>>(logits, rows, E, k, renorm, counts,
+                                                     offsets, R, ids, w, status);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status moe_route_topk(const float* d_logits, int64_t rows, int E, int k,
+                                     int renormalize, const int32_t* d_counts,
+                                     const int32_t* d_offsets, int R, int32_t* d_ids, float* d_w,
+                                     uint32_t* d_status, void* stream) {
+  if (rows < 0 || rows > INT32_MAX || R < 1 || R > MOE_MAX_REPLICAS) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E || k > MOE_MAX_TOPK)
+    return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (d_logits == nullptr || d_counts == nullptr || d_offsets == nullptr || d_ids == nullptr ||
+      d_w == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  if (E <= 32)
+    launch_route<1>(d_logits, rows, E, k, renormalize, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+  else if (E <= 64)
+    launch_route<2>(d_logits, rows, E, k, renormalize, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+  else if (E <= 128)
+    launch_route<4>(d_logits, rows, E, k, renormalize, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+  else if (E <= 256)
+    launch_route<8>(d_logits, rows, E, k, renormalize, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+  else if (E <= 512)
+    launch_route<16>(d_logits, rows, E, k, renormalize, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+  else
+    launch_route<32>(d_logits, rows, E, k, renormalize, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+  return launch_status();
+}

@@ -1,0 +1,310 @@
+"""Python binding of libmoe_dp (C ABI in include/moe_dp.h).
+
+Argument marshalling only: every function here forwards torch tensors' device
+pointers, sizes and the current CUDA stream to the C entry point of the same
+name and raises MoeError on a non-zero status.  No arithmetic of the layer
+happens in Python, and nothing falls back to the CPU: if the shared library
+is missing the call raises.
+
+``MoeLayer`` strings the six device calls into one MoE layer step with
+buffers allocated once (PyTorch is the allocator).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_CAPACITY, MOE_ERR_BOUND_EXCEEDED = 0, 1, 2, 3
+MOE_ERR_DEVICE_INPUT, MOE_ERR_TIMEOUT, MOE_ERR_CUDA, MOE_ERR_UNSUPPORTED = 4, 5, 6, 7
+MOE_PAD_SUM, MOE_PAD_MAX, MOE_PAD_STATIC = 0, 1, 2
+MOE_F32, MOE_BF16 = 0, 1
+MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_MAP, MOE_DEV_CAPACITY = 0x1, 0x2, 0x4
+MOE_DEV_TIMEOUT, MOE_DEV_BAD_COUNTS = 0x8, 0x10
+
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "moe_dp_layout": (_I, [_P, _I, _I, _I, _I, _P, _P]),
+    "moe_dp_padding_mode": (_I, [_P, _I, _I, _I, _I]),
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_dispatch_cap_bound": (_I64, [_I64, _I, _I, _I]),
+    "moe_dispatch_ws_bytes": (_SZ, [_I64, _I, _I]),
+    "moe_grouped_ffn_ws_bytes": (_SZ, [_I64, _I, _I]),
+    "moe_dp_gather": (_I, [_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P]),
+    "moe_route_topk": (_I, [_P, _I64, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]),
+    "moe_dispatch": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _I, _I, _I64, _P, _P, _P,
+                          _P, _P, _P, _SZ, _P, _P]),
+    "moe_grouped_ffn": (_I, [_P, _P, _I, _I, _I, _I64, _P, _P, _I, _I, _I, _P, _P, _SZ, _P,
+                             _P]),
+    "moe_combine": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I64, _P, _P, _P]),
+    "moe_dp_scatter": (_I, [_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P]),
+}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        name = lib().moe_status_string(code).decode() if _lib is not None else str(code)
+        super().__init__(f"{fn} failed: status {code} ({name})")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libmoe_dp.so (built in-tree by combine_dp_gather_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(
+                    f"{_build.LIB} is missing: build it with "
+                    "`python -m combine_dp_gather_gb300.build` (there is no CPU fallback)")
+            handle = ctypes.CDLL(_build.LIB)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+        return _lib
+
+
+def exported_symbols() -> List[str]:
+    return list(_SIGS)
+
+
+def _check(fn: str, code: int):
+    if code != MOE_OK:
+        raise MoeError(fn, code)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return MOE_BF16
+    if dt == torch.float32:
+        return MOE_F32
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def _host_i32(values: Sequence[int]):
+    arr = (ctypes.c_int32 * len(values))(*[int(v) for v in values])
+    return arr
+
+
+# ---------------------------------------------------------------- host helpers
+def moe_dp_layout(counts: Sequence[int], mode: int, static_bound: int = 0,
+                  tokens_per_req: int = 1):
+    """Host layout: returns (offsets list of R+1 ints, rows)."""
+    c = _host_i32(counts)
+    offs = (ctypes.c_int32 * (len(counts) + 1))()
+    rows = ctypes.c_int64(0)
+    _check("moe_dp_layout", lib().moe_dp_layout(ctypes.cast(c, _P), len(counts), mode,
+                                                 static_bound, tokens_per_req,
+                                                 ctypes.cast(offs, _P), ctypes.byref(rows)))
+    return list(offs), int(rows.value)
+
+
+def moe_dp_padding_mode(counts: Sequence[int], gather_width: int, is_extend_in_batch: bool,
+                        max_len_with_idle: bool) -> int:
+    c = _host_i32(counts)
+    m = lib().moe_dp_padding_mode(ctypes.cast(c, _P), len(counts), gather_width,
+                                  int(is_extend_in_batch), int(max_len_with_idle))
+    if m < 0:
+        raise MoeError("moe_dp_padding_mode", MOE_ERR_INVALID_ARG)
+    return m
+
+
+def moe_dispatch_cap_bound(rows: int, k: int, P: int, align: int) -> int:
+    return int(lib().moe_dispatch_cap_bound(rows, k, P, align))
+
+
+def moe_dispatch_ws_bytes(rows: int, k: int, E: int) -> int:
+    return int(lib().moe_dispatch_ws_bytes(rows, k, E))
+
+
+def moe_grouped_ffn_ws_bytes(cap: int, I: int, dtype: torch.dtype) -> int:
+    return int(lib().moe_grouped_ffn_ws_bytes(cap, I, dtype_code(dtype)))
+
+
+def utilization_rate(per_range_counts: Sequence[float]) -> float:
+    """Balancedness (mean + 1e-5) / (max + 1e-5) of per-rank token counts (SGLang
+    chapter 17, section "不均衡的代价与冗余专家的思路", compute_utilization_rate)."""
+    vals = [float(v) for v in per_range_counts]
+    return (sum(vals) / len(vals) + 1e-5) / (max(vals) + 1e-5)
+
+
+# ---------------------------------------------------------------- device calls
+def moe_dp_gather(local: Sequence[torch.Tensor], d_counts, d_offsets, out: torch.Tensor,
+                  d_status=None, stream=None):
+    R = len(local)
+    ptrs = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local])
+    _check("moe_dp_gather", lib().moe_dp_gather(
+        ctypes.cast(ptrs, _P), _ptr(d_counts), _ptr(d_offsets), R, out.shape[0], out.shape[1],
+        dtype_code(out.dtype), _ptr(out), _ptr(d_status), _stream(stream)))
+
+
+def moe_route_topk(logits: torch.Tensor, k: int, renormalize: bool, d_counts, d_offsets,
+                   ids: torch.Tensor, w: torch.Tensor, d_status=None, stream=None):
+    rows, E = logits.shape
+    _check("moe_route_topk", lib().moe_route_topk(
+        _ptr(logits), rows, E, k, int(renormalize), _ptr(d_counts), _ptr(d_offsets),
+        d_counts.numel(), _ptr(ids), _ptr(w), _ptr(d_status), _stream(stream)))
+
+
+def moe_dispatch(x: Optional[torch.Tensor], ids: torch.Tensor, E: int, P: int, counts_P, offsets_P,
+                 perm, inv, sorted_out: Optional[torch.Tensor], ws: torch.Tensor, l2p=None,
+                 nrep=None, align: int = 1, d_status=None, stream=None):
+    rows, k = ids.shape
+    H = x.shape[1] if x is not None else 0
+    dt = dtype_code(x.dtype) if x is not None else MOE_BF16
+    X = l2p.shape[1] if l2p is not None else 0
+    _check("moe_dispatch", lib().moe_dispatch(
+        _ptr(x), _ptr(ids), rows, k, H, dt, E, P, _ptr(l2p), _ptr(nrep), X, align,
+        perm.numel(), _ptr(counts_P), _ptr(offsets_P), _ptr(perm), _ptr(inv), _ptr(sorted_out),
+        _ptr(ws), ws.numel() * ws.element_size(), _ptr(d_status), _stream(stream)))
+
+
+def moe_grouped_ffn(xs: torch.Tensor, offsets_P: torch.Tensor, w_gate_up: torch.Tensor,
+                    w_down: torch.Tensor, ys: torch.Tensor, ws: torch.Tensor, slot_lo: int = 0,
+                    slot_hi: Optional[int] = None, d_status=None, stream=None):
+    P = w_gate_up.shape[0]
+    slot_hi = P if slot_hi is None else slot_hi
+    H = xs.shape[1]
+    I = w_down.shape[2]
+    _check("moe_grouped_ffn", lib().moe_grouped_ffn(
+        _ptr(xs), _ptr(offsets_P), P, slot_lo, slot_hi, xs.shape[0], _ptr(w_gate_up),
+        _ptr(w_down), H, I, dtype_code(xs.dtype), _ptr(ys), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(d_status), _stream(stream)))
+
+
+def moe_combine(ys: torch.Tensor, inv: torch.Tensor, w: torch.Tensor, out: torch.Tensor,
+                d_status=None, stream=None):
+    rows, k = inv.shape
+    _check("moe_combine", lib().moe_combine(
+        _ptr(ys), _ptr(inv), _ptr(w), rows, k, out.shape[1], dtype_code(out.dtype),
+        ys.shape[0], _ptr(out), _ptr(d_status), _stream(stream)))
+
+
+def moe_dp_scatter(global_buf: torch.Tensor, d_counts, d_offsets, local: Sequence[torch.Tensor],
+                   d_status=None, stream=None):
+    R = len(local)
+    ptrs = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local])
+    _check("moe_dp_scatter", lib().moe_dp_scatter(
+        _ptr(global_buf), _ptr(d_counts), _ptr(d_offsets), R, global_buf.shape[0],
+        global_buf.shape[1], dtype_code(global_buf.dtype), ctypes.cast(ptrs, _P),
+        _ptr(d_status), _stream(stream)))
+
+
+# ---------------------------------------------------------------- one layer
+class MoeLayer:
+    """One MoE layer between DP attention and EP on one GPU.
+
+    Buffers are sized once for `max_rows` global rows; `forward` runs
+    gather -> route -> dispatch -> grouped FFN -> combine -> scatter on the
+    current stream without a host synchronisation."""
+
+    def __init__(self, *, R: int, H: int, E: int, k: int, I: int, w_gate_up: torch.Tensor,
+                 w_down: torch.Tensor, max_rows: int, mode: int = MOE_PAD_SUM,
+                 static_bound: int = 0, tokens_per_req: int = 1, renormalize: bool = True,
+                 align: int = 1, l2p: Optional[torch.Tensor] = None,
+                 nrep: Optional[torch.Tensor] = None, slot_range=None):
+        dev = w_gate_up.device
+        self.R, self.H, self.E, self.k, self.I = R, H, E, k, I
+        self.P = w_gate_up.shape[0]
+        self.dtype = w_gate_up.dtype
+        self.mode, self.static_bound, self.tpr = mode, static_bound, tokens_per_req
+        self.renormalize, self.align = renormalize, align
+        self.wgu, self.wd, self.l2p, self.nrep = w_gate_up, w_down, l2p, nrep
+        self.slot_range = slot_range or (0, self.P)
+        self.max_rows = max_rows
+        self.cap = moe_dispatch_cap_bound(max_rows, k, self.P, align)
+        i32 = dict(device=dev, dtype=torch.int32)
+        self.d_counts = torch.zeros(R, **i32)
+        self.d_offsets = torch.zeros(R + 1, **i32)
+        self.h_meta = torch.zeros(2 * R + 1, dtype=torch.int32, pin_memory=True)
+        self._meta_done = torch.cuda.Event()
+        self._meta_done.record()
+        self.status = torch.zeros(1, **i32)
+        self.xg = torch.empty(max_rows, H, device=dev, dtype=self.dtype)
+        self.logits_g = torch.empty(max_rows, E, device=dev, dtype=torch.float32)
+        self.ids = torch.empty(max_rows, k, **i32)
+        self.w = torch.empty(max_rows, k, device=dev, dtype=torch.float32)
+        self.counts_P = torch.empty(self.P, **i32)
+        self.offsets_P = torch.empty(self.P + 1, **i32)
+        self.perm = torch.empty(self.cap, **i32)
+        self.inv = torch.empty(max_rows, k, **i32)
+        self.xs = torch.empty(self.cap, H, device=dev, dtype=self.dtype)
+        self.ys = torch.empty(self.cap, H, device=dev, dtype=self.dtype)
+        self.yg = torch.empty(max_rows, H, device=dev, dtype=self.dtype)
+        self.ws_dispatch = torch.empty(max(moe_dispatch_ws_bytes(max_rows, k, E), 16),
+                                       device=dev, dtype=torch.uint8)
+        self.ws_ffn = torch.empty(max(moe_grouped_ffn_ws_bytes(self.cap, I, self.dtype), 16),
+                                  device=dev, dtype=torch.uint8)
+        self.rows = 0
+
+    def set_counts(self, counts: Sequence[int]) -> int:
+        """Host layout for this step's replica counts; stages counts and offsets on
+        the device (one pinned H2D copy).  Returns the global row count."""
+        offsets, rows = moe_dp_layout(counts, self.mode, self.static_bound, self.tpr)
+        if rows > self.max_rows:
+            raise MoeError("MoeLayer.set_counts", MOE_ERR_CAPACITY)
+        self._meta_done.synchronize()  # the previous copy has read the pinned buffer
+        self.h_meta[: self.R] = torch.tensor(list(counts), dtype=torch.int32)
+        self.h_meta[self.R:] = torch.tensor(offsets, dtype=torch.int32)
+        self.d_counts.copy_(self.h_meta[: self.R], non_blocking=True)
+        self.d_offsets.copy_(self.h_meta[self.R:], non_blocking=True)
+        self._meta_done.record()
+        self.rows = rows
+        return rows
+
+    def forward(self, local_x: Sequence[torch.Tensor], local_logits: Sequence[torch.Tensor],
+                out: Sequence[torch.Tensor], counts: Optional[Sequence[int]] = None,
+                stream=None, timings=None):
+        if counts is not None:
+            self.set_counts(counts)
+        rows = self.rows
+        st = self.status
+        xg, lg = self.xg[:rows], self.logits_g[:rows]
+        ids, w, inv, yg = self.ids[:rows], self.w[:rows], self.inv[:rows], self.yg[:rows]
+        ev = timings.mark if timings is not None else (lambda name: None)
+        ev("start")
+        moe_dp_gather(local_x, self.d_counts, self.d_offsets, xg, st, stream)
+        moe_dp_gather(local_logits, self.d_counts, self.d_offsets, lg, st, stream)
+        ev("gather")
+        moe_route_topk(lg, self.k, self.renormalize, self.d_counts, self.d_offsets, ids, w, st,
+                       stream)
+        ev("route")
+        moe_dispatch(xg, ids, self.E, self.P, self.counts_P, self.offsets_P, self.perm, inv,
+                     self.xs, self.ws_dispatch, self.l2p, self.nrep, self.align, st, stream)
+        ev("dispatch")
+        moe_grouped_ffn(self.xs, self.offsets_P, self.wgu, self.wd, self.ys, self.ws_ffn,
+                        self.slot_range[0], self.slot_range[1], st, stream)
+        ev("ffn")
+        moe_combine(self.ys, inv, w, yg, st, stream)
+        ev("combine")
+        moe_dp_scatter(yg, self.d_counts, self.d_offsets, out, st, stream)
+        ev("scatter")
+        return out

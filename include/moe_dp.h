@@ -1,0 +1,240 @@
+/*
+ * moe_dp.h -- C ABI of libmoe_dp, the GB300 (sm_103a) MoE layer that sits
+ * between data-parallel attention and expert parallelism, run on one GPU.
+ *
+ * One layer is six stream-ordered device calls:
+ *
+ *   moe_dp_gather    per-replica token segments  -> one global buffer
+ *   moe_route_topk   router logits               -> top-k expert ids + weights
+ *   moe_dispatch     ids (+ expert map)          -> per-slot counts/offsets,
+ *                                                   permutation, sorted rows
+ *   moe_grouped_ffn  sorted rows + expert weights -> SwiGLU expert outputs
+ *   moe_combine      expert outputs + weights    -> token-order outputs
+ *   moe_dp_scatter   global buffer               -> per-replica segments
+ *
+ * plus host helpers for the global-buffer layout (moe_dp_layout,
+ * moe_dp_padding_mode) and workspace sizing.
+ *
+ * Sources of the operations (web pages this library follows):
+ *   [P1] "SGLang 源码完全拆解(十七): DP Attention 与专家并行" -- SGLang source
+ *        walkthrough, chapter 17: DP attention and expert parallelism.
+ *   [P2] "vLLM 源码完全拆解(二十七): Dual Batch Overlap".
+ *   [P4] "DP" (zdszero, data_parallelism): DP vs TP, MLP sync, static bound.
+ *
+ * Conventions (every entry point):
+ *   - Ownership: the caller owns every buffer.  The library allocates no
+ *     memory and keeps no state between calls, except a per-process cache of
+ *     the driver's tensor-map encoder and of SM counts.
+ *   - "d_" pointers are device pointers; "h_" or unprefixed array pointers
+ *     are host pointers.  Shapes are row-major.
+ *   - Device calls are asynchronous on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream) and never synchronise the
+ *     host.
+ *   - Host-checkable errors (null pointers, bad sizes, unsupported dtype or
+ *     shape) return an error status before anything is launched.  A failed
+ *     launch returns MOE_ERR_CUDA.
+ *   - Data-dependent errors found on the device (an expert id outside
+ *     [0, E), a bad map entry, capacity exceeded, a count larger than its
+ *     segment, a bounded wait that gave up) are OR-ed into *d_status as
+ *     MOE_DEV_* bits.  The caller zeroes *d_status before a layer and reads
+ *     it after synchronising.  Kernels skip the offending accesses; they
+ *     never trap.
+ *   - Rows move as 16-byte vectors: the row width in bytes of every copied
+ *     or combined tensor must be a multiple of 16 and every base pointer
+ *     16-byte aligned.
+ */
+#ifndef MOE_DP_H
+#define MOE_DP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,     /* null pointer, negative or inconsistent size */
+  MOE_ERR_CAPACITY = 2,        /* a caller-provided buffer is too small */
+  MOE_ERR_BOUND_EXCEEDED = 3,  /* a replica count exceeds the static bound */
+  MOE_ERR_DEVICE_INPUT = 4,    /* reserved for callers mapping MOE_DEV_* bits */
+  MOE_ERR_TIMEOUT = 5,         /* reserved for callers mapping MOE_DEV_TIMEOUT */
+  MOE_ERR_CUDA = 6,            /* a CUDA runtime call or launch failed */
+  MOE_ERR_UNSUPPORTED = 7      /* dtype / shape / device not supported */
+} moe_status;
+
+/* Global-buffer padding modes: [P1] section "DpPaddingMode" (MAX_LEN, SUM_LEN)
+ * and [P4] section "跳过同步: 用约定代替通信" (static bound B). */
+typedef enum { MOE_PAD_SUM = 0, MOE_PAD_MAX = 1, MOE_PAD_STATIC = 2 } moe_pad_mode;
+
+/* Element types: MOE_F32 rows are float32; MOE_BF16 rows are bfloat16 with
+ * float32 accumulation wherever the layer sums. */
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Bits OR-ed into the device status word. */
+#define MOE_DEV_BAD_EXPERT_ID 0x1u /* routed id outside [-1, E) */
+#define MOE_DEV_BAD_MAP 0x2u       /* num_valid outside [1, X] or slot outside [0, P) */
+#define MOE_DEV_CAPACITY 0x4u      /* padded slot total exceeds cap */
+#define MOE_DEV_TIMEOUT 0x8u       /* a bounded device wait gave up */
+#define MOE_DEV_BAD_COUNTS 0x10u   /* a replica count exceeds its segment, or an
+                                      index points outside its buffer */
+
+#define MOE_MAX_REPLICAS 256 /* R limit (replica pointers travel as kernel arguments) */
+#define MOE_MAX_SLOTS 1024   /* P limit of the grouped FFN's tile scheduler */
+#define MOE_MAX_EXPERTS 1024 /* E limit of moe_route_topk */
+#define MOE_MAX_TOPK 32      /* k limit */
+
+/* ========================================================================
+ * Host helpers (pure integer; no CUDA call, usable without a GPU)
+ * ======================================================================== */
+
+/* Offsets of the replicas' segments in the global buffer.
+ * [P1] section "本 rank 的切片位置怎么算" (get_dp_local_info): replica r starts
+ * at the exclusive prefix sum of the counts.  [P1] section "DpPaddingMode":
+ * MAX pads each replica to the largest count (offset r * max), SUM packs them
+ * back to back.  [P4] section "跳过同步": with a static bound B every replica
+ * gets B requests of tokens_per_req tokens (offset r * B * tokens_per_req;
+ * [P4] section "整体流程" for requests times draft + 1).
+ *   counts          host int32[R], tokens per replica (>= 0; 0 = idle replica)
+ *   R               1 .. MOE_MAX_REPLICAS
+ *   mode            moe_pad_mode
+ *   static_bound    B (requests per replica), used by MOE_PAD_STATIC only
+ *   tokens_per_req  >= 1, used by MOE_PAD_STATIC only
+ *   offsets         host int32[R + 1] out; offsets[R] = rows
+ *   rows            host out, global buffer rows (real + padding)
+ * Returns MOE_ERR_BOUND_EXCEEDED if a count exceeds B * tokens_per_req,
+ * MOE_ERR_INVALID_ARG for negative counts or a total above INT32_MAX. */
+moe_status moe_dp_layout(const int32_t* counts, int R, int mode, int static_bound,
+                         int tokens_per_req, int32_t* offsets, int64_t* rows);
+
+/* The padding-mode heuristic of [P1] section "DpPaddingMode"
+ * (get_dp_padding_mode) without its a2a-backend branches: with prefill in the
+ * batch and gather_width > 1 it returns SUM (MAX if max_len_with_idle and some
+ * count is 0); otherwise MAX iff 2 * sum(counts) >= max(counts) * gather_width.
+ * Returns a moe_pad_mode, or -1 on invalid arguments. */
+int moe_dp_padding_mode(const int32_t* counts, int R, int gather_width, int is_extend_in_batch,
+                        int max_len_with_idle);
+
+/* Human-readable name of a moe_status value (static storage). */
+const char* moe_status_string(int status);
+
+/* Upper bound of the dispatch capacity: every routed (row, j) pair plus
+ * alignment padding, rows * k + P * (align - 1). */
+int64_t moe_dispatch_cap_bound(int64_t rows, int k, int P, int align);
+
+/* Bytes of device workspace moe_dispatch needs for rows x k routed pairs over
+ * E logical experts (per-chunk histograms). */
+size_t moe_dispatch_ws_bytes(int64_t rows, int k, int E);
+
+/* Bytes of device workspace moe_grouped_ffn needs: the SwiGLU activations
+ * h[cap, I] in the layer dtype. */
+size_t moe_grouped_ffn_ws_bytes(int64_t cap, int I, int dtype);
+
+/* ========================================================================
+ * Device calls
+ * ======================================================================== */
+
+/* DP gather: copy replica r's counts[r] rows to global rows
+ * [offsets[r], offsets[r] + counts[r]) and zero every other row.
+ * [P1] section "两种 gather: all_reduce 与 all_gather" (path one: fill the
+ * global buffer with zeros, copy the local segment at its start row; on one
+ * device the all-reduce adds nothing else).
+ *   local      HOST array of R device pointers; local[r] is [counts[r], H]
+ *   d_counts   device int32[R]; d_offsets device int32[R + 1] (moe_dp_layout)
+ *   rows       global rows (= offsets[R]); H row width in elements
+ *   d_global   device [rows, H] out
+ * A count larger than its segment sets MOE_DEV_BAD_COUNTS and copies only the
+ * rows that fit. */
+moe_status moe_dp_gather(const void* const* local, const int32_t* d_counts,
+                         const int32_t* d_offsets, int R, int64_t rows, int H, int dtype,
+                         void* d_global, uint32_t* d_status, void* stream);
+
+/* Top-k routing of every real row of the global buffer.  [P1] names the
+ * result TopKOutput{topk_ids, topk_weights} (sections "normal dispatch 的调用链"
+ * and "Two-batch Overlap"); the scoring is softmax routing: the k largest
+ * logits win (equal logits: lower expert id first), listed best first; with
+ * renormalize the weights are the softmax of the k chosen logits, else the
+ * full softmax probabilities of the chosen experts.  Pad rows (not among the
+ * first counts[r] rows of their segment) get id -1 and weight 0.
+ *   d_logits  device float32[rows, E], finite values
+ *   E         1 .. MOE_MAX_EXPERTS; k 1 .. min(E, MOE_MAX_TOPK)
+ *   d_ids     device int32[rows, k] out; d_w device float32[rows, k] out */
+moe_status moe_route_topk(const float* d_logits, int64_t rows, int E, int k, int renormalize,
+                          const int32_t* d_counts, const int32_t* d_offsets, int R,
+                          int32_t* d_ids, float* d_w, uint32_t* d_status, void* stream);
+
+/* Dispatch: stable sort of the routed (row, j) pairs by physical expert slot.
+ * [P1] section "normal dispatch 的调用链" (get_dispatch_layout: tokens per
+ * expert; expert_alignment rounds each expert's count up to a multiple of
+ * 128 for the grouped GEMM).  [P1] sections "逻辑与物理的两套映射" and
+ * "推理时怎么选副本" (logical_to_all_physical_map[E, X] with num_valid[E];
+ * one rank-invariant replica per token): occurrence p of logical expert l,
+ * counted in (row, j) order, goes to replica p mod num_valid[l].
+ *   d_global   device [rows, H] rows to permute (may be NULL: indices only)
+ *   d_ids      device int32[rows, k]; -1 marks a pad row
+ *   E, P       logical experts, physical slots (P == E when d_l2p is NULL)
+ *   d_l2p      device int32[E, X] slot of each replica, or NULL
+ *   d_nrep     device int32[E] replicas per logical expert, or NULL
+ *   align      >= 1; each slot's count is rounded up to a multiple of align
+ *   cap        rows of d_perm / d_sorted (moe_dispatch_cap_bound suffices)
+ * Outputs (device): d_counts_P int32[P] tokens per slot; d_offsets_P
+ * int32[P + 1] slot starts (exclusive scan of the rounded counts);
+ * d_perm int32[cap] source row of each sorted position (-1 at alignment
+ * padding; defined for positions < d_offsets_P[P]); d_inv int32[rows, k]
+ * sorted position of each (row, j) (-1 for pad rows); d_sorted [cap, H]
+ * permuted rows (alignment padding rows zeroed).
+ *   d_ws, ws_bytes   workspace of at least moe_dispatch_ws_bytes(rows, k, E)
+ * Device errors: MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_MAP, MOE_DEV_CAPACITY (no
+ * write goes past cap). */
+moe_status moe_dispatch(const void* d_global, const int32_t* d_ids, int64_t rows, int k, int H,
+                        int dtype, int E, int P, const int32_t* d_l2p, const int32_t* d_nrep,
+                        int X, int align, int64_t cap, int32_t* d_counts_P,
+                        int32_t* d_offsets_P, int32_t* d_perm, int32_t* d_inv, void* d_sorted,
+                        void* d_ws, size_t ws_bytes, uint32_t* d_status, void* stream);
+
+/* Grouped SwiGLU expert FFN over the sorted rows of slots [slot_lo, slot_hi)
+ * (one contiguous slot range stands for one EP rank).  For each slot s and
+ * each row x in [offsets[s], offsets[s + 1]):
+ *   h = silu(x Wg_s^T) * (x Wu_s^T),  y = h Wd_s^T
+ * ([P1] opening sections: gate_proj and up_proj are [I, H], down_proj is
+ * [H, I]; [P2] figure "MoE 模块化内核的 PrepareAndFinalize 块结构": MM1,
+ * activation, MM2.)
+ *   d_sorted     device [cap, H]
+ *   d_offsets_P  device int32[P + 1] from moe_dispatch
+ *   d_w_gate_up  device [P, 2I, H]: gate rows 0..I-1, up rows I..2I-1
+ *   d_w_down     device [P, H, I]
+ *   d_out_sorted device [cap, H] out; rows of other slots are not written
+ *   d_ws         workspace >= moe_grouped_ffn_ws_bytes(cap, I, dtype)
+ * MOE_BF16 runs on the tcgen05 tensor cores (fp32 accumulation in tensor
+ * memory, h rounded to bf16) and needs H % 256 == 0, I % 128 == 0 and
+ * P <= MOE_MAX_SLOTS; MOE_F32 runs a CUDA-core kernel (fp32 throughout). */
+moe_status moe_grouped_ffn(const void* d_sorted, const int32_t* d_offsets_P, int P, int slot_lo,
+                           int slot_hi, int64_t cap, const void* d_w_gate_up,
+                           const void* d_w_down, int H, int I, int dtype, void* d_out_sorted,
+                           void* d_ws, size_t ws_bytes, uint32_t* d_status, void* stream);
+
+/* Combine: un-permute and apply the top-k weights.
+ * [P2] figure "MoE 模块化内核的 PrepareAndFinalize 块结构" (finalize applies
+ * the top-k weights): out[row] = sum_{j<k} w[row, j] * y[inv[row, j]],
+ * accumulated in float32 in j order and rounded once; rows whose inv entries
+ * are all -1 (pad rows) are zero.
+ *   d_out_sorted device [cap, H]; d_inv device int32[rows, k];
+ *   d_w device float32[rows, k]; d_global_out device [rows, H] out.
+ * An inv entry >= cap sets MOE_DEV_BAD_COUNTS and is skipped. */
+moe_status moe_combine(const void* d_out_sorted, const int32_t* d_inv, const float* d_w,
+                       int64_t rows, int k, int H, int dtype, int64_t cap, void* d_global_out,
+                       uint32_t* d_status, void* stream);
+
+/* DP scatter: copy global rows [offsets[r], offsets[r] + counts[r]) back to
+ * replica r.  [P1] section "scatter: 把 MoE 的输出还回本副本" (reduce_scatterv
+ * split by the same global_num_tokens that placed the rows).
+ *   local  HOST array of R device pointers; local[r] is [counts[r], H] out */
+moe_status moe_dp_scatter(const void* d_global, const int32_t* d_counts, const int32_t* d_offsets,
+                          int R, int64_t rows, int H, int dtype, void* const* local,
+                          uint32_t* d_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_DP_H */

@@ -1,0 +1,193 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+symbol include/moe_dp.h declares, its host helpers agree with the oracle, and
+every device entry point rejects invalid arguments before launching anything
+(host-side fault injection)."""
+import ctypes
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT, ints, read_golden
+
+HEADER = os.path.join(ROOT, "include", "moe_dp.h")
+
+
+@pytest.fixture(scope="module")
+def md():
+    from combine_dp_gather_gb300 import build, moe_dp
+    build.build()
+    moe_dp.lib()
+    return moe_dp
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(
+        r"^\s*(?:moe_status|int|int64_t|size_t|const char\*)\s+(moe_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declarations_are_exported(md):
+    names = declared_symbols()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(md.lib_path())
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(md.exported_symbols()) == names
+
+
+@pytest.mark.parametrize("row", read_golden("dp_layout.txt"))
+def test_layout_golden(md, row):
+    counts, mode, B, tpr, offs, rows = row
+    o, n = md.moe_dp_layout(ints(counts), {"sum": 0, "max": 1, "static": 2}[mode], int(B),
+                            int(tpr))
+    assert o == ints(offs) and n == int(rows)
+
+
+@pytest.mark.parametrize("row", read_golden("dp_layout_errors.txt"))
+def test_layout_errors_golden(md, row):
+    counts, mode, B, tpr, err = row
+    with pytest.raises(md.MoeError) as ei:
+        md.moe_dp_layout(ints(counts), {"sum": 0, "max": 1, "static": 2}[mode], int(B), int(tpr))
+    assert ei.value.code == {"bound": md.MOE_ERR_BOUND_EXCEEDED, "arg": md.MOE_ERR_INVALID_ARG}[err]
+
+
+@pytest.mark.parametrize("row", read_golden("dp_padding_mode.txt"))
+def test_padding_mode_golden(md, row):
+    counts, width, ext, idle, mode = row
+    assert md.moe_dp_padding_mode(ints(counts), int(width), bool(int(ext)), bool(int(idle))) == \
+        {"sum": 0, "max": 1}[mode]
+
+
+def test_layout_and_mode_agree_with_oracle_exhaustively(md, orc):
+    for R in (1, 2, 3):
+        for counts in itertools.product([0, 1, 3, 24, 25], repeat=R):
+            counts = list(counts)
+            for mode in (0, 1):
+                assert md.moe_dp_layout(counts, mode)[0] == orc.dp_layout(counts, mode)[0].tolist()
+            for B, tpr in ((24, 1), (6, 4)):
+                try:
+                    ref = orc.dp_layout(counts, 2, B, tpr)
+                except orc.OracleError as e:
+                    with pytest.raises(md.MoeError) as ei:
+                        md.moe_dp_layout(counts, 2, B, tpr)
+                    assert ei.value.code == e.code
+                else:
+                    assert md.moe_dp_layout(counts, 2, B, tpr) == (ref[0].tolist(), ref[1])
+            for w, ext, idle in itertools.product((1, R, 4), (0, 1), (0, 1)):
+                assert md.moe_dp_padding_mode(counts, w, ext, idle) == \
+                    orc.dp_padding_mode(counts, w, ext, idle)
+
+
+@pytest.mark.parametrize("row", read_golden("balancedness.txt"))
+def test_balancedness_golden(md, row):
+    assert md.utilization_rate(ints(row[0])) == pytest.approx(float(row[1]), rel=1e-15)
+
+
+def test_sizes(md):
+    assert md.moe_dispatch_cap_bound(8192, 8, 256, 1) == 65536
+    assert md.moe_dispatch_cap_bound(10, 2, 4, 128) == 20 + 4 * 127
+    assert md.moe_dispatch_ws_bytes(8192, 8, 256) == 64 * 256 * 4
+    assert md.moe_grouped_ffn_ws_bytes(100, 2048, __import__("torch").bfloat16) == 100 * 2048 * 2
+
+
+# ---------------------------------------------------------------- fault injection
+NULL = None
+FAKE = ctypes.c_void_p(0x1000)      # aligned, never dereferenced: calls must fail first
+MISAL = ctypes.c_void_p(0x1008)     # not 16-byte aligned
+
+
+def _ptrs(*p):
+    return ctypes.cast((ctypes.c_void_p * len(p))(*p), ctypes.c_void_p)
+
+
+def test_gather_scatter_reject_bad_args(md):
+    L = md.lib()
+    two = _ptrs(0x2000, 0x3000)
+    E_ARG, E_UNS = md.MOE_ERR_INVALID_ARG, md.MOE_ERR_UNSUPPORTED
+    assert L.moe_dp_gather(two, NULL, FAKE, 2, 8, 64, 1, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_dp_gather(two, FAKE, FAKE, 0, 8, 64, 1, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_dp_gather(two, FAKE, FAKE, 300, 8, 64, 1, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_dp_gather(two, FAKE, FAKE, 2, -1, 64, 1, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_dp_gather(two, FAKE, FAKE, 2, 8, 7, 1, FAKE, NULL, NULL) == E_ARG  # 14 B rows
+    assert L.moe_dp_gather(two, FAKE, FAKE, 2, 8, 64, 9, FAKE, NULL, NULL) == E_UNS
+    assert L.moe_dp_gather(two, FAKE, FAKE, 2, 8, 64, 1, MISAL, NULL, NULL) == E_ARG
+    assert L.moe_dp_gather(_ptrs(0x2008, 0x3000), FAKE, FAKE, 2, 8, 64, 1, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_dp_gather(NULL, FAKE, FAKE, 2, 8, 64, 1, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_dp_scatter(FAKE, FAKE, FAKE, 2, 8, 64, 1, NULL, NULL, NULL) == E_ARG
+    assert L.moe_dp_scatter(FAKE, NULL, FAKE, 2, 8, 64, 1, two, NULL, NULL) == E_ARG
+
+
+def test_route_rejects_bad_args(md):
+    L = md.lib()
+    E_ARG = md.MOE_ERR_INVALID_ARG
+    ok = dict(rows=8, E=256, k=8)
+    assert L.moe_route_topk(FAKE, 8, 256, 0, 1, FAKE, FAKE, 2, FAKE, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_route_topk(FAKE, 8, 4, 5, 1, FAKE, FAKE, 2, FAKE, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_route_topk(FAKE, 8, 2048, 8, 1, FAKE, FAKE, 2, FAKE, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_route_topk(FAKE, 8, 256, 33, 1, FAKE, FAKE, 2, FAKE, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_route_topk(NULL, 8, 256, 8, 1, FAKE, FAKE, 2, FAKE, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_route_topk(FAKE, 8, 256, 8, 1, FAKE, FAKE, 0, FAKE, FAKE, NULL, NULL) == E_ARG
+    del ok
+
+
+def test_dispatch_rejects_bad_args(md):
+    L = md.lib()
+    E_ARG, E_CAP = md.MOE_ERR_INVALID_ARG, md.MOE_ERR_CAPACITY
+
+    def call(**kw):
+        a = dict(g=FAKE, ids=FAKE, rows=16, k=2, H=64, dt=1, E=8, P=8, l2p=NULL, nrep=NULL, X=0,
+                 align=1, cap=32, cnt=FAKE, off=FAKE, perm=FAKE, inv=FAKE, xs=FAKE, ws=FAKE,
+                 wsb=1 << 20)
+        a.update(kw)
+        return L.moe_dispatch(a["g"], a["ids"], a["rows"], a["k"], a["H"], a["dt"], a["E"],
+                              a["P"], a["l2p"], a["nrep"], a["X"], a["align"], a["cap"], a["cnt"],
+                              a["off"], a["perm"], a["inv"], a["xs"], a["ws"], a["wsb"], NULL,
+                              NULL)
+
+    assert call(P=9) == E_ARG                  # P != E without a map
+    assert call(l2p=FAKE) == E_ARG             # map without num_valid
+    assert call(l2p=FAKE, nrep=FAKE, X=0, P=9) == E_ARG
+    assert call(align=0) == E_ARG
+    assert call(k=0) == E_ARG
+    assert call(P=2000, E=2000) == E_ARG
+    assert call(ids=NULL) == E_ARG
+    assert call(xs=NULL) == E_ARG              # rows without a destination
+    assert call(xs=MISAL) == E_ARG
+    assert call(H=7) == E_ARG
+    assert call(wsb=0) == E_CAP
+
+
+def test_ffn_and_combine_reject_bad_args(md):
+    L = md.lib()
+    E_ARG, E_UNS, E_CAP = md.MOE_ERR_INVALID_ARG, md.MOE_ERR_UNSUPPORTED, md.MOE_ERR_CAPACITY
+
+    def ffn(**kw):
+        a = dict(xs=FAKE, off=FAKE, P=8, lo=0, hi=8, cap=64, wgu=FAKE, wd=FAKE, H=512, I=256, dt=1,
+                 ys=FAKE, ws=FAKE, wsb=1 << 30)
+        a.update(kw)
+        return L.moe_grouped_ffn(a["xs"], a["off"], a["P"], a["lo"], a["hi"], a["cap"], a["wgu"],
+                                 a["wd"], a["H"], a["I"], a["dt"], a["ys"], a["ws"], a["wsb"],
+                                 NULL, NULL)
+
+    assert ffn(hi=9) == E_ARG
+    assert ffn(lo=5, hi=4) == E_ARG
+    assert ffn(wsb=10) == E_CAP
+    assert ffn(H=384) == E_UNS                 # bf16 path needs H % 256 == 0
+    assert ffn(I=192) == E_UNS                 # and I % 128 == 0
+    assert ffn(P=2000, hi=2000) == E_UNS
+    assert ffn(dt=5) == E_UNS
+    assert ffn(wgu=MISAL) == E_ARG
+    assert ffn(off=NULL) == E_ARG
+    assert L.moe_combine(FAKE, FAKE, FAKE, 8, 0, 64, 1, 64, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_combine(FAKE, FAKE, FAKE, 8, 2, 4, 1, 64, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_combine(FAKE, NULL, FAKE, 8, 2, 64, 1, 64, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_combine(FAKE, FAKE, FAKE, 8, 2, 64, 3, 64, FAKE, NULL, NULL) == E_UNS
+
+
+def test_status_strings(md):
+    for code in range(8):
+        assert md.lib().moe_status_string(code).decode() != "unknown status"
+    assert md.lib().moe_status_string(99).decode() == "unknown status"
