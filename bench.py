@@ -1,0 +1,461 @@
+"""Benchmark of one MoE layer between DP attention and EP on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode|prefill|...]
+    python bench.py --impl reference ...      # the CPU oracle, timed on host cores
+
+A step is one pass of the whole hot path over one batch: DP gather (hidden
+states and router logits), top-k routing, dispatch, grouped SwiGLU expert FFN
+on the tensor cores, combine and DP scatter.  The default workload is the
+DeepSeek-V3-shaped decode layer: 8 DP replicas with seeded token counts in
+[0, 64] (one idle), MAX padding, hidden 7168, 256 experts, top-8, expert
+intermediate 2048, bf16 weights/activations with fp32 accumulation.
+
+Printed: one JSON line (rank 0).  `value` is tokens/s with inputs resident in
+HBM; `e2e` is the same metric through the same C-ABI calls with the step's
+inputs copied from pinned host buffers and its outputs copied back inside the
+timed region.  `roofline` reports the grouped FFN (the dominant call: two
+tcgen05 kernel launches that stream the expert weights) against the measured
+HBM copy bandwidth.  N > 1 runs independent replicas, one per GPU (the layer
+has no cross-GPU exchange on this path), and reports the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from combine_dp_gather_gb300 import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s on 1 GB300"
+UNIT = "tokens/s"
+L2_NOTE = "inputs larger than L2: every step streams the touched experts' weights from HBM"
+
+# Launches of this library per step (gather x2, route, dispatch hist/scan/rank/copy,
+# grouped FFN MM1+SwiGLU and MM2, combine, scatter); +1 when align > 1.
+LAUNCHES_PER_STEP = 11
+
+# dram__bytes_read.sum + dram__bytes_write.sum of the two grouped-FFN launches of one
+# decode step (ncu, --clock-control none), valid for the ffn_tc.cu source whose SHA-256
+# prefix is recorded; any other source reports traffic null.
+FFN_TRAFFIC = {"decode": {"sha256_16": None, "bytes": None}}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", default="decode",
+                    choices=["decode", "prefill", "pad_sweep", "eplb", "tiny"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    return ap.parse_args()
+
+
+def make_spec(name: str, seed: int):
+    if name == "decode":
+        return synth.spec_decode(seed=seed)
+    if name == "prefill":
+        return synth.spec_prefill()
+    if name == "pad_sweep":
+        return synth.spec_pad_sweep("mix1", 4, synth.PAD_MAX)
+    if name == "eplb":
+        return synth.spec_eplb()
+    return synth.spec_tiny()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        busy = [s for s in sms if mx and s > 0.5 * mx] or sms
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ------------------------------------------------------------------ native arm
+class StepEvents:
+    """CUDA events recorded on the launching stream at each stage boundary."""
+
+    def __init__(self):
+        self.marks = []
+
+    def mark(self, name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        self.marks.append((name, e))
+
+    def durations(self):
+        out = {}
+        for (a, ea), (b, eb) in zip(self.marks, self.marks[1:]):
+            out[b] = ea.elapsed_time(eb)
+        return out
+
+
+def ffn_traffic(config: str):
+    rec = FFN_TRAFFIC.get(config)
+    if not rec or rec["bytes"] is None:
+        return None
+    src = os.path.join(ROOT, "combine_dp_gather_gb300", "csrc", "ffn_tc.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec["bytes"] if h == rec["sha256_16"] else None
+
+
+def run_native(args, rank, world, local_rank):
+    from combine_dp_gather_gb300 import build as cbuild
+    from combine_dp_gather_gb300 import moe_dp as md
+    if rank == 0 or not os.path.exists(cbuild.LIB):
+        cbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    spec = make_spec(args.config, args.seed)
+    l2p_np, nrep_np, p2l = synth.make_map(spec)
+    x_loc = synth.hidden_states(spec, dev)
+    lg_loc = synth.router_logits(spec, dev)
+    wgu, wd = synth.expert_weights(spec, p2l, dev)
+    offs, rows = md.moe_dp_layout(spec.counts, spec.mode, spec.static_bound, spec.tokens_per_req)
+    layer = md.MoeLayer(
+        R=spec.R, H=spec.H, E=spec.E, k=spec.k, I=spec.I, w_gate_up=wgu, w_down=wd,
+        max_rows=max(rows, 1), mode=spec.mode, static_bound=spec.static_bound,
+        tokens_per_req=spec.tokens_per_req, renormalize=spec.renormalize, align=spec.align,
+        l2p=None if l2p_np is None else torch.from_numpy(l2p_np).to(dev),
+        nrep=None if nrep_np is None else torch.from_numpy(nrep_np).to(dev))
+    out = [torch.empty(c, spec.H, device=dev, dtype=wgu.dtype) for c in spec.counts]
+    layer.set_counts(spec.counts)
+    for _ in range(args.warmup):
+        layer.forward(x_loc, lg_loc, out)
+    torch.cuda.synchronize()
+    if int(layer.status.item()) != 0:
+        raise RuntimeError(f"device status {int(layer.status.item()):#x} after warm-up")
+
+    # ---- timed region: K steps, inputs resident in HBM
+    evs = [StepEvents() for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(args.steps):
+            layer.forward(x_loc, lg_loc, out, timings=evs[i])
+        t1.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = t0.elapsed_time(t1)
+    clocks = clk.summary()
+    stage = {}
+    for e in evs:
+        for k, v in e.durations().items():
+            stage.setdefault(k, []).append(v)
+    stage_ms = {k: statistics.mean(v) for k, v in stage.items()}
+
+    counts_P = layer.counts_P.cpu().numpy()
+    touched = int((counts_P > 0).sum())
+    routed = int(layer.offsets_P[-1].item())
+    T = spec.T
+    b = 2 if spec.dtype == "bf16" else 4
+    ffn_bytes = touched * 3 * spec.I * spec.H * b + routed * (2 * spec.H + 2 * spec.I) * b
+    ffn_flops = synth.flops_ffn(T, spec.k, spec.H, spec.I)
+    ffn_ms = stage_ms["ffn"]
+    pk = peaks()
+    hbm_bound = ffn_flops / (ffn_bytes) < (pk["bf16_tflops"] * 1e12) / (pk["hbm_gbs"] * 1e9)
+    if hbm_bound:
+        achieved = ffn_bytes / (ffn_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4)}
+    else:
+        achieved = ffn_flops / (ffn_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4)}
+    roof.update({"traffic": ffn_traffic(args.config), "kernel": "moe_grouped_ffn (ffn_tc_kernel "
+                 "MM1+SwiGLU and MM2 launches)", "peak_source": pk["source"],
+                 "algorithmic_bytes": int(ffn_bytes), "algorithmic_flops": int(ffn_flops),
+                 "touched_slots": touched, "ms_per_launch_pair": round(ffn_ms, 4)})
+
+    # ---- e2e: same calls, inputs from pinned host memory, outputs back to host
+    e2e = None
+    if not args.no_e2e:
+        hx = [t.cpu().pin_memory() for t in x_loc]
+        hl = [t.cpu().pin_memory() for t in lg_loc]
+        ho = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out]
+        dx = [torch.empty_like(t) for t in x_loc]
+        dl = [torch.empty_like(t) for t in lg_loc]
+        for _ in range(3):
+            for a, h in zip(dx, hx):
+                a.copy_(h, non_blocking=True)
+            for a, h in zip(dl, hl):
+                a.copy_(h, non_blocking=True)
+            layer.forward(dx, dl, out, counts=spec.counts)
+            for h, a in zip(ho, out):
+                h.copy_(a, non_blocking=True)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.e2e_steps):
+            for a, h in zip(dx, hx):
+                a.copy_(h, non_blocking=True)
+            for a, h in zip(dl, hl):
+                a.copy_(h, non_blocking=True)
+            layer.forward(dx, dl, out, counts=spec.counts)
+            for h, a in zip(ho, out):
+                h.copy_(a, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        h2d = sum(t.numel() * t.element_size() for t in hx + hl) + 4 * (2 * spec.R + 1)
+        d2h = sum(t.numel() * t.element_size() for t in ho)
+        e2e = {"ms_total": e2e_ms, "steps": args.e2e_steps, "h2d": h2d, "d2h": d2h}
+    if int(layer.status.item()) != 0:
+        raise RuntimeError(f"device status {int(layer.status.item()):#x}")
+    return dict(spec=spec, ms_total=ms_total, clocks=clocks, stage_ms=stage_ms, roof=roof,
+                e2e=e2e, rows=rows, touched=touched,
+                inputs=(x_loc, lg_loc, wgu, wd, l2p_np, nrep_np))
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+def oracle_sample_step(spec, n_tokens, x_loc, lg_loc, wgu, wd, l2p, nrep):
+    """One oracle pass over the first n_tokens tokens of the workload (replica
+    order, MAX/SUM/static layout of the truncated counts).  Returns (seconds of
+    oracle compute, cpu seconds)."""
+    import oracle
+    counts, left = [], n_tokens
+    for c in spec.counts:
+        counts.append(min(c, left))
+        left -= counts[-1]
+
+    def bits(t):
+        return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    to32 = (lambda t: oracle.bf16_bits_to_f32(bits(t))) if spec.dtype == "bf16" else (
+        lambda t: t.detach().cpu().numpy())
+    xs = [to32(x[:c]) for x, c in zip(x_loc, counts)]
+    lgs = [lg[:c].detach().cpu().numpy() for lg, c in zip(lg_loc, counts)]
+    w0, c0 = time.perf_counter(), time.process_time()
+    offs, rows = oracle.dp_layout(counts, spec.mode, spec.static_bound, spec.tokens_per_req)
+    valid = oracle.valid_rows(counts, offs, rows)
+    xg = oracle.dp_gather(xs, counts, offs, rows)
+    lg = oracle.dp_gather(lgs, counts, offs, rows)
+    ids, w = oracle.route_topk(lg, spec.k, spec.renormalize, valid)
+    cnt, o, perm, inv = oracle.dispatch(ids, spec.E, spec.slots, l2p, nrep, spec.align)
+    xsrt = oracle.permute_rows(xg, perm[: o[-1]])
+    wall = time.perf_counter() - w0
+    cpu = time.process_time() - c0
+    ys = np.zeros(xsrt.shape, np.float64)
+    for s in range(spec.slots):
+        a, b_ = int(o[s]), int(o[s + 1])
+        if b_ == a:
+            continue
+        wg_s, wd_s = to32(wgu[s]), to32(wd[s])        # input conversion, not timed
+        w0, c0 = time.perf_counter(), time.process_time()
+        ys[a:b_] = oracle.expert_ffn(xsrt[a:b_], wg_s, wd_s)
+        wall += time.perf_counter() - w0
+        cpu += time.process_time() - c0
+    w0, c0 = time.perf_counter(), time.process_time()
+    yg = oracle.combine(ys, inv, w)
+    oracle.dp_scatter(yg, counts, offs)
+    wall += time.perf_counter() - w0
+    cpu += time.process_time() - c0
+    return wall, cpu
+
+
+def oracle_inputs(spec):
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    l2p, nrep, p2l = synth.make_map(spec)
+    x_loc = synth.hidden_states(spec, dev)
+    lg_loc = synth.router_logits(spec, dev)
+    wgu, wd = synth.expert_weights(spec, p2l, dev)
+    return x_loc, lg_loc, wgu, wd, l2p, nrep
+
+
+def cpu_baseline(spec, budget_s=20.0, inputs=None):
+    import oracle
+    oracle.build()
+    x_loc, lg_loc, wgu, wd, l2p, nrep = inputs or oracle_inputs(spec)
+    wall1, _ = oracle_sample_step(spec, 1, x_loc, lg_loc, wgu, wd, l2p, nrep)
+    n = int(max(1, min(spec.T, budget_s / max(wall1, 1e-3))))
+    wall, cpu = oracle_sample_step(spec, n, x_loc, lg_loc, wgu, wd, l2p, nrep)
+    return {"value": round(n / wall, 3), "unit": UNIT, "cores": round(cpu / wall, 2),
+            "kind": "oracle",
+            "sample": f"first {n} of the {spec.T} tokens of {spec.name}, whole layer (gather, "
+                      f"top-{spec.k}, dispatch, fp64 SwiGLU FFN, combine, scatter), "
+                      f"{wall:.1f} s wall; cores = CPU time / wall time"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    spec = make_spec(args.config, args.seed)
+    import oracle
+    oracle.build()
+    inputs = oracle_inputs(spec)
+    wall1, _ = oracle_sample_step(spec, 1, *inputs)
+    budget = 120.0
+    n = int(max(1, min(spec.T, budget / (args.steps + args.warmup) / max(wall1, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample_step(spec, n, *inputs)
+    walls, cpus = [], []
+    for _ in range(args.steps):
+        w, c = oracle_sample_step(spec, n, *inputs)
+        walls.append(w)
+        cpus.append(c)
+    tot = sum(walls)
+    value = n * args.steps / tot
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * tot / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": dict(synth.describe(spec), sample_tokens_per_step=n),
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT,
+                             "cores": round(sum(cpus) / tot, 2), "kind": "oracle",
+                             "sample": f"first {n} tokens of {spec.name} per step"},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main
+def aggregate(ms_total: float, tokens: float, e2e_ms: float, world: int, device):
+    """Whole-job figures: the slowest rank's times and the tokens of all ranks."""
+    t = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=device)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(n, op=torch.distributed.ReduceOp.SUM)
+    return {"ms_max": float(t[0].item()), "e2e_ms_max": float(t[1].item()),
+            "tokens": float(n.item())}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        args.warmup = 3
+    if world > 1:
+        backend = "nccl" if args.impl == "native" else "gloo"
+        if args.impl == "native":
+            torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+            return
+        r = run_native(args, rank, world, local_rank)
+        spec = r["spec"]
+        agg = aggregate(r["ms_total"], spec.T * args.steps,
+                        r["e2e"]["ms_total"] if r["e2e"] else 0.0, world,
+                        torch.device("cuda", local_rank))
+        if rank != 0:
+            return
+        ms_total = agg["ms_max"]
+        value = agg["tokens"] / (ms_total / 1e3)
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
+            "config": dict(synth.describe(spec), global_rows=r["rows"], l2=L2_NOTE,
+                           parallelism=f"{world} independent replica(s), one per GPU",
+                           stage_ms={k: round(v, 4) for k, v in r["stage_ms"].items()}),
+            "roofline": r["roof"],
+            "clocks": r["clocks"],
+            "gpu_launches": LAUNCHES_PER_STEP * args.steps + (args.steps if spec.align > 1 else 0),
+        }
+        if r["e2e"]:
+            e = r["e2e"]
+            e2e_val = float(spec.T * e["steps"] * world) / (agg["e2e_ms_max"] / 1e3)
+            line["e2e"] = {"value": round(e2e_val, 1), "unit": UNIT,
+                           "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                           "ms_per_step": round(agg["e2e_ms_max"] / e["steps"], 4)}
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(spec, inputs=r["inputs"])
+        print(json.dumps(line), flush=True)
+    finally:
+        if world > 1 and torch.distributed.is_initialized():
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
