@@ -50,7 +50,10 @@ _SIGS = {
                              _P]),
     "moe_combine": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I64, _P, _P, _P]),
     "moe_dp_scatter": (_I, [_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P]),
+    "moe_dispatch_noalloc": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _I, _I, _I64, _P,
+                                  _P, _P, _P, _P, _P, _P]),
 }
+MOE_NOALLOC_SCRATCH_BYTES = 256 * 1024
 
 
 class MoeError(RuntimeError):
@@ -185,6 +188,21 @@ def moe_dispatch(x: Optional[torch.Tensor], ids: torch.Tensor, E: int, P: int, c
         _ptr(x), _ptr(ids), rows, k, H, dt, E, P, _ptr(l2p), _ptr(nrep), X, align,
         perm.numel(), _ptr(counts_P), _ptr(offsets_P), _ptr(perm), _ptr(inv), _ptr(sorted_out),
         _ptr(ws), ws.numel() * ws.element_size(), _ptr(d_status), _stream(stream)))
+
+
+def moe_dispatch_noalloc(x: Optional[torch.Tensor], ids: torch.Tensor, E: int, P: int,
+                         counts_P, offsets_P, perm, inv, sorted_out: Optional[torch.Tensor],
+                         l2p=None, nrep=None, align: int = 1, d_status=None, stream=None):
+    """moe_dispatch without a workspace argument: the library's fixed device
+    scratch holds the histograms (for callers that cannot allocate)."""
+    rows, k = ids.shape
+    H = x.shape[1] if x is not None else 0
+    dt = dtype_code(x.dtype) if x is not None else MOE_BF16
+    X = l2p.shape[1] if l2p is not None else 0
+    _check("moe_dispatch_noalloc", lib().moe_dispatch_noalloc(
+        _ptr(x), _ptr(ids), rows, k, H, dt, E, P, _ptr(l2p), _ptr(nrep), X, align,
+        perm.numel(), _ptr(counts_P), _ptr(offsets_P), _ptr(perm), _ptr(inv), _ptr(sorted_out),
+        _ptr(d_status), _stream(stream)))
 
 
 def moe_grouped_ffn(xs: torch.Tensor, offsets_P: torch.Tensor, w_gate_up: torch.Tensor,

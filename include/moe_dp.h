@@ -234,6 +234,33 @@ moe_status moe_dp_scatter(const void* d_global, const int32_t* d_counts, const i
                           int R, int64_t rows, int H, int dtype, void* const* local,
                           uint32_t* d_status, void* stream);
 
+/* Same as moe_dispatch, but allocates nothing and takes no workspace: the
+ * per-chunk histograms live in a fixed device array inside the library.
+ * The pages have no counterpart; this entry point exists for callers that
+ * cannot allocate device memory where they dispatch (a plugin whose host
+ * framework owns all device allocations, or a decode loop that must not call
+ * cudaMalloc/cudaFree because they can synchronise the device).
+ *   Arguments and outputs: as moe_dispatch, without d_ws / ws_bytes.
+ *   Limit: moe_dispatch_ws_bytes(rows, k, E) <= MOE_NOALLOC_SCRATCH_BYTES
+ *          (65536 chunk-histogram entries, e.g. 262144 routed pairs at E = 256);
+ *          larger problems return MOE_ERR_CAPACITY before anything runs.
+ *   Set-up: the first call on each device looks up the array's device address
+ *          (cudaGetSymbolAddress) with that device current; make that first
+ *          call before any stream capture.
+ *   Sharing: every call on a device uses the same array, which keeps the last
+ *          call's contents (each call overwrites what it reads, so nothing
+ *          has to be cleared); calls that overlap on the GPU (different
+ *          streams, or different host threads) race on it and must be
+ *          serialised by the caller.
+ *   The array occupies MOE_NOALLOC_SCRATCH_BYTES on every GPU that loads the
+ *   library until the process exits. */
+#define MOE_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+moe_status moe_dispatch_noalloc(const void* d_global, const int32_t* d_ids, int64_t rows, int k,
+                                int H, int dtype, int E, int P, const int32_t* d_l2p,
+                                const int32_t* d_nrep, int X, int align, int64_t cap,
+                                int32_t* d_counts_P, int32_t* d_offsets_P, int32_t* d_perm,
+                                int32_t* d_inv, void* d_sorted, uint32_t* d_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
