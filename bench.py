@@ -64,12 +64,20 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--experts", type=int, default=None,
+                    help="shrink the layer to this many experts at the same rows per expert "
+                         "(small cases for profiling)")
     return ap.parse_args()
 
 
-def make_spec(name: str, seed: int):
+def make_spec(name: str, seed: int, experts=None):
+    if name == "prefill" and experts:
+        return synth.spec_prefill(T=8192 * experts // 256, E=experts)
     if name == "decode":
-        return synth.spec_decode(seed=seed)
+        spec = synth.spec_decode(seed=seed)
+        if experts:
+            spec.E = experts
+        return spec
     if name == "prefill":
         return synth.spec_prefill()
     if name == "pad_sweep":
@@ -183,7 +191,7 @@ def run_native(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    spec = make_spec(args.config, args.seed)
+    spec = make_spec(args.config, args.seed, args.experts)
     l2p_np, nrep_np, p2l = synth.make_map(spec)
     x_loc = synth.hidden_states(spec, dev)
     lg_loc = synth.router_logits(spec, dev)
@@ -364,7 +372,7 @@ def cpu_baseline(spec, budget_s=20.0, inputs=None):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    spec = make_spec(args.config, args.seed)
+    spec = make_spec(args.config, args.seed, args.experts)
     import oracle
     oracle.build()
     inputs = oracle_inputs(spec)

@@ -7,25 +7,40 @@
 // PrepareAndFinalize 块结构": MM1, activation, MM2.
 //
 // Two launches of one persistent, warp-specialised kernel:
-//   MM1 + SwiGLU:  acc[128 x 256] = xs_tile . [Wg rows n..n+127 ; Wu rows n..n+127]^T
+//   MM1 + SwiGLU:  acc[M x 256] = xs_tile . [Wg rows n..n+127 ; Wu rows n..n+127]^T
 //                  h[:, n..n+127] = bf16( silu(acc[:, 0:128]) * acc[:, 128:256] )
-//   MM2:           acc[128 x 256] = h_tile . Wd[rows n..n+255]^T
+//   MM2:           acc[M x 256] = h_tile . Wd[rows n..n+255]^T
 //                  ys[:, n..n+255] = bf16(acc)
-// Work tiles are (slot, n-tile, m-tile) with the m-tiles of one slot and
-// n-tile adjacent, so CTAs running at the same time share the weight tile
-// through L2; tile counts come from the device-side slot offsets, so the host
-// never synchronises after dispatch.  A tile's rows start at the slot's
-// first row (no alignment needed); rows past the slot's end are computed
-// from whatever follows and never stored.
+// Work units are (slot, n-tile, m-group) with the m-groups of one slot and
+// n-tile adjacent, so units running at the same time share the weight tile
+// through L2; unit counts come from the device-side slot offsets, so the host
+// never synchronises after dispatch.  A unit's rows start at the slot's first
+// row (no alignment needed); rows past the slot's end are computed from
+// whatever follows and never stored.
+//
+// CL = 2 (chosen when the sorted buffer holds >= 192 rows per slot on
+// average): a cluster of two CTAs on two SMs runs one M = 256 MMA
+// (tcgen05.mma.cta_group::2).  Each CTA holds its own 128 rows of A and one
+// 128-row half of the weight tile B in shared memory; the MMA reads both
+// CTAs' halves.  Per SM and 64-deep k-block that is 32 KB written by TMA and
+// 32 KB read by the tensor core, against 48 + 48 KB for one 128 x 256 tile per
+// SM (CL = 1), whose shared-memory traffic caps the tensor pipe near two
+// thirds of its rate.  With few rows per slot (decode) the weight stream is
+// the whole cost and the single-SM kernel (CL = 1, 4 stages of 48 KB) keeps
+// more weight bytes in flight per SM, so the launcher picks CL by rows per slot.
 //
 // Roles (192 threads, one CTA per SM):
-//   warp 0    TMA producer: A box 64x128 and two B boxes 64x128 per stage,
-//             128-byte swizzle, 4-stage mbarrier ring (48 KB per stage)
-//   warp 1    allocates 512 TMEM columns (two 128x256 fp32 accumulators);
-//             lane 0 issues tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32)
-//             and tcgen05.commit to release stages and publish accumulators
-//   warps 2-5 epilogue: tcgen05.ld 32 columns at a time from the warp's TMEM
-//             lane quarter, activation, bf16 pack, 64-byte row stores
+//   warp 0    TMA producer (both CTAs): own A box 64x128 and own B box 64x128
+//             per stage, 128-byte swizzle; completion is signalled on the
+//             leader CTA's "full" barrier; 6-stage ring (32 KB per stage)
+//   warp 1    TMEM allocation (512 columns: two 128x256 fp32 accumulators per
+//             CTA); in the leader CTA lane 0 issues the MMAs (M=256, N=256,
+//             K=16, bf16 -> fp32) and tcgen05.commit, multicast to both CTAs
+//             to release stages and publish accumulators
+//   warps 2-5 epilogue (both CTAs): tcgen05.ld 32 columns at a time from the
+//             warp's TMEM lane quarter, activation, bf16 pack, 64-byte row
+//             stores; one arrival per warp on the leader's "accumulator free"
+//             barrier
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets
 // MOE_DEV_TIMEOUT, the other roles stop at their next wait, TMEM is freed and
 // the kernel returns.
@@ -40,37 +55,49 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
-constexpr int STAGES = 4;
+// The pair kernel (CL = 2) needs a full 256-row group per unit to pay off;
+// below this many rows per slot on average the single-SM kernel (CL = 1)
+// streams the weights faster (decode-sized batches).
+constexpr int64_t kPairRowsPerSlot = 192;
+
+constexpr int BM = 128;  // rows per CTA
+constexpr int BN = 256;  // accumulator columns
+constexpr int BK = 64;   // 64 bf16 = 128 bytes = one swizzle row
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_HALF_BYTES = 128 * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int B_BOX_BYTES = 128 * BK * 2;  // one 64 x 128 TMA box
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
-// instruction descriptor, kind::f16: D f32, A bf16, B bf16, both K-major,
-// N = 256, M = 128
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                           ((uint32_t)(BM >> 4) << 24);
+template <int CL>
+struct Cfg {
+  static constexpr int B_BYTES = (BN / CL) * BK * 2;  // this CTA's share of the B tile
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = CL == 2 ? 6 : 4;
+  static constexpr int M = BM * CL;
+  // instruction descriptor, kind::f16: D f32, A bf16, B bf16, both K-major
+  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
+                                    ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+};
 
+constexpr int MAX_STAGES = 6;
 struct SmemLayout {
   // stage buffers come first (1024-byte aligned base)
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint32_t tmem_base;
   int32_t abort_flag;
-  int32_t total_tiles;
+  int32_t total_units;
   int32_t warp_sums[THREADS / 32];
-  int32_t pref[MOE_MAX_SLOTS + 1];  // tile prefix over the slot range
-  int32_t mt[MOE_MAX_SLOTS];        // m-tiles per slot
+  int32_t pref[MOE_MAX_SLOTS + 1];  // unit prefix over the slot range
+  int32_t mt[MOE_MAX_SLOTS];        // 128-row m-tiles per slot
 };
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemLayout);
+template <int CL>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)Cfg<CL>::STAGES * Cfg<CL>::STAGE_BYTES + sizeof(SmemLayout);
+}
 
 struct TcParams {
   const int32_t* offsets;
@@ -91,6 +118,22 @@ struct TcParams {
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// All threads of every CTA of the cluster; release/acquire at cluster scope.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -100,6 +143,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Arrive on an mbarrier given by its shared::cluster address (own or peer CTA).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar)
+               : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -135,13 +183,24 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
   return __all_sync(0xffffffffu, ok);
 }
+// TMA 2-D tile load into this CTA's shared memory, completion on an mbarrier of
+// this CTA (CL == 1) or of the leader CTA of the pair (CL == 2, cluster address).
+template <int CL>
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t c0,
                                             int32_t c1, uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
-      : "memory");
+  if constexpr (CL == 1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+        : "memory");
+  } else {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+        : "memory");
+  }
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
@@ -159,19 +218,63 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
+template <int CL>
+__device__ __forceinline__ void tmem_alloc(uint32_t dst) {
+  if constexpr (CL == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
 }
+template <int CL>
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr) {
+  if constexpr (CL == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(TMEM_COLS)
+                 : "memory");
+}
+// Arrive on `bar` (same offset in every CTA of the pair) once all MMAs issued
+// so far by this thread have completed.
+template <int CL>
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  if constexpr (CL == 1)
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"((uint16_t)3)
+        : "memory");
+}
+template <int CL>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
+                                       uint32_t accumulate) {
+  if constexpr (CL == 1)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(Cfg<1>::IDESC), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(Cfg<2>::IDESC), "r"(accumulate)
+        : "memory");
 }
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
 // groups 1024 bytes apart (SBO), descriptor version 1.
@@ -200,39 +303,45 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Tile t -> (slot, m-tile, n-tile) through the prefix over the slot range.
-struct Tile {
-  int slot, m, n;
+// Work unit u -> (slot, m-group, n-tile) through the prefix over the slot range.
+// An m-group is CL consecutive 128-row m-tiles (one per CTA of the cluster).
+struct Unit {
+  int slot, mg, n;
 };
-__device__ __forceinline__ Tile decode_tile(const SmemLayout& L, int nslots, int t) {
+__device__ __forceinline__ Unit decode_unit(const SmemLayout& L, int nslots, int u, int CL) {
   int lo = 0, hi = nslots - 1;
-  while (lo < hi) {  // largest s with pref[s] <= t
+  while (lo < hi) {  // largest s with pref[s] <= u
     int mid = (lo + hi + 1) >> 1;
-    if (L.pref[mid] <= t)
+    if (L.pref[mid] <= u)
       lo = mid;
     else
       hi = mid - 1;
   }
-  int local = t - L.pref[lo];
-  int mt = L.mt[lo];
-  Tile r;
+  const int local = u - L.pref[lo];
+  const int groups = (L.mt[lo] + CL - 1) / CL;
+  Unit r;
   r.slot = lo;
-  r.m = local % mt;
-  r.n = local / mt;
+  r.mg = local % groups;
+  r.n = local / groups;
   return r;
 }
 
-template <bool SWIGLU>
+template <bool SWIGLU, int CL>
 __global__ void __launch_bounds__(THREADS, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const TcParams p) {
+  using C = Cfg<CL>;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stage_base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  SmemLayout& L = *reinterpret_cast<SmemLayout*>(stage_base + (size_t)STAGES * STAGE_BYTES);
+  SmemLayout& L = *reinterpret_cast<SmemLayout*>(stage_base + (size_t)STAGES * C::STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
+  const bool leader = crank == 0;
+  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
 
-  // ---- tile table: m-tiles per slot, exclusive prefix of tiles
+  // ---- unit table: m-tiles per slot, exclusive prefix of units
   {
     const int per = (p.nslots + THREADS - 1) / THREADS;
     const int s0 = threadIdx.x * per;
@@ -243,7 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int64_t rows = (int64_t)p.offsets[p.slot_lo + s + 1] - p.offsets[p.slot_lo + s];
         int32_t mt = rows > 0 ? (int32_t)((rows + BM - 1) / BM) : 0;
         L.mt[s] = mt;
-        local += mt * p.n_tiles;
+        local += (mt + CL - 1) / CL * p.n_tiles;
       }
     }
     int32_t x = local;
@@ -256,22 +365,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
       L.abort_flag = 0;
       for (int i = 0; i < STAGES; ++i) {
-        mbar_init(smem_u32(&L.full[i]), 1);
-        mbar_init(smem_u32(&L.empty[i]), 1);
+        mbar_init(smem_u32(&L.full[i]), 1);   // leader: its producer's expect_tx
+        mbar_init(smem_u32(&L.empty[i]), 1);  // the leader's MMA commit
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(smem_u32(&L.tmem_full[i]), 1);
-        mbar_init(smem_u32(&L.tmem_empty[i]), 128);
+        mbar_init(smem_u32(&L.tmem_empty[i]), 4 * CL);  // one per epilogue warp of the pair
       }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {  // whole warp allocates the accumulators
-      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                       smem_u32(&L.tmem_base)),
-                   "r"(TMEM_COLS)
-                   : "memory");
-      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    if (warp == 1) tmem_alloc<CL>(smem_u32(&L.tmem_base));  // whole warp, both CTAs
     __syncthreads();
     int32_t before = 0;
     for (int w = 0; w < warp; ++w) before += L.warp_sums[w];
@@ -280,20 +383,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       int s = s0 + i;
       if (s < p.nslots) {
         L.pref[s] = run;
-        run += L.mt[s] * p.n_tiles;
+        run += (L.mt[s] + CL - 1) / CL * p.n_tiles;
       }
     }
     if (threadIdx.x == THREADS - 1) {
       int32_t tot = 0;
       for (int w = 0; w < THREADS / 32; ++w) tot += L.warp_sums[w];
       L.pref[p.nslots] = tot;
-      L.total_tiles = tot;
+      L.total_units = tot;
     }
     tc_fence_before();
-    __syncthreads();
+    if (CL > 1)
+      cluster_sync();  // the leader's barriers exist before the peer signals them
+    else
+      __syncthreads();
     tc_fence_after();
   }
-  const int total = L.total_tiles;
+  const int total = L.total_units;
   const uint32_t tmem_base = L.tmem_base;
   volatile int32_t* abort_flag = &L.abort_flag;
 
@@ -306,11 +412,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
     }
     uint32_t it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile(L, p.nslots, t);
-      const int slot = p.slot_lo + tl.slot;
-      const int32_t row0 = p.offsets[slot] + tl.m * BM;
-      const int32_t brow1 = slot * p.b_rows_per_slot + tl.n * p.b_tile_step;
+    for (int u = cid; u < total; u += ncl) {
+      const Unit un = decode_unit(L, p.nslots, u, CL);
+      const int slot = p.slot_lo + un.slot;
+      const int32_t row0 = p.offsets[slot] + (un.mg * CL + (int)crank) * BM;
+      const int32_t brow1 = slot * p.b_rows_per_slot + un.n * p.b_tile_step;
       const int32_t brow2 = brow1 + p.b_second;
       bool ok = true;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
@@ -320,64 +426,71 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         if (lane == 0) {
-          const uint32_t full = smem_u32(&L.full[st]);
-          const uint32_t sa = smem_u32(stage_base + (size_t)st * STAGE_BYTES);
+          const uint32_t full_local = smem_u32(&L.full[st]);
+          const uint32_t full = CL > 1 ? map_to_rank(full_local, 0) : full_local;
+          const uint32_t sa = smem_u32(stage_base + (size_t)st * C::STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
-          mbar_arrive_expect_tx(full, STAGE_BYTES);
-          tma_load_2d(sa, &tmA, kb * BK, row0, full, pol_act);
-          tma_load_2d(sb, &tmB, kb * BK, brow1, full, pol_w);
-          tma_load_2d(sb + B_HALF_BYTES, &tmB, kb * BK, brow2, full, pol_w);
+          if (leader) mbar_arrive_expect_tx(full_local, CL * C::STAGE_BYTES);
+          tma_load_2d<CL>(sa, &tmA, kb * BK, row0, full, pol_act);
+          if (CL == 1) {
+            tma_load_2d<CL>(sb, &tmB, kb * BK, brow1, full, pol_w);
+            tma_load_2d<CL>(sb + B_BOX_BYTES, &tmB, kb * BK, brow2, full, pol_w);
+          } else {
+            tma_load_2d<CL>(sb, &tmB, kb * BK, crank ? brow2 : brow1, full, pol_w);
+          }
         }
         __syncwarp();
       }
       if (!ok) break;
     }
-    // drain: every load issued must land before the CTA can exit
+    // drain: every "stage free" arrival bound for this CTA (the leader's MMA
+    // commits, which follow the loads they consumed) has happened before exit
     for (uint32_t j = (it >= STAGES ? it - STAGES : 0); j < it; ++j) {
       const uint32_t st = j % STAGES, ph = (j / STAGES) & 1u;
-      volatile int32_t never = 0;
-      if (!wait_bar(smem_u32(&L.full[st]), ph, &never, p.status)) break;
+      if (!wait_bar(smem_u32(&L.empty[st]), ph, abort_flag, p.status)) break;
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    uint32_t it = 0, local_tile = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++local_tile) {
-      const uint32_t acc = local_tile & 1u, acc_ph = (local_tile >> 1) & 1u;
-      if (!wait_bar(smem_u32(&L.tmem_empty[acc]), acc_ph ^ 1u, abort_flag, p.status)) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
-      bool ok = true;
-      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-        const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
-        if (!wait_bar(smem_u32(&L.full[st]), ph, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
+    // ------------------------------------------------------------ MMA issuer (leader CTA)
+    if (leader) {
+      uint32_t it = 0, local_tile = 0;
+      for (int u = cid; u < total; u += ncl, ++local_tile) {
+        const uint32_t acc = local_tile & 1u, acc_ph = (local_tile >> 1) & 1u;
+        if (!wait_bar(smem_u32(&L.tmem_empty[acc]), acc_ph ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t sa = smem_u32(stage_base + (size_t)st * STAGE_BYTES);
-          const uint64_t adesc = sw128_desc(sa);
-          const uint64_t bdesc = sw128_desc(sa + A_BYTES);
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!wait_bar(smem_u32(&L.full[st]), ph, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = smem_u32(stage_base + (size_t)st * C::STAGE_BYTES);
+            const uint64_t adesc = sw128_desc(sa);
+            const uint64_t bdesc = sw128_desc(sa + A_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes per K=16 step inside the swizzle row
-            tc_mma(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, IDESC, (kb | kk) != 0);
-          tc_commit(smem_u32(&L.empty[st]));
+            for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes per K=16 step in the swizzle row
+              tc_mma<CL>(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, (kb | kk) != 0);
+            tc_commit<CL>(smem_u32(&L.empty[st]));
+          }
+          __syncwarp();
         }
+        if (!ok) break;
+        if (lane == 0) tc_commit<CL>(smem_u32(&L.tmem_full[acc]));
         __syncwarp();
       }
-      if (!ok) break;
-      if (lane == 0) tc_commit(smem_u32(&L.tmem_full[acc]));
-      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
     const int row_in_tile = quad * 32 + lane;
     uint32_t local_tile = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++local_tile) {
-      const Tile tl = decode_tile(L, p.nslots, t);
-      const int slot = p.slot_lo + tl.slot;
-      const int64_t row0 = (int64_t)p.offsets[slot] + (int64_t)tl.m * BM;
+    for (int u = cid; u < total; u += ncl, ++local_tile) {
+      const Unit un = decode_unit(L, p.nslots, u, CL);
+      const int slot = p.slot_lo + un.slot;
+      const int64_t row0 = (int64_t)p.offsets[slot] + (int64_t)(un.mg * CL + (int)crank) * BM;
       const int64_t row_end = p.offsets[slot + 1];
       const uint32_t acc = local_tile & 1u, acc_ph = (local_tile >> 1) & 1u;
       if (!wait_bar(smem_u32(&L.tmem_full[acc]), acc_ph, abort_flag, p.status)) break;
@@ -385,19 +498,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t row = row0 + row_in_tile;
       const bool valid = row < row_end && row < p.cap;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
-      __nv_bfloat16* orow = p.out + row * p.out_ld + (int64_t)tl.n * p.out_tile_cols;
+      __nv_bfloat16* orow = p.out + row * p.out_ld + (int64_t)un.n * p.out_tile_cols;
       if (SWIGLU) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
-          uint32_t g[32], u[32];
+          uint32_t g[32], v[32];
           tmem_ld32(taddr + c, g);
-          tmem_ld32(taddr + 128 + c, u);
+          tmem_ld32(taddr + 128 + c, v);
           tmem_wait_ld();
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             float g0 = __uint_as_float(g[2 * e]), g1 = __uint_as_float(g[2 * e + 1]);
-            float u0 = __uint_as_float(u[2 * e]), u1 = __uint_as_float(u[2 * e + 1]);
+            float u0 = __uint_as_float(v[2 * e]), u1 = __uint_as_float(v[2 * e + 1]);
             float h0 = g0 / (1.0f + expf(-g0)) * u0;
             float h1 = g1 / (1.0f + expf(-g1)) * u1;
             pk[e] = pack_bf16x2(h0, h1);
@@ -405,8 +518,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
           }
         }
       } else {
@@ -422,24 +535,32 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&L.tmem_empty[acc]));
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t bar = smem_u32(&L.tmem_empty[acc]);
+        if (CL == 1)
+          mbar_arrive(bar);
+        else
+          mbar_arrive_cluster(map_to_rank(bar, 0));  // the leader's barrier
+      }
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  // No CTA may leave while its peer can still signal its barriers or read its
+  // shared memory through the pair MMA.
+  if (CL > 1)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
-  if (warp == 1) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(TMEM_COLS)
-                 : "memory");
-  }
+  if (warp == 1) tmem_dealloc<CL>(tmem_base);
 }
 
 // ------------------------------------------------------------- host side
@@ -471,37 +592,68 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) 
   return r == CUDA_SUCCESS;
 }
 
-bool set_smem_attr() {
+template <int CL>
+cudaLaunchConfig_t launch_cfg(int clusters, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL * clusters);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem_bytes<CL>();
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Per device and cluster size: raise the dynamic shared-memory limit and find
+// how many clusters fit at once (the persistent grid must be fully resident).
+template <int CL>
+bool device_setup(int* max_clusters) {
   static std::mutex mu;
-  static bool done[64] = {false};
+  static int clusters[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   std::lock_guard<std::mutex> lock(mu);
-  if (!done[dev]) {
-    if (cudaFuncSetAttribute(ffn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(ffn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess)
+  if (clusters[dev] == 0) {
+    const int bytes = (int)smem_bytes<CL>();
+    if (cudaFuncSetAttribute(ffn_tc_kernel<true, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(ffn_tc_kernel<false, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) != cudaSuccess)
       return false;
-    done[dev] = true;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_cfg<CL>(num_sms() / CL, nullptr, attr);
+    int c1 = 0, c2 = 0;
+    if (cudaOccupancyMaxActiveClusters(&c1, ffn_tc_kernel<true, CL>, &cfg) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&c2, ffn_tc_kernel<false, CL>, &cfg) != cudaSuccess)
+      return false;
+    const int n = c1 < c2 ? c1 : c2;
+    if (n < 1) return false;
+    clusters[dev] = n;
   }
+  *max_clusters = clusters[dev];
   return true;
 }
 
-}  // namespace
+template <bool SWIGLU, int CL>
+cudaError_t launch(const CUtensorMap& mA, const CUtensorMap& mB, const TcParams& p, int clusters,
+                   cudaStream_t s) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_cfg<CL>(clusters, s, attr);
+  return cudaLaunchKernelEx(&cfg, ffn_tc_kernel<SWIGLU, CL>, mA, mB, p);
+}
 
-moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
+template <int CL>
+moe_status run_ffn(const FfnArgs& a, const CUtensorMap& mA1, const CUtensorMap& mB1,
+                   const CUtensorMap& mA2, const CUtensorMap& mB2, cudaStream_t s) {
   const int nslots = a.slot_hi - a.slot_lo;
-  if (nslots <= 0 || a.cap <= 0) return MOE_OK;
-  if (!set_smem_attr()) return MOE_ERR_CUDA;
-  CUtensorMap mA1, mB1, mA2, mB2;
-  if (!make_map(&mA1, a.xs, (uint64_t)a.H, (uint64_t)a.cap) ||
-      !make_map(&mB1, a.wgu, (uint64_t)a.H, (uint64_t)a.P * 2 * a.I) ||
-      !make_map(&mA2, a.h, (uint64_t)a.I, (uint64_t)a.cap) ||
-      !make_map(&mB2, a.wd, (uint64_t)a.I, (uint64_t)a.P * a.H))
-    return MOE_ERR_CUDA;
-  const int64_t m_bound = (a.cap + BM - 1) / BM + nslots;
-  const int sms = num_sms();
+  int max_clusters = 0;
+  if (!device_setup<CL>(&max_clusters)) return MOE_ERR_CUDA;
+  // upper bound of m-groups over the slot range (device-side counts unknown here)
+  const int64_t m_bound = ((a.cap + BM - 1) / BM + nslots) / CL + nslots;
 
   TcParams p1;
   p1.offsets = a.offsets;
@@ -517,10 +669,10 @@ moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   p1.out_tile_cols = 128;
   p1.out = static_cast<__nv_bfloat16*>(a.h);
   p1.status = a.status;
-  int64_t bound1 = m_bound * p1.n_tiles;
-  int grid1 = (int)(bound1 < sms ? bound1 : sms);
-  ffn_tc_kernel<true><<<grid1, THREADS, SMEM_BYTES, s>>>(mA1, mB1, p1);
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  const int64_t bound1 = m_bound * p1.n_tiles;
+  if (launch<true, CL>(mA1, mB1, p1, (int)(bound1 < max_clusters ? bound1 : max_clusters), s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
 
   TcParams p2 = p1;
   p2.num_kb = a.I / BK;
@@ -531,11 +683,28 @@ moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   p2.out_ld = a.H;
   p2.out_tile_cols = BN;
   p2.out = static_cast<__nv_bfloat16*>(a.ys);
-  int64_t bound2 = m_bound * p2.n_tiles;
-  int grid2 = (int)(bound2 < sms ? bound2 : sms);
-  ffn_tc_kernel<false><<<grid2, THREADS, SMEM_BYTES, s>>>(mA2, mB2, p2);
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  const int64_t bound2 = m_bound * p2.n_tiles;
+  if (launch<false, CL>(mA2, mB2, p2, (int)(bound2 < max_clusters ? bound2 : max_clusters), s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+}  // namespace
+
+moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
+  const int nslots = a.slot_hi - a.slot_lo;
+  if (nslots <= 0 || a.cap <= 0) return MOE_OK;
+  CUtensorMap mA1, mB1, mA2, mB2;
+  if (!make_map(&mA1, a.xs, (uint64_t)a.H, (uint64_t)a.cap) ||
+      !make_map(&mB1, a.wgu, (uint64_t)a.H, (uint64_t)a.P * 2 * a.I) ||
+      !make_map(&mA2, a.h, (uint64_t)a.I, (uint64_t)a.cap) ||
+      !make_map(&mB2, a.wd, (uint64_t)a.I, (uint64_t)a.P * a.H))
+    return MOE_ERR_CUDA;
+  // rows per slot the sorted buffer can hold on average, over the whole layer
+  const int64_t rows_per_slot = a.cap / (a.P > 0 ? a.P : 1);
+  if (rows_per_slot >= kPairRowsPerSlot) return run_ffn<2>(a, mA1, mB1, mA2, mB2, s);
+  return run_ffn<1>(a, mA1, mB1, mA2, mB2, s);
 }
 
 }  // namespace moe

@@ -209,6 +209,32 @@ def test_grouped_ffn_bf16_tcgen05(md, orc, counts):
     assert (got[n:] == sentinel).all()                  # rows past the last slot untouched
 
 
+@pytest.mark.parametrize("counts,lo,hi", [([300, 0, 257, 129, 512, 1], 0, 6),
+                                           ([256, 255, 0, 385, 200, 640], 1, 5),
+                                           ([1000, 0, 0, 3], 0, 4)])
+def test_grouped_ffn_bf16_pair_kernel(md, orc, counts, lo, hi):
+    """>= 192 rows per slot on average selects the two-SM (cta_group::2) kernel:
+    ragged groups, odd m-tile counts, empty slots and slot ranges."""
+    H, I = 512, 256
+    offsets, cap, xs, wgu, wd = _ffn_inputs(counts, H, I, torch.bfloat16, seed=len(counts) + lo,
+                                            extra_rows=40)
+    assert cap // len(counts) >= 192
+    sentinel = 1232.0
+    ys = torch.full((cap, H), sentinel, device=DEV, dtype=torch.bfloat16)
+    ws = torch.empty(md.moe_grouped_ffn_ws_bytes(cap, I, torch.bfloat16), dtype=torch.uint8,
+                     device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    md.moe_grouped_ffn(xs, dev_i32(offsets), wgu, wd, ys, ws, lo, hi, d_status=st)
+    assert status_of(st) == 0
+    a, b = int(offsets[lo]), int(offsets[hi])
+    ref = orc.grouped_ffn(as_f32(to_np(xs)), offsets, as_f32(to_np(wgu)), as_f32(to_np(wd)),
+                          lo, hi)
+    got = as_f32(to_np(ys)).astype(np.float64)
+    assert_close(got[a:b], ref[a:b], BF16_ATOL, BF16_RTOL, "pair kernel")
+    assert rel_fro(got[a:b], ref[a:b]) < 8e-3
+    assert (got[:a] == sentinel).all() and (got[b:] == sentinel).all()
+
+
 def test_grouped_ffn_slot_range_and_dsv3_width(md, orc):
     counts = [40, 0, 130, 7, 256, 1]
     H, I = 7168, 2048
