@@ -43,7 +43,9 @@ UNIT = "tokens/s"
 L2_NOTE = "inputs larger than L2: every step streams the touched experts' weights from HBM"
 
 # Launches of this library per step (gather x2, route, dispatch hist/scan/rank/copy,
-# grouped FFN MM1+SwiGLU and MM2, combine, scatter); +1 when align > 1.
+# grouped FFN MM1+SwiGLU and MM2, combine, scatter); +1 when align > 1, +2 when the
+# grouped FFN runs its two-SM pair launches plus single-SM tail launches (>= 192
+# sorted rows per slot).
 LAUNCHES_PER_STEP = 11
 
 # dram__bytes_read.sum + dram__bytes_write.sum of the two grouped-FFN launches of one
@@ -297,6 +299,7 @@ def run_native(args, rank, world, local_rank):
         raise RuntimeError(f"device status {int(layer.status.item()):#x}")
     return dict(spec=spec, ms_total=ms_total, clocks=clocks, stage_ms=stage_ms, roof=roof,
                 e2e=e2e, rows=rows, touched=touched,
+                pair_ffn=layer.cap // max(layer.P, 1) >= 192,
                 inputs=(x_loc, lg_loc, wgu, wd, l2p_np, nrep_np))
 
 
@@ -449,7 +452,8 @@ def main():
                            stage_ms={k: round(v, 4) for k, v in r["stage_ms"].items()}),
             "roofline": r["roof"],
             "clocks": r["clocks"],
-            "gpu_launches": LAUNCHES_PER_STEP * args.steps + (args.steps if spec.align > 1 else 0),
+            "gpu_launches": args.steps * (LAUNCHES_PER_STEP + (1 if spec.align > 1 else 0)
+                                          + (2 if r["pair_ffn"] else 0)),
         }
         if r["e2e"]:
             e = r["e2e"]

@@ -8,17 +8,18 @@
 // are all -1 (pad rows) are zero.  No float atomics: each output row has one
 // owner warp, so the result is deterministic.
 //
-// Design: one warp per output row; the row is walked in chunks of
-// 32 lanes x kUnroll 16-byte vectors; for each chunk the k source rows are
-// read (k * kUnroll independent loads per lane in flight) and accumulated in
-// registers.
+// Design: one warp per (output row, segment of 64 16-byte vectors); the k
+// source rows are read kBatch at a time with every load of a batch in flight
+// and accumulated in registers.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kUnroll = 2;
+constexpr int kUnroll = 2;                // 16-byte vectors per lane per segment
+constexpr int kSegVecs = 32 * kUnroll;    // vectors per warp segment of a row
+constexpr int kBatch = 4;                 // source rows loaded together
 
 __device__ __forceinline__ uint4 ld_nc(const uint4* p) {
   uint4 v;
@@ -29,6 +30,24 @@ __device__ __forceinline__ uint4 ld_nc(const uint4* p) {
 }
 
 template <bool BF16>
+__device__ __forceinline__ void fma_vec(float* acc, const uint4& t, float wj) {
+  const uint32_t q[4] = {t.x, t.y, t.z, t.w};
+  if (BF16) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc[2 * e] = fmaf(wj, bf16lo(q[e]), acc[2 * e]);
+      acc[2 * e + 1] = fmaf(wj, bf16hi(q[e]), acc[2 * e + 1]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] = fmaf(wj, __uint_as_float(q[e]), acc[e]);
+  }
+}
+
+// One warp per (output row, segment of 64 vectors).  Source rows are taken
+// kBatch at a time with all kBatch x kUnroll loads in flight, then added in j
+// order, so the result does not depend on the batching.
+template <bool BF16>
 __global__ void __launch_bounds__(kWarps * 32)
     combine_kernel(const uint4* __restrict__ ys, const int32_t* __restrict__ inv,
                    const float* __restrict__ w, int64_t rows, int k, int vpr, int64_t cap,
@@ -37,68 +56,68 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarps;
-  for (int64_t g = warp0; g < rows; g += nwarps) {
+  const int segs = (vpr + kSegVecs - 1) / kSegVecs;
+  const int64_t items = rows * segs;
+  for (int64_t item = warp0; item < items; item += nwarps) {
+    const int64_t g = item / segs;
+    const int v0 = (int)(item - g * segs) * kSegVecs;
     int32_t my_d = -1;
     float my_w = 0.f;
     if (lane < k) {
       my_d = inv[g * k + lane];
       my_w = w[g * k + lane];
       if (my_d >= cap) {
-        flag(status, MOE_DEV_BAD_COUNTS);
+        if (v0 == 0) flag(status, MOE_DEV_BAD_COUNTS);
         my_d = -1;
       }
     }
+    float acc[kUnroll][EPV];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) acc[u][e] = 0.f;
+    for (int j0 = 0; j0 < k; j0 += kBatch) {
+      uint4 t[kBatch][kUnroll];
+      int32_t d[kBatch];
+      float wj[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int j = j0 + b;
+        d[b] = __shfl_sync(0xffffffffu, my_d, j & 31);
+        wj[b] = __shfl_sync(0xffffffffu, my_w, j & 31);
+        if (j >= k) d[b] = -1;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int v = v0 + u * 32 + lane;
+          t[b][u] = make_uint4(0, 0, 0, 0);
+          if (d[b] >= 0 && v < vpr) t[b][u] = ld_nc(ys + (int64_t)d[b] * vpr + v);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        if (d[b] < 0) continue;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) fma_vec<BF16>(acc[u], t[b][u], wj[b]);
+      }
+    }
     uint4* dst = out + g * vpr;
-    for (int v0 = lane; v0 < vpr; v0 += 32 * kUnroll) {
-      float acc[kUnroll][EPV];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u)
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) acc[u][e] = 0.f;
-      for (int j = 0; j < k; ++j) {
-        const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
-        const float wj = __shfl_sync(0xffffffffu, my_w, j);
-        if (d < 0) continue;
-        const uint4* src = ys + (int64_t)d * vpr;
-        uint4 t[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          int v = v0 + u * 32;
-          if (v < vpr) t[u] = ld_nc(src + v);
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const uint32_t q[4] = {t[u].x, t[u].y, t[u].z, t[u].w};
-          if (BF16) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              acc[u][2 * e] = fmaf(wj, bf16lo(q[e]), acc[u][2 * e]);
-              acc[u][2 * e + 1] = fmaf(wj, bf16hi(q[e]), acc[u][2 * e + 1]);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[u][e] = fmaf(wj, __uint_as_float(q[e]), acc[u][e]);
-          }
-        }
+    for (int u = 0; u < kUnroll; ++u) {
+      const int v = v0 + u * 32 + lane;
+      if (v >= vpr) continue;
+      uint4 r;
+      if (BF16) {
+        r.x = pack_bf16x2(acc[u][0], acc[u][1]);
+        r.y = pack_bf16x2(acc[u][2], acc[u][3]);
+        r.z = pack_bf16x2(acc[u][4], acc[u][5]);
+        r.w = pack_bf16x2(acc[u][6], acc[u][7]);
+      } else {
+        r.x = __float_as_uint(acc[u][0]);
+        r.y = __float_as_uint(acc[u][1]);
+        r.z = __float_as_uint(acc[u][2]);
+        r.w = __float_as_uint(acc[u][3]);
       }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        int v = v0 + u * 32;
-        if (v >= vpr) continue;
-        uint4 r;
-        if (BF16) {
-          r.x = pack_bf16x2(acc[u][0], acc[u][1]);
-          r.y = pack_bf16x2(acc[u][2], acc[u][3]);
-          r.z = pack_bf16x2(acc[u][4], acc[u][5]);
-          r.w = pack_bf16x2(acc[u][6], acc[u][7]);
-        } else {
-          r.x = __float_as_uint(acc[u][0]);
-          r.y = __float_as_uint(acc[u][1]);
-          r.z = __float_as_uint(acc[u][2]);
-          r.w = __float_as_uint(acc[u][3]);
-        }
-        dst[v] = r;
-      }
+      dst[v] = r;
     }
   }
 }
@@ -122,8 +141,9 @@ extern "C" moe_status moe_combine(const void* d_out_sorted, const int32_t* d_inv
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(d_out_sorted) || !aligned16(d_global_out)) return MOE_ERR_INVALID_ARG;
   const int vpr = (int)((int64_t)H * eb / 16);
-  int64_t want = (rows + kWarps - 1) / kWarps;
-  int64_t lim = (int64_t)num_sms() * 16;
+  const int64_t items = rows * ((vpr + kSegVecs - 1) / kSegVecs);
+  int64_t want = (items + kWarps - 1) / kWarps;
+  int64_t lim = (int64_t)num_sms() * 8;
   int grid = (int)(want < lim ? want : lim);
   cudaStream_t s = as_stream(stream);
   if (dtype == MOE_BF16)

@@ -17,11 +17,12 @@
 //   1. hist   one block per chunk of kChunk pairs: per-chunk logical histogram
 //   2. scan   one block: per-expert exclusive scan over chunks, per-slot
 //             counts from the replica rule, aligned exclusive scan -> offsets
-//   3. rank   one warp per chunk, 32 pairs per step in order: __match_any_sync
-//             groups equal ids, popc of the lower lanes gives the in-step
-//             rank, a shared running count carries it across steps
-//   4. copy   one warp per source row: the row is read once and written to
-//             its k destinations with 16-byte vectors
+//   3. rank   one warp per chunk, its ids loaded up front, then 32 pairs per
+//             step in order: __match_any_sync groups equal ids, popc of the
+//             lower lanes gives the in-step rank, a shared running count
+//             carries it across steps
+//   4. copy   one warp per (source row, 2 KB segment): the segment is read
+//             once and written to the row's k destinations, 16-byte vectors
 //   5. pad    (align > 1) zero the alignment rows and mark them perm = -1
 #include "common.cuh"
 
@@ -154,12 +155,20 @@ __global__ void __launch_bounds__(32)
   const int64_t base = (int64_t)blockIdx.x * kChunk;
   const int32_t* cb = chunk_base + (int64_t)blockIdx.x * E;
   const uint32_t lt = (1u << lane) - 1u;
-  for (int step = 0; step < kChunk; step += 32) {
-    int64_t q = base + step + lane;
-    int32_t l = q < pairs ? ids[q] : -1;
-    bool valid = l >= 0 && l < E;
-    uint32_t mask = __match_any_sync(0xffffffffu, valid ? l : -1);
-    int rank = __popc(mask & lt);
+  // the chunk's ids, all loaded up front (one memory round trip, not 32)
+  int32_t idv[kChunk / 32];
+#pragma unroll
+  for (int s = 0; s < kChunk / 32; ++s) {
+    const int64_t q = base + s * 32 + lane;
+    idv[s] = q < pairs ? ids[q] : -1;
+  }
+#pragma unroll
+  for (int s = 0; s < kChunk / 32; ++s) {
+    const int64_t q = base + s * 32 + lane;
+    const int32_t l = idv[s];
+    const bool valid = l >= 0 && l < E;
+    const uint32_t mask = __match_any_sync(0xffffffffu, valid ? l : -1);
+    const int rank = __popc(mask & lt);
     int32_t p = 0;
     if (valid) p = cb[l] + s_run[l] + rank;
     __syncwarp();
@@ -171,7 +180,7 @@ __global__ void __launch_bounds__(32)
       int32_t slot = l, pos = p;
       bool ok = true;
       if (l2p != nullptr) {
-        int32_t nv = nrep[l];
+        const int32_t nv = nrep[l];
         if (nv < 1 || nv > X) {
           ok = false;
         } else {
@@ -181,7 +190,7 @@ __global__ void __launch_bounds__(32)
         }
       }
       if (ok) {
-        int64_t d = (int64_t)offsets_P[slot] + pos;
+        const int64_t d = (int64_t)offsets_P[slot] + pos;
         if (d < cap && d < offsets_P[slot + 1]) {
           dest = (int32_t)d;
           perm[d] = (int32_t)(q / k);
@@ -204,34 +213,39 @@ __device__ __forceinline__ uint4 ld_nc(const uint4* p) {
 
 constexpr int kCopyWarps = 8;
 constexpr int kCopyUnroll = 4;
+constexpr int kSegVecs = 32 * kCopyUnroll;  // vectors per warp segment of a row
 
+// One warp per (source row, segment): the segment is read once (every lane's
+// loads in flight together) and written to the row's k destinations.
 __global__ void __launch_bounds__(kCopyWarps * 32)
     dispatch_copy_kernel(const uint4* __restrict__ xg, const int32_t* __restrict__ inv,
                          int64_t rows, int k, int vpr, int64_t cap, uint4* __restrict__ xs) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t)blockIdx.x * kCopyWarps + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kCopyWarps;
-  for (int64_t g = warp0; g < rows; g += nwarps) {
+  const int segs = (vpr + kSegVecs - 1) / kSegVecs;
+  const int64_t items = rows * segs;
+  for (int64_t w = warp0; w < items; w += nwarps) {
+    const int64_t g = w / segs;
+    const int v0 = (int)(w - g * segs) * kSegVecs;
     int32_t my_d = lane < k ? inv[g * k + lane] : -1;
     if (my_d >= cap) my_d = -1;
     if (__ballot_sync(0xffffffffu, my_d >= 0) == 0) continue;  // pad row
     const uint4* src = xg + g * vpr;
-    for (int v0 = lane; v0 < vpr; v0 += 32 * kCopyUnroll) {
-      uint4 t[kCopyUnroll];
+    uint4 t[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int v = v0 + u * 32 + lane;
+      if (v < vpr) t[u] = ld_nc(src + v);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int32_t d = __shfl_sync(0xffffffffu, my_d, j);
+      if (d < 0) continue;
+      uint4* dst = xs + (int64_t)d * vpr;
 #pragma unroll
       for (int u = 0; u < kCopyUnroll; ++u) {
-        int v = v0 + u * 32;
-        if (v < vpr) t[u] = ld_nc(src + v);
-      }
-      for (int j = 0; j < k; ++j) {
-        int32_t d = __shfl_sync(0xffffffffu, my_d, j);
-        if (d < 0) continue;
-        uint4* dst = xs + (int64_t)d * vpr;
-#pragma unroll
-        for (int u = 0; u < kCopyUnroll; ++u) {
-          int v = v0 + u * 32;
-          if (v < vpr) dst[v] = t[u];
-        }
+        const int v = v0 + u * 32 + lane;
+        if (v < vpr) dst[v] = t[u];
       }
     }
   }
@@ -308,8 +322,9 @@ extern "C" moe_status moe_dispatch(const void* d_global, const int32_t* d_ids, i
         d_ids, pairs, k, E, hist, d_l2p, d_nrep, X, P, d_offsets_P, cap, d_perm, d_inv, d_status);
   }
   if (move_rows && rows > 0) {
-    int64_t want = (rows + kCopyWarps - 1) / kCopyWarps;
-    int64_t lim = (int64_t)num_sms() * 16;
+    const int64_t items = rows * ((vpr + kSegVecs - 1) / kSegVecs);
+    int64_t want = (items + kCopyWarps - 1) / kCopyWarps;
+    int64_t lim = (int64_t)num_sms() * 8;
     dispatch_copy_kernel<<<(unsigned)(want < lim ? want : lim), kCopyWarps * 32, 0, s>>>(
         static_cast<const uint4*>(d_global), d_inv, rows, k, vpr, cap,
         static_cast<uint4*>(d_sorted));

@@ -7,9 +7,11 @@
 // is a copy plus zero padding.  Section "scatter: 把 MoE 的输出还回本副本":
 // the scatter cuts the buffer back by the same counts.
 //
-// Design: one warp per global row, 16-byte vectors, several vectors in flight
-// per lane; replica pointers travel by value in the kernel arguments, the
-// counts and offsets are read once per block into shared memory.
+// Design: one warp per (row, segment of 32 x kUnroll 16-byte vectors), so a
+// 14 KB row is spread over 7 warps and every lane has all its loads in flight
+// at once (one memory round trip per segment); replica pointers travel by
+// value in the kernel arguments, counts and offsets are read once per block
+// into shared memory.
 #include "common.cuh"
 
 namespace moe {
@@ -26,26 +28,23 @@ __device__ __forceinline__ uint4 ld_nc(const uint4* p) {
   return v;
 }
 
-__device__ __forceinline__ void copy_row(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                         int vpr, int lane) {
-  for (int v0 = lane; v0 < vpr; v0 += 32 * kUnroll) {
-    uint4 t[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      int v = v0 + u * 32;
-      if (v < vpr) t[u] = ld_nc(src + v);
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      int v = v0 + u * 32;
-      if (v < vpr) dst[v] = t[u];
-    }
-  }
-}
+constexpr int kSegVecs = 32 * kUnroll;  // vectors per warp segment
 
-__device__ __forceinline__ void zero_row(uint4* __restrict__ dst, int vpr, int lane) {
-  const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int v = lane; v < vpr; v += 32) dst[v] = z;
+// Copy (src != nullptr) or zero one warp segment [v0, v0 + kSegVecs) of a row.
+__device__ __forceinline__ void copy_seg(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                         int v0, int vpr, int lane) {
+  uint4 t[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    int v = v0 + u * 32 + lane;
+    t[u] = make_uint4(0, 0, 0, 0);
+    if (src != nullptr && v < vpr) t[u] = ld_nc(src + v);
+  }
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    int v = v0 + u * 32 + lane;
+    if (v < vpr) dst[v] = t[u];
+  }
 }
 
 __global__ void __launch_bounds__(kWarps * 32)
@@ -62,24 +61,25 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarps;
-  for (int64_t g = warp0; g < rows; g += nwarps) {
+  const int segs = (vpr + kSegVecs - 1) / kSegVecs;
+  const int64_t items = rows * segs;
+  for (int64_t w = warp0; w < items; w += nwarps) {
+    const int64_t g = w / segs;
+    const int v0 = (int)(w - g * segs) * kSegVecs;
     int r = find_segment(s_off, R, g);
     int64_t i = g - s_off[r];
     int64_t seg = (int64_t)s_off[r + 1] - s_off[r];
     int64_t c = s_cnt[r];
     if (c > seg) {
-      if (i == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
+      if (i == 0 && v0 == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
       c = seg;
     }
     if (c > 0 && src.p[r] == nullptr) {
-      if (i == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
+      if (i == 0 && v0 == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
       c = 0;
     }
-    uint4* dst = global + g * vpr;
-    if (i >= 0 && i < c)
-      copy_row(static_cast<const uint4*>(src.p[r]) + i * vpr, dst, vpr, lane);
-    else
-      zero_row(dst, vpr, lane);
+    const uint4* from = (i >= 0 && i < c) ? static_cast<const uint4*>(src.p[r]) + i * vpr : nullptr;
+    copy_seg(from, global + g * vpr, v0, vpr, lane);
   }
 }
 
@@ -97,22 +97,26 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarps;
-  for (int64_t g = warp0; g < rows; g += nwarps) {
+  const int segs = (vpr + kSegVecs - 1) / kSegVecs;
+  const int64_t items = rows * segs;
+  for (int64_t w = warp0; w < items; w += nwarps) {
+    const int64_t g = w / segs;
+    const int v0 = (int)(w - g * segs) * kSegVecs;
     int r = find_segment(s_off, R, g);
     int64_t i = g - s_off[r];
     int64_t seg = (int64_t)s_off[r + 1] - s_off[r];
     int64_t c = s_cnt[r];
     if (c > seg) {
-      if (i == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
+      if (i == 0 && v0 == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
       c = seg;
     }
     if (c > 0 && dst.p[r] == nullptr) {
-      if (i == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
+      if (i == 0 && v0 == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
       c = 0;
     }
     if (i >= 0 && i < c)
-      copy_row(global + g * vpr,
-               static_cast<uint4*>(const_cast<void*>(dst.p[r])) + i * vpr, vpr, lane);
+      copy_seg(global + g * vpr, static_cast<uint4*>(const_cast<void*>(dst.p[r])) + i * vpr, v0,
+               vpr, lane);
   }
 }
 
@@ -129,9 +133,10 @@ moe_status check_common(const int32_t* d_counts, const int32_t* d_offsets, int R
   return MOE_OK;
 }
 
-int grid_for_rows(int64_t rows) {
-  int64_t want = (rows + kWarps - 1) / kWarps;
-  int64_t cap = (int64_t)num_sms() * 16;
+int grid_for_rows(int64_t rows, int vpr) {
+  const int64_t items = rows * ((vpr + kSegVecs - 1) / kSegVecs);
+  int64_t want = (items + kWarps - 1) / kWarps;
+  int64_t cap = (int64_t)num_sms() * 8;
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
@@ -152,7 +157,7 @@ extern "C" moe_status moe_dp_gather(const void* const* local, const int32_t* d_c
     ptrs.p[r] = local[r];
   }
   const int vpr = (int)((int64_t)H * dtype_bytes(dtype) / 16);
-  dp_gather_kernel<<<grid_for_rows(rows), kWarps * 32, 0, as_stream(stream)>>>(
+  dp_gather_kernel<<<grid_for_rows(rows, vpr), kWarps * 32, 0, as_stream(stream)>>>(
       ptrs, d_counts, d_offsets, R, rows, vpr, static_cast<uint4*>(d_global), d_status);
   return launch_status();
 }
@@ -170,7 +175,7 @@ extern "C" moe_status moe_dp_scatter(const void* d_global, const int32_t* d_coun
     ptrs.p[r] = local[r];
   }
   const int vpr = (int)((int64_t)H * dtype_bytes(dtype) / 16);
-  dp_scatter_kernel<<<grid_for_rows(rows), kWarps * 32, 0, as_stream(stream)>>>(
+  dp_scatter_kernel<<<grid_for_rows(rows, vpr), kWarps * 32, 0, as_stream(stream)>>>(
       static_cast<const uint4*>(d_global), d_counts, d_offsets, R, rows, vpr, ptrs, d_status);
   return launch_status();
 }

@@ -25,9 +25,13 @@
 // CTAs' halves.  Per SM and 64-deep k-block that is 32 KB written by TMA and
 // 32 KB read by the tensor core, against 48 + 48 KB for one 128 x 256 tile per
 // SM (CL = 1), whose shared-memory traffic caps the tensor pipe near two
-// thirds of its rate.  With few rows per slot (decode) the weight stream is
-// the whole cost and the single-SM kernel (CL = 1, 4 stages of 48 KB) keeps
-// more weight bytes in flight per SM, so the launcher picks CL by rows per slot.
+// thirds of its rate.  A pair launch covers whole 256-row groups (and a last
+// group more than half full); a second, single-SM launch covers each slot's
+// remaining <= 128 rows as one 128-row tile, so a slot of 256 + t rows costs
+// one group plus one half-size tile instead of two groups.  With few rows per
+// slot (decode) the weight stream is the whole cost and the single-SM kernel
+// (CL = 1, 4 stages of 48 KB) keeps more weight bytes in flight per SM, so
+// the launcher picks by rows per slot.
 //
 // Roles (192 threads, one CTA per SM):
 //   warp 0    TMA producer (both CTAs): own A box 64x128 and own B box 64x128
@@ -58,7 +62,10 @@ namespace {
 // The pair kernel (CL = 2) needs a full 256-row group per unit to pay off;
 // below this many rows per slot on average the single-SM kernel (CL = 1)
 // streams the weights faster (decode-sized batches).
-constexpr int64_t kPairRowsPerSlot = 192;
+#ifndef MOE_FFN_PAIR_ROWS
+#define MOE_FFN_PAIR_ROWS 192
+#endif
+constexpr int64_t kPairRowsPerSlot = MOE_FFN_PAIR_ROWS;
 
 constexpr int BM = 128;  // rows per CTA
 constexpr int BN = 256;  // accumulator columns
@@ -92,15 +99,29 @@ struct SmemLayout {
   int32_t total_units;
   int32_t warp_sums[THREADS / 32];
   int32_t pref[MOE_MAX_SLOTS + 1];  // unit prefix over the slot range
-  int32_t mt[MOE_MAX_SLOTS];        // 128-row m-tiles per slot
+  int32_t mt[MOE_MAX_SLOTS];        // 128-row m-tiles per slot in this launch
+  int32_t row_base[MOE_MAX_SLOTS];  // first row of the slot this launch covers
+  int32_t row_end[MOE_MAX_SLOTS];   // one past the last row it covers
 };
 template <int CL>
 constexpr size_t smem_bytes() {
   return 1024 + (size_t)Cfg<CL>::STAGES * Cfg<CL>::STAGE_BYTES + sizeof(SmemLayout);
 }
 
+// Which rows of each slot a launch covers.  kAllRows: every row, in groups of
+// CL m-tiles.  kPairGroups (CL = 2): whole 256-row groups, plus the last
+// partial group only when it is more than half full.  kTailRows (CL = 1): the
+// <= 128 rows kPairGroups leaves, as one 128-row tile.  kPairGroups followed
+// by kTailRows covers every row exactly once.
+enum Part { kAllRows = 0, kPairGroups = 1, kTailRows = 2 };
+
+__host__ __device__ __forceinline__ int32_t pair_groups(int64_t rows) {
+  return (int32_t)(rows / 256 + ((rows % 256) > 128 ? 1 : 0));
+}
+
 struct TcParams {
   const int32_t* offsets;
+  int part;
   int slot_lo, nslots;
   int64_t cap;
   int num_kb;
@@ -349,9 +370,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < per; ++i) {
       int s = s0 + i;
       if (s < p.nslots) {
-        int64_t rows = (int64_t)p.offsets[p.slot_lo + s + 1] - p.offsets[p.slot_lo + s];
-        int32_t mt = rows > 0 ? (int32_t)((rows + BM - 1) / BM) : 0;
+        const int64_t o0 = p.offsets[p.slot_lo + s];
+        int64_t rows = (int64_t)p.offsets[p.slot_lo + s + 1] - o0;
+        if (rows < 0) rows = 0;
+        int64_t base = 0, end = rows;
+        if (p.part == kPairGroups) {
+          end = (int64_t)pair_groups(rows) * 256;
+          if (end > rows) end = rows;
+        } else if (p.part == kTailRows) {
+          base = (int64_t)pair_groups(rows) * 256;
+          if (base > rows) base = rows;
+        }
+        const int32_t mt = end > base ? (int32_t)((end - base + BM - 1) / BM) : 0;
         L.mt[s] = mt;
+        L.row_base[s] = (int32_t)(o0 + base);
+        L.row_end[s] = (int32_t)(o0 + end);
         local += (mt + CL - 1) / CL * p.n_tiles;
       }
     }
@@ -415,7 +448,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int u = cid; u < total; u += ncl) {
       const Unit un = decode_unit(L, p.nslots, u, CL);
       const int slot = p.slot_lo + un.slot;
-      const int32_t row0 = p.offsets[slot] + (un.mg * CL + (int)crank) * BM;
+      const int32_t row0 = L.row_base[un.slot] + (un.mg * CL + (int)crank) * BM;
       const int32_t brow1 = slot * p.b_rows_per_slot + un.n * p.b_tile_step;
       const int32_t brow2 = brow1 + p.b_second;
       bool ok = true;
@@ -490,8 +523,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int u = cid; u < total; u += ncl, ++local_tile) {
       const Unit un = decode_unit(L, p.nslots, u, CL);
       const int slot = p.slot_lo + un.slot;
-      const int64_t row0 = (int64_t)p.offsets[slot] + (int64_t)(un.mg * CL + (int)crank) * BM;
-      const int64_t row_end = p.offsets[slot + 1];
+      const int64_t row0 = (int64_t)L.row_base[un.slot] + (int64_t)(un.mg * CL + (int)crank) * BM;
+      const int64_t row_end = L.row_end[un.slot];
       const uint32_t acc = local_tile & 1u, acc_ph = (local_tile >> 1) & 1u;
       if (!wait_bar(smem_u32(&L.tmem_full[acc]), acc_ph, abort_flag, p.status)) break;
       tc_fence_after();
@@ -646,48 +679,47 @@ cudaError_t launch(const CUtensorMap& mA, const CUtensorMap& mB, const TcParams&
   return cudaLaunchKernelEx(&cfg, ffn_tc_kernel<SWIGLU, CL>, mA, mB, p);
 }
 
+// One launch of MM1 + SwiGLU (gemm1) or MM2 over the rows `part` selects.
 template <int CL>
-moe_status run_ffn(const FfnArgs& a, const CUtensorMap& mA1, const CUtensorMap& mB1,
-                   const CUtensorMap& mA2, const CUtensorMap& mB2, cudaStream_t s) {
+moe_status run_ffn(const FfnArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, int part,
+                   bool gemm1, cudaStream_t s) {
   const int nslots = a.slot_hi - a.slot_lo;
   int max_clusters = 0;
   if (!device_setup<CL>(&max_clusters)) return MOE_ERR_CUDA;
   // upper bound of m-groups over the slot range (device-side counts unknown here)
-  const int64_t m_bound = ((a.cap + BM - 1) / BM + nslots) / CL + nslots;
-
-  TcParams p1;
-  p1.offsets = a.offsets;
-  p1.slot_lo = a.slot_lo;
-  p1.nslots = nslots;
-  p1.cap = a.cap;
-  p1.num_kb = a.H / BK;
-  p1.n_tiles = a.I / 128;
-  p1.b_rows_per_slot = 2 * a.I;
-  p1.b_tile_step = 128;
-  p1.b_second = a.I;
-  p1.out_ld = a.I;
-  p1.out_tile_cols = 128;
-  p1.out = static_cast<__nv_bfloat16*>(a.h);
-  p1.status = a.status;
-  const int64_t bound1 = m_bound * p1.n_tiles;
-  if (launch<true, CL>(mA1, mB1, p1, (int)(bound1 < max_clusters ? bound1 : max_clusters), s) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
-
-  TcParams p2 = p1;
-  p2.num_kb = a.I / BK;
-  p2.n_tiles = a.H / BN;
-  p2.b_rows_per_slot = a.H;
-  p2.b_tile_step = BN;
-  p2.b_second = 128;
-  p2.out_ld = a.H;
-  p2.out_tile_cols = BN;
-  p2.out = static_cast<__nv_bfloat16*>(a.ys);
-  const int64_t bound2 = m_bound * p2.n_tiles;
-  if (launch<false, CL>(mA2, mB2, p2, (int)(bound2 < max_clusters ? bound2 : max_clusters), s) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  const int64_t m_bound = part == kTailRows ? nslots
+                                            : ((a.cap + BM - 1) / BM + nslots) / CL + nslots;
+  TcParams p;
+  p.offsets = a.offsets;
+  p.part = part;
+  p.slot_lo = a.slot_lo;
+  p.nslots = nslots;
+  p.cap = a.cap;
+  p.status = a.status;
+  if (gemm1) {
+    p.num_kb = a.H / BK;
+    p.n_tiles = a.I / 128;
+    p.b_rows_per_slot = 2 * a.I;
+    p.b_tile_step = 128;
+    p.b_second = a.I;
+    p.out_ld = a.I;
+    p.out_tile_cols = 128;
+    p.out = static_cast<__nv_bfloat16*>(a.h);
+  } else {
+    p.num_kb = a.I / BK;
+    p.n_tiles = a.H / BN;
+    p.b_rows_per_slot = a.H;
+    p.b_tile_step = BN;
+    p.b_second = 128;
+    p.out_ld = a.H;
+    p.out_tile_cols = BN;
+    p.out = static_cast<__nv_bfloat16*>(a.ys);
+  }
+  const int64_t bound = m_bound * p.n_tiles;
+  const int clusters = (int)(bound < max_clusters ? bound : max_clusters);
+  const cudaError_t e = gemm1 ? launch<true, CL>(mA, mB, p, clusters, s)
+                              : launch<false, CL>(mA, mB, p, clusters, s);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace
@@ -703,8 +735,16 @@ moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
     return MOE_ERR_CUDA;
   // rows per slot the sorted buffer can hold on average, over the whole layer
   const int64_t rows_per_slot = a.cap / (a.P > 0 ? a.P : 1);
-  if (rows_per_slot >= kPairRowsPerSlot) return run_ffn<2>(a, mA1, mB1, mA2, mB2, s);
-  return run_ffn<1>(a, mA1, mB1, mA2, mB2, s);
+  moe_status st;
+  if (rows_per_slot >= kPairRowsPerSlot) {
+    // pair groups on two SMs, then each slot's short remainder on one SM
+    if ((st = run_ffn<2>(a, mA1, mB1, kPairGroups, true, s)) != MOE_OK) return st;
+    if ((st = run_ffn<1>(a, mA1, mB1, kTailRows, true, s)) != MOE_OK) return st;
+    if ((st = run_ffn<2>(a, mA2, mB2, kPairGroups, false, s)) != MOE_OK) return st;
+    return run_ffn<1>(a, mA2, mB2, kTailRows, false, s);
+  }
+  if ((st = run_ffn<1>(a, mA1, mB1, kAllRows, true, s)) != MOE_OK) return st;
+  return run_ffn<1>(a, mA2, mB2, kAllRows, false, s);
 }
 
 }  // namespace moe
