@@ -42,11 +42,15 @@ METRIC = "MoE-layer tokens/s on 1 GB300"
 UNIT = "tokens/s"
 L2_NOTE = "inputs larger than L2: every step streams the touched experts' weights from HBM"
 
-# Launches of this library per step (gather x2, route, dispatch hist/scan/rank/copy,
-# grouped FFN MM1+SwiGLU and MM2, combine, scatter); +1 when align > 1, +2 when the
-# grouped FFN runs its two-SM pair launches plus single-SM tail launches (>= 192
-# sorted rows per slot).
-LAUNCHES_PER_STEP = 11
+def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int) -> int:
+    """Kernel launches of one layer step: gather (hidden states and logits), route,
+    dispatch (one CTA-wide kernel for <= 16384 routed pairs and <= 256 experts, else
+    histogram + scan + rank; then the row copy; + the alignment pad kernel when
+    align > 1), grouped FFN (MM1+SwiGLU and MM2; each split into a two-SM pair launch
+    and a single-SM tail launch at >= 192 sorted rows per slot), combine, scatter."""
+    dispatch = (1 if rows * k <= 16384 and E <= 256 else 3) + 1 + (1 if align > 1 else 0)
+    ffn = 4 if cap // max(P, 1) >= 192 else 2
+    return 2 + 1 + dispatch + ffn + 1 + 1
 
 # dram__bytes_read.sum + dram__bytes_write.sum of the two grouped-FFN launches of one
 # decode step (ncu, --clock-control none), valid for the ffn_tc.cu source whose SHA-256
@@ -299,7 +303,8 @@ def run_native(args, rank, world, local_rank):
         raise RuntimeError(f"device status {int(layer.status.item()):#x}")
     return dict(spec=spec, ms_total=ms_total, clocks=clocks, stage_ms=stage_ms, roof=roof,
                 e2e=e2e, rows=rows, touched=touched,
-                pair_ffn=layer.cap // max(layer.P, 1) >= 192,
+                launches=launches_per_step(max(rows, 1), spec.k, spec.E, layer.P, layer.cap,
+                                           spec.align),
                 inputs=(x_loc, lg_loc, wgu, wd, l2p_np, nrep_np))
 
 
@@ -452,8 +457,7 @@ def main():
                            stage_ms={k: round(v, 4) for k, v in r["stage_ms"].items()}),
             "roofline": r["roof"],
             "clocks": r["clocks"],
-            "gpu_launches": args.steps * (LAUNCHES_PER_STEP + (1 if spec.align > 1 else 0)
-                                          + (2 if r["pair_ffn"] else 0)),
+            "gpu_launches": args.steps * r["launches"],
         }
         if r["e2e"]:
             e = r["e2e"]

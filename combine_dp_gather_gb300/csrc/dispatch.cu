@@ -141,57 +141,55 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
-__global__ void __launch_bounds__(32)
-    dispatch_rank_kernel(const int32_t* __restrict__ ids, int64_t pairs, int k, int E,
-                         const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ l2p,
-                         const int32_t* __restrict__ nrep, int X, int P,
-                         const int32_t* __restrict__ offsets_P, int64_t cap,
-                         int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-                         uint32_t* status) {
-  extern __shared__ int32_t s_run[];
-  const int lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) s_run[e] = 0;
-  __syncwarp();
-  const int64_t base = (int64_t)blockIdx.x * kChunk;
-  const int32_t* cb = chunk_base + (int64_t)blockIdx.x * E;
-  const uint32_t lt = (1u << lane) - 1u;
-  // the chunk's ids, all loaded up front (one memory round trip, not 32)
-  int32_t idv[kChunk / 32];
-#pragma unroll
-  for (int s = 0; s < kChunk / 32; ++s) {
-    const int64_t q = base + s * 32 + lane;
-    idv[s] = q < pairs ? ids[q] : -1;
+// Slot and in-slot position of occurrence p of logical expert l (replica rule
+// of the header: occurrence p goes to replica p mod num_valid, position
+// p div num_valid).  Returns false for a bad map entry.
+__device__ __forceinline__ bool place(int32_t l, int32_t p, const int32_t* l2p,
+                                      const int32_t* nrep, int X, int P, int32_t* slot,
+                                      int32_t* pos) {
+  if (l2p == nullptr) {
+    *slot = l;
+    *pos = p;
+    return true;
   }
+  const int32_t nv = nrep[l];
+  if (nv < 1 || nv > X) return false;
+  *slot = l2p[(int64_t)l * X + p % nv];
+  *pos = p / nv;
+  return *slot >= 0 && *slot < P;
+}
+
+// Rank the pairs of one warp's segment in order: __match_any_sync groups equal
+// ids in a 32-pair step, popc of the lower lanes gives the in-step rank,
+// run[l] carries the count of l across steps.  idv holds the segment's ids.
+template <int STEPS>
+__device__ __forceinline__ void rank_segment(const int32_t (&idv)[STEPS], int64_t base,
+                                             int64_t end, int k, int E, int32_t* run,
+                                             const int32_t* l2p, const int32_t* nrep, int X,
+                                             int P, const int32_t* offP, int64_t cap,
+                                             int32_t* __restrict__ perm,
+                                             int32_t* __restrict__ inv, uint32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
-  for (int s = 0; s < kChunk / 32; ++s) {
+  for (int s = 0; s < STEPS; ++s) {
+    if (base + s * 32 >= end) break;  // warp-uniform
     const int64_t q = base + s * 32 + lane;
     const int32_t l = idv[s];
     const bool valid = l >= 0 && l < E;
     const uint32_t mask = __match_any_sync(0xffffffffu, valid ? l : -1);
     const int rank = __popc(mask & lt);
     int32_t p = 0;
-    if (valid) p = cb[l] + s_run[l] + rank;
+    if (valid) p = run[l] + rank;
     __syncwarp();
-    if (valid && rank == __popc(mask) - 1) s_run[l] += __popc(mask);
+    if (valid && rank == __popc(mask) - 1) run[l] += __popc(mask);
     __syncwarp();
-    if (q >= pairs) continue;
-    int32_t dest = -1;
+    if (q >= end) continue;
+    int32_t dest = -1, slot = 0, pos = 0;
     if (valid) {
-      int32_t slot = l, pos = p;
-      bool ok = true;
-      if (l2p != nullptr) {
-        const int32_t nv = nrep[l];
-        if (nv < 1 || nv > X) {
-          ok = false;
-        } else {
-          slot = l2p[(int64_t)l * X + p % nv];
-          pos = p / nv;
-          ok = slot >= 0 && slot < P;
-        }
-      }
-      if (ok) {
-        const int64_t d = (int64_t)offsets_P[slot] + pos;
-        if (d < cap && d < offsets_P[slot + 1]) {
+      if (place(l, p, l2p, nrep, X, P, &slot, &pos)) {
+        const int64_t d = (int64_t)offP[slot] + pos;
+        if (d < cap && d < offP[slot + 1]) {
           dest = (int32_t)d;
           perm[d] = (int32_t)(q / k);
         } else {
@@ -201,6 +199,149 @@ __global__ void __launch_bounds__(32)
     }
     inv[q] = dest;
   }
+}
+
+// One warp per chunk.  The chunk's base counts, the slot offsets and the
+// replica tables are staged in shared memory first, so the in-order ranking
+// touches only registers and shared memory.
+__global__ void __launch_bounds__(32)
+    dispatch_rank_kernel(const int32_t* __restrict__ ids, int64_t pairs, int k, int E,
+                         const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ l2p,
+                         const int32_t* __restrict__ nrep, int X, int P,
+                         const int32_t* __restrict__ offsets_P, int64_t cap,
+                         int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                         int stage_map, uint32_t* status) {
+  extern __shared__ int32_t smem[];
+  int32_t* s_run = smem;               // [E]  running count (starts at the chunk base)
+  int32_t* s_off = s_run + E;          // [P + 1]
+  int32_t* s_nrep = s_off + P + 1;     // [E]   (map only)
+  int32_t* s_l2p = s_nrep + E;         // [E*X] (map only)
+  const int lane = threadIdx.x;
+  const int64_t base = (int64_t)blockIdx.x * kChunk;
+  int32_t idv[kChunk / 32];
+#pragma unroll
+  for (int s = 0; s < kChunk / 32; ++s) {
+    const int64_t q = base + s * 32 + lane;
+    idv[s] = q < pairs ? ids[q] : -1;
+  }
+  const int32_t* cb = chunk_base + (int64_t)blockIdx.x * E;
+  for (int e = lane; e < E; e += 32) s_run[e] = cb[e];
+  for (int e = lane; e <= P; e += 32) s_off[e] = offsets_P[e];
+  const int32_t* m_l2p = l2p;
+  const int32_t* m_nrep = nrep;
+  if (l2p != nullptr && stage_map) {
+    for (int e = lane; e < E; e += 32) s_nrep[e] = nrep[e];
+    for (int e = lane; e < E * X; e += 32) s_l2p[e] = l2p[e];
+    m_l2p = s_l2p;
+    m_nrep = s_nrep;
+  }
+  __syncwarp();
+  const int64_t end = base + kChunk < pairs ? base + kChunk : pairs;
+  rank_segment<kChunk / 32>(idv, base, end, k, E, s_run, m_l2p, m_nrep, X, P, s_off, cap, perm,
+                            inv, status);
+}
+
+// Small problems (<= kSmallPairs routed pairs, E <= kSmallExperts) in one CTA:
+// per-warp histograms, per-expert scan over warps, slot counts and aligned
+// offsets, then each warp ranks its own segment -- one launch instead of three.
+constexpr int kSmallWarps = 32;
+constexpr int kSmallSteps = 16;  // 32-pair steps per warp segment
+constexpr int64_t kSmallPairs = (int64_t)kSmallWarps * kSmallSteps * 32;
+constexpr int kSmallExperts = 256;
+
+__global__ void __launch_bounds__(kSmallWarps * 32)
+    dispatch_small_kernel(const int32_t* __restrict__ ids, int64_t pairs, int k, int E, int P,
+                          const int32_t* __restrict__ l2p, const int32_t* __restrict__ nrep,
+                          int X, int align, int64_t cap, int32_t* __restrict__ counts_P,
+                          int32_t* __restrict__ offsets_P, int32_t* __restrict__ perm,
+                          int32_t* __restrict__ inv, uint32_t* status) {
+  extern __shared__ int32_t smem[];
+  int32_t* s_hist = smem;                           // [kSmallWarps][E]
+  int32_t* s_off = s_hist + kSmallWarps * E;        // [P + 1]
+  int32_t* s_slot = s_off + P + 1;                  // [P]
+  int32_t* s_claim = s_slot + P;                    // [P]
+  int32_t* s_cnt = s_claim + P;                     // [E]
+  __shared__ int32_t s_warp[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) s_hist[i] = 0;
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    s_slot[i] = 0;
+    s_claim[i] = 0;
+  }
+  // warp segments of whole 32-pair steps
+  const int64_t seg = ((pairs + kSmallWarps - 1) / kSmallWarps + 31) / 32 * 32;
+  const int64_t base = (int64_t)wid * seg;
+  const int64_t end = base + seg < pairs ? base + seg : pairs;
+  int32_t idv[kSmallSteps];
+#pragma unroll
+  for (int s = 0; s < kSmallSteps; ++s) {
+    const int64_t q = base + s * 32 + lane;
+    idv[s] = (s * 32 < seg && q < end) ? ids[q] : -1;
+  }
+  __syncthreads();
+  int32_t* my_hist = s_hist + wid * E;
+#pragma unroll
+  for (int s = 0; s < kSmallSteps; ++s) {
+    const int32_t l = idv[s];
+    const int64_t q = base + s * 32 + lane;
+    if (l >= 0 && l < E)
+      atomicAdd(&my_hist[l], 1);
+    else if (l != -1 && q < end)
+      flag(status, MOE_DEV_BAD_EXPERT_ID);
+  }
+  __syncthreads();
+  // per-expert exclusive scan over warps (hist becomes each warp's base)
+  for (int l = threadIdx.x; l < E; l += blockDim.x) {
+    int32_t run = 0;
+    for (int w = 0; w < kSmallWarps; ++w) {
+      const int32_t t = s_hist[w * E + l];
+      s_hist[w * E + l] = run;
+      run += t;
+    }
+    s_cnt[l] = run;
+  }
+  __syncthreads();
+  if (l2p == nullptr) {
+    for (int sl = threadIdx.x; sl < P; sl += blockDim.x) s_slot[sl] = s_cnt[sl];
+  } else {
+    for (int l = threadIdx.x; l < E; l += blockDim.x) {
+      const int32_t nv = nrep[l];
+      const int32_t cl = s_cnt[l];
+      if (nv < 1 || nv > X) {
+        if (cl > 0) flag(status, MOE_DEV_BAD_MAP);
+        continue;
+      }
+      for (int r = 0; r < nv; ++r) {
+        const int32_t slot = l2p[(int64_t)l * X + r];
+        if (slot < 0 || slot >= P || atomicAdd(&s_claim[slot], 1) != 0) {
+          flag(status, MOE_DEV_BAD_MAP);
+          continue;
+        }
+        s_slot[slot] = cl > r ? (cl - 1 - r) / nv + 1 : 0;
+      }
+    }
+  }
+  __syncthreads();
+  {
+    const int sl = threadIdx.x;  // P <= MOE_MAX_SLOTS = blockDim.x
+    const int32_t cnt = sl < P ? s_slot[sl] : 0;
+    const int32_t padded = (int32_t)(((int64_t)cnt + align - 1) / align * align);
+    int32_t total = 0;
+    const int32_t excl = block_exclusive_scan(padded, s_warp, &total);
+    if (sl < P) {
+      counts_P[sl] = cnt;
+      offsets_P[sl] = excl;
+      s_off[sl] = excl;
+    }
+    if (sl == 0) {
+      offsets_P[P] = total;
+      s_off[P] = total;
+      if ((int64_t)total > cap) flag(status, MOE_DEV_CAPACITY);
+    }
+  }
+  __syncthreads();
+  rank_segment<kSmallSteps>(idv, base, end, k, E, my_hist, l2p, nrep, X, P, s_off, cap, perm,
+                            inv, status);
 }
 
 __device__ __forceinline__ uint4 ld_nc(const uint4* p) {
@@ -311,15 +452,25 @@ extern "C" moe_status moe_dispatch(const void* d_global, const int32_t* d_ids, i
   const int64_t pairs = rows * k;
   const int64_t chunks = n_chunks(pairs);
   int32_t* hist = static_cast<int32_t*>(d_ws);
-  if (chunks > 0) {
+  if (pairs <= kSmallPairs && E <= kSmallExperts) {
+    const size_t smem = sizeof(int32_t) * ((size_t)kSmallWarps * E + (P + 1) + 2 * (size_t)P + E);
+    dispatch_small_kernel<<<1, kSmallWarps * 32, smem, s>>>(
+        d_ids, pairs, k, E, P, d_l2p, d_nrep, X, align, cap, d_counts_P, d_offsets_P, d_perm,
+        d_inv, d_status);
+  } else if (chunks == 0) {
+    dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, 0, E, P, d_l2p, d_nrep, X, align, cap,
+                                            d_counts_P, d_offsets_P, d_status);
+  } else {
     dispatch_hist_kernel<<<(unsigned)chunks, 256, E * sizeof(int32_t), s>>>(d_ids, pairs, E, hist,
                                                                             d_status);
-  }
-  dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, chunks, E, P, d_l2p, d_nrep, X, align, cap,
-                                          d_counts_P, d_offsets_P, d_status);
-  if (chunks > 0) {
-    dispatch_rank_kernel<<<(unsigned)chunks, 32, E * sizeof(int32_t), s>>>(
-        d_ids, pairs, k, E, hist, d_l2p, d_nrep, X, P, d_offsets_P, cap, d_perm, d_inv, d_status);
+    dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, chunks, E, P, d_l2p, d_nrep, X, align, cap,
+                                            d_counts_P, d_offsets_P, d_status);
+    // replica tables staged in shared memory when they fit (else read from global)
+    const int stage_map = d_l2p != nullptr && (int64_t)E * X <= 4096;
+    const size_t smem = sizeof(int32_t) * (E + (P + 1) + (stage_map ? E + (size_t)E * X : 0));
+    dispatch_rank_kernel<<<(unsigned)chunks, 32, smem, s>>>(d_ids, pairs, k, E, hist, d_l2p,
+                                                           d_nrep, X, P, d_offsets_P, cap, d_perm,
+                                                           d_inv, stage_map, d_status);
   }
   if (move_rows && rows > 0) {
     const int64_t items = rows * ((vpr + kSegVecs - 1) / kSegVecs);

@@ -522,7 +522,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t local_tile = 0;
     for (int u = cid; u < total; u += ncl, ++local_tile) {
       const Unit un = decode_unit(L, p.nslots, u, CL);
-      const int slot = p.slot_lo + un.slot;
       const int64_t row0 = (int64_t)L.row_base[un.slot] + (int64_t)(un.mg * CL + (int)crank) * BM;
       const int64_t row_end = L.row_end[un.slot];
       const uint32_t acc = local_tile & 1u, acc_ph = (local_tile >> 1) & 1u;

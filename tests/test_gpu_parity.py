@@ -120,9 +120,14 @@ def _distinct_ids(rows, k, E, seed, pad_every=7):
     return ids.contiguous()
 
 
-@pytest.mark.parametrize("use_map,align", [(False, 1), (False, 128), (True, 1), (True, 4)])
-def test_dispatch_bitexact(md, orc, use_map, align):
-    rows, k, E, H = 3001, 8, 64, 512                     # 24 chunks of 1024 pairs + ragged tail
+@pytest.mark.parametrize("rows,E,use_map,align", [
+    (3001, 64, False, 1), (3001, 64, False, 128), (3001, 64, True, 1), (3001, 64, True, 4),
+    (500, 64, False, 1), (500, 64, True, 4), (1900, 256, True, 1), (2047, 300, False, 1),
+    (1, 64, False, 1)])
+def test_dispatch_bitexact(md, orc, rows, E, use_map, align):
+    """rows x 8 pairs: <= 16384 with E <= 256 runs the one-CTA path, more (or E > 256)
+    the chunked path (24 chunks of 1024 pairs + a ragged tail at 3001 rows)."""
+    k, H = 8, 512
     l2p = nrep = None
     P = E
     if use_map:
@@ -152,8 +157,22 @@ def test_dispatch_bitexact(md, orc, use_map, align):
     assert np.array_equal(to_np(xs)[:n], orc.permute_rows(to_np(x), p_o[:n]))
 
 
-def test_dispatch_device_errors_flag_without_fault(md):
-    rows, k, E, H = 200, 4, 16, 64
+def test_dispatch_zero_rows(md):
+    E, k, H = 16, 4, 64
+    counts_P = torch.full((E,), 7, dtype=torch.int32, device=DEV)
+    offsets_P = torch.full((E + 1,), 7, dtype=torch.int32, device=DEV)
+    ws = torch.empty(max(md.moe_dispatch_ws_bytes(0, k, E), 16), dtype=torch.uint8, device=DEV)
+    empty_i = torch.empty(0, k, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    md.moe_dispatch(None, empty_i, E, E, counts_P, offsets_P, torch.empty(0, dtype=torch.int32,
+                    device=DEV), empty_i, None, ws, d_status=st)
+    assert status_of(st) == 0
+    assert not counts_P.any() and not offsets_P.any()
+
+
+@pytest.mark.parametrize("E", [16, 300])                 # one-CTA path, chunked path
+def test_dispatch_device_errors_flag_without_fault(md, E):
+    rows, k, H = 200, 4, 64
     ids = _distinct_ids(rows, k, E, seed=3, pad_every=1000)
     ids[5, 1] = E            # out of range
     ids[9, 0] = -7           # negative, not the pad marker
