@@ -122,11 +122,12 @@ def _distinct_ids(rows, k, E, seed, pad_every=7):
 
 @pytest.mark.parametrize("rows,E,use_map,align", [
     (3001, 64, False, 1), (3001, 64, False, 128), (3001, 64, True, 1), (3001, 64, True, 4),
-    (500, 64, False, 1), (500, 64, True, 4), (1900, 256, True, 1), (2047, 300, False, 1),
-    (1, 64, False, 1)])
+    (500, 64, False, 1), (500, 64, True, 4), (1900, 256, True, 1), (2048, 256, False, 1),
+    (8192, 256, False, 1), (9001, 64, True, 4), (2047, 300, False, 1), (1, 64, False, 1)])
 def test_dispatch_bitexact(md, orc, rows, E, use_map, align):
-    """rows x 8 pairs: <= 16384 with E <= 256 runs the one-CTA path, more (or E > 256)
-    the chunked path (24 chunks of 1024 pairs + a ragged tail at 3001 rows)."""
+    """rows x 8 pairs: <= 16384 with E <= 256 runs the one-CTA path (2048 rows is
+    exactly the limit); more pairs (3001 rows: 24 chunks of 1024 + a ragged tail) or
+    E > 256 run the chunked histogram / scan / rank path."""
     k, H = 8, 512
     l2p = nrep = None
     P = E
