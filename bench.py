@@ -55,7 +55,7 @@ def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int) -
 # dram__bytes_read.sum + dram__bytes_write.sum of the two grouped-FFN launches of one
 # decode step (ncu, --clock-control none), valid for the ffn_tc.cu source whose SHA-256
 # prefix is recorded; any other source reports traffic null.
-FFN_TRAFFIC = {"decode": {"sha256_16": None, "bytes": None}}
+FFN_TRAFFIC = {"decode": {"sha256_16": "739b95c830baf672", "bytes": 5582133248}}
 
 
 def parse():
@@ -73,12 +73,15 @@ def parse():
     ap.add_argument("--experts", type=int, default=None,
                     help="shrink the layer to this many experts at the same rows per expert "
                          "(small cases for profiling)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="prefill token count (with --experts: many rows, few weights)")
     return ap.parse_args()
 
 
-def make_spec(name: str, seed: int, experts=None):
-    if name == "prefill" and experts:
-        return synth.spec_prefill(T=8192 * experts // 256, E=experts)
+def make_spec(name: str, seed: int, experts=None, tokens=None):
+    if name == "prefill" and (experts or tokens):
+        E = experts or 256
+        return synth.spec_prefill(T=tokens or 8192 * E // 256, E=E)
     if name == "decode":
         spec = synth.spec_decode(seed=seed)
         if experts:
@@ -197,7 +200,7 @@ def run_native(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    spec = make_spec(args.config, args.seed, args.experts)
+    spec = make_spec(args.config, args.seed, args.experts, args.tokens)
     l2p_np, nrep_np, p2l = synth.make_map(spec)
     x_loc = synth.hidden_states(spec, dev)
     lg_loc = synth.router_logits(spec, dev)
@@ -380,7 +383,7 @@ def cpu_baseline(spec, budget_s=20.0, inputs=None):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    spec = make_spec(args.config, args.seed, args.experts)
+    spec = make_spec(args.config, args.seed, args.experts, args.tokens)
     import oracle
     oracle.build()
     inputs = oracle_inputs(spec)
