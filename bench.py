@@ -182,8 +182,10 @@ class StepEvents:
         return out
 
 
-def ffn_traffic(config: str):
-    rec = FFN_TRAFFIC.get(config)
+def ffn_traffic(args):
+    if args.experts is not None or args.tokens is not None or args.seed != 0:
+        return None  # recorded for the default workload only
+    rec = FFN_TRAFFIC.get(args.config)
     if not rec or rec["bytes"] is None:
         return None
     src = os.path.join(ROOT, "combine_dp_gather_gb300", "csrc", "ffn_tc.cu")
@@ -261,7 +263,7 @@ def run_native(args, rank, world, local_rank):
         achieved = ffn_flops / (ffn_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4)}
-    roof.update({"traffic": ffn_traffic(args.config), "kernel": "moe_grouped_ffn (ffn_tc_kernel "
+    roof.update({"traffic": ffn_traffic(args), "kernel": "moe_grouped_ffn (ffn_tc_kernel "
                  "MM1+SwiGLU and MM2 launches)", "peak_source": pk["source"],
                  "algorithmic_bytes": int(ffn_bytes), "algorithmic_flops": int(ffn_flops),
                  "touched_slots": touched, "ms_per_launch_pair": round(ffn_ms, 4)})
