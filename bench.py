@@ -65,7 +65,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="decode",
-                    choices=["decode", "prefill", "pad_sweep", "eplb", "tiny"])
+                    help="decode | prefill | eplb | tiny | pad_sweep[:mix:tokens_per_req:mode]")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -89,8 +89,14 @@ def make_spec(name: str, seed: int, experts=None, tokens=None):
         return spec
     if name == "prefill":
         return synth.spec_prefill()
-    if name == "pad_sweep":
-        return synth.spec_pad_sweep("mix1", 4, synth.PAD_MAX)
+    if name.startswith("pad_sweep"):
+        # pad_sweep[:mix:tokens_per_req:mode], e.g. pad_sweep:mix0:4:static
+        parts = name.split(":")
+        mix = parts[1] if len(parts) > 1 else "mix1"
+        tpr = int(parts[2]) if len(parts) > 2 else 4
+        mode = {"sum": synth.PAD_SUM, "max": synth.PAD_MAX, "static": synth.PAD_STATIC}[
+            parts[3] if len(parts) > 3 else "max"]
+        return synth.spec_pad_sweep(mix, tpr, mode)
     if name == "eplb":
         return synth.spec_eplb()
     return synth.spec_tiny()
@@ -306,7 +312,26 @@ def run_native(args, rank, world, local_rank):
         e2e = {"ms_total": e2e_ms, "steps": args.e2e_steps, "h2d": h2d, "d2h": d2h}
     if int(layer.status.item()) != 0:
         raise RuntimeError(f"device status {int(layer.status.item()):#x}")
+    extra = {}
+    if spec.mode != synth.PAD_SUM or args.config.startswith("pad_sweep"):
+        # padding overhead: rows the global buffer carries that hold no token
+        extra["wasted_row_fraction"] = round((rows - spec.T) / max(rows, 1), 4)
+    if spec.P is not None and spec.P != spec.E:
+        ranges = synth.slot_ranges(spec.P, spec.n_ranges)
+        loads = [int(counts_P[a:b].sum()) for a, b in ranges]
+        # the same routing on the trivial layout (slot = logical id, E slots in
+        # n_ranges equal ranges): logical counts are the per-slot counts summed
+        # over each logical expert's replicas
+        logical = np.zeros(spec.E, np.int64)
+        np.add.at(logical, p2l, counts_P)
+        per = spec.E // spec.n_ranges
+        triv = [int(logical[r * per:(r + 1) * per].sum()) for r in range(spec.n_ranges)]
+        from combine_dp_gather_gb300 import moe_dp as _md
+        extra["range_loads"] = loads
+        extra["balancedness"] = round(_md.utilization_rate(loads), 4)
+        extra["balancedness_trivial_layout"] = round(_md.utilization_rate(triv), 4)
     return dict(spec=spec, ms_total=ms_total, clocks=clocks, stage_ms=stage_ms, roof=roof,
+                extra=extra,
                 e2e=e2e, rows=rows, touched=touched,
                 launches=launches_per_step(max(rows, 1), spec.k, spec.E, layer.P, layer.cap,
                                            spec.align),
@@ -457,7 +482,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
-            "config": dict(synth.describe(spec), global_rows=r["rows"], l2=L2_NOTE,
+            "config": dict(synth.describe(spec), global_rows=r["rows"], l2=L2_NOTE, **r["extra"],
                            parallelism=f"{world} independent replica(s), one per GPU",
                            stage_ms={k: round(v, 4) for k, v in r["stage_ms"].items()}),
             "roofline": r["roof"],
