@@ -262,9 +262,14 @@ class MoeLayer:
         i32 = dict(device=dev, dtype=torch.int32)
         self.d_counts = torch.zeros(R, **i32)
         self.d_offsets = torch.zeros(R + 1, **i32)
-        self.h_meta = torch.zeros(2 * R + 1, dtype=torch.int32, pin_memory=True)
-        self._meta_done = torch.cuda.Event()
-        self._meta_done.record()
+        # ring of pinned staging buffers for the per-step counts/offsets copy, so
+        # the host only waits when it laps a copy still in flight
+        self._meta_ring = [torch.zeros(2 * R + 1, dtype=torch.int32, pin_memory=True)
+                           for _ in range(4)]
+        self._meta_done = [torch.cuda.Event() for _ in range(4)]
+        for ev in self._meta_done:
+            ev.record()
+        self._meta_i = 0
         self.status = torch.zeros(1, **i32)
         self.xg = torch.empty(max_rows, H, device=dev, dtype=self.dtype)
         self.logits_g = torch.empty(max_rows, E, device=dev, dtype=torch.float32)
@@ -289,12 +294,15 @@ class MoeLayer:
         offsets, rows = moe_dp_layout(counts, self.mode, self.static_bound, self.tpr)
         if rows > self.max_rows:
             raise MoeError("MoeLayer.set_counts", MOE_ERR_CAPACITY)
-        self._meta_done.synchronize()  # the previous copy has read the pinned buffer
-        self.h_meta[: self.R] = torch.tensor(list(counts), dtype=torch.int32)
-        self.h_meta[self.R:] = torch.tensor(offsets, dtype=torch.int32)
-        self.d_counts.copy_(self.h_meta[: self.R], non_blocking=True)
-        self.d_offsets.copy_(self.h_meta[self.R:], non_blocking=True)
-        self._meta_done.record()
+        i = self._meta_i
+        self._meta_i = (i + 1) % len(self._meta_ring)
+        self._meta_done[i].synchronize()  # the copy that last used this buffer has run
+        h = self._meta_ring[i]
+        h[: self.R] = torch.tensor(list(counts), dtype=torch.int32)
+        h[self.R:] = torch.tensor(offsets, dtype=torch.int32)
+        self.d_counts.copy_(h[: self.R], non_blocking=True)
+        self.d_offsets.copy_(h[self.R:], non_blocking=True)
+        self._meta_done[i].record()
         self.rows = rows
         return rows
 
