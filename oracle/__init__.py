@@ -15,6 +15,7 @@ Parity status per function (pins in ``tests/test_oracle_pins.py``):
   dispatch, permute_rows ................................ pinned
   expert_ffn / grouped_ffn .............................. pinned
   combine ............................................... pinned
+  add_rmsnorm ........................................... pinned
 """
 from __future__ import annotations
 
@@ -78,6 +79,8 @@ def _load():
             "orc_permute_rows": (None, [P, P, i64, i64, P]),
             "orc_expert_ffn": (None, [P, i64, ctypes.c_int, ctypes.c_int, P, P, P]),
             "orc_combine": (None, [P, P, P, i64, ctypes.c_int, ctypes.c_int, P]),
+            "orc_add_rmsnorm": (None, [P, P, P, i64, ctypes.c_int, ctypes.c_double,
+                                       ctypes.c_int, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -255,6 +258,19 @@ def combine(ys, inv, w) -> np.ndarray:
     out = np.empty((rows, H), np.float64)
     _load().orc_combine(_p(ys), _p(inv), _p(w), rows, k, H, _p(out))
     return out
+
+
+def add_rmsnorm(hidden, residual, gamma, eps: float, round_bf16: bool):
+    """Residual add + RMSNorm of one replica's rows (float32 inputs; bf16 values widened).
+    Returns (updated residual float32 [n, H], normed rows float64 [n, H])."""
+    h = _c(hidden, np.float32)
+    r = _c(residual, np.float32).copy()
+    g = _c(gamma, np.float32)
+    n, H = h.shape
+    y = np.empty((n, H), np.float64)
+    if n:
+        _load().orc_add_rmsnorm(_p(h), _p(r), _p(g), n, H, float(eps), int(round_bf16), _p(y))
+    return r, y
 
 
 def layer(locals_f32, logits, counts, mode, k, renormalize, wgu, wd, E, P=None,

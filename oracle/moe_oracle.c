@@ -380,3 +380,47 @@ void orc_combine(const double *ys, const int32_t *inv, const double *w, int64_t 
     }
   }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Residual add + RMSNorm fused ahead of the DP gather.                      */
+/* [P1] section "边界判定的融合" (_reduce_update_read_dp_gather): after the    */
+/* attention-TP sum (nothing to sum on one device) the hidden states are     */
+/* added into the residual ("update", written back in place), the FFN input  */
+/* is read as RMSNorm of the updated residual ("read"), and that input is    */
+/* DP-gathered.  Reading taken: the add is done in float32 and rounded once  */
+/* to the layer's element type (this rounding decides stored bits, so it is  */
+/* done in the same precision as the kernel: float32 add, then round to      */
+/* nearest even); the norm reads the stored residual:                        */
+/*   y = r / sqrt(mean(r^2) + eps) * gamma   (double here).                  */
+/* Rows are float32 (bf16 layers arrive widened; round_bf16 = 1 asks for the */
+/* bf16 rounding of the updated residual).                                   */
+/* Parity: pinned (numpy restatement of RMSNorm, zero residual, gamma = 1).  */
+/* ------------------------------------------------------------------------ */
+static float orc_round_bf16(float x) {
+  uint32_t u;
+  memcpy(&u, &x, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u) return x; /* inf / nan unchanged */
+  uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7fffu + lsb;
+  u &= 0xffff0000u;
+  float y;
+  memcpy(&y, &u, 4);
+  return y;
+}
+
+void orc_add_rmsnorm(const float *hidden, float *residual, const float *gamma, int64_t n, int H,
+                     double eps, int round_bf16, double *y) {
+  for (int64_t r = 0; r < n; ++r) {
+    const float *h = hidden + r * H;
+    float *res = residual + r * H;
+    double ss = 0.0;
+    for (int c = 0; c < H; ++c) {
+      float s = h[c] + res[c];
+      if (round_bf16) s = orc_round_bf16(s);
+      res[c] = s;
+      ss += (double)s * (double)s;
+    }
+    double inv = 1.0 / sqrt(ss / H + eps);
+    for (int c = 0; c < H; ++c) y[r * H + c] = (double)res[c] * inv * (double)gamma[c];
+  }
+}

@@ -450,3 +450,35 @@ def test_layer_with_replicated_map_equals_without(orc):
     assert (mapped["counts"][spec.E:] > 0).any()   # replicas really used
     for a, b in zip(base["outs"], mapped["outs"]):
         assert np.array_equal(a, b)
+
+
+# ----------------------------------------------------------------- add + RMSNorm
+def test_add_rmsnorm_matches_numpy_and_special_cases(orc):
+    rng = np.random.default_rng(21)
+    n, H = 7, 96
+    h = rng.standard_normal((n, H)).astype(np.float32)
+    r = rng.standard_normal((n, H)).astype(np.float32)
+    g = (1 + 0.1 * rng.standard_normal(H)).astype(np.float32)
+    r_new, y = orc.add_rmsnorm(h, r, g, 1e-6, False)
+    s = h.astype(np.float32) + r.astype(np.float32)          # float32 add, no rounding
+    assert np.array_equal(r_new, s)
+    ref = s.astype(np.float64) / np.sqrt(np.mean(s.astype(np.float64) ** 2, axis=1,
+                                                 keepdims=True) + 1e-6) * g
+    assert np.allclose(y, ref, rtol=1e-13, atol=0)
+    # unit gamma, zero hidden: the norm of a row has root-mean-square 1
+    _, y1 = orc.add_rmsnorm(np.zeros_like(h), r, np.ones(H, np.float32), 0.0, False)
+    assert np.allclose(np.sqrt(np.mean(y1 ** 2, axis=1)), 1.0, rtol=1e-13)
+    # scale invariance: scaling the residual leaves the normed rows unchanged (eps = 0)
+    _, y2 = orc.add_rmsnorm(np.zeros_like(h), 4 * r, np.ones(H, np.float32), 0.0, False)
+    assert np.allclose(y1, y2, rtol=1e-13, atol=1e-15)
+
+
+def test_add_rmsnorm_bf16_rounding_matches_torch(orc):
+    rng = np.random.default_rng(22)
+    h = torch.randn(5, 64, dtype=torch.float32).to(torch.bfloat16)
+    r = torch.randn(5, 64, dtype=torch.float32).to(torch.bfloat16)
+    r_new, _ = orc.add_rmsnorm(h.float().numpy(), r.float().numpy(), np.ones(64, np.float32),
+                               1e-6, True)
+    ref = (h.float() + r.float()).to(torch.bfloat16).float().numpy()   # fp32 add, RNE to bf16
+    assert np.array_equal(r_new, ref)
+    del rng
