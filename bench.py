@@ -73,6 +73,8 @@ def parse():
     ap.add_argument("--experts", type=int, default=None,
                     help="shrink the layer to this many experts at the same rows per expert "
                          "(small cases for profiling)")
+    ap.add_argument("--boundary", default="plain", choices=["plain", "addnorm"],
+                    help="addnorm: residual add + RMSNorm fused into the hidden-state gather")
     ap.add_argument("--tokens", type=int, default=None,
                     help="prefill token count (with --experts: many rows, few weights)")
     return ap.parse_args()
@@ -221,9 +223,16 @@ def run_native(args, rank, world, local_rank):
         l2p=None if l2p_np is None else torch.from_numpy(l2p_np).to(dev),
         nrep=None if nrep_np is None else torch.from_numpy(nrep_np).to(dev))
     out = [torch.empty(c, spec.H, device=dev, dtype=wgu.dtype) for c in spec.counts]
+    res_loc = None
+    if args.boundary == "addnorm":
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(spec.seed * 1000 + 5)
+        res_loc = [torch.randn(c, spec.H, generator=gen, device=dev).to(wgu.dtype)
+                   for c in spec.counts]
+        layer.norm_gamma = torch.ones(spec.H, device=dev, dtype=wgu.dtype)
     layer.set_counts(spec.counts)
     for _ in range(args.warmup):
-        layer.forward(x_loc, lg_loc, out)
+        layer.forward(x_loc, lg_loc, out, local_residual=res_loc)
     torch.cuda.synchronize()
     if int(layer.status.item()) != 0:
         raise RuntimeError(f"device status {int(layer.status.item()):#x} after warm-up")
@@ -238,7 +247,7 @@ def run_native(args, rank, world, local_rank):
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
         for i in range(args.steps):
-            layer.forward(x_loc, lg_loc, out, timings=evs[i])
+            layer.forward(x_loc, lg_loc, out, timings=evs[i], local_residual=res_loc)
         t1.record()
         torch.cuda.synchronize()
     if world > 1:
@@ -306,7 +315,7 @@ def run_native(args, rank, world, local_rank):
             b = i % 2
             comp.wait_event(h2d_done[b])
             comp.wait_event(d2h_done[b])  # dout[b] was read back
-            layer.forward(dx[b], dl[b], dout[b], counts=spec.counts)
+            layer.forward(dx[b], dl[b], dout[b], counts=spec.counts, local_residual=res_loc)
             fwd_done[b].record(comp)
             if i + 1 < n:
                 h2d(1 - b)
@@ -335,7 +344,7 @@ def run_native(args, rank, world, local_rank):
         e1.record(comp)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1)
-        for a, b in zip(ho[(args.e2e_steps - 1) % 2], out):
+        for a, b in zip(ho[(args.e2e_steps - 1) % 2], out if res_loc is None else []):
             if not torch.equal(a.to(b.device).view(torch.int16) if a.dtype == torch.bfloat16
                                else a.to(b.device), b.view(torch.int16)
                                if b.dtype == torch.bfloat16 else b):
@@ -516,6 +525,7 @@ def main():
             "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
             "config": dict(synth.describe(spec), global_rows=r["rows"], l2=L2_NOTE, **r["extra"],
+                           boundary=args.boundary,
                            parallelism=f"{world} independent replica(s), one per GPU",
                            stage_ms={k: round(v, 4) for k, v in r["stage_ms"].items()}),
             "roofline": r["roof"],

@@ -120,6 +120,125 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
+// ------------------------------------------------------------------ fused
+// Residual add + RMSNorm + DP gather (SGLang chapter 17, section "边界判定的融合",
+// _reduce_update_read_dp_gather: update the residual with the hidden states,
+// read the FFN input as RMSNorm of the updated residual, then gather it).
+// One block per global row; each thread keeps up to kNormVecs 16-byte vectors
+// of the row in registers, so the row is read once and written twice
+// (updated residual, normed row in the global buffer).
+constexpr int kNormThreads = 256;
+constexpr int kNormVecs = 4;  // 16-byte vectors per thread: rows up to 16 KB
+
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+  const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+  if (BF16) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      f[2 * e] = bf16lo(q[e]);
+      f[2 * e + 1] = bf16hi(q[e]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) f[e] = __uint_as_float(q[e]);
+  }
+}
+template <bool BF16>
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  uint4 r;
+  if (BF16) {
+    r.x = pack_bf16x2(f[0], f[1]);
+    r.y = pack_bf16x2(f[2], f[3]);
+    r.z = pack_bf16x2(f[4], f[5]);
+    r.w = pack_bf16x2(f[6], f[7]);
+  } else {
+    r.x = __float_as_uint(f[0]);
+    r.y = __float_as_uint(f[1]);
+    r.z = __float_as_uint(f[2]);
+    r.w = __float_as_uint(f[3]);
+  }
+  return r;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kNormThreads)
+    dp_gather_add_rmsnorm_kernel(ReplicaPtrs hidden, ReplicaPtrs residual,
+                                 const uint4* __restrict__ gamma, float eps,
+                                 const int32_t* __restrict__ counts,
+                                 const int32_t* __restrict__ offsets, int R, int64_t rows, int H,
+                                 int vpr, uint4* __restrict__ global, uint32_t* status) {
+  constexpr int EPV = BF16 ? 8 : 4;
+  __shared__ int32_t s_off[MOE_MAX_REPLICAS + 1];
+  __shared__ int32_t s_cnt[MOE_MAX_REPLICAS];
+  __shared__ float s_part[kNormThreads / 32];
+  for (int i = threadIdx.x; i <= R; i += blockDim.x) {
+    s_off[i] = offsets[i];
+    if (i < R) s_cnt[i] = counts[i];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int64_t g = blockIdx.x; g < rows; g += gridDim.x) {
+    const int r = find_segment(s_off, R, g);
+    const int64_t i = g - s_off[r];
+    int64_t c = s_cnt[r];
+    const int64_t seg = (int64_t)s_off[r + 1] - s_off[r];
+    if (c > seg) {
+      if (i == 0 && threadIdx.x == 0) flag(status, MOE_DEV_BAD_COUNTS);
+      c = seg;
+    }
+    if (c > 0 && (hidden.p[r] == nullptr || residual.p[r] == nullptr)) {
+      if (i == 0 && threadIdx.x == 0) flag(status, MOE_DEV_BAD_COUNTS);
+      c = 0;
+    }
+    uint4* dst = global + g * vpr;
+    if (!(i >= 0 && i < c)) {  // pad row (block-uniform)
+      for (int v = threadIdx.x; v < vpr; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* hrow = static_cast<const uint4*>(hidden.p[r]) + i * vpr;
+    uint4* rrow = static_cast<uint4*>(const_cast<void*>(residual.p[r])) + i * vpr;
+    float x[kNormVecs][EPV];
+    float ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < kNormVecs; ++u) {
+      const int v = threadIdx.x + u * kNormThreads;
+      if (v < vpr) {
+        float a[EPV], b[EPV];
+        unpack8<BF16>(hrow[v], a);
+        unpack8<BF16>(rrow[v], b);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) x[u][e] = a[e] + b[e];   // float32 add
+        const uint4 stored = pack8<BF16>(x[u]);                   // round once
+        rrow[v] = stored;                                          // updated residual
+        unpack8<BF16>(stored, x[u]);                               // the norm reads it
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) ss = fmaf(x[u][e], x[u][e], ss);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (lane == 0) s_part[wid] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kNormThreads / 32; ++w) tot += s_part[w];
+    __syncthreads();  // s_part is reused by the next row
+    const float inv = rsqrtf(tot / (float)H + eps);
+#pragma unroll
+    for (int u = 0; u < kNormVecs; ++u) {
+      const int v = threadIdx.x + u * kNormThreads;
+      if (v < vpr) {
+        float gm[EPV], y[EPV];
+        unpack8<BF16>(gamma[v], gm);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) y[e] = x[u][e] * inv * gm[e];
+        dst[v] = pack8<BF16>(y);
+      }
+    }
+  }
+}
+
 moe_status check_common(const int32_t* d_counts, const int32_t* d_offsets, int R, int64_t rows,
                         int H, int dtype, const void* d_global) {
   if (R < 1 || R > MOE_MAX_REPLICAS || rows < 0 || rows > INT32_MAX || H < 1)
@@ -159,6 +278,40 @@ extern "C" moe_status moe_dp_gather(const void* const* local, const int32_t* d_c
   const int vpr = (int)((int64_t)H * dtype_bytes(dtype) / 16);
   dp_gather_kernel<<<grid_for_rows(rows, vpr), kWarps * 32, 0, as_stream(stream)>>>(
       ptrs, d_counts, d_offsets, R, rows, vpr, static_cast<uint4*>(d_global), d_status);
+  return launch_status();
+}
+
+extern "C" moe_status moe_dp_gather_add_rmsnorm(const void* const* local_hidden,
+                                                void* const* local_residual, const void* d_gamma,
+                                                float eps, const int32_t* d_counts,
+                                                const int32_t* d_offsets, int R, int64_t rows,
+                                                int H, int dtype, void* d_global,
+                                                uint32_t* d_status, void* stream) {
+  moe_status st = check_common(d_counts, d_offsets, R, rows, H, dtype, d_global);
+  if (st != MOE_OK || rows == 0) return st;
+  if (local_hidden == nullptr || local_residual == nullptr || d_gamma == nullptr ||
+      !aligned16(d_gamma) || !(eps >= 0.f))
+    return MOE_ERR_INVALID_ARG;
+  const int vpr = (int)((int64_t)H * dtype_bytes(dtype) / 16);
+  if (vpr > kNormThreads * kNormVecs) return MOE_ERR_UNSUPPORTED;  // rows above 16 KB
+  ReplicaPtrs hp, rp;
+  for (int r = 0; r < R; ++r) {
+    if ((local_hidden[r] != nullptr && !aligned16(local_hidden[r])) ||
+        (local_residual[r] != nullptr && !aligned16(local_residual[r])))
+      return MOE_ERR_INVALID_ARG;
+    hp.p[r] = local_hidden[r];
+    rp.p[r] = local_residual[r];
+  }
+  const int64_t lim = (int64_t)num_sms() * 8;
+  const int grid = (int)(rows < lim ? rows : lim);
+  if (dtype == MOE_BF16)
+    dp_gather_add_rmsnorm_kernel<true><<<grid, kNormThreads, 0, as_stream(stream)>>>(
+        hp, rp, static_cast<const uint4*>(d_gamma), eps, d_counts, d_offsets, R, rows, H, vpr,
+        static_cast<uint4*>(d_global), d_status);
+  else
+    dp_gather_add_rmsnorm_kernel<false><<<grid, kNormThreads, 0, as_stream(stream)>>>(
+        hp, rp, static_cast<const uint4*>(d_gamma), eps, d_counts, d_offsets, R, rows, H, vpr,
+        static_cast<uint4*>(d_global), d_status);
   return launch_status();
 }
 

@@ -50,6 +50,8 @@ _SIGS = {
                              _P]),
     "moe_combine": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I64, _P, _P, _P]),
     "moe_dp_scatter": (_I, [_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P]),
+    "moe_dp_gather_add_rmsnorm": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _I, _I64, _I, _I, _P,
+                                       _P, _P]),
     "moe_dispatch_noalloc": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _I, _I, _I64, _P,
                                   _P, _P, _P, _P, _P, _P]),
 }
@@ -169,6 +171,20 @@ def moe_dp_gather(local: Sequence[torch.Tensor], d_counts, d_offsets, out: torch
         dtype_code(out.dtype), _ptr(out), _ptr(d_status), _stream(stream)))
 
 
+def moe_dp_gather_add_rmsnorm(local_hidden: Sequence[torch.Tensor],
+                              local_residual: Sequence[torch.Tensor], gamma: torch.Tensor,
+                              eps: float, d_counts, d_offsets, out: torch.Tensor, d_status=None,
+                              stream=None):
+    """Residual add (in place) + RMSNorm + DP gather of the normed rows."""
+    R = len(local_hidden)
+    hp = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_hidden])
+    rp = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_residual])
+    _check("moe_dp_gather_add_rmsnorm", lib().moe_dp_gather_add_rmsnorm(
+        ctypes.cast(hp, _P), ctypes.cast(rp, _P), _ptr(gamma), float(eps), _ptr(d_counts),
+        _ptr(d_offsets), R, out.shape[0], out.shape[1], dtype_code(out.dtype), _ptr(out),
+        _ptr(d_status), _stream(stream)))
+
+
 def moe_route_topk(logits: torch.Tensor, k: int, renormalize: bool, d_counts, d_offsets,
                    ids: torch.Tensor, w: torch.Tensor, d_status=None, stream=None):
     rows, E = logits.shape
@@ -248,7 +264,8 @@ class MoeLayer:
                  w_down: torch.Tensor, max_rows: int, mode: int = MOE_PAD_SUM,
                  static_bound: int = 0, tokens_per_req: int = 1, renormalize: bool = True,
                  align: int = 1, l2p: Optional[torch.Tensor] = None,
-                 nrep: Optional[torch.Tensor] = None, slot_range=None):
+                 nrep: Optional[torch.Tensor] = None, slot_range=None,
+                 norm_gamma: Optional[torch.Tensor] = None, norm_eps: float = 1e-6):
         dev = w_gate_up.device
         self.R, self.H, self.E, self.k, self.I = R, H, E, k, I
         self.P = w_gate_up.shape[0]
@@ -257,6 +274,7 @@ class MoeLayer:
         self.renormalize, self.align = renormalize, align
         self.wgu, self.wd, self.l2p, self.nrep = w_gate_up, w_down, l2p, nrep
         self.slot_range = slot_range or (0, self.P)
+        self.norm_gamma, self.norm_eps = norm_gamma, norm_eps
         self.max_rows = max_rows
         self.cap = moe_dispatch_cap_bound(max_rows, k, self.P, align)
         i32 = dict(device=dev, dtype=torch.int32)
@@ -308,7 +326,11 @@ class MoeLayer:
 
     def forward(self, local_x: Sequence[torch.Tensor], local_logits: Sequence[torch.Tensor],
                 out: Sequence[torch.Tensor], counts: Optional[Sequence[int]] = None,
-                stream=None, timings=None):
+                stream=None, timings=None,
+                local_residual: Optional[Sequence[torch.Tensor]] = None):
+        """One layer step.  With local_residual (and norm_gamma set at construction)
+        the hidden states are first added into the residual in place and the
+        RMSNorm of the updated residual is what gets gathered and routed."""
         if counts is not None:
             self.set_counts(counts)
         rows = self.rows
@@ -317,7 +339,13 @@ class MoeLayer:
         ids, w, inv, yg = self.ids[:rows], self.w[:rows], self.inv[:rows], self.yg[:rows]
         ev = timings.mark if timings is not None else (lambda name: None)
         ev("start")
-        moe_dp_gather(local_x, self.d_counts, self.d_offsets, xg, st, stream)
+        if local_residual is not None:
+            if self.norm_gamma is None:
+                raise ValueError("local_residual needs norm_gamma")
+            moe_dp_gather_add_rmsnorm(local_x, local_residual, self.norm_gamma, self.norm_eps,
+                                      self.d_counts, self.d_offsets, xg, st, stream)
+        else:
+            moe_dp_gather(local_x, self.d_counts, self.d_offsets, xg, st, stream)
         moe_dp_gather(local_logits, self.d_counts, self.d_offsets, lg, st, stream)
         ev("gather")
         moe_route_topk(lg, self.k, self.renormalize, self.d_counts, self.d_offsets, ids, w, st,

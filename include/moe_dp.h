@@ -150,6 +150,27 @@ moe_status moe_dp_gather(const void* const* local, const int32_t* d_counts,
                          const int32_t* d_offsets, int R, int64_t rows, int H, int dtype,
                          void* d_global, uint32_t* d_status, void* stream);
 
+/* Residual add + RMSNorm fused ahead of the DP gather.  [P1] section
+ * "边界判定的融合" (_reduce_update_read_dp_gather): the attention output is added
+ * into the residual ("update", written back in place) and the FFN input is read
+ * as RMSNorm of the updated residual ("read") before the DP gather; with one
+ * device there is no attention-TP sum to complete.  For each real row i of
+ * replica r:
+ *   residual[r][i] = round(hidden[r][i] + residual[r][i])   (float32 add)
+ *   global[offsets[r] + i] = round(res / sqrt(mean(res^2) + eps) * gamma)
+ * where res is the stored (rounded) residual; pad rows of the global buffer
+ * are zero.
+ *   local_hidden    HOST array of R device pointers, [counts[r], H]
+ *   local_residual  HOST array of R device pointers, [counts[r], H], updated
+ *   d_gamma         device [H] norm weight, layer dtype
+ *   eps             >= 0
+ *   other arguments as moe_dp_gather; rows of at most 16 KB (H <= 8192 bf16,
+ *   4096 fp32), else MOE_ERR_UNSUPPORTED. */
+moe_status moe_dp_gather_add_rmsnorm(const void* const* local_hidden, void* const* local_residual,
+                                     const void* d_gamma, float eps, const int32_t* d_counts,
+                                     const int32_t* d_offsets, int R, int64_t rows, int H,
+                                     int dtype, void* d_global, uint32_t* d_status, void* stream);
+
 /* Top-k routing of every real row of the global buffer.  [P1] names the
  * result TopKOutput{topk_ids, topk_weights} (sections "normal dispatch 的调用链"
  * and "Two-batch Overlap"); the scoring is softmax routing: the k largest

@@ -120,6 +120,23 @@ def test_gather_scatter_reject_bad_args(md):
     assert L.moe_dp_scatter(FAKE, NULL, FAKE, 2, 8, 64, 1, two, NULL, NULL) == E_ARG
 
 
+def test_gather_add_rmsnorm_rejects_bad_args(md):
+    L = md.lib()
+    two = _ptrs(0x2000, 0x3000)
+    E_ARG, E_UNS = md.MOE_ERR_INVALID_ARG, md.MOE_ERR_UNSUPPORTED
+    f = ctypes.c_float
+    assert L.moe_dp_gather_add_rmsnorm(two, two, NULL, f(1e-6), FAKE, FAKE, 2, 8, 64, 1, FAKE,
+                                       NULL, NULL) == E_ARG               # no gamma
+    assert L.moe_dp_gather_add_rmsnorm(two, two, FAKE, f(-1.0), FAKE, FAKE, 2, 8, 64, 1, FAKE,
+                                       NULL, NULL) == E_ARG               # negative eps
+    assert L.moe_dp_gather_add_rmsnorm(NULL, two, FAKE, f(1e-6), FAKE, FAKE, 2, 8, 64, 1, FAKE,
+                                       NULL, NULL) == E_ARG
+    assert L.moe_dp_gather_add_rmsnorm(two, two, FAKE, f(1e-6), FAKE, FAKE, 2, 8, 16384, 1,
+                                       FAKE, NULL, NULL) == E_UNS          # 32 KB rows
+    assert L.moe_dp_gather_add_rmsnorm(two, two, MISAL, f(1e-6), FAKE, FAKE, 2, 8, 64, 1, FAKE,
+                                       NULL, NULL) == E_ARG
+
+
 def test_route_rejects_bad_args(md):
     L = md.lib()
     E_ARG = md.MOE_ERR_INVALID_ARG

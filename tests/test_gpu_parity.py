@@ -92,6 +92,34 @@ def test_gather_all_idle_and_bad_counts(md):
     assert torch.equal(g.float(), torch.ones(8, 64, device=DEV))
 
 
+@pytest.mark.parametrize("dtype,H,mode", [(torch.bfloat16, 7168, 1), (torch.bfloat16, 512, 0),
+                                          (torch.float32, 1024, 2)])
+def test_gather_add_rmsnorm(md, orc, dtype, H, mode):
+    counts = [5, 0, 33, 1, 17]
+    offs, rows = md.moe_dp_layout(counts, mode, 40, 1)
+    g = torch.Generator(device=DEV).manual_seed(H + mode)
+    hid = [torch.randn(c, H, generator=g, device=DEV).to(dtype) for c in counts]
+    res = [torch.randn(c, H, generator=g, device=DEV).to(dtype) for c in counts]
+    gamma = (1 + 0.1 * torch.randn(H, generator=g, device=DEV)).to(dtype)
+    res0 = [t.clone() for t in res]
+    out = torch.full((rows, H), 3.0, device=DEV, dtype=dtype)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    md.moe_dp_gather_add_rmsnorm(hid, res, gamma, 1e-6, dev_i32(counts), dev_i32(offs), out, st)
+    assert status_of(st) == 0
+    bf = dtype == torch.bfloat16
+    f32 = lambda t: as_f32(to_np(t))
+    y = np.zeros((rows, H))
+    for r, c in enumerate(counts):
+        r_new, y_r = orc.add_rmsnorm(f32(hid[r]), f32(res0[r]), f32(gamma), 1e-6, bf)
+        assert np.array_equal(f32(res[r]), r_new)                   # stored residual: exact
+        y[offs[r]: offs[r] + c] = y_r
+    valid = orc.valid_rows(counts, np.array(offs, np.int32), rows)
+    got = f32(out).astype(np.float64)
+    tol = (1e-6, 8e-3) if bf else (1e-6, 1e-5)   # one bf16 rounding (<= 1 ulp apart)
+    assert_close(got[valid == 1], y[valid == 1], *tol, what="normed rows")
+    assert not got[valid == 0].any()
+
+
 # ------------------------------------------------------------------ routing
 @pytest.mark.parametrize("E,k", [(8, 2), (256, 8), (300, 6), (64, 1), (32, 32), (1024, 4)])
 @pytest.mark.parametrize("renorm", [True, False])
