@@ -74,6 +74,8 @@ def _load():
             "orc_dp_scatter": (None, [P, P, P, ctypes.c_int, i64, P]),
             "orc_route_topk": (ctypes.c_int, [P, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                               P, P, P]),
+            "orc_route_topk_shared": (ctypes.c_int, [P, i64, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int, ctypes.c_int, P, P, P]),
             "orc_dispatch": (ctypes.c_int, [P, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             P, P, ctypes.c_int, ctypes.c_int, i64, P, P, P, P]),
             "orc_permute_rows": (None, [P, P, i64, i64, P]),
@@ -173,14 +175,16 @@ def dp_scatter(global_arr, counts, offsets):
     return outs
 
 
-def route_topk(logits, k: int, renormalize: bool, valid):
+def route_topk(logits, k: int, renormalize: bool, valid, n_shared: int = 0):
+    """Top-k routing; with n_shared > 0 every real row also lists the shared experts
+    E .. E + n_shared - 1 (weight 1) after its k routed ids."""
     logits = _c(logits, np.float32)
     rows, E = logits.shape
     valid = _c(valid, np.uint8)
-    ids = np.empty((rows, k), np.int32)
-    w = np.empty((rows, k), np.float64)
-    st = _load().orc_route_topk(_p(logits), rows, E, k, int(renormalize), _p(valid),
-                                _p(ids), _p(w))
+    ids = np.empty((rows, k + n_shared), np.int32)
+    w = np.empty((rows, k + n_shared), np.float64)
+    st = _load().orc_route_topk_shared(_p(logits), rows, E, k, int(renormalize), n_shared,
+                                       _p(valid), _p(ids), _p(w))
     if st:
         raise OracleError(st)
     return ids, w
@@ -274,16 +278,16 @@ def add_rmsnorm(hidden, residual, gamma, eps: float, round_bf16: bool):
 
 
 def layer(locals_f32, logits, counts, mode, k, renormalize, wgu, wd, E, P=None,
-          l2p=None, nrep=None, align=1, static_bound=0, tokens_per_req=1):
+          l2p=None, nrep=None, align=1, static_bound=0, tokens_per_req=1, n_shared=0):
     """Whole layer, step by step: layout, gather, route, dispatch, FFN, combine,
     scatter.  locals_f32: per-replica float32 hidden states (bf16 already
     widened).  Returns a dict of every intermediate."""
-    P = E if P is None else P
+    P = E + n_shared if P is None else P
     offsets, rows = dp_layout(counts, mode, static_bound, tokens_per_req)
     valid = valid_rows(counts, offsets, rows)
     xg = dp_gather(locals_f32, counts, offsets, rows)
-    ids, w = route_topk(logits, k, renormalize, valid)
-    cnt, offs, perm, inv = dispatch(ids, E, P, l2p, nrep, align)
+    ids, w = route_topk(logits, k, renormalize, valid, n_shared)
+    cnt, offs, perm, inv = dispatch(ids, E + n_shared, P, l2p, nrep, align)
     xs = permute_rows(xg, perm[: offs[-1]])
     ys = grouped_ffn(xs, offs, wgu, wd)
     yg = combine(ys, inv, w)

@@ -164,8 +164,51 @@ void orc_dp_scatter(const void *global, const int32_t *counts, const int32_t *of
 /* chosen experts.  Pad rows get id -1 and weight 0.                         */
 /* Parity: pinned (brute force over all k-subsets, scipy softmax, k=1, k=E). */
 /* ------------------------------------------------------------------------ */
+/* Shared experts: [P2] section "共享专家: 在被让出的空档里干活" -- a shared
+ * expert's input bypasses routing; every token goes through it and its output
+ * is added to the routed mixture.  Reading taken: shared expert s is logical
+ * expert E + s, listed after the k routed ids of every real row with weight 1,
+ * so dispatch, the grouped FFN and combine treat it as one more slot.
+ * ids / w are [rows, k + n_shared].  Parity: pinned (dense per-token sum). */
+int orc_route_topk_shared(const float *logits, int64_t rows, int E, int k, int renormalize,
+                          int n_shared, const uint8_t *valid, int32_t *ids, double *w);
+int orc_route_topk_routed(const float *logits, int64_t rows, int E, int k, int renormalize,
+                          const uint8_t *valid, int32_t *ids, double *w);
+
 int orc_route_topk(const float *logits, int64_t rows, int E, int k, int renormalize,
                    const uint8_t *valid, int32_t *ids, double *w) {
+  return orc_route_topk_shared(logits, rows, E, k, renormalize, 0, valid, ids, w);
+}
+
+int orc_route_topk_shared(const float *logits, int64_t rows, int E, int k, int renormalize,
+                          int n_shared, const uint8_t *valid, int32_t *ids_out, double *w_out) {
+  if (E < 1 || k < 1 || k > E || n_shared < 0) return ORC_ERR_ARG;
+  const int kk = k + n_shared;
+  int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)(rows > 0 ? rows * k : 1));
+  double *w = (double *)malloc(sizeof(double) * (size_t)(rows > 0 ? rows * k : 1));
+  if (ids == NULL || w == NULL) {
+    free(ids);
+    free(w);
+    return ORC_ERR_ARG;
+  }
+  int st = orc_route_topk_routed(logits, rows, E, k, renormalize, valid, ids, w);
+  for (int64_t g = 0; g < rows && st == ORC_OK; ++g) {
+    for (int j = 0; j < k; ++j) {
+      ids_out[g * kk + j] = ids[g * k + j];
+      w_out[g * kk + j] = w[g * k + j];
+    }
+    for (int s = 0; s < n_shared; ++s) {
+      ids_out[g * kk + k + s] = valid[g] ? E + s : -1;
+      w_out[g * kk + k + s] = valid[g] ? 1.0 : 0.0;
+    }
+  }
+  free(ids);
+  free(w);
+  return st;
+}
+
+int orc_route_topk_routed(const float *logits, int64_t rows, int E, int k, int renormalize,
+                          const uint8_t *valid, int32_t *ids, double *w) {
   if (E < 1 || k < 1 || k > E) return ORC_ERR_ARG;
   uint8_t *taken = (uint8_t *)malloc((size_t)E);
   if (taken == NULL) return ORC_ERR_ARG;

@@ -482,3 +482,35 @@ def test_add_rmsnorm_bf16_rounding_matches_torch(orc):
     ref = (h.float() + r.float()).to(torch.bfloat16).float().numpy()   # fp32 add, RNE to bf16
     assert np.array_equal(r_new, ref)
     del rng
+
+
+# ----------------------------------------------------------------- shared experts
+def test_shared_experts_follow_routed_ids(orc):
+    rng = np.random.default_rng(23)
+    logits = rng.standard_normal((9, 8)).astype(np.float32)
+    valid = np.ones(9, np.uint8)
+    valid[4] = 0
+    ids, w = orc.route_topk(logits, 2, True, valid, n_shared=2)
+    ids0, w0 = orc.route_topk(logits, 2, True, valid)
+    assert np.array_equal(ids[:, :2], ids0) and np.array_equal(w[:, :2], w0)
+    assert ids[valid == 1][:, 2:].tolist() == [[8, 9]] * 8
+    assert (w[valid == 1][:, 2:] == 1.0).all()
+    assert (ids[4] == -1).all() and (w[4] == 0).all()
+
+
+def test_layer_with_shared_expert_matches_dense_definition(orc):
+    from combine_dp_gather_gb300 import synth
+    spec = synth.spec_tiny()
+    xs = [t.numpy() for t in synth.hidden_states(spec)]
+    lg = [t.numpy() for t in synth.router_logits(spec)]
+    rng = np.random.default_rng(24)
+    wgu = (0.02 * rng.standard_normal((9, 2 * spec.I, spec.H))).astype(np.float32)
+    wd = (0.02 * rng.standard_normal((9, spec.H, spec.I))).astype(np.float32)
+    offs, rows = orc.dp_layout(spec.counts, 0)
+    logits = orc.dp_gather(lg, spec.counts, offs, rows)
+    res = orc.layer(xs, logits, spec.counts, 0, spec.k, True, wgu, wd, spec.E, n_shared=1)
+    x = np.concatenate(xs)
+    dense = dense_layer(x, np.concatenate(lg), spec.k, wgu[:8], wd[:8])
+    dense += numpy_swiglu(x, wgu[8], wd[8])           # the shared expert, weight 1
+    got = np.concatenate(res["outs"])
+    assert np.allclose(got, dense, rtol=1e-10, atol=1e-12)
