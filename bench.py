@@ -44,11 +44,12 @@ L2_NOTE = "inputs larger than L2: every step streams the touched experts' weight
 
 def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int) -> int:
     """Kernel launches of one layer step: gather (hidden states and logits), route,
-    dispatch (one CTA-wide kernel for <= 16384 routed pairs and <= 256 experts, else
+    dispatch (one CTA-wide kernel for <= 16384 routed pairs whose tables fit 48 KB, else
     histogram + scan + rank; then the row copy; + the alignment pad kernel when
     align > 1), grouped FFN (MM1+SwiGLU and MM2; each split into a two-SM pair launch
     and a single-SM tail launch at >= 192 sorted rows per slot), combine, scatter."""
-    dispatch = (1 if rows * k <= 16384 and E <= 256 else 3) + 1 + (1 if align > 1 else 0)
+    small = rows * k <= 16384 and 4 * (33 * E + 3 * P + 1) <= 48 * 1024
+    dispatch = (1 if small else 3) + 1 + (1 if align > 1 else 0)
     ffn = 4 if cap // max(P, 1) >= 192 else 2
     return 2 + 1 + dispatch + ffn + 1 + 1
 
@@ -73,6 +74,8 @@ def parse():
     ap.add_argument("--experts", type=int, default=None,
                     help="shrink the layer to this many experts at the same rows per expert "
                          "(small cases for profiling)")
+    ap.add_argument("--shared", type=int, default=0,
+                    help="shared experts, always selected with weight 1 (0 = none)")
     ap.add_argument("--boundary", default="plain", choices=["plain", "addnorm"],
                     help="addnorm: residual add + RMSNorm fused into the hidden-state gather")
     ap.add_argument("--tokens", type=int, default=None,
@@ -211,6 +214,10 @@ def run_native(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     spec = make_spec(args.config, args.seed, args.experts, args.tokens)
+    if args.shared:
+        if spec.P is not None and spec.P != spec.E:
+            raise SystemExit("--shared is not combined with an expert map")
+        spec.n_shared = args.shared
     l2p_np, nrep_np, p2l = synth.make_map(spec)
     x_loc = synth.hidden_states(spec, dev)
     lg_loc = synth.router_logits(spec, dev)
@@ -221,7 +228,8 @@ def run_native(args, rank, world, local_rank):
         max_rows=max(rows, 1), mode=spec.mode, static_bound=spec.static_bound,
         tokens_per_req=spec.tokens_per_req, renormalize=spec.renormalize, align=spec.align,
         l2p=None if l2p_np is None else torch.from_numpy(l2p_np).to(dev),
-        nrep=None if nrep_np is None else torch.from_numpy(nrep_np).to(dev))
+        nrep=None if nrep_np is None else torch.from_numpy(nrep_np).to(dev),
+        n_shared=spec.n_shared)
     out = [torch.empty(c, spec.H, device=dev, dtype=wgu.dtype) for c in spec.counts]
     res_loc = None
     if args.boundary == "addnorm":
@@ -266,7 +274,7 @@ def run_native(args, rank, world, local_rank):
     T = spec.T
     b = 2 if spec.dtype == "bf16" else 4
     ffn_bytes = touched * 3 * spec.I * spec.H * b + routed * (2 * spec.H + 2 * spec.I) * b
-    ffn_flops = synth.flops_ffn(T, spec.k, spec.H, spec.I)
+    ffn_flops = synth.flops_ffn(T, spec.k + spec.n_shared, spec.H, spec.I)
     ffn_ms = stage_ms["ffn"]
     pk = peaks()
     hbm_bound = ffn_flops / (ffn_bytes) < (pk["bf16_tflops"] * 1e12) / (pk["hbm_gbs"] * 1e9)
@@ -375,7 +383,8 @@ def run_native(args, rank, world, local_rank):
     return dict(spec=spec, ms_total=ms_total, clocks=clocks, stage_ms=stage_ms, roof=roof,
                 extra=extra,
                 e2e=e2e, rows=rows, touched=touched,
-                launches=launches_per_step(max(rows, 1), spec.k, spec.E, layer.P, layer.cap,
+                launches=launches_per_step(max(rows, 1), spec.k + spec.n_shared,
+                                           spec.E + spec.n_shared, layer.P, layer.cap,
                                            spec.align),
                 inputs=(x_loc, lg_loc, wgu, wd, l2p_np, nrep_np))
 
@@ -403,8 +412,9 @@ def oracle_sample_step(spec, n_tokens, x_loc, lg_loc, wgu, wd, l2p, nrep):
     valid = oracle.valid_rows(counts, offs, rows)
     xg = oracle.dp_gather(xs, counts, offs, rows)
     lg = oracle.dp_gather(lgs, counts, offs, rows)
-    ids, w = oracle.route_topk(lg, spec.k, spec.renormalize, valid)
-    cnt, o, perm, inv = oracle.dispatch(ids, spec.E, spec.slots, l2p, nrep, spec.align)
+    ids, w = oracle.route_topk(lg, spec.k, spec.renormalize, valid, spec.n_shared)
+    cnt, o, perm, inv = oracle.dispatch(ids, spec.E + spec.n_shared, spec.slots, l2p, nrep,
+                                        spec.align)
     xsrt = oracle.permute_rows(xg, perm[: o[-1]])
     wall = time.perf_counter() - w0
     cpu = time.process_time() - c0
@@ -525,7 +535,7 @@ def main():
             "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
             "config": dict(synth.describe(spec), global_rows=r["rows"], l2=L2_NOTE, **r["extra"],
-                           boundary=args.boundary,
+                           boundary=args.boundary, shared_experts=spec.n_shared,
                            parallelism=f"{world} independent replica(s), one per GPU",
                            stage_ms={k: round(v, 4) for k, v in r["stage_ms"].items()}),
             "roofline": r["roof"],

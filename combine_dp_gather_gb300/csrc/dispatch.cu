@@ -241,13 +241,13 @@ __global__ void __launch_bounds__(32)
                             inv, status);
 }
 
-// Small problems (<= kSmallPairs routed pairs, E <= kSmallExperts) in one CTA:
+// Small problems (<= kSmallPairs routed pairs, tables within kSmallSmemBytes) in one CTA:
 // per-warp histograms, per-expert scan over warps, slot counts and aligned
 // offsets, then each warp ranks its own segment -- one launch instead of three.
 constexpr int kSmallWarps = 32;
 constexpr int kSmallSteps = 16;  // 32-pair steps per warp segment
 constexpr int64_t kSmallPairs = (int64_t)kSmallWarps * kSmallSteps * 32;
-constexpr int kSmallExperts = 256;
+constexpr size_t kSmallSmemBytes = 48 * 1024;  // per-warp histograms + slot tables
 
 __global__ void __launch_bounds__(kSmallWarps * 32)
     dispatch_small_kernel(const int32_t* __restrict__ ids, int64_t pairs, int k, int E, int P,
@@ -452,8 +452,10 @@ extern "C" moe_status moe_dispatch(const void* d_global, const int32_t* d_ids, i
   const int64_t pairs = rows * k;
   const int64_t chunks = n_chunks(pairs);
   int32_t* hist = static_cast<int32_t*>(d_ws);
-  if (pairs <= kSmallPairs && E <= kSmallExperts) {
-    const size_t smem = sizeof(int32_t) * ((size_t)kSmallWarps * E + (P + 1) + 2 * (size_t)P + E);
+  const size_t small_smem =
+      sizeof(int32_t) * ((size_t)kSmallWarps * E + (P + 1) + 2 * (size_t)P + E);
+  if (pairs <= kSmallPairs && small_smem <= kSmallSmemBytes) {
+    const size_t smem = small_smem;
     dispatch_small_kernel<<<1, kSmallWarps * 32, smem, s>>>(
         d_ids, pairs, k, E, P, d_l2p, d_nrep, X, align, cap, d_counts_P, d_offsets_P, d_perm,
         d_inv, d_status);

@@ -8,6 +8,11 @@
 // otherwise.  Rows past counts[r] inside replica r's segment are padding:
 // id -1, weight 0.
 //
+// Shared experts (vLLM chapter 27, section "共享专家: 在被让出的空档里干活": every
+// token also goes through them): expert E + s is listed after the k routed ids
+// of every real row with weight 1, so dispatch, the grouped FFN and combine
+// treat it as one more slot.
+//
 // Design: one warp per row.  Lane l holds experts l, l+32, ... (coalesced
 // 128-byte loads); k rounds of a warp arg-max on (logit desc, id asc) pick
 // the experts; lane j keeps the j-th pick; the weights use expf in float32
@@ -24,8 +29,10 @@ constexpr int kWarps = 8;
 template <int EPL>
 __global__ void __launch_bounds__(kWarps * 32)
     route_topk_kernel(const float* __restrict__ logits, int64_t rows, int E, int k, int renorm,
-                      const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
-                      int R, int32_t* __restrict__ ids, float* __restrict__ w, uint32_t* status) {
+                      int n_shared, const int32_t* __restrict__ counts,
+                      const int32_t* __restrict__ offsets, int R, int32_t* __restrict__ ids,
+                      float* __restrict__ w, uint32_t* status) {
+  const int kk = k + n_shared;  // row stride of ids / w
   __shared__ int32_t s_off[MOE_MAX_REPLICAS + 1];
   __shared__ int32_t s_cnt[MOE_MAX_REPLICAS];
   for (int i = threadIdx.x; i <= R; i += blockDim.x) {
@@ -46,9 +53,9 @@ __global__ void __launch_bounds__(kWarps * 32)
       c = seg;
     }
     if (!(i >= 0 && i < c)) {
-      if (lane < k) {
-        ids[g * k + lane] = -1;
-        w[g * k + lane] = 0.f;
+      if (lane < kk) {
+        ids[g * kk + lane] = -1;
+        w[g * kk + lane] = 0.f;
       }
       continue;
     }
@@ -106,21 +113,24 @@ __global__ void __launch_bounds__(kWarps * 32)
       denom = part;
     }
     if (lane < k) {
-      ids[g * k + lane] = my_id;
-      w[g * k + lane] = ex / denom;
+      ids[g * kk + lane] = my_id;
+      w[g * kk + lane] = ex / denom;
+    } else if (lane < kk) {  // shared experts: always selected, weight 1
+      ids[g * kk + lane] = E + (lane - k);
+      w[g * kk + lane] = 1.f;
     }
   }
 }
 
 template <int EPL>
-void launch_route(const float* logits, int64_t rows, int E, int k, int renorm,
+void launch_route(const float* logits, int64_t rows, int E, int k, int renorm, int n_shared,
                   const int32_t* counts, const int32_t* offsets, int R, int32_t* ids, float* w,
                   uint32_t* status, cudaStream_t s) {
   int64_t want = (rows + kWarps - 1) / kWarps;
   int64_t cap = (int64_t)num_sms() * 8;
   int grid = (int)(want < cap ? want : cap);
-  route_topk_kernel<EPL><<<grid, kWarps * 32, 0, s>>>(logits, rows, E, k, renorm, counts,
-                                                     offsets, R, ids, w, status);
+  route_topk_kernel<EPL><<<grid, kWarps * 32, 0, s>>>(logits, rows, E, k, renorm, n_shared,
+                                                     counts, offsets, R, ids, w, status);
 }
 
 }  // namespace
@@ -128,29 +138,40 @@ void launch_route(const float* logits, int64_t rows, int E, int k, int renorm,
 
 using namespace moe;
 
-extern "C" moe_status moe_route_topk(const float* d_logits, int64_t rows, int E, int k,
-                                     int renormalize, const int32_t* d_counts,
-                                     const int32_t* d_offsets, int R, int32_t* d_ids, float* d_w,
-                                     uint32_t* d_status, void* stream) {
+extern "C" moe_status moe_route_topk_shared(const float* d_logits, int64_t rows, int E, int k,
+                                            int renormalize, int n_shared,
+                                            const int32_t* d_counts, const int32_t* d_offsets,
+                                            int R, int32_t* d_ids, float* d_w, uint32_t* d_status,
+                                            void* stream) {
   if (rows < 0 || rows > INT32_MAX || R < 1 || R > MOE_MAX_REPLICAS) return MOE_ERR_INVALID_ARG;
-  if (E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E || k > MOE_MAX_TOPK)
+  if (E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E || n_shared < 0 ||
+      k + n_shared > MOE_MAX_TOPK)
     return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
   if (d_logits == nullptr || d_counts == nullptr || d_offsets == nullptr || d_ids == nullptr ||
       d_w == nullptr)
     return MOE_ERR_INVALID_ARG;
   cudaStream_t s = as_stream(stream);
+  const int ns = n_shared;
   if (E <= 32)
-    launch_route<1>(d_logits, rows, E, k, renormalize, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+    launch_route<1>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
   else if (E <= 64)
-    launch_route<2>(d_logits, rows, E, k, renormalize, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+    launch_route<2>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
   else if (E <= 128)
-    launch_route<4>(d_logits, rows, E, k, renormalize, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+    launch_route<4>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
   else if (E <= 256)
-    launch_route<8>(d_logits, rows, E, k, renormalize, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+    launch_route<8>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
   else if (E <= 512)
-    launch_route<16>(d_logits, rows, E, k, renormalize, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+    launch_route<16>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
   else
-    launch_route<32>(d_logits, rows, E, k, renormalize, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+    launch_route<32>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
   return launch_status();
+}
+
+extern "C" moe_status moe_route_topk(const float* d_logits, int64_t rows, int E, int k,
+                                     int renormalize, const int32_t* d_counts,
+                                     const int32_t* d_offsets, int R, int32_t* d_ids, float* d_w,
+                                     uint32_t* d_status, void* stream) {
+  return moe_route_topk_shared(d_logits, rows, E, k, renormalize, 0, d_counts, d_offsets, R,
+                               d_ids, d_w, d_status, stream);
 }

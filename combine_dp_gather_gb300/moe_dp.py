@@ -50,6 +50,7 @@ _SIGS = {
                              _P]),
     "moe_combine": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I64, _P, _P, _P]),
     "moe_dp_scatter": (_I, [_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P]),
+    "moe_route_topk_shared": (_I, [_P, _I64, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]),
     "moe_dp_gather_add_rmsnorm": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _I, _I64, _I, _I, _P,
                                        _P, _P]),
     "moe_dispatch_noalloc": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _I, _I, _I64, _P,
@@ -186,8 +187,17 @@ def moe_dp_gather_add_rmsnorm(local_hidden: Sequence[torch.Tensor],
 
 
 def moe_route_topk(logits: torch.Tensor, k: int, renormalize: bool, d_counts, d_offsets,
-                   ids: torch.Tensor, w: torch.Tensor, d_status=None, stream=None):
+                   ids: torch.Tensor, w: torch.Tensor, d_status=None, stream=None,
+                   n_shared: int = 0):
+    """Top-k routing; n_shared > 0 appends the shared experts (weight 1) to every
+    real row (ids / w then have k + n_shared columns)."""
     rows, E = logits.shape
+    if n_shared:
+        _check("moe_route_topk_shared", lib().moe_route_topk_shared(
+            _ptr(logits), rows, E, k, int(renormalize), n_shared, _ptr(d_counts),
+            _ptr(d_offsets), d_counts.numel(), _ptr(ids), _ptr(w), _ptr(d_status),
+            _stream(stream)))
+        return
     _check("moe_route_topk", lib().moe_route_topk(
         _ptr(logits), rows, E, k, int(renormalize), _ptr(d_counts), _ptr(d_offsets),
         d_counts.numel(), _ptr(ids), _ptr(w), _ptr(d_status), _stream(stream)))
@@ -265,7 +275,8 @@ class MoeLayer:
                  static_bound: int = 0, tokens_per_req: int = 1, renormalize: bool = True,
                  align: int = 1, l2p: Optional[torch.Tensor] = None,
                  nrep: Optional[torch.Tensor] = None, slot_range=None,
-                 norm_gamma: Optional[torch.Tensor] = None, norm_eps: float = 1e-6):
+                 norm_gamma: Optional[torch.Tensor] = None, norm_eps: float = 1e-6,
+                 n_shared: int = 0):
         dev = w_gate_up.device
         self.R, self.H, self.E, self.k, self.I = R, H, E, k, I
         self.P = w_gate_up.shape[0]
@@ -275,8 +286,11 @@ class MoeLayer:
         self.wgu, self.wd, self.l2p, self.nrep = w_gate_up, w_down, l2p, nrep
         self.slot_range = slot_range or (0, self.P)
         self.norm_gamma, self.norm_eps = norm_gamma, norm_eps
+        # shared experts: logical ids E .. E+n_shared-1, the last slots of the weights
+        self.n_shared = n_shared
+        self.kk = k + n_shared
         self.max_rows = max_rows
-        self.cap = moe_dispatch_cap_bound(max_rows, k, self.P, align)
+        self.cap = moe_dispatch_cap_bound(max_rows, k + n_shared, self.P, align)
         i32 = dict(device=dev, dtype=torch.int32)
         self.d_counts = torch.zeros(R, **i32)
         self.d_offsets = torch.zeros(R + 1, **i32)
@@ -291,16 +305,17 @@ class MoeLayer:
         self.status = torch.zeros(1, **i32)
         self.xg = torch.empty(max_rows, H, device=dev, dtype=self.dtype)
         self.logits_g = torch.empty(max_rows, E, device=dev, dtype=torch.float32)
-        self.ids = torch.empty(max_rows, k, **i32)
-        self.w = torch.empty(max_rows, k, device=dev, dtype=torch.float32)
+        self.ids = torch.empty(max_rows, self.kk, **i32)
+        self.w = torch.empty(max_rows, self.kk, device=dev, dtype=torch.float32)
         self.counts_P = torch.empty(self.P, **i32)
         self.offsets_P = torch.empty(self.P + 1, **i32)
         self.perm = torch.empty(self.cap, **i32)
-        self.inv = torch.empty(max_rows, k, **i32)
+        self.inv = torch.empty(max_rows, self.kk, **i32)
         self.xs = torch.empty(self.cap, H, device=dev, dtype=self.dtype)
         self.ys = torch.empty(self.cap, H, device=dev, dtype=self.dtype)
         self.yg = torch.empty(max_rows, H, device=dev, dtype=self.dtype)
-        self.ws_dispatch = torch.empty(max(moe_dispatch_ws_bytes(max_rows, k, E), 16),
+        self.ws_dispatch = torch.empty(max(moe_dispatch_ws_bytes(max_rows, self.kk,
+                                                                 E + n_shared), 16),
                                        device=dev, dtype=torch.uint8)
         self.ws_ffn = torch.empty(max(moe_grouped_ffn_ws_bytes(self.cap, I, self.dtype), 16),
                                   device=dev, dtype=torch.uint8)
@@ -349,9 +364,9 @@ class MoeLayer:
         moe_dp_gather(local_logits, self.d_counts, self.d_offsets, lg, st, stream)
         ev("gather")
         moe_route_topk(lg, self.k, self.renormalize, self.d_counts, self.d_offsets, ids, w, st,
-                       stream)
+                       stream, n_shared=self.n_shared)
         ev("route")
-        moe_dispatch(xg, ids, self.E, self.P, self.counts_P, self.offsets_P, self.perm, inv,
+        moe_dispatch(xg, ids, self.E + self.n_shared, self.P, self.counts_P, self.offsets_P, self.perm, inv,
                      self.xs, self.ws_dispatch, self.l2p, self.nrep, self.align, st, stream)
         ev("dispatch")
         moe_grouped_ffn(self.xs, self.offsets_P, self.wgu, self.wd, self.ys, self.ws_ffn,

@@ -55,6 +55,7 @@ class LayerSpec:
     align: int = 1
     seed: int = 0
     w_std: float = 0.02
+    n_shared: int = 0          # shared experts (logical ids E .. E + n_shared - 1)
 
     @property
     def R(self) -> int:
@@ -66,7 +67,8 @@ class LayerSpec:
 
     @property
     def slots(self) -> int:
-        return self.P if self.P is not None else self.E
+        """Physical slots, shared experts included (they are the last slots)."""
+        return (self.P if self.P is not None else self.E) + self.n_shared
 
 
 # ------------------------------------------------------------------ specs
@@ -175,11 +177,17 @@ def expert_weights(spec: LayerSpec, slot_to_logical: Optional[np.ndarray] = None
     """Slot weights wgu [P, 2I, H] and wd [P, H, I]; slot s holds the weights of
     logical expert slot_to_logical[s] (identity without a map)."""
     P = spec.slots
-    s2l = np.arange(P) % spec.E if slot_to_logical is None else np.asarray(slot_to_logical)
+    if slot_to_logical is None:
+        s2l = np.arange(P) % spec.E
+    else:
+        s2l = np.asarray(slot_to_logical)
+    if spec.n_shared:  # shared expert s sits in slot P - n_shared + s
+        s2l = np.concatenate([s2l[: P - spec.n_shared],
+                              spec.E + np.arange(spec.n_shared)])
     dt = torch_dtype(spec.dtype)
     wgu = torch.empty(P, 2 * spec.I, spec.H, device=device, dtype=dt)
     wd = torch.empty(P, spec.H, spec.I, device=device, dtype=dt)
-    for e in range(spec.E):
+    for e in range(spec.E + spec.n_shared):
         slots = np.nonzero(s2l == e)[0]
         if len(slots) == 0:
             continue

@@ -185,6 +185,19 @@ moe_status moe_route_topk(const float* d_logits, int64_t rows, int E, int k, int
                           const int32_t* d_counts, const int32_t* d_offsets, int R,
                           int32_t* d_ids, float* d_w, uint32_t* d_status, void* stream);
 
+/* moe_route_topk plus n_shared shared experts.  [P2] section "共享专家: 在被让出的
+ * 空档里干活": a shared expert's input bypasses routing and its output is added
+ * to the routed mixture.  Every real row lists its k routed ids followed by
+ * the shared experts E .. E + n_shared - 1 with weight 1; pad rows get -1 / 0
+ * in all k + n_shared columns.  d_ids and d_w are [rows, k + n_shared];
+ * k + n_shared <= MOE_MAX_TOPK.  Dispatch then runs over E + n_shared logical
+ * experts, the weights hold the shared experts as the last slots, and combine
+ * adds them with weight 1. */
+moe_status moe_route_topk_shared(const float* d_logits, int64_t rows, int E, int k,
+                                 int renormalize, int n_shared, const int32_t* d_counts,
+                                 const int32_t* d_offsets, int R, int32_t* d_ids, float* d_w,
+                                 uint32_t* d_status, void* stream);
+
 /* Dispatch: stable sort of the routed (row, j) pairs by physical expert slot.
  * [P1] section "normal dispatch 的调用链" (get_dispatch_layout: tokens per
  * expert; expert_alignment rounds each expert's count up to a multiple of

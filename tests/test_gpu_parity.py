@@ -151,11 +151,12 @@ def _distinct_ids(rows, k, E, seed, pad_every=7):
 @pytest.mark.parametrize("rows,E,use_map,align", [
     (3001, 64, False, 1), (3001, 64, False, 128), (3001, 64, True, 1), (3001, 64, True, 4),
     (500, 64, False, 1), (500, 64, True, 4), (1900, 256, True, 1), (2048, 256, False, 1),
-    (8192, 256, False, 1), (9001, 64, True, 4), (2047, 300, False, 1), (1, 64, False, 1)])
+    (8192, 256, False, 1), (9001, 64, True, 4), (2047, 300, False, 1), (2047, 400, False, 1),
+    (1, 64, False, 1)])
 def test_dispatch_bitexact(md, orc, rows, E, use_map, align):
-    """rows x 8 pairs: <= 16384 with E <= 256 runs the one-CTA path (2048 rows is
-    exactly the limit); more pairs (3001 rows: 24 chunks of 1024 + a ragged tail) or
-    E > 256 run the chunked histogram / scan / rank path."""
+    """rows x 8 pairs: <= 16384 whose per-warp tables fit 48 KB (E <= ~340) runs the
+    one-CTA path (2048 rows is exactly the pair limit); more pairs (3001 rows: 24 chunks
+    of 1024 + a ragged tail) or E = 400 run the chunked histogram / scan / rank path."""
     k, H = 8, 512
     l2p = nrep = None
     P = E
@@ -199,7 +200,7 @@ def test_dispatch_zero_rows(md):
     assert not counts_P.any() and not offsets_P.any()
 
 
-@pytest.mark.parametrize("E", [16, 300])                 # one-CTA path, chunked path
+@pytest.mark.parametrize("E", [16, 400])                 # one-CTA path, chunked path
 def test_dispatch_device_errors_flag_without_fault(md, E):
     rows, k, H = 200, 4, 64
     ids = _distinct_ids(rows, k, E, seed=3, pad_every=1000)
@@ -383,7 +384,8 @@ def _layer_gpu(md, spec, l2p_np=None, nrep_np=None, p2l=None, ranges=None):
     layer = md.MoeLayer(R=spec.R, H=spec.H, E=spec.E, k=spec.k, I=spec.I, w_gate_up=wgu,
                         w_down=wd, max_rows=max(rows, 1), mode=spec.mode,
                         static_bound=spec.static_bound, tokens_per_req=spec.tokens_per_req,
-                        renormalize=spec.renormalize, align=spec.align, l2p=l2p, nrep=nrep)
+                        renormalize=spec.renormalize, align=spec.align, l2p=l2p, nrep=nrep,
+                        n_shared=spec.n_shared)
     out = [torch.empty(c, spec.H, device=DEV, dtype=wgu.dtype) for c in spec.counts]
     layer.forward(x_loc, lg_loc, out, counts=spec.counts)
     if ranges is not None:          # re-run the FFN as one call per simulated EP rank
@@ -408,13 +410,15 @@ def _check_layer(md, orc, spec, layer, out, x_loc, lg_loc, wgu, wd, offs, rows, 
     xg_o = orc.dp_gather(x_bits, spec.counts, offs_o, rows_o)
     assert np.array_equal(to_np(layer.xg[:rows]), xg_o)
     lg_o = orc.dp_gather([to_np(t) for t in lg_loc], spec.counts, offs_o, rows_o)
-    ids_o, w_o = orc.route_topk(lg_o, spec.k, spec.renormalize, valid)
+    ids_o, w_o = orc.route_topk(lg_o, spec.k, spec.renormalize, valid, spec.n_shared)
+    kk = spec.k + spec.n_shared
     assert np.array_equal(to_np(layer.ids[:rows]), ids_o)
     assert_close(to_np(layer.w[:rows]), w_o, W_ATOL, W_RTOL, "route weights")
     P = layer.P
-    c_o, o_o, p_o, i_o = orc.dispatch(ids_o, spec.E, P, l2p, nrep, spec.align, layer.cap)
+    c_o, o_o, p_o, i_o = orc.dispatch(ids_o, spec.E + spec.n_shared, P, l2p, nrep, spec.align,
+                                      layer.cap)
     n = int(o_o[-1])
-    assert int(c_o.sum()) == spec.T * spec.k
+    assert int(c_o.sum()) == spec.T * kk
     assert n == int(sum((int(c) + spec.align - 1) // spec.align * spec.align for c in c_o))
     assert np.array_equal(to_np(layer.counts_P), c_o)
     assert np.array_equal(to_np(layer.offsets_P), o_o)
@@ -432,7 +436,7 @@ def _check_layer(md, orc, spec, layer, out, x_loc, lg_loc, wgu, wd, offs, rows, 
     slot_of = np.searchsorted(o_o, np.arange(n), side="right") - 1
     need = {}
     for g in toks:
-        for j in range(spec.k):
+        for j in range(kk):
             need.setdefault(int(slot_of[i_o[g, j]]), []).append((int(g), j))
     y_ref = {}
     for s, pairs in need.items():
@@ -445,7 +449,7 @@ def _check_layer(md, orc, spec, layer, out, x_loc, lg_loc, wgu, wd, offs, rows, 
     worst = 0.0
     for g in toks:
         ref = np.zeros(spec.H)
-        for j in range(spec.k):
+        for j in range(kk):
             y = y_ref[(int(g), j)]
             worst = max(worst, assert_close(ys_gpu[int(i_o[g, j])], y, atol, rtol,
                                             f"expert out row {g} j {j}"))
@@ -470,6 +474,21 @@ def test_layer_tiny_bf16_all_rows(md, orc, mode):
                            dtype="bf16", w_std=0.05, zipf_s=1.1)
     res = _layer_gpu(md, spec)
     _check_layer(md, orc, spec, *res)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_layer_shared_expert_all_rows(md, orc, mode):
+    spec = synth.LayerSpec("tiny_shared", [16, 0, 140, 8, 1], mode, H=512, E=16, k=4, I=256,
+                           dtype="bf16", w_std=0.05, zipf_s=1.1, n_shared=1)
+    res = _layer_gpu(md, spec)
+    _check_layer(md, orc, spec, *res)
+
+
+def test_layer_dsv3_decode_with_shared_expert(md, orc):
+    spec = synth.spec_decode(seed=1)
+    spec.n_shared = 1
+    res = _layer_gpu(md, spec)
+    _check_layer(md, orc, spec, *res, sample=6)
 
 
 def test_layer_dsv3_decode_full_size(md, orc):
