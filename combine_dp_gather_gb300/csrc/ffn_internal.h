@@ -23,6 +23,9 @@ struct FfnArgs {
 
 // bf16 operands on the tcgen05 tensor cores (TMA-fed, TMEM accumulators).
 moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s);
+// The same with the weights as the MMA's M operand and tokens as N, on pairs
+// of SMs (many tokens per slot).
+moe_status launch_ffn_tc_swap(const FfnArgs& a, cudaStream_t s);
 // float32 on the CUDA cores.
 moe_status launch_ffn_simt_f32(const FfnArgs& a, cudaStream_t s);
 

@@ -48,16 +48,16 @@
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets
 // MOE_DEV_TIMEOUT, the other roles stop at their next wait, TMEM is freed and
 // the kernel returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <mutex>
 
 #include "common.cuh"
 #include "ffn_internal.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
+
+using namespace tc;
 
 // The pair kernel (CL = 2) needs a full 256-row group per unit to pay off;
 // below this many rows per slot on average the single-SM kernel (CL = 1)
@@ -66,6 +66,9 @@ namespace {
 #define MOE_FFN_PAIR_ROWS 192
 #endif
 constexpr int64_t kPairRowsPerSlot = MOE_FFN_PAIR_ROWS;
+#ifndef MOE_FFN_SWAP
+#define MOE_FFN_SWAP 1
+#endif
 
 constexpr int BM = 128;  // rows per CTA
 constexpr int BN = 256;  // accumulator columns
@@ -73,8 +76,6 @@ constexpr int BK = 64;   // 64 bf16 = 128 bytes = one swizzle row
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BOX_BYTES = 128 * BK * 2;  // one 64 x 128 TMA box
 constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
 template <int CL>
 struct Cfg {
@@ -82,9 +83,7 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = CL == 2 ? 6 : 4;
   static constexpr int M = BM * CL;
-  // instruction descriptor, kind::f16: D f32, A bf16, B bf16, both K-major
-  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
-                                    ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+  static constexpr uint32_t IDESC = idesc_bf16(M, BN);
 };
 
 constexpr int MAX_STAGES = 6;
@@ -134,195 +133,6 @@ struct TcParams {
   __nv_bfloat16* out;
   uint32_t* status;
 };
-
-// ------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Address of the same shared variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-// All threads of every CTA of the cluster; release/acquire at cluster scope.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-// Arrive on an mbarrier given by its shared::cluster address (own or peer CTA).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait; the whole warp calls it and gets one warp-uniform answer.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag,
-                                         uint32_t* status) {
-  bool ok = mbar_try_wait(bar, parity);
-  if (!ok) {
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-      if (mbar_try_wait(bar, parity)) {
-        ok = true;
-        break;
-      }
-      if ((it & 63u) == 0) {
-        if (*abort_flag) break;
-        if (globaltimer_ns() - t0 > kTimeoutNs) {
-          flag(status, MOE_DEV_TIMEOUT);
-          *abort_flag = 1;
-          break;
-        }
-      }
-    }
-  }
-  return __all_sync(0xffffffffu, ok);
-}
-// TMA 2-D tile load into this CTA's shared memory, completion on an mbarrier of
-// this CTA (CL == 1) or of the leader CTA of the pair (CL == 2, cluster address).
-template <int CL>
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t c0,
-                                            int32_t c1, uint32_t bar, uint64_t policy) {
-  if constexpr (CL == 1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
-        : "memory");
-  } else {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".cta_group::2.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
-        : "memory");
-  }
-}
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-template <int CL>
-__device__ __forceinline__ void tmem_alloc(uint32_t dst) {
-  if constexpr (CL == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  } else {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-  }
-}
-template <int CL>
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr) {
-  if constexpr (CL == 1)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
-                 "r"(TMEM_COLS)
-                 : "memory");
-  else
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
-                 "r"(TMEM_COLS)
-                 : "memory");
-}
-// Arrive on `bar` (same offset in every CTA of the pair) once all MMAs issued
-// so far by this thread have completed.
-template <int CL>
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  if constexpr (CL == 1)
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-  else
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"((uint16_t)3)
-        : "memory");
-}
-template <int CL>
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t accumulate) {
-  if constexpr (CL == 1)
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(Cfg<1>::IDESC), "r"(accumulate)
-        : "memory");
-  else
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(Cfg<2>::IDESC), "r"(accumulate)
-        : "memory");
-}
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
-// groups 1024 bytes apart (SBO), descriptor version 1.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;              // LBO (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;    // SBO
-  d |= (uint64_t)1 << 46;              // version
-  d |= (uint64_t)2 << 61;              // SWIZZLE_128B
-  return d;
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 
 // Work unit u -> (slot, m-group, n-tile) through the prefix over the slot range.
 // An m-group is CL consecutive 128-row m-tiles (one per CTA of the cluster).
@@ -425,12 +235,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       L.pref[p.nslots] = tot;
       L.total_units = tot;
     }
-    tc_fence_before();
+    fence_before();
     if (CL > 1)
       cluster_sync();  // the leader's barriers exist before the peer signals them
     else
       __syncthreads();
-    tc_fence_after();
+    fence_after();
   }
   const int total = L.total_units;
   const uint32_t tmem_base = L.tmem_base;
@@ -489,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int u = cid; u < total; u += ncl, ++local_tile) {
         const uint32_t acc = local_tile & 1u, acc_ph = (local_tile >> 1) & 1u;
         if (!wait_bar(smem_u32(&L.tmem_empty[acc]), acc_ph ^ 1u, abort_flag, p.status)) break;
-        tc_fence_after();
+        fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         bool ok = true;
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
@@ -498,20 +308,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          tc_fence_after();
+          fence_after();
           if (lane == 0) {
             const uint32_t sa = smem_u32(stage_base + (size_t)st * C::STAGE_BYTES);
             const uint64_t adesc = sw128_desc(sa);
             const uint64_t bdesc = sw128_desc(sa + A_BYTES);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes per K=16 step in the swizzle row
-              tc_mma<CL>(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, (kb | kk) != 0);
-            tc_commit<CL>(smem_u32(&L.empty[st]));
+              mma<CL>(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, C::IDESC, (kb | kk) != 0);
+            commit<CL>(smem_u32(&L.empty[st]));
           }
           __syncwarp();
         }
         if (!ok) break;
-        if (lane == 0) tc_commit<CL>(smem_u32(&L.tmem_full[acc]));
+        if (lane == 0) commit<CL>(smem_u32(&L.tmem_full[acc]));
         __syncwarp();
       }
     }
@@ -526,7 +336,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t row_end = L.row_end[un.slot];
       const uint32_t acc = local_tile & 1u, acc_ph = (local_tile >> 1) & 1u;
       if (!wait_bar(smem_u32(&L.tmem_full[acc]), acc_ph, abort_flag, p.status)) break;
-      tc_fence_after();
+      fence_after();
       const int64_t row = row0 + row_in_tile;
       const bool valid = row < row_end && row < p.cap;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
@@ -572,7 +382,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      tc_fence_before();
+      fence_before();
       __syncwarp();
       if (lane == 0) {
         const uint32_t bar = smem_u32(&L.tmem_empty[acc]);
@@ -584,46 +394,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
 
-  tc_fence_before();
+  fence_before();
   // No CTA may leave while its peer can still signal its barriers or read its
   // shared memory through the pair MMA.
   if (CL > 1)
     cluster_sync();
   else
     __syncthreads();
-  tc_fence_after();
+  fence_after();
   if (warp == 1) tmem_dealloc<CL>(tmem_base);
 }
 
 // ------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// 2-D bf16 tensor [outer, inner] row-major, box 64 x 128, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BK, 128};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int CL>
 cudaLaunchConfig_t launch_cfg(int clusters, cudaStream_t s, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
@@ -727,15 +509,18 @@ moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   const int nslots = a.slot_hi - a.slot_lo;
   if (nslots <= 0 || a.cap <= 0) return MOE_OK;
   CUtensorMap mA1, mB1, mA2, mB2;
-  if (!make_map(&mA1, a.xs, (uint64_t)a.H, (uint64_t)a.cap) ||
-      !make_map(&mB1, a.wgu, (uint64_t)a.H, (uint64_t)a.P * 2 * a.I) ||
-      !make_map(&mA2, a.h, (uint64_t)a.I, (uint64_t)a.cap) ||
-      !make_map(&mB2, a.wd, (uint64_t)a.I, (uint64_t)a.P * a.H))
+  if (!make_map(&mA1, a.xs, (uint64_t)a.H, (uint64_t)a.cap, 128) ||
+      !make_map(&mB1, a.wgu, (uint64_t)a.H, (uint64_t)a.P * 2 * a.I, 128) ||
+      !make_map(&mA2, a.h, (uint64_t)a.I, (uint64_t)a.cap, 128) ||
+      !make_map(&mB2, a.wd, (uint64_t)a.I, (uint64_t)a.P * a.H, 128))
     return MOE_ERR_CUDA;
   // rows per slot the sorted buffer can hold on average, over the whole layer
   const int64_t rows_per_slot = a.cap / (a.P > 0 ? a.P : 1);
   moe_status st;
   if (rows_per_slot >= kPairRowsPerSlot) {
+#if MOE_FFN_SWAP
+    return launch_ffn_tc_swap(a, s);
+#endif
     // pair groups on two SMs, then each slot's short remainder on one SM
     if ((st = run_ffn<2>(a, mA1, mB1, kPairGroups, true, s)) != MOE_OK) return st;
     if ((st = run_ffn<1>(a, mA1, mB1, kTailRows, true, s)) != MOE_OK) return st;

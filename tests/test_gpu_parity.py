@@ -260,10 +260,13 @@ def test_grouped_ffn_bf16_tcgen05(md, orc, counts):
 
 @pytest.mark.parametrize("counts,lo,hi", [([300, 0, 257, 129, 512, 1], 0, 6),
                                            ([256, 255, 0, 385, 200, 640], 1, 5),
-                                           ([1000, 0, 0, 3], 0, 4)])
+                                           ([1000, 0, 0, 3], 0, 4),
+                                           ([15, 33, 255, 321, 641, 240, 48, 272], 0, 8)])
 def test_grouped_ffn_bf16_pair_kernel(md, orc, counts, lo, hi):
-    """>= 192 rows per slot on average selects the two-SM (cta_group::2) kernel:
-    ragged groups, odd m-tile counts, empty slots and slot ranges."""
+    """>= 192 rows per slot on average selects the two-SM (cta_group::2) kernel with the
+    weights as M and a slot's tokens as N: token groups of up to 320 (one MMA of N <= 256,
+    or 256 plus 16..64), ragged widths rounded up to 16, several groups per slot, empty
+    slots and slot ranges."""
     H, I = 512, 256
     offsets, cap, xs, wgu, wd = _ffn_inputs(counts, H, I, torch.bfloat16, seed=len(counts) + lo,
                                             extra_rows=40)
