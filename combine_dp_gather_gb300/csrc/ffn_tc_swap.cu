@@ -23,12 +23,14 @@
 //
 //   MM1 + SwiGLU: CTA c of the pair holds gate rows f+64c .. f+64c+63 and the
 //                 up rows of the same features (A, 128 rows, one 3-D box over
-//                 [slot, gate|up, row, k]); TMEM lanes 0-63 hold gate, 64-127 up.  Epilogue warps of lanes q and q+2
-//                 trade one 32-token chunk through shared memory, each
-//                 computes h = silu(gate) * up for every other chunk.
+//                 [slot, gate|up, row, k]); TMEM lanes 0-63 hold gate, 64-127
+//                 up.  The epilogue warps of lanes q and q+2 trade one
+//                 32-column chunk through shared memory and each computes
+//                 h = silu(gate) * up for one of the two chunks.
 //   MM2:          CTA c holds down-projection rows f+128c .. f+128c+127.
 // The epilogue stages each 32-token x 32-feature block through shared memory
-// and writes token rows with 16-byte stores (h and ys stay [tokens, features]).
+// (in a hand-over buffer already read) and writes token rows with 16-byte
+// stores (h and ys stay [tokens, features]).
 //
 // TMEM holds two 256-column fp32 accumulators per SM.  A unit of N <= 256
 // tokens takes one (the next unit's MMAs overlap its epilogue), a unit of
@@ -36,13 +38,14 @@
 // read it.  Token rows past the slot's end are computed from whatever follows
 // and never stored; rows past the buffer read as zero.
 //
-// Roles (192 threads, one CTA per SM, clusters of two):
+// Roles (320 threads, one CTA per SM, clusters of two):
 //   warp 0    TMA producer (both CTAs): one weight box (128 rows) and one
 //             token box (N/2 rows) per stage, completion on the leader CTA's
 //             "full" barrier; 5-stage ring
 //   warp 1    TMEM allocation; in the leader CTA lane 0 issues the MMAs
 //             (cta_group::2, bf16 -> fp32) and the commits, multicast to both
-//   warps 2-5 epilogue (both CTAs)
+//   warps 2-9 epilogue (both CTAs): two warps per TMEM lane quarter take
+//             alternate chunks (MM2) or chunk pairs (MM1)
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets
 // MOE_DEV_TIMEOUT, the other roles stop at their next wait, TMEM is freed and
 // the kernel returns.
@@ -64,11 +67,10 @@ constexpr int B_ROWS = NMAX / 2;                // token rows per CTA
 constexpr int B_BYTES = B_ROWS * BK * 2;        // 20 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 36 KB
 constexpr int STAGES = 5;
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;
 constexpr int ACC_COLS = 256;                   // one accumulator buffer
-constexpr int EPI_WARPS = 4;
+constexpr int EPI_WARPS = 8;                    // two per TMEM lane quarter
 constexpr int XCH_BYTES = 32 * 32 * 4;          // per epilogue warp: 32 lanes x 32 fp32
-constexpr int STG_BYTES = 32 * 32 * 2;          // per epilogue warp: 32 tokens x 32 bf16
 constexpr int NUM_BOXES = B_ROWS / 8;           // token boxes of 8, 16, ..., 160 rows
 
 struct Maps {
@@ -104,7 +106,7 @@ struct SmemLayout {
   int32_t row0[MOE_MAX_SLOTS];      // first sorted row of the slot
   int32_t rows[MOE_MAX_SLOTS];      // tokens of the slot
 };
-constexpr size_t kEpiBytes = (size_t)EPI_WARPS * (XCH_BYTES + STG_BYTES);
+constexpr size_t kEpiBytes = (size_t)EPI_WARPS * XCH_BYTES;
 constexpr size_t smem_bytes() {
   return 1024 + (size_t)STAGES * STAGE_BYTES + kEpiBytes + sizeof(SmemLayout);
 }
@@ -166,10 +168,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* stage_base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   float* xch = reinterpret_cast<float*>(stage_base + (size_t)STAGES * STAGE_BYTES);
-  __nv_bfloat16* stg =
-      reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(xch) + EPI_WARPS * XCH_BYTES);
-  SmemLayout& L = *reinterpret_cast<SmemLayout*>(reinterpret_cast<uint8_t*>(stg) +
-                                                 EPI_WARPS * STG_BYTES);
+  SmemLayout& L = *reinterpret_cast<SmemLayout*>(reinterpret_cast<uint8_t*>(xch) + kEpiBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();
   const bool leader = crank == 0;
@@ -335,10 +334,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lanes this warp may read: 32q .. 32q+31
-    float* xmine = xch + q * (XCH_BYTES / 4);
-    const float* xpeer = xch + (q ^ 2) * (XCH_BYTES / 4);
-    __nv_bfloat16* wstg = stg + q * (STG_BYTES / 2);
+    const int q = warp & 3;            // TMEM lanes this warp may read: 32q .. 32q+31
+    const int grp = (warp - 2) >> 2;   // two warps per lane quarter take alternate chunks
+    const int e = grp * 4 + q, e_peer = grp * 4 + (q ^ 2);
+    float* xmine = xch + e * (XCH_BYTES / 4);
+    float* xpeer = xch + e_peer * (XCH_BYTES / 4);
+    const uint32_t bar_id = 1u + (uint32_t)(q & 1) + 2u * (uint32_t)grp;  // lanes q and q ^ 2
     uint32_t bseq = 0;
     for (int u = cid; u < total; u += ncl) {
       const SUnit un = decode_unit(L, p.nslots, u);
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         ok = wait_bar(smem_u32(&L.tmem_full[buf1]), ((bseq + 1) >> 1) & 1u, abort_flag, p.status);
       // the gate and up warps of a feature range leave together, or the one
       // still in the chunk loop would wait for its partner forever
-      if (SWIGLU) ok = named_all(1u + (uint32_t)(q & 1), 64, ok);
+      if (SWIGLU) ok = named_all(bar_id, 64, ok);
       if (!ok) break;
       fence_after();
       const uint32_t lanes = tmem_base + ((uint32_t)(q * 32) << 16);
@@ -360,18 +361,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       auto chunk_addr = [&](int c) {
         return lanes + (c < nch0 ? buf0 : buf1) * ACC_COLS + (uint32_t)chunk_col(c);
       };
-      // buffer 0 goes back to the MMA issuer as soon as its last chunk is in registers
+      // buffer 0 goes back to the MMA issuer once this warp has no chunk of it left
       bool freed0 = false;
-      auto free_buf0 = [&](int last_loaded) {
-        if (nbuf == 2 && !freed0 && last_loaded >= nch0 - 1) {
+      auto free_buf0 = [&](int next_chunk) {
+        if (nbuf == 2 && !freed0 && next_chunk >= nch0) {
           freed0 = true;
           fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&L.tmem_empty[buf0]), 0));
         }
       };
-      // 32 columns x 32 features of this warp -> token rows of `out`, 16-byte stores
-      auto store_block = [&](const float (&v)[32], int c, int feat) {
+      // 32 columns x 32 features of this warp -> token rows of `out`, 16-byte
+      // stores through a staging tile (`wstg`, a hand-over buffer no longer read)
+      auto store_block = [&](const float (&v)[32], int c, int feat, __nv_bfloat16* wstg) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) wstg[j * 32 + lane] = __float2bfloat16_rn(v[j]);
         __syncwarp();
@@ -390,15 +392,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (SWIGLU) {
         const bool is_gate = q < 2;
         const int feat = un.tile * 128 + (int)crank * 64 + (q & 1) * 32;
-        const uint32_t bar_id = 1u + (uint32_t)(q & 1);  // the warps of lanes q and q ^ 2
 #pragma unroll 1
-        for (int c = 0; c < nch; c += 2) {
+        for (int c = 2 * grp; c < nch; c += 4) {
           const bool has2 = c + 1 < nch;
           uint32_t v0[32], v1[32];
           tmem_ld32(chunk_addr(c), v0);
           if (has2) tmem_ld32(chunk_addr(c + 1), v1);
           tmem_wait_ld();
-          free_buf0(has2 ? c + 1 : c);
+          free_buf0(c + 4);
           // the gate warp computes chunk c, the up warp chunk c + 1; each hands
           // the other the values it lacks
           if (is_gate) {
@@ -418,24 +419,25 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = 0; j < 32; ++j) {
               const float g = is_gate ? __uint_as_float(v0[j]) : xpeer[j * 32 + lane];
               const float up = is_gate ? xpeer[j * 32 + lane] : __uint_as_float(v1[j]);
-              hv[j] = g / (1.0f + expf(-g)) * up;
+              hv[j] = __fdividef(g, 1.0f + __expf(-g)) * up;
             }
-            store_block(hv, cc, feat);
+            // the partner's hand-over is in registers now: stage there
+            store_block(hv, cc, feat, reinterpret_cast<__nv_bfloat16*>(xpeer));
           }
           named_sync(bar_id, 64);  // the partner has read this warp's hand-over
         }
       } else {
         const int feat = un.tile * 256 + (int)crank * 128 + q * 32;
 #pragma unroll 1
-        for (int c = 0; c < nch; ++c) {
+        for (int c = grp; c < nch; c += 2) {
           uint32_t v[32];
           tmem_ld32(chunk_addr(c), v);
           tmem_wait_ld();
-          free_buf0(c);
+          free_buf0(c + 2);
           float y[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(v[j]);
-          store_block(y, c, feat);
+          store_block(y, c, feat, reinterpret_cast<__nv_bfloat16*>(xmine));
         }
       }
       fence_before();
