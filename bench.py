@@ -46,17 +46,34 @@ def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int) -
     """Kernel launches of one layer step: gather (hidden states and logits), route,
     dispatch (one CTA-wide kernel for <= 16384 routed pairs whose tables fit 48 KB, else
     histogram + scan + rank; then the row copy; + the alignment pad kernel when
-    align > 1), grouped FFN (MM1+SwiGLU and MM2; each split into a two-SM pair launch
-    and a single-SM tail launch at >= 192 sorted rows per slot), combine, scatter."""
+    align > 1), grouped FFN (MM1+SwiGLU and MM2), combine, scatter."""
     small = rows * k <= 16384 and 4 * (33 * E + 3 * P + 1) <= 48 * 1024
     dispatch = (1 if small else 3) + 1 + (1 if align > 1 else 0)
-    ffn = 4 if cap // max(P, 1) >= 192 else 2
-    return 2 + 1 + dispatch + ffn + 1 + 1
+    return 2 + 1 + dispatch + 2 + 1 + 1
+
+
+def ffn_kernel(cap: int, P: int) -> str:
+    """The grouped-FFN kernel the library picks: weights as M on SM pairs from 192
+    sorted rows per slot on average, else tokens as M on single SMs."""
+    return "ffn_swap_kernel" if cap // max(P, 1) >= 192 else "ffn_tc_kernel"
 
 # dram__bytes_read.sum + dram__bytes_write.sum of the two grouped-FFN launches of one
-# decode step (ncu, --clock-control none), valid for the ffn_tc.cu source whose SHA-256
-# prefix is recorded; any other source reports traffic null.
-FFN_TRAFFIC = {"decode": {"sha256_16": "739b95c830baf672", "bytes": 5582133248}}
+# step of the default workload (ncu, --clock-control none), valid while the kernel's
+# sources hash to the recorded SHA-256 prefix; any other source reports traffic null.
+FFN_TRAFFIC = {
+    "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "ffc89c55dbd49c95",
+               "bytes": 5581868544},
+    "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "b7099fd4b3c2faf1",
+                "bytes": 25903843328},
+}
+
+
+def sources_sha(names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "combine_dp_gather_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def parse():
@@ -199,9 +216,7 @@ def ffn_traffic(args):
     rec = FFN_TRAFFIC.get(args.config)
     if not rec or rec["bytes"] is None:
         return None
-    src = os.path.join(ROOT, "combine_dp_gather_gb300", "csrc", "ffn_tc.cu")
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return rec["bytes"] if h == rec["sha256_16"] else None
+    return rec["bytes"] if sources_sha(rec["sources"]) == rec["sha256_16"] else None
 
 
 def run_native(args, rank, world, local_rank):
@@ -286,8 +301,15 @@ def run_native(args, rank, world, local_rank):
         achieved = ffn_flops / (ffn_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4)}
-    roof.update({"traffic": ffn_traffic(args), "kernel": "moe_grouped_ffn (ffn_tc_kernel "
-                 "MM1+SwiGLU and MM2 launches)", "peak_source": pk["source"],
+    tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12
+    roof.update({"traffic": ffn_traffic(args),
+                 "kernel": f"moe_grouped_ffn ({ffn_kernel(layer.cap, layer.P)} MM1+SwiGLU "
+                           "and MM2 launches)",
+                 "tflops": round(tflops, 1),
+                 "frac_of_bf16_peak": round(tflops / pk["bf16_tflops"], 4),
+                 "frac_of_bf16_sustained": (round(tflops / pk["bf16_tflops_sustained"], 4)
+                                            if pk.get("bf16_tflops_sustained") else None),
+                 "peak_source": pk["source"],
                  "algorithmic_bytes": int(ffn_bytes), "algorithmic_flops": int(ffn_flops),
                  "touched_slots": touched, "ms_per_launch_pair": round(ffn_ms, 4)})
 
