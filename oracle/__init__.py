@@ -83,6 +83,13 @@ def _load():
             "orc_combine": (None, [P, P, P, i64, ctypes.c_int, ctypes.c_int, P]),
             "orc_add_rmsnorm": (None, [P, P, P, i64, ctypes.c_int, ctypes.c_double,
                                        ctypes.c_int, P]),
+            "orc_e4m3_encode_array": (None, [P, i64, P]),
+            "orc_e4m3_decode_array": (None, [P, i64, P]),
+            "orc_ue8m0_exp_array": (None, [P, i64, P]),
+            "orc_quant_groups": (None, [P, i64, ctypes.c_int, P, P]),
+            "orc_quant_blocks": (None, [P, i64, ctypes.c_int, P, P]),
+            "orc_expert_ffn_fp8": (None, [P, P, i64, ctypes.c_int, ctypes.c_int, P, P, P, P,
+                                          P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -294,3 +301,82 @@ def layer(locals_f32, logits, counts, mode, k, renormalize, wgu, wd, E, P=None,
     outs = dp_scatter(yg, counts, offsets)
     return dict(offsets=offsets, rows=rows, valid=valid, xg=xg, ids=ids, w=w, counts=cnt,
                 slot_offsets=offs, perm=perm, inv=inv, xs=xs, ys=ys, yg=yg, outs=outs)
+
+
+# ---------------------------------------------------------------- FP8 path
+def e4m3_encode(x) -> np.ndarray:
+    """Real values -> e4m3 codes (uint8): nearest, ties to even, saturating at +-448."""
+    x = _c(x, np.float64)
+    out = np.empty(x.shape, np.uint8)
+    if x.size:
+        _load().orc_e4m3_encode_array(_p(x), x.size, _p(out))
+    return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    out = np.empty(codes.shape, np.float64)
+    if codes.size:
+        _load().orc_e4m3_decode_array(_p(codes), codes.size, _p(out))
+    return out
+
+
+def ue8m0_exp(amax) -> np.ndarray:
+    """Smallest e with amax <= 448 * 2**e (0 for amax == 0), clamped to [-127, 127]."""
+    amax = _c(amax, np.float64)
+    out = np.empty(amax.shape, np.int32)
+    if amax.size:
+        _load().orc_ue8m0_exp_array(_p(amax), amax.size, _p(out))
+    return out
+
+
+def quant_groups(x):
+    """Per-token groups of 128 along the last axis: (codes [n, K] u8, scale bytes [n, K/128])."""
+    x = _c(x, np.float64)
+    n, K = x.shape
+    assert K % 128 == 0
+    q = np.empty((n, K), np.uint8)
+    e = np.empty((n, K // 128), np.uint8)
+    if n:
+        _load().orc_quant_groups(_p(x), n, K, _p(q), _p(e))
+    return q, e
+
+
+def quant_blocks(w):
+    """128 x 128 blocks of w [R, K]: (codes [R, K] u8, scale bytes [R/128, K/128])."""
+    w = _c(w, np.float64)
+    R, K = w.shape
+    assert R % 128 == 0 and K % 128 == 0
+    q = np.empty((R, K), np.uint8)
+    e = np.empty((R // 128, K // 128), np.uint8)
+    _load().orc_quant_blocks(_p(w), R, K, _p(q), _p(e))
+    return q, e
+
+
+def expert_ffn_fp8(xq, xe, wguq, wgue, wdq, wde) -> np.ndarray:
+    """SwiGLU FFN of one expert on FP8 operands (codes + scale bytes) -> [n, H] f64."""
+    xq, xe = _c(xq, np.uint8), _c(xe, np.uint8)
+    wguq, wgue, wdq, wde = (_c(a, np.uint8) for a in (wguq, wgue, wdq, wde))
+    n, H = xq.shape
+    I = wdq.shape[1]
+    assert wguq.shape == (2 * I, H) and wdq.shape == (H, I)
+    assert xe.shape == (n, H // 128) and wgue.shape == (2 * I // 128, H // 128)
+    assert wde.shape == (H // 128, I // 128)
+    y = np.empty((n, H), np.float64)
+    if n:
+        _load().orc_expert_ffn_fp8(_p(xq), _p(xe), n, H, I, _p(wguq), _p(wgue), _p(wdq),
+                                   _p(wde), _p(y))
+    return y
+
+
+def grouped_ffn_fp8(xq, xe, offsets, wq, slot_lo: int = 0, slot_hi: int | None = None):
+    """Per slot s: rows [offsets[s], offsets[s+1]) of (xq, xe) through expert s;
+    wq(s) -> (wguq, wgue, wdq, wde).  Rows of other slots are NaN."""
+    P = len(offsets) - 1
+    slot_hi = P if slot_hi is None else slot_hi
+    ys = np.full(xq.shape, np.nan, np.float64)
+    for s in range(slot_lo, slot_hi):
+        a, b = int(offsets[s]), int(offsets[s + 1])
+        if b > a:
+            ys[a:b] = expert_ffn_fp8(xq[a:b], xe[a:b], *wq(s))
+    return ys

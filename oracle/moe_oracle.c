@@ -467,3 +467,162 @@ void orc_add_rmsnorm(const float *hidden, float *residual, const float *gamma, i
     for (int c = 0; c < H; ++c) y[r * H + c] = (double)res[c] * inv * (double)gamma[c];
   }
 }
+
+/* ------------------------------------------------------------------------ */
+/* FP8 path.                                                                */
+/*                                                                          */
+/* [P1] section "prefll 侧的一个必要步骤:per-token-group 量化": before        */
+/*   dispatch the hidden states are quantised to FP8 in groups of 128       */
+/*   consecutive features of one token (the group size is fixed at 128, the */
+/*   same number as expert_alignment); with DeepGEMM the scale factors are  */
+/*   UE8M0, i.e. powers of two, for its 1x128 fine-grained scaling.          */
+/* Readings (the pages leave these open):                                    */
+/*   * the FP8 format is e4m3 without infinities (max 448), round to        */
+/*     nearest with ties to even, saturating at +-448;                      */
+/*   * a group's scale is the smallest power of two 2^e with                 */
+/*     amax <= 448 * 2^e (amax = largest magnitude in the group; e = 0 for  */
+/*     an all-zero group), stored as the byte e + 127; codes are            */
+/*     e4m3(x / 2^e);                                                       */
+/*   * expert weights use the same rule on 128 x 128 blocks (output rows x  */
+/*     input features), gate and up rows in separate blocks;               */
+/*   * the SwiGLU activation h is quantised the same way (groups of 128     */
+/*     intermediate features per token) before the down projection;        */
+/*   * the GEMM sums dequantised products: for output (m, n),               */
+/*     sum over k-blocks b of 2^(ea[m,b] + ew[n/128,b]) *                   */
+/*     sum_{k in b} e4m3(qa[m,k]) * e4m3(qw[n,k]).                           */
+/* Parity: pinned (e4m3 against torch's float8_e4m3fn conversion, the scale */
+/* rule's closed form, the FFN against an independent numpy evaluation).   */
+/* ------------------------------------------------------------------------ */
+uint8_t orc_e4m3_encode(double x) {
+  uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  double a = fabs(x);
+  if (isnan(a)) return 0x7F;
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);       /* saturate */
+  if (a < 0.015625) {                                  /* below 2^-6: steps of 2^-9 */
+    double m = rint(a * 512.0);                        /* 0 .. 8; 8 is 2^-6 (code 0x08) */
+    return (uint8_t)(sign | (uint8_t)m);
+  }
+  int E;
+  double f = frexp(a, &E);                             /* a = f * 2^E, f in [0.5, 1) */
+  int e = E - 1;                                       /* a = (2f) * 2^e, 2f in [1, 2) */
+  double mant = rint((2.0 * f - 1.0) * 8.0);           /* 3 fraction bits, 0 .. 8 */
+  if (mant == 8.0) {
+    mant = 0.0;
+    e += 1;
+  }
+  int field = e + 7;
+  if (field > 15 || (field == 15 && mant == 7.0)) return (uint8_t)(sign | 0x7E);
+  return (uint8_t)(sign | (uint8_t)(field << 3) | (uint8_t)mant);
+}
+
+double orc_e4m3_decode(uint8_t c) {
+  int field = (c >> 3) & 15, mant = c & 7;
+  double s = (c & 0x80) ? -1.0 : 1.0;
+  if (field == 15 && mant == 7) return NAN;
+  if (field == 0) return s * ldexp((double)mant, -9);
+  return s * ldexp(1.0 + mant / 8.0, field - 7);
+}
+
+int orc_ue8m0_exp(double amax) {
+  if (!(amax > 0.0)) return 0;
+  int E;
+  double f = frexp(amax, &E);          /* amax = f * 2^E; 448 = 0.875 * 2^9 */
+  int e = E - 9 + (f > 0.875 ? 1 : 0);
+  if (e < -127) e = -127;
+  if (e > 127) e = 127;
+  return e;
+}
+
+void orc_e4m3_encode_array(const double *x, int64_t n, uint8_t *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(x[i]);
+}
+void orc_e4m3_decode_array(const uint8_t *c, int64_t n, double *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_decode(c[i]);
+}
+void orc_ue8m0_exp_array(const double *amax, int64_t n, int32_t *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_ue8m0_exp(amax[i]);
+}
+
+/* Groups of 128 along each row of x [n, K] (K a multiple of 128):
+ * q [n, K] codes, sexp [n, K / 128] scale bytes (e + 127). */
+void orc_quant_groups(const double *x, int64_t n, int K, uint8_t *q, uint8_t *sexp) {
+  const int G = K / 128;
+  for (int64_t r = 0; r < n; ++r) {
+    for (int g = 0; g < G; ++g) {
+      const double *xs = x + r * K + (int64_t)g * 128;
+      double amax = 0.0;
+      for (int i = 0; i < 128; ++i)
+        if (fabs(xs[i]) > amax) amax = fabs(xs[i]);
+      int e = orc_ue8m0_exp(amax);
+      sexp[r * G + g] = (uint8_t)(e + 127);
+      for (int i = 0; i < 128; ++i) q[r * K + (int64_t)g * 128 + i] = orc_e4m3_encode(ldexp(xs[i], -e));
+    }
+  }
+}
+
+/* 128 x 128 blocks of w [R, K] (R and K multiples of 128):
+ * q [R, K] codes, sexp [R / 128, K / 128] scale bytes. */
+void orc_quant_blocks(const double *w, int64_t R, int K, uint8_t *q, uint8_t *sexp) {
+  const int G = K / 128;
+  for (int64_t br = 0; br < R / 128; ++br) {
+    for (int g = 0; g < G; ++g) {
+      double amax = 0.0;
+      for (int64_t r = br * 128; r < br * 128 + 128; ++r)
+        for (int i = 0; i < 128; ++i) {
+          double v = fabs(w[r * K + (int64_t)g * 128 + i]);
+          if (v > amax) amax = v;
+        }
+      int e = orc_ue8m0_exp(amax);
+      sexp[br * G + g] = (uint8_t)(e + 127);
+      for (int64_t r = br * 128; r < br * 128 + 128; ++r)
+        for (int i = 0; i < 128; ++i)
+          q[r * K + (int64_t)g * 128 + i] = orc_e4m3_encode(ldexp(w[r * K + (int64_t)g * 128 + i], -e));
+    }
+  }
+}
+
+/* One dequantised dot product of FP8 rows a, w of length K: sum over
+ * 128-blocks b of 2^(ea[b] + ew[b]) * sum_{k in b} e4m3(a_k) * e4m3(w_k). */
+static double orc_fp8_dot(const uint8_t *a, const uint8_t *ea, const uint8_t *w,
+                          const uint8_t *ew, int K) {
+  double total = 0.0;
+  for (int b = 0; b < K / 128; ++b) {
+    double s = 0.0;
+    for (int k = b * 128; k < b * 128 + 128; ++k) s += orc_e4m3_decode(a[k]) * orc_e4m3_decode(w[k]);
+    total += ldexp(s, ((int)ea[b] - 127) + ((int)ew[b] - 127));
+  }
+  return total;
+}
+
+/* SwiGLU FFN of one expert on FP8 operands.
+ *   xq [n, H] codes, xe [n, H/128] scale bytes (token groups)
+ *   wguq [2I, H] codes, wgue [2I/128, H/128] (gate rows 0..I-1, up rows I..2I-1)
+ *   wdq [H, I] codes, wde [H/128, I/128]
+ *   y [n, H] double.  h is quantised per token in groups of 128 before MM2. */
+void orc_expert_ffn_fp8(const uint8_t *xq, const uint8_t *xe, int64_t n, int H, int I,
+                        const uint8_t *wguq, const uint8_t *wgue, const uint8_t *wdq,
+                        const uint8_t *wde, double *y) {
+  const int GH = H / 128, GI = I / 128;
+#pragma omp parallel
+  {
+    double *a = (double *)malloc(sizeof(double) * (size_t)I);
+    uint8_t *aq = (uint8_t *)malloc((size_t)I);
+    uint8_t *ae = (uint8_t *)malloc((size_t)GI);
+#pragma omp for schedule(static)
+    for (int64_t r = 0; r < n; ++r) {
+      const uint8_t *xr = xq + r * H, *xer = xe + r * GH;
+      for (int i = 0; i < I; ++i) {
+        double g = orc_fp8_dot(xr, xer, wguq + (int64_t)i * H, wgue + (int64_t)(i / 128) * GH, H);
+        double u = orc_fp8_dot(xr, xer, wguq + (int64_t)(I + i) * H,
+                               wgue + (int64_t)((I + i) / 128) * GH, H);
+        a[i] = g / (1.0 + exp(-g)) * u;
+      }
+      orc_quant_groups(a, 1, I, aq, ae);
+      for (int o = 0; o < H; ++o)
+        y[r * H + o] = orc_fp8_dot(aq, ae, wdq + (int64_t)o * I, wde + (int64_t)(o / 128) * GI, I);
+    }
+    free(a);
+    free(aq);
+    free(ae);
+  }
+}

@@ -514,3 +514,158 @@ def test_layer_with_shared_expert_matches_dense_definition(orc):
     dense += numpy_swiglu(x, wgu[8], wd[8])           # the shared expert, weight 1
     got = np.concatenate(res["outs"])
     assert np.allclose(got, dense, rtol=1e-10, atol=1e-12)
+
+
+# ----------------------------------------------------------------- FP8 path
+# Independent e4m3 rounding: the values of the 127 non-negative finite codes come
+# from torch's float8_e4m3fn decoding (a library routine), ascending with the code;
+# a value goes to the nearest of them, ties to the even code, |x| >= 448 saturates.
+_E4M3_POS = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+
+
+def _nearest_e4m3(v):
+    v = np.asarray(v, np.float64)
+    a = np.minimum(np.abs(v), 448.0)
+    idx = np.searchsorted(_E4M3_POS, a)
+    lo = np.clip(idx - 1, 0, 126)
+    hi = np.clip(idx, 0, 126)
+    dlo, dhi = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    return (pick | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+
+
+def _scale_exp_by_search(amax):
+    """Smallest integer e with amax <= 448 * 2**e, found by stepping (0 for amax 0)."""
+    out = []
+    for a in np.ravel(amax):
+        if a == 0:
+            out.append(0)
+            continue
+        e = 0
+        while a > 448.0 * 2.0 ** e:
+            e += 1
+        while a <= 448.0 * 2.0 ** (e - 1):
+            e -= 1
+        out.append(max(-127, min(127, e)))
+    return np.array(out, np.int64).reshape(np.shape(amax))
+
+
+def test_e4m3_encode_matches_nearest_and_torch(orc):
+    rng = np.random.default_rng(5)
+    mags = (2.0 ** rng.uniform(-12, 9, 20000)).astype(np.float32).astype(np.float64)
+    x = np.where(rng.random(20000) < 0.5, -mags, mags)
+    mids = (_E4M3_POS[1:] + _E4M3_POS[:-1]) / 2          # every tie between neighbours
+    x = np.concatenate([x, mids, -mids, _E4M3_POS, [0.0, -0.0, 447.875, 463.9921875, 464.0]])
+    got = orc.e4m3_encode(x)
+    assert (got == _nearest_e4m3(x)).all()
+    ok = np.abs(x) <= 464.0                              # torch overflows to NaN above 464
+    x32 = x[ok].astype(np.float32)
+    assert (x32.astype(np.float64) == x[ok]).all()       # exact in float32
+    via_torch = torch.from_numpy(x32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (got[ok] == via_torch).all()
+
+
+def test_e4m3_saturation_and_decode(orc):
+    assert orc.e4m3_encode(np.array([448.0, 500.0, 1e30, -1e30, -449.0])).tolist() == \
+        [0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+    assert orc.e4m3_encode(np.array([np.nan]))[0] & 0x7F == 0x7F
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    via_torch = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert (orc.e4m3_decode(codes) == via_torch).all()
+    assert (orc.e4m3_encode(orc.e4m3_decode(codes)) == codes).all()   # round trip
+
+
+def test_ue8m0_scale_rule(orc):
+    rng = np.random.default_rng(6)
+    amax = np.concatenate([2.0 ** rng.uniform(-40, 40, 5000), 448.0 * 2.0 ** np.arange(-20, 21),
+                           [0.0, 448.0, 448.0000001, 224.0, 1.0]])
+    e = orc.ue8m0_exp(amax).astype(np.int64)
+    assert (e == _scale_exp_by_search(amax)).all()
+    pos = amax > 0
+    assert (amax[pos] <= 448.0 * 2.0 ** e[pos]).all()
+    assert (amax[pos] > 448.0 * 2.0 ** (e[pos] - 1)).all()
+
+
+def test_quant_groups_scales_codes_and_indexing(orc):
+    rng = np.random.default_rng(7)
+    n, K = 5, 512
+    x = rng.standard_normal((n, K)) * (2.0 ** np.repeat(np.arange(K // 128) * 3, 128))[None, :]
+    x[2, 128:256] = 0.0                                  # an all-zero group
+    q, e = orc.quant_groups(x)
+    amax = np.abs(x).reshape(n, K // 128, 128).max(-1)
+    ee = _scale_exp_by_search(amax)
+    assert (e.astype(np.int64) - 127 == ee).all()
+    assert e[2, 1] == 127
+    assert (np.diff(ee[[0, 1, 3, 4]], axis=1) >= 2).all()   # group g scaled by 8**g
+    scaled = x / 2.0 ** np.repeat(ee, 128, axis=1)
+    assert (q == _nearest_e4m3(scaled)).all()
+    assert np.abs(orc.e4m3_decode(q)).max() <= 448.0
+    # the largest element of each non-zero group lands in (224, 448]
+    top = np.abs(orc.e4m3_decode(q)).reshape(n, K // 128, 128).max(-1)
+    assert ((top > 224.0) | (amax == 0)).all()
+
+
+def test_quant_blocks_indexing(orc):
+    rng = np.random.default_rng(8)
+    R, K = 256, 384
+    bi = np.repeat(np.arange(R // 128), 128)[:, None]
+    bj = np.repeat(np.arange(K // 128), 128)[None, :]
+    w = rng.uniform(-1, 1, (R, K)) * 2.0 ** (3 * bi + bj)
+    q, e = orc.quant_blocks(w)
+    amax = np.abs(w).reshape(R // 128, 128, K // 128, 128).max(axis=(1, 3))
+    ee = _scale_exp_by_search(amax)
+    assert (e.astype(np.int64) - 127 == ee).all()
+    assert (q == _nearest_e4m3(w / 2.0 ** ee[bi[:, 0]][:, bj[0]])).all()
+
+
+def _deq_groups(q, e):
+    return _E4M3_SIGNED(q) * 2.0 ** np.repeat(e.astype(np.int64) - 127, 128, axis=1)
+
+
+def _deq_blocks(q, e):
+    s = 2.0 ** (e.astype(np.int64) - 127)
+    return _E4M3_SIGNED(q) * np.repeat(np.repeat(s, 128, axis=0), 128, axis=1)
+
+
+def _E4M3_SIGNED(q):
+    return torch.from_numpy(np.ascontiguousarray(q)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def _fp8_ffn_numpy(xq, xe, wguq, wgue, wdq, wde, up_block_shift=True):
+    """Dense numpy evaluation on dequantised operands; h re-quantised per token in
+    groups of 128 with the independent rounding above.  up_block_shift=False is a
+    mutant that reads the up rows' scales from the gate rows' blocks."""
+    I = wdq.shape[1]
+    wgu = _deq_blocks(wguq, wgue)
+    if not up_block_shift:
+        wgu[I:] = _E4M3_SIGNED(wguq[I:]) * np.repeat(np.repeat(
+            2.0 ** (wgue[: I // 128].astype(np.int64) - 127), 128, axis=0), 128, axis=1)
+    x = _deq_groups(xq, xe)
+    g, u = x @ wgu[:I].T, x @ wgu[I:].T
+    h = g / (1.0 + np.exp(-g)) * u
+    he = _scale_exp_by_search(np.abs(h).reshape(len(h), I // 128, 128).max(-1))
+    hq = _nearest_e4m3(h / 2.0 ** np.repeat(he, 128, axis=1))
+    return _deq_groups(hq, (he + 127).astype(np.uint8)) @ _deq_blocks(wdq, wde).T
+
+
+def test_ffn_fp8_matches_numpy_on_dequantised_operands(orc):
+    rng = np.random.default_rng(9)
+    n, H, I = 4, 256, 256
+    x = rng.standard_normal((n, H))
+    # every weight block gets its own magnitude, gate and up blocks differ
+    wgu = rng.standard_normal((2 * I, H)) * 0.05 * \
+        2.0 ** rng.integers(-3, 4, (2 * I // 128, H // 128)).repeat(128, 0).repeat(128, 1)
+    wd = rng.standard_normal((H, I)) * 0.05 * \
+        2.0 ** rng.integers(-3, 4, (H // 128, I // 128)).repeat(128, 0).repeat(128, 1)
+    xq, xe = orc.quant_groups(x)
+    wguq, wgue = orc.quant_blocks(wgu)
+    wdq, wde = orc.quant_blocks(wd)
+    y = orc.expert_ffn_fp8(xq, xe, wguq, wgue, wdq, wde)
+    ref = _fp8_ffn_numpy(xq, xe, wguq, wgue, wdq, wde)
+    np.testing.assert_allclose(y, ref, rtol=1e-9, atol=1e-12)
+    mutant = _fp8_ffn_numpy(xq, xe, wguq, wgue, wdq, wde, up_block_shift=False)
+    assert not np.allclose(y, mutant, rtol=1e-3, atol=1e-6)
+    # FP8 stays close to the unquantised FFN (3 mantissa bits: a few % error)
+    dense = orc.expert_ffn(x.astype(np.float32), wgu.astype(np.float32), wd.astype(np.float32))
+    rel = np.linalg.norm(y - dense) / np.linalg.norm(dense)
+    assert rel < 0.1, rel
