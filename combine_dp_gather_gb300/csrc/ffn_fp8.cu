@@ -1,0 +1,509 @@
+// Grouped SwiGLU expert FFN on FP8 operands (e4m3 codes with UE8M0 scales per
+// 128-value group) on the tcgen05 tensor cores (sm_103a).
+//
+// SGLang chapter 17, section "prefll 侧的一个必要步骤:per-token-group 量化":
+// tokens enter the grouped GEMM as FP8 in groups of 128 features with UE8M0
+// scale factors (DeepGEMM's 1x128 fine-grained scaling); the expert weights
+// carry one scale per 128 x 128 block.  Opening sections: a DeepSeek-V3 expert
+// has gate/up [2048, 7168] and down [7168, 2048].
+//
+// One 128-deep k-block is exactly one scale block of both operands, so each
+// k-block's four MMAs (kind::f8f6f4, K = 32 each) write a fresh fp32 partial
+// in tensor memory, and the epilogue warps add it into fp32 registers scaled
+// by 2^(e_token + e_weight):
+//   acc[row, t] += 2^(ex[t, kb] + ew[row / 128, kb]) * partial_kb[row, t]
+// The weights are the MMA's M operand (128 rows per CTA) and up to 32 of a
+// slot's tokens its N, so the accumulator of a unit lives in registers (one
+// weight row per thread, 32 token columns).
+//   MM1 + SwiGLU: unit = (slot, 128 features f, token group); A = gate rows
+//                 f..f+127 and the same up rows (one 3-D TMA box), two MMAs
+//                 per K step; the epilogue forms h = silu(gate) * up and
+//                 quantises it per token over its 128 features (one group),
+//                 writing codes and the scale byte for the down projection.
+//   MM2:          unit = (slot, 128 output rows, token group); bf16 output.
+// With few tokens per slot (decode) the weight stream is the whole cost, and
+// FP8 weights halve it.
+//
+// Roles (192 threads, one CTA per SM):
+//   warp 0    TMA producer: weight box + token box per stage
+//   warp 1    TMEM allocation; lane 0 issues the MMAs and commits (stage free,
+//             partial ready); partials ping-pong between two TMEM buffers
+//   warps 2-5 epilogue: per k-block tcgen05.ld of the partial(s), release,
+//             scale and accumulate; per unit SwiGLU + quantisation or bf16 out
+// Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets
+// MOE_DEV_TIMEOUT, the other roles stop at their next wait, TMEM is freed and
+// the kernel returns.
+#include <mutex>
+
+#include "common.cuh"
+#include "fp8.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int BK = 128;     // fp8 values per k-block = one 128-byte swizzle row = one scale group
+constexpr int NT = 32;      // tokens per unit
+constexpr int THREADS = 192;
+
+template <bool SWIGLU>
+struct F8Cfg {
+  static constexpr int A_ROWS = SWIGLU ? 256 : 128;  // gate + up, or down rows
+  static constexpr int A_BYTES = A_ROWS * BK;
+  static constexpr int B_BYTES = NT * BK;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = SWIGLU ? 5 : 9;
+  static constexpr int PCOLS = SWIGLU ? 2 * NT : NT;  // partial columns per buffer
+};
+
+struct F8Smem {
+  uint64_t full[9];
+  uint64_t empty[9];
+  uint64_t pfull[2];
+  uint64_t pempty[2];
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  int32_t total_units;
+  int32_t warp_sums[THREADS / 32];
+  float wmax[4][NT];                 // per-warp token maxima of h
+  int32_t pref[MOE_MAX_SLOTS + 1];   // unit prefix over the slot range
+  int32_t row0[MOE_MAX_SLOTS];
+  int32_t rows[MOE_MAX_SLOTS];
+};
+template <bool SWIGLU>
+constexpr size_t f8_smem_bytes() {
+  return 1024 + (size_t)F8Cfg<SWIGLU>::STAGES * F8Cfg<SWIGLU>::STAGE_BYTES + sizeof(F8Smem);
+}
+
+struct F8Params {
+  const int32_t* offsets;
+  int slot_lo, nslots;
+  int64_t cap;
+  int num_kb;          // K / 128
+  int n_tiles;         // 128-row weight tiles per slot
+  int wrows_per_slot;  // MM2: H
+  int K;               // reduction length (H for MM1, I for MM2)
+  const uint8_t* xscale;   // [cap, K / 128] token scale bytes
+  const uint8_t* wscale;   // weight scale bytes [P, rows / 128, K / 128]
+  int wscale_rows;         // rows / 128 per slot: 2I/128 (MM1) or H/128 (MM2)
+  int up_block;            // MM1: I / 128 (first up block)
+  int out_ld;
+  uint8_t* hq;             // MM1: h codes [cap, I]
+  uint8_t* hscale;         // MM1: h scale bytes [cap, I / 128]
+  __nv_bfloat16* y;        // MM2: [cap, H]
+  uint32_t* status;
+};
+
+__host__ __device__ __forceinline__ int32_t token_groups(int32_t rows) {
+  return rows > 0 ? (rows + NT - 1) / NT : 0;
+}
+
+struct F8Unit {
+  int slot, tile;
+  int32_t tok0, ntok;
+  int N;  // MMA width: tokens rounded up to 16
+};
+__device__ __forceinline__ F8Unit decode_unit(const F8Smem& L, int nslots, int u) {
+  int lo = 0, hi = nslots - 1;
+  while (lo < hi) {  // largest s with pref[s] <= u
+    const int mid = (lo + hi + 1) >> 1;
+    if (L.pref[mid] <= u)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int local = u - L.pref[lo];
+  const int32_t T = L.rows[lo];
+  const int32_t g = token_groups(T);
+  F8Unit r;
+  r.slot = lo;
+  r.tile = local / g;
+  const int32_t grp = local % g;
+  r.tok0 = L.row0[lo] + grp * NT;
+  const int32_t left = T - grp * NT;
+  r.ntok = left < NT ? left : NT;
+  r.N = (r.ntok + 15) & ~15;
+  return r;
+}
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(THREADS, 1)
+    ffn_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB16,
+                   const __grid_constant__ CUtensorMap tmB32, const F8Params p) {
+  using C = F8Cfg<SWIGLU>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stage_base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  F8Smem& L = *reinterpret_cast<F8Smem*>(stage_base + (size_t)STAGES * C::STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- unit table: token groups per slot, exclusive prefix of units
+  {
+    const int per = (p.nslots + THREADS - 1) / THREADS;
+    const int s0 = threadIdx.x * per;
+    int32_t local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int s = s0 + i;
+      if (s < p.nslots) {
+        const int32_t o0 = p.offsets[p.slot_lo + s];
+        int32_t rows = p.offsets[p.slot_lo + s + 1] - o0;
+        if (rows < 0) rows = 0;
+        L.row0[s] = o0;
+        L.rows[s] = rows;
+        local += token_groups(rows) * p.n_tiles;
+      }
+    }
+    int32_t x = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) L.warp_sums[warp] = x;
+    if (threadIdx.x == 0) {
+      L.abort_flag = 0;
+      for (int i = 0; i < STAGES; ++i) {
+        mbar_init(smem_u32(&L.full[i]), 1);   // the producer's expect_tx
+        mbar_init(smem_u32(&L.empty[i]), 1);  // the MMA commit
+      }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(smem_u32(&L.pfull[i]), 1);   // the MMA commit
+        mbar_init(smem_u32(&L.pempty[i]), 4);  // every epilogue warp
+      }
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc<1>(smem_u32(&L.tmem_base));
+    __syncthreads();
+    int32_t before = 0;
+    for (int w = 0; w < warp; ++w) before += L.warp_sums[w];
+    int32_t run = before + x - local;
+    for (int i = 0; i < per; ++i) {
+      const int s = s0 + i;
+      if (s < p.nslots) {
+        L.pref[s] = run;
+        run += token_groups(L.rows[s]) * p.n_tiles;
+      }
+    }
+    if (threadIdx.x == THREADS - 1) {
+      int32_t tot = 0;
+      for (int w = 0; w < THREADS / 32; ++w) tot += L.warp_sums[w];
+      L.pref[p.nslots] = tot;
+      L.total_units = tot;
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+  }
+  const int total = L.total_units;
+  const uint32_t tmem_base = L.tmem_base;
+  volatile int32_t* abort_flag = &L.abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_tok = policy_evict_last();
+    const uint64_t pol_w = policy_evict_first();
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const F8Unit un = decode_unit(L, p.nslots, u);
+      const int32_t slot = p.slot_lo + un.slot;
+      const CUtensorMap* bmap = un.N == 16 ? &tmB16 : &tmB32;
+      const uint32_t tx = (uint32_t)(C::A_BYTES + un.N * BK);
+      bool ok = true;
+      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
+        if (!wait_bar(smem_u32(&L.empty[st]), ph ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t full = smem_u32(&L.full[st]);
+          const uint32_t sa = smem_u32(stage_base + (size_t)st * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::A_BYTES;
+          const int32_t kc = kb * BK;
+          mbar_arrive_expect_tx(full, tx);
+          if (SWIGLU)
+            tma_load_3d<1>(sa, &tmA, kc, un.tile * 128, 2 * slot, full, pol_w);
+          else
+            tma_load_2d<1>(sa, &tmA, kc, slot * p.wrows_per_slot + un.tile * 128, full, pol_w);
+          tma_load_2d<1>(sb, bmap, kc, un.tok0, full, pol_tok);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+    }
+    for (uint32_t j = (it >= STAGES ? it - STAGES : 0); j < it; ++j) {
+      const uint32_t st = j % STAGES, ph = (j / STAGES) & 1u;
+      if (!wait_bar(smem_u32(&L.empty[st]), ph, abort_flag, p.status)) break;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const F8Unit un = decode_unit(L, p.nslots, u);
+      const uint32_t idesc = idesc_e4m3(128, un.N);
+      bool ok = true;
+      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
+        const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
+        if (!wait_bar(smem_u32(&L.full[st]), ph, abort_flag, p.status) ||
+            !wait_bar(smem_u32(&L.pempty[pb]), pph ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        if (lane == 0) {
+          const uint32_t sa = smem_u32(stage_base + (size_t)st * C::STAGE_BYTES);
+          const uint64_t adesc = sw128_desc(sa);
+          const uint64_t adesc_up = sw128_desc(sa + 128 * BK);
+          const uint64_t bdesc = sw128_desc(sa + C::A_BYTES);
+          const uint32_t d = tmem_base + pb * C::PCOLS;
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {  // +32 bytes per K=32 step in the swizzle row
+            mma_e4m3(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk != 0);
+            if (SWIGLU) mma_e4m3(d + NT, adesc_up + 2 * kk, bdesc + 2 * kk, idesc, kk != 0);
+          }
+          commit<1>(smem_u32(&L.empty[st]));
+          commit<1>(smem_u32(&L.pfull[pb]));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 = weight rows of the tile
+    const uint32_t lanes = tmem_base + ((uint32_t)(q * 32) << 16);
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const F8Unit un = decode_unit(L, p.nslots, u);
+      const int32_t slot = p.slot_lo + un.slot;
+      // scale bytes, loaded one k-block ahead: lane j holds token j's byte,
+      // every lane the weight blocks' bytes
+      const int64_t trow = (int64_t)un.tok0 + lane;
+      const bool tv = lane < un.ntok && trow < p.cap;
+      const uint8_t* xs_row = p.xscale + (tv ? trow : 0) * p.num_kb;
+      const int64_t wb0 = (int64_t)slot * p.wscale_rows + un.tile;
+      const uint8_t* ws0 = p.wscale + wb0 * p.num_kb;
+      const uint8_t* ws1 = p.wscale + (wb0 + p.up_block) * p.num_kb;
+      uint32_t nx = tv ? xs_row[0] : 127u, nw0 = ws0[0], nw1 = SWIGLU ? ws1[0] : 127u;
+      float acc0[NT], acc1[NT];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) acc0[j] = acc1[j] = 0.0f;
+      bool ok = true;
+      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        const uint32_t ex = nx, ew0 = nw0, ew1 = nw1;
+        if (kb + 1 < p.num_kb) {
+          nx = tv ? xs_row[kb + 1] : 127u;
+          nw0 = ws0[kb + 1];
+          if (SWIGLU) nw1 = ws1[kb + 1];
+        }
+        const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
+        if (!wait_bar(smem_u32(&L.pfull[pb]), pph, abort_flag, p.status)) {
+          ok = false;
+          it += p.num_kb - kb;
+          break;
+        }
+        fence_after();
+        uint32_t r0[32], r1[32];
+        tmem_ld32(lanes + pb * C::PCOLS, r0);
+        if (SWIGLU) tmem_ld32(lanes + pb * C::PCOLS + NT, r1);
+        tmem_wait_ld();
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&L.pempty[pb]));
+        const float cx_mine = pow2i((int)ex - 127);
+        const float cw0 = pow2i((int)ew0 - 127);
+        const float cw1 = SWIGLU ? pow2i((int)ew1 - 127) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const float cx = __shfl_sync(0xffffffffu, cx_mine, j);
+          acc0[j] = fmaf(__uint_as_float(r0[j]), cx * cw0, acc0[j]);
+          if (SWIGLU) acc1[j] = fmaf(__uint_as_float(r1[j]), cx * cw1, acc1[j]);
+        }
+      }
+      if (SWIGLU) ok = named_all(1, 128, ok);  // the four warps leave together
+      if (!ok) break;
+      const int feat = un.tile * 128 + q * 32 + lane;
+      if (SWIGLU) {
+        // h = silu(gate) * up, then per token one scale over its 128 features
+        float m[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          acc0[j] = acc0[j] / (1.0f + expf(-acc0[j])) * acc1[j];
+          m[j] = fabsf(acc0[j]);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+          for (int j = 0; j < NT; ++j) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], off));
+        if (lane == 0)
+#pragma unroll
+          for (int j = 0; j < NT; ++j) L.wmax[q][j] = m[j];
+        named_sync(1, 128);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const float amax = fmaxf(fmaxf(L.wmax[0][j], L.wmax[1][j]), fmaxf(L.wmax[2][j], L.wmax[3][j]));
+          const int e = fp8_scale_exp(amax);
+          const int64_t row = (int64_t)un.tok0 + j;
+          if (j < un.ntok && row < p.cap) {
+            p.hq[row * p.out_ld + feat] = (uint8_t)(e4m3x4(acc0[j] * pow2i(-e), 0.f, 0.f, 0.f) & 0xFFu);
+            if (q == 0 && lane == 0)
+              p.hscale[row * (p.out_ld / 128) + un.tile] = (uint8_t)(e + 127);
+          }
+        }
+        named_sync(1, 128);  // the maxima are read before the next unit writes them
+      } else {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const int64_t row = (int64_t)un.tok0 + j;
+          if (j < un.ntok && row < p.cap) p.y[row * p.out_ld + feat] = __float2bfloat16_rn(acc0[j]);
+        }
+      }
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 1) tmem_dealloc<1>(tmem_base);
+}
+
+// ------------------------------------------------------------- host side
+template <bool SWIGLU>
+bool f8_setup(int* max_ctas) {
+  static std::mutex mu;
+  static int ctas[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ctas[dev] == 0) {
+    const int bytes = (int)f8_smem_bytes<SWIGLU>();
+    if (cudaFuncSetAttribute(ffn_fp8_kernel<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) != cudaSuccess)
+      return false;
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, ffn_fp8_kernel<SWIGLU>, THREADS,
+                                                      bytes) != cudaSuccess ||
+        b < 1)
+      return false;
+    ctas[dev] = b * num_sms();
+  }
+  *max_ctas = ctas[dev];
+  return true;
+}
+
+struct F8Args {
+  const uint8_t *xq, *xscale;
+  const int32_t* offsets;
+  int P, slot_lo, slot_hi;
+  int64_t cap;
+  const uint8_t *wguq, *wgus, *wdq, *wds;
+  int H, I;
+  uint8_t *hq, *hs;
+  __nv_bfloat16* y;
+  uint32_t* status;
+};
+
+template <bool SWIGLU>
+moe_status run_f8(const F8Args& a, cudaStream_t s) {
+  int max_ctas = 0;
+  if (!f8_setup<SWIGLU>(&max_ctas)) return MOE_ERR_CUDA;
+  CUtensorMap mA, mB16, mB32;
+  const uint8_t* tok = SWIGLU ? a.xq : a.hq;
+  const uint64_t K = SWIGLU ? (uint64_t)a.H : (uint64_t)a.I;
+  const bool ok = (SWIGLU ? make_map_u8_gate_up(&mA, a.wguq, a.H, a.I, a.P, 128)
+                          : make_map_u8(&mA, a.wdq, a.I, (uint64_t)a.P * a.H, 128)) &&
+                  make_map_u8(&mB16, tok, K, (uint64_t)a.cap, 16) &&
+                  make_map_u8(&mB32, tok, K, (uint64_t)a.cap, 32);
+  if (!ok) return MOE_ERR_CUDA;
+  F8Params p;
+  p.offsets = a.offsets;
+  p.slot_lo = a.slot_lo;
+  p.nslots = a.slot_hi - a.slot_lo;
+  p.cap = a.cap;
+  p.num_kb = (int)(K / BK);
+  p.n_tiles = SWIGLU ? a.I / 128 : a.H / 128;
+  p.wrows_per_slot = a.H;
+  p.K = (int)K;
+  p.xscale = SWIGLU ? a.xscale : a.hs;
+  p.wscale = SWIGLU ? a.wgus : a.wds;
+  p.wscale_rows = SWIGLU ? 2 * a.I / 128 : a.H / 128;
+  p.up_block = SWIGLU ? a.I / 128 : 0;
+  p.out_ld = SWIGLU ? a.I : a.H;
+  p.hq = a.hq;
+  p.hscale = a.hs;
+  p.y = a.y;
+  p.status = a.status;
+  // upper bound of units (device-side counts unknown here)
+  const int64_t bound = (a.cap / NT + p.nslots) * (int64_t)p.n_tiles;
+  const int grid = (int)(bound < max_ctas ? bound : max_ctas);
+  ffn_fp8_kernel<SWIGLU><<<grid, THREADS, f8_smem_bytes<SWIGLU>(), s>>>(mA, mB16, mB32, p);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+size_t hscale_offset(int64_t cap, int I) { return ((size_t)cap * I + 255) & ~(size_t)255; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_grouped_ffn_fp8_ws_bytes(int64_t cap, int I) {
+  if (cap < 0 || I < 128 || I % 128 != 0) return 0;
+  return hscale_offset(cap, I) + (size_t)cap * (I / 128);
+}
+
+extern "C" moe_status moe_grouped_ffn_fp8(const uint8_t* d_sorted_q,
+                                          const uint8_t* d_sorted_scales,
+                                          const int32_t* d_offsets_P, int P, int slot_lo,
+                                          int slot_hi, int64_t cap, const uint8_t* d_w_gate_up_q,
+                                          const uint8_t* d_w_gate_up_scales,
+                                          const uint8_t* d_w_down_q,
+                                          const uint8_t* d_w_down_scales, int H, int I,
+                                          void* d_out_sorted, void* d_ws, size_t ws_bytes,
+                                          uint32_t* d_status, void* stream) {
+  if (P < 1 || P > MOE_MAX_SLOTS || slot_lo < 0 || slot_hi > P || slot_lo > slot_hi || cap < 0 ||
+      cap > INT32_MAX || H < 128 || H % 128 != 0 || I < 128 || I % 128 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if ((int64_t)P * H > INT32_MAX || (int64_t)2 * P * I > INT32_MAX) return MOE_ERR_INVALID_ARG;
+  if (cap == 0 || slot_lo == slot_hi) return MOE_OK;
+  if (d_sorted_q == nullptr || d_sorted_scales == nullptr || d_offsets_P == nullptr ||
+      d_w_gate_up_q == nullptr || d_w_gate_up_scales == nullptr || d_w_down_q == nullptr ||
+      d_w_down_scales == nullptr || d_out_sorted == nullptr || d_ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(d_sorted_q) || !aligned16(d_w_gate_up_q) || !aligned16(d_w_down_q) ||
+      !aligned16(d_out_sorted) || !aligned16(d_ws))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_grouped_ffn_fp8_ws_bytes(cap, I)) return MOE_ERR_CAPACITY;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
+  F8Args a;
+  a.xq = d_sorted_q;
+  a.xscale = d_sorted_scales;
+  a.offsets = d_offsets_P;
+  a.P = P;
+  a.slot_lo = slot_lo;
+  a.slot_hi = slot_hi;
+  a.cap = cap;
+  a.wguq = d_w_gate_up_q;
+  a.wgus = d_w_gate_up_scales;
+  a.wdq = d_w_down_q;
+  a.wds = d_w_down_scales;
+  a.H = H;
+  a.I = I;
+  a.hq = static_cast<uint8_t*>(d_ws);
+  a.hs = static_cast<uint8_t*>(d_ws) + hscale_offset(cap, I);
+  a.y = static_cast<__nv_bfloat16*>(d_out_sorted);
+  a.status = d_status;
+  cudaStream_t s = as_stream(stream);
+  moe_status st = run_f8<true>(a, s);
+  if (st != MOE_OK) return st;
+  return run_f8<false>(a, s);
+}

@@ -55,6 +55,13 @@ _SIGS = {
                                        _P, _P]),
     "moe_dispatch_noalloc": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _I, _I, _I64, _P,
                                   _P, _P, _P, _P, _P, _P]),
+    "moe_quantize_fp8_groups": (_I, [_P, _I64, _I, _I, _P, _P, _P]),
+    "moe_quantize_fp8_blocks": (_I, [_P, _I64, _I, _I, _P, _P, _P]),
+    "moe_dispatch_fp8": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _I, _I, _I64, _P, _P,
+                              _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "moe_grouped_ffn_fp8_ws_bytes": (_SZ, [_I64, _I]),
+    "moe_grouped_ffn_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I64, _P, _P, _P, _P, _I, _I, _P, _P,
+                                 _SZ, _P, _P]),
 }
 MOE_NOALLOC_SCRATCH_BYTES = 256 * 1024
 
@@ -229,6 +236,69 @@ def moe_dispatch_noalloc(x: Optional[torch.Tensor], ids: torch.Tensor, E: int, P
         _ptr(x), _ptr(ids), rows, k, H, dt, E, P, _ptr(l2p), _ptr(nrep), X, align,
         perm.numel(), _ptr(counts_P), _ptr(offsets_P), _ptr(perm), _ptr(inv), _ptr(sorted_out),
         _ptr(d_status), _stream(stream)))
+
+
+# ---------------------------------------------------------------- FP8 path
+def moe_quantize_fp8_groups(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, stream=None):
+    """Per-token groups of 128: x [n, K] bf16/f32 -> q uint8 [n, K], scales uint8 [n, K/128]."""
+    n, K = x.shape
+    _check("moe_quantize_fp8_groups", lib().moe_quantize_fp8_groups(
+        _ptr(x), n, K, dtype_code(x.dtype), _ptr(q), _ptr(scales), _stream(stream)))
+
+
+def moe_quantize_fp8_blocks(w: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, stream=None):
+    """128 x 128 blocks: w [R, K] -> q uint8 [R, K], scales uint8 [R/128, K/128]."""
+    R, K = w.shape
+    _check("moe_quantize_fp8_blocks", lib().moe_quantize_fp8_blocks(
+        _ptr(w), R, K, dtype_code(w.dtype), _ptr(q), _ptr(scales), _stream(stream)))
+
+
+def quantize_expert_weights_fp8(w_gate_up: torch.Tensor, w_down: torch.Tensor, stream=None):
+    """[P, 2I, H] and [P, H, I] expert weights -> (gate_up codes, gate_up scales [P, 2I/128,
+    H/128], down codes, down scales [P, H/128, I/128]), all uint8 on the weights' device."""
+    P, I2, H = w_gate_up.shape
+    I = w_down.shape[2]
+    u8 = dict(dtype=torch.uint8, device=w_gate_up.device)
+    guq = torch.empty(P, I2, H, **u8)
+    gus = torch.empty(P, I2 // 128, H // 128, **u8)
+    dq = torch.empty(P, H, I, **u8)
+    ds = torch.empty(P, H // 128, I // 128, **u8)
+    moe_quantize_fp8_blocks(w_gate_up.reshape(P * I2, H), guq.view(P * I2, H),
+                            gus.view(P * I2 // 128, H // 128), stream)
+    moe_quantize_fp8_blocks(w_down.reshape(P * H, I), dq.view(P * H, I),
+                            ds.view(P * H // 128, I // 128), stream)
+    return guq, gus, dq, ds
+
+
+def moe_dispatch_fp8(x: torch.Tensor, ids: torch.Tensor, E: int, P: int, counts_P, offsets_P,
+                     perm, inv, sorted_q: torch.Tensor, sorted_scales: torch.Tensor,
+                     ws: torch.Tensor, l2p=None, nrep=None, align: int = 1, d_status=None,
+                     stream=None):
+    rows, k = ids.shape
+    H = x.shape[1]
+    X = l2p.shape[1] if l2p is not None else 0
+    _check("moe_dispatch_fp8", lib().moe_dispatch_fp8(
+        _ptr(x), _ptr(ids), rows, k, H, dtype_code(x.dtype), E, P, _ptr(l2p), _ptr(nrep), X,
+        align, perm.numel(), _ptr(counts_P), _ptr(offsets_P), _ptr(perm), _ptr(inv),
+        _ptr(sorted_q), _ptr(sorted_scales), _ptr(ws), ws.numel() * ws.element_size(),
+        _ptr(d_status), _stream(stream)))
+
+
+def moe_grouped_ffn_fp8_ws_bytes(cap: int, I: int) -> int:
+    return int(lib().moe_grouped_ffn_fp8_ws_bytes(cap, I))
+
+
+def moe_grouped_ffn_fp8(xq: torch.Tensor, x_scales: torch.Tensor, offsets_P: torch.Tensor,
+                        w_fp8, ys: torch.Tensor, ws: torch.Tensor, slot_lo: int = 0,
+                        slot_hi: Optional[int] = None, d_status=None, stream=None):
+    """w_fp8 = quantize_expert_weights_fp8(...); ys bf16 [cap, H] out."""
+    guq, gus, dq, ds = w_fp8
+    P, I2, H = guq.shape
+    slot_hi = P if slot_hi is None else slot_hi
+    _check("moe_grouped_ffn_fp8", lib().moe_grouped_ffn_fp8(
+        _ptr(xq), _ptr(x_scales), _ptr(offsets_P), P, slot_lo, slot_hi, xq.shape[0], _ptr(guq),
+        _ptr(gus), _ptr(dq), _ptr(ds), H, I2 // 2, _ptr(ys), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(d_status), _stream(stream)))
 
 
 def moe_grouped_ffn(xs: torch.Tensor, offsets_P: torch.Tensor, w_gate_up: torch.Tensor,

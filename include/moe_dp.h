@@ -295,6 +295,64 @@ moe_status moe_dispatch_noalloc(const void* d_global, const int32_t* d_ids, int6
                                 int32_t* d_counts_P, int32_t* d_offsets_P, int32_t* d_perm,
                                 int32_t* d_inv, void* d_sorted, uint32_t* d_status, void* stream);
 
+/* ------------------------------------------------------------------ FP8 path
+ * [P1] section "prefll 侧的一个必要步骤:per-token-group 量化": before dispatch
+ * the hidden states are quantised to FP8 in groups of 128 consecutive
+ * features of one token (the same 128 as expert_alignment) with UE8M0 scale
+ * factors for DeepGEMM's 1x128 fine-grained scaling.  Here:
+ *   codes   e4m3 (no infinities, max 448), round to nearest with ties to
+ *           even, saturating at +-448; one byte per value;
+ *   scales  per group of 128 values the smallest power of two 2^e with
+ *           amax <= 448 * 2^e (e = 0 for an all-zero group), stored as the
+ *           byte e + 127; code = e4m3(x / 2^e), value = e4m3 * 2^e.
+ * Expert weights use the same rule on 128 x 128 blocks (output rows x input
+ * features); gate and up rows of [P, 2I, H] fall in separate blocks. */
+
+/* Per-token groups: x [n, K] (K a multiple of 128, MOE_BF16 or MOE_F32,
+ * 16-byte aligned) -> d_q uint8[n, K] codes, d_scales uint8[n, K / 128]. */
+moe_status moe_quantize_fp8_groups(const void* d_x, int64_t n, int K, int dtype, uint8_t* d_q,
+                                   uint8_t* d_scales, void* stream);
+
+/* 128 x 128 blocks: w [R, K] (R and K multiples of 128) -> d_q uint8[R, K],
+ * d_scales uint8[R / 128, K / 128] (row-major over blocks).  Weights of all
+ * slots quantise as one [P * rows, K] matrix. */
+moe_status moe_quantize_fp8_blocks(const void* d_w, int64_t R, int K, int dtype, uint8_t* d_q,
+                                   uint8_t* d_scales, void* stream);
+
+/* moe_dispatch whose permuted rows are quantised on the way: every routed
+ * copy of row g is the per-token-group FP8 quantisation of d_global row g.
+ *   d_sorted_q       device uint8[cap, H] codes (16-byte aligned)
+ *   d_sorted_scales  device uint8[cap, H / 128] scale bytes
+ * H must be a multiple of 128.  Alignment padding rows get zero codes and
+ * scale byte 127.  Counts, offsets, perm, inv and errors as moe_dispatch. */
+moe_status moe_dispatch_fp8(const void* d_global, const int32_t* d_ids, int64_t rows, int k,
+                            int H, int dtype, int E, int P, const int32_t* d_l2p,
+                            const int32_t* d_nrep, int X, int align, int64_t cap,
+                            int32_t* d_counts_P, int32_t* d_offsets_P, int32_t* d_perm,
+                            int32_t* d_inv, uint8_t* d_sorted_q, uint8_t* d_sorted_scales,
+                            void* d_ws, size_t ws_bytes, uint32_t* d_status, void* stream);
+
+/* Workspace of moe_grouped_ffn_fp8: the FP8 SwiGLU activation (codes and
+ * scale bytes) of cap rows. */
+size_t moe_grouped_ffn_fp8_ws_bytes(int64_t cap, int I);
+
+/* Grouped SwiGLU FFN on FP8 operands (moe_grouped_ffn's computation): per
+ * slot s in [slot_lo, slot_hi) and row x, with every GEMM summing
+ * 2^(e_row + e_weight_block) * (e4m3 products) over 128-deep blocks in fp32:
+ *   h = silu(x . Wg_s^T) * (x . Wu_s^T), quantised per token in groups of
+ *   128 features; y = h . Wd_s^T, rounded to bf16.
+ *   d_sorted_q, d_sorted_scales   moe_dispatch_fp8's output
+ *   d_w_gate_up_q [P, 2I, H], d_w_gate_up_scales [P, 2I/128, H/128]
+ *   d_w_down_q [P, H, I], d_w_down_scales [P, H/128, I/128]
+ *   d_out_sorted  device bf16 [cap, H] out (rows of the slot range)
+ * H and I multiples of 128; sm_103 only (else MOE_ERR_UNSUPPORTED). */
+moe_status moe_grouped_ffn_fp8(const uint8_t* d_sorted_q, const uint8_t* d_sorted_scales,
+                               const int32_t* d_offsets_P, int P, int slot_lo, int slot_hi,
+                               int64_t cap, const uint8_t* d_w_gate_up_q,
+                               const uint8_t* d_w_gate_up_scales, const uint8_t* d_w_down_q,
+                               const uint8_t* d_w_down_scales, int H, int I, void* d_out_sorted,
+                               void* d_ws, size_t ws_bytes, uint32_t* d_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

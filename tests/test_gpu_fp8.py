@@ -1,0 +1,180 @@
+"""GPU parity of the FP8 path against the oracle: quantisation and dispatch codes
+bit-exact, the FP8 grouped FFN within the bf16 output tolerance.
+
+Expected values come from the oracle only; the FP8 operands fed to the FFN are
+the oracle's quantisation of the seeded inputs."""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import BF16_ATOL, BF16_RTOL, as_f32, assert_close, rel_fro, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def md():
+    from combine_dp_gather_gb300 import build, moe_dp
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    moe_dp.lib()
+    return moe_dp
+
+
+@pytest.fixture(autouse=True)
+def _free_gpu():
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _status(st):
+    torch.cuda.synchronize()
+    return int(st.item())
+
+
+def _rows(n, K, seed, dtype=torch.bfloat16):
+    """Rows with per-group magnitudes from 2^-20 to 2^12, zero groups and exact ties."""
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    x = torch.randn(n, K, generator=g, device=DEV)
+    mag = 2.0 ** torch.randint(-20, 13, (n, K // 128), generator=g, device=DEV).float()
+    x = x * mag.repeat_interleave(128, dim=1)
+    if n > 2:
+        x[1, :128] = 0.0                              # an all-zero group
+        x[2, :4] = torch.tensor([448.0, 464.0, -0.5, 3.25])  # codes at and near the top
+    return x.to(dtype).contiguous()
+
+
+@pytest.mark.parametrize("n,K,dtype", [(37, 256, torch.bfloat16), (1, 7168, torch.bfloat16),
+                                       (129, 1152, torch.float32), (0, 128, torch.bfloat16)])
+def test_quantize_groups_bitexact(md, orc, n, K, dtype):
+    x = _rows(n, K, seed=n + K, dtype=dtype) if n else torch.empty(0, K, device=DEV, dtype=dtype)
+    q = torch.full((n, K), 0x55, dtype=torch.uint8, device=DEV)
+    s = torch.full((n, K // 128), 0x55, dtype=torch.uint8, device=DEV)
+    md.moe_quantize_fp8_groups(x, q, s)
+    torch.cuda.synchronize()
+    if n == 0:
+        return
+    xq_o, xs_o = orc.quant_groups(as_f32(to_np(x)))
+    assert np.array_equal(to_np(q), xq_o)
+    assert np.array_equal(to_np(s), xs_o)
+
+
+@pytest.mark.parametrize("R,K,dtype", [(256, 384, torch.bfloat16), (128, 7168, torch.float32)])
+def test_quantize_blocks_bitexact(md, orc, R, K, dtype):
+    g = torch.Generator(device=DEV).manual_seed(R + K)
+    w = torch.randn(R, K, generator=g, device=DEV) * 0.02
+    mag = 2.0 ** torch.randint(-6, 7, (R // 128, K // 128), generator=g, device=DEV).float()
+    w = (w * mag.repeat_interleave(128, 0).repeat_interleave(128, 1)).to(dtype).contiguous()
+    q = torch.empty(R, K, dtype=torch.uint8, device=DEV)
+    s = torch.empty(R // 128, K // 128, dtype=torch.uint8, device=DEV)
+    md.moe_quantize_fp8_blocks(w, q, s)
+    torch.cuda.synchronize()
+    wq_o, ws_o = orc.quant_blocks(as_f32(to_np(w)))
+    assert np.array_equal(to_np(q), wq_o)
+    assert np.array_equal(to_np(s), ws_o)
+
+
+@pytest.mark.parametrize("rows,E,align", [(300, 16, 1), (3001, 64, 128), (700, 64, 1)])
+def test_dispatch_fp8_bitexact(md, orc, rows, E, align):
+    k, H = 8, 1152          # 9 groups: one 1024-value segment plus a 128-value tail
+    g = torch.Generator(device=DEV).manual_seed(rows)
+    ids = torch.rand(rows, E, generator=g, device=DEV).argsort(dim=1)[:, :k].to(torch.int32)
+    ids[::7] = -1
+    ids = ids.contiguous()
+    x = _rows(rows, H, seed=rows + 1)
+    cap = md.moe_dispatch_cap_bound(rows, k, E, align)
+    counts_P = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets_P = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(cap, dtype=torch.int32, device=DEV)
+    inv = torch.empty(rows, k, dtype=torch.int32, device=DEV)
+    xq = torch.full((cap, H), 0x55, dtype=torch.uint8, device=DEV)
+    xs = torch.full((cap, H // 128), 0x55, dtype=torch.uint8, device=DEV)
+    ws = torch.empty(md.moe_dispatch_ws_bytes(rows, k, E), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    md.moe_dispatch_fp8(x, ids, E, E, counts_P, offsets_P, perm, inv, xq, xs, ws, align=align,
+                        d_status=st)
+    assert _status(st) == 0
+    c_o, o_o, p_o, i_o = orc.dispatch(to_np(ids), E, E, None, None, align, cap)
+    n = int(o_o[-1])
+    assert np.array_equal(to_np(counts_P), c_o)
+    assert np.array_equal(to_np(offsets_P), o_o)
+    assert np.array_equal(to_np(perm)[:n], p_o[:n])
+    assert np.array_equal(to_np(inv), i_o)
+    q_o, s_o = orc.quant_groups(as_f32(to_np(x)))
+    real = p_o[:n] >= 0
+    got_q, got_s = to_np(xq)[:n], to_np(xs)[:n]
+    assert np.array_equal(got_q[real], q_o[p_o[:n][real]])
+    assert np.array_equal(got_s[real], s_o[p_o[:n][real]])
+    assert (got_q[~real] == 0).all() and (got_s[~real] == 127).all()   # alignment padding
+    assert (to_np(xq)[n:] == 0x55).all()                                  # past the last slot
+
+
+def _fp8_inputs(orc, counts, H, I, seed, extra_rows=40):
+    P = len(counts)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    cap = int(offsets[-1]) + extra_rows
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((cap, H)).astype(np.float32)
+    xq, xe = orc.quant_groups(x)
+    # per-block weight magnitudes differ, so a misread block scale shows
+    def blocks(R, K):
+        m = 2.0 ** rng.integers(-3, 4, (R // 128, K // 128))
+        return (rng.standard_normal((R, K)) * 0.05 * m.repeat(128, 0).repeat(128, 1))
+    wgu = [orc.quant_blocks(blocks(2 * I, H)) for _ in range(P)]
+    wd = [orc.quant_blocks(blocks(H, I)) for _ in range(P)]
+    return offsets, cap, xq, xe, wgu, wd
+
+
+def _dev_u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+@pytest.mark.parametrize("counts,lo,hi", [
+    ([0, 1, 15, 16, 17, 31, 32, 33, 64, 100], 0, 10),
+    ([5, 0, 40, 3], 1, 3),
+    ([1] * 6, 0, 6)])
+def test_grouped_ffn_fp8(md, orc, counts, lo, hi):
+    """Token groups of 32 per unit: N = 16 or 32, ragged groups, several groups per slot,
+    empty slots, slot ranges; rows outside the range untouched."""
+    H, I = 512, 256
+    offsets, cap, xq, xe, wgu, wd = _fp8_inputs(orc, counts, H, I, seed=sum(counts) + lo)
+    P = len(counts)
+    w_fp8 = (_dev_u8(np.stack([w[0] for w in wgu])), _dev_u8(np.stack([w[1] for w in wgu])),
+             _dev_u8(np.stack([w[0] for w in wd])), _dev_u8(np.stack([w[1] for w in wd])))
+    sentinel = 1232.0
+    ys = torch.full((cap, H), sentinel, device=DEV, dtype=torch.bfloat16)
+    ws = torch.empty(md.moe_grouped_ffn_fp8_ws_bytes(cap, I), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    md.moe_grouped_ffn_fp8(_dev_u8(xq), _dev_u8(xe), torch.from_numpy(offsets).to(DEV), w_fp8, ys,
+                           ws, lo, hi, d_status=st)
+    assert _status(st) == 0
+    a, b = int(offsets[lo]), int(offsets[hi])
+    ref = orc.grouped_ffn_fp8(xq, xe, offsets, lambda s: (*wgu[s], *wd[s]), lo, hi)
+    got = as_f32(to_np(ys)).astype(np.float64)
+    assert_close(got[a:b], ref[a:b], BF16_ATOL, BF16_RTOL, "grouped FFN fp8")
+    assert rel_fro(got[a:b], ref[a:b]) < 1e-2
+    assert (got[:a] == sentinel).all() and (got[b:] == sentinel).all()
+
+
+def test_grouped_ffn_fp8_dsv3_width(md, orc):
+    """DeepSeek-V3 expert shapes (H=7168, I=2048): 56 and 16 k-blocks per unit."""
+    counts = [3, 20, 0, 9]
+    H, I = 7168, 2048
+    offsets, cap, xq, xe, wgu, wd = _fp8_inputs(orc, counts, H, I, seed=3, extra_rows=8)
+    w_fp8 = (_dev_u8(np.stack([w[0] for w in wgu])), _dev_u8(np.stack([w[1] for w in wgu])),
+             _dev_u8(np.stack([w[0] for w in wd])), _dev_u8(np.stack([w[1] for w in wd])))
+    ys = torch.zeros((cap, H), device=DEV, dtype=torch.bfloat16)
+    ws = torch.empty(md.moe_grouped_ffn_fp8_ws_bytes(cap, I), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    md.moe_grouped_ffn_fp8(_dev_u8(xq), _dev_u8(xe), torch.from_numpy(offsets).to(DEV), w_fp8, ys,
+                           ws, d_status=st)
+    assert _status(st) == 0
+    n = int(offsets[-1])
+    ref = orc.grouped_ffn_fp8(xq, xe, offsets, lambda s: (*wgu[s], *wd[s]))
+    got = as_f32(to_np(ys)).astype(np.float64)
+    assert_close(got[:n], ref[:n], BF16_ATOL, BF16_RTOL, "grouped FFN fp8, DSV3 width")
+    assert rel_fro(got[:n], ref[:n]) < 1e-2
