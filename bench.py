@@ -42,19 +42,24 @@ METRIC = "MoE-layer tokens/s on 1 GB300"
 UNIT = "tokens/s"
 L2_NOTE = "inputs larger than L2: every step streams the touched experts' weights from HBM"
 
-def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int) -> int:
+def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
+                      fp8: bool = False) -> int:
     """Kernel launches of one layer step: gather (hidden states and logits), route,
     dispatch (one CTA-wide kernel for <= 16384 routed pairs whose tables fit 48 KB, else
     histogram + scan + rank; then the row copy; + the alignment pad kernel when
-    align > 1), grouped FFN (MM1+SwiGLU and MM2), combine, scatter."""
+    align > 1, plus the FP8 rows' pad kernel on the FP8 path), grouped FFN (MM1+SwiGLU
+    and MM2), combine, scatter."""
     small = rows * k <= 16384 and 4 * (33 * E + 3 * P + 1) <= 48 * 1024
-    dispatch = (1 if small else 3) + 1 + (1 if align > 1 else 0)
+    dispatch = (1 if small else 3) + 1 + (1 + (1 if fp8 else 0) if align > 1 else 0)
     return 2 + 1 + dispatch + 2 + 1 + 1
 
 
-def ffn_kernel(cap: int, P: int) -> str:
-    """The grouped-FFN kernel the library picks: weights as M on SM pairs from 192
-    sorted rows per slot on average, else tokens as M on single SMs."""
+def ffn_kernel(cap: int, P: int, fp8: bool = False) -> str:
+    """The grouped-FFN kernel the library picks: on FP8 operands the weights-as-M
+    single-SM kernel; in bf16 weights as M on SM pairs from 192 sorted rows per slot
+    on average, else tokens as M on single SMs."""
+    if fp8:
+        return "ffn_fp8_kernel"
     return "ffn_swap_kernel" if cap // max(P, 1) >= 192 else "ffn_tc_kernel"
 
 # dram__bytes_read.sum + dram__bytes_write.sum of the two grouped-FFN launches of one
@@ -95,6 +100,9 @@ def parse():
                     help="shared experts, always selected with weight 1 (0 = none)")
     ap.add_argument("--boundary", default="plain", choices=["plain", "addnorm"],
                     help="addnorm: residual add + RMSNorm fused into the hidden-state gather")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 dispatch and grouped FFN (e4m3, UE8M0 scales per 128-token group "
+                         "and 128x128 weight block); layer input and output stay bf16")
     ap.add_argument("--tokens", type=int, default=None,
                     help="prefill token count (with --experts: many rows, few weights)")
     return ap.parse_args()
@@ -213,7 +221,7 @@ class StepEvents:
 def ffn_traffic(args):
     if args.experts is not None or args.tokens is not None or args.seed != 0:
         return None  # recorded for the default workload only
-    rec = FFN_TRAFFIC.get(args.config)
+    rec = FFN_TRAFFIC.get(args.config + ("_fp8" if args.fp8 else ""))
     if not rec or rec["bytes"] is None:
         return None
     return rec["bytes"] if sources_sha(rec["sources"]) == rec["sha256_16"] else None
@@ -244,7 +252,7 @@ def run_native(args, rank, world, local_rank):
         tokens_per_req=spec.tokens_per_req, renormalize=spec.renormalize, align=spec.align,
         l2p=None if l2p_np is None else torch.from_numpy(l2p_np).to(dev),
         nrep=None if nrep_np is None else torch.from_numpy(nrep_np).to(dev),
-        n_shared=spec.n_shared)
+        n_shared=spec.n_shared, fp8=args.fp8)
     out = [torch.empty(c, spec.H, device=dev, dtype=wgu.dtype) for c in spec.counts]
     res_loc = None
     if args.boundary == "addnorm":
@@ -288,22 +296,30 @@ def run_native(args, rank, world, local_rank):
     routed = int(layer.offsets_P[-1].item())
     T = spec.T
     b = 2 if spec.dtype == "bf16" else 4
-    ffn_bytes = touched * 3 * spec.I * spec.H * b + routed * (2 * spec.H + 2 * spec.I) * b
+    if args.fp8:
+        # e4m3 weights + one scale byte per 128x128 block; per routed row: FP8 input row
+        # and scales, h written and read back (codes + scales), bf16 output row
+        ffn_bytes = touched * 3 * spec.I * spec.H * (1 + 1 / 16384) + routed * (
+            spec.H * (1 + 1 / 128) + 2 * spec.I * (1 + 1 / 128) + 2 * spec.H)
+    else:
+        ffn_bytes = touched * 3 * spec.I * spec.H * b + routed * (2 * spec.H + 2 * spec.I) * b
     ffn_flops = synth.flops_ffn(T, spec.k + spec.n_shared, spec.H, spec.I)
     ffn_ms = stage_ms["ffn"]
     pk = peaks()
-    hbm_bound = ffn_flops / (ffn_bytes) < (pk["bf16_tflops"] * 1e12) / (pk["hbm_gbs"] * 1e9)
+    # an FP8 contraction takes the bf16 measured peak x 2 (the nominal fp8:bf16 ratio)
+    tc_peak = pk["bf16_tflops"] * (2 if args.fp8 else 1)
+    hbm_bound = ffn_flops / (ffn_bytes) < (tc_peak * 1e12) / (pk["hbm_gbs"] * 1e9)
     if hbm_bound:
         achieved = ffn_bytes / (ffn_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4)}
     else:
         achieved = ffn_flops / (ffn_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4)}
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tc_peak,
+                "unit": "TFLOP/s", "frac": round(achieved / tc_peak, 4)}
     tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12
     roof.update({"traffic": ffn_traffic(args),
-                 "kernel": f"moe_grouped_ffn ({ffn_kernel(layer.cap, layer.P)} MM1+SwiGLU "
+                 "kernel": f"moe_grouped_ffn ({ffn_kernel(layer.cap, layer.P, args.fp8)} MM1+SwiGLU "
                            "and MM2 launches)",
                  "tflops": round(tflops, 1),
                  "frac_of_bf16_peak": round(tflops / pk["bf16_tflops"], 4),
@@ -407,15 +423,17 @@ def run_native(args, rank, world, local_rank):
                 e2e=e2e, rows=rows, touched=touched,
                 launches=launches_per_step(max(rows, 1), spec.k + spec.n_shared,
                                            spec.E + spec.n_shared, layer.P, layer.cap,
-                                           spec.align),
+                                           spec.align, args.fp8),
                 inputs=(x_loc, lg_loc, wgu, wd, l2p_np, nrep_np))
 
 
 # ------------------------------------------------------------------ oracle (CPU)
-def oracle_sample_step(spec, n_tokens, x_loc, lg_loc, wgu, wd, l2p, nrep):
+def oracle_sample_step(spec, n_tokens, x_loc, lg_loc, wgu, wd, l2p, nrep, fp8=False):
     """One oracle pass over the first n_tokens tokens of the workload (replica
-    order, MAX/SUM/static layout of the truncated counts).  Returns (seconds of
-    oracle compute, cpu seconds)."""
+    order, MAX/SUM/static layout of the truncated counts).  With fp8 the permuted
+    rows are quantised (timed) and the experts run on FP8 operands (weight
+    quantisation is preparation, not timed).  Returns (seconds of oracle compute,
+    cpu seconds)."""
     import oracle
     counts, left = [], n_tokens
     for c in spec.counts:
@@ -438,6 +456,8 @@ def oracle_sample_step(spec, n_tokens, x_loc, lg_loc, wgu, wd, l2p, nrep):
     cnt, o, perm, inv = oracle.dispatch(ids, spec.E + spec.n_shared, spec.slots, l2p, nrep,
                                         spec.align)
     xsrt = oracle.permute_rows(xg, perm[: o[-1]])
+    if fp8:
+        xq, xe = oracle.quant_groups(xsrt)
     wall = time.perf_counter() - w0
     cpu = time.process_time() - c0
     ys = np.zeros(xsrt.shape, np.float64)
@@ -446,8 +466,13 @@ def oracle_sample_step(spec, n_tokens, x_loc, lg_loc, wgu, wd, l2p, nrep):
         if b_ == a:
             continue
         wg_s, wd_s = to32(wgu[s]), to32(wd[s])        # input conversion, not timed
+        if fp8:
+            wq = (*oracle.quant_blocks(wg_s), *oracle.quant_blocks(wd_s))
         w0, c0 = time.perf_counter(), time.process_time()
-        ys[a:b_] = oracle.expert_ffn(xsrt[a:b_], wg_s, wd_s)
+        if fp8:
+            ys[a:b_] = oracle.expert_ffn_fp8(xq[a:b_], xe[a:b_], *wq)
+        else:
+            ys[a:b_] = oracle.expert_ffn(xsrt[a:b_], wg_s, wd_s)
         wall += time.perf_counter() - w0
         cpu += time.process_time() - c0
     w0, c0 = time.perf_counter(), time.process_time()
@@ -467,17 +492,18 @@ def oracle_inputs(spec):
     return x_loc, lg_loc, wgu, wd, l2p, nrep
 
 
-def cpu_baseline(spec, budget_s=20.0, inputs=None):
+def cpu_baseline(spec, budget_s=20.0, inputs=None, fp8=False):
     import oracle
     oracle.build()
     x_loc, lg_loc, wgu, wd, l2p, nrep = inputs or oracle_inputs(spec)
-    wall1, _ = oracle_sample_step(spec, 1, x_loc, lg_loc, wgu, wd, l2p, nrep)
+    wall1, _ = oracle_sample_step(spec, 1, x_loc, lg_loc, wgu, wd, l2p, nrep, fp8)
     n = int(max(1, min(spec.T, budget_s / max(wall1, 1e-3))))
-    wall, cpu = oracle_sample_step(spec, n, x_loc, lg_loc, wgu, wd, l2p, nrep)
+    wall, cpu = oracle_sample_step(spec, n, x_loc, lg_loc, wgu, wd, l2p, nrep, fp8)
+    ffn = "FP8 (e4m3) SwiGLU FFN in fp64" if fp8 else "fp64 SwiGLU FFN"
     return {"value": round(n / wall, 3), "unit": UNIT, "cores": round(cpu / wall, 2),
             "kind": "oracle",
             "sample": f"first {n} of the {spec.T} tokens of {spec.name}, whole layer (gather, "
-                      f"top-{spec.k}, dispatch, fp64 SwiGLU FFN, combine, scatter), "
+                      f"top-{spec.k}, dispatch, {ffn}, combine, scatter), "
                       f"{wall:.1f} s wall; cores = CPU time / wall time"}
 
 
@@ -488,14 +514,14 @@ def run_reference(args, rank, world):
     import oracle
     oracle.build()
     inputs = oracle_inputs(spec)
-    wall1, _ = oracle_sample_step(spec, 1, *inputs)
+    wall1, _ = oracle_sample_step(spec, 1, *inputs, args.fp8)
     budget = 120.0
     n = int(max(1, min(spec.T, budget / (args.steps + args.warmup) / max(wall1, 1e-3))))
     for _ in range(args.warmup):
-        oracle_sample_step(spec, n, *inputs)
+        oracle_sample_step(spec, n, *inputs, args.fp8)
     walls, cpus = [], []
     for _ in range(args.steps):
-        w, c = oracle_sample_step(spec, n, *inputs)
+        w, c = oracle_sample_step(spec, n, *inputs, args.fp8)
         walls.append(w)
         cpus.append(c)
     tot = sum(walls)
@@ -505,7 +531,8 @@ def run_reference(args, rank, world):
             "ms_per_step": round(1e3 * tot / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": dict(synth.describe(spec), sample_tokens_per_step=n),
+            "config": dict(synth.describe(spec), sample_tokens_per_step=n,
+                           fp8="e4m3 operands, fp64 arithmetic" if args.fp8 else None),
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT,
                              "cores": round(sum(cpus) / tot, 2), "kind": "oracle",
                              "sample": f"first {n} tokens of {spec.name} per step"},
@@ -555,9 +582,12 @@ def main():
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8-e4m3" if args.fp8 else spec.dtype, "data": "synthetic",
             "config": dict(synth.describe(spec), global_rows=r["rows"], l2=L2_NOTE, **r["extra"],
                            boundary=args.boundary, shared_experts=spec.n_shared,
+                           fp8=("e4m3 codes, UE8M0 scales per 128-token group and 128x128 "
+                                "weight block; bf16 layer input/output") if args.fp8 else None,
                            parallelism=f"{world} independent replica(s), one per GPU",
                            stage_ms={k: round(v, 4) for k, v in r["stage_ms"].items()}),
             "roofline": r["roof"],
@@ -571,7 +601,7 @@ def main():
                            "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                            "ms_per_step": round(agg["e2e_ms_max"] / e["steps"], 4)}
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(spec, inputs=r["inputs"])
+            line["cpu_baseline"] = cpu_baseline(spec, inputs=r["inputs"], fp8=args.fp8)
         print(json.dumps(line), flush=True)
     finally:
         if world > 1 and torch.distributed.is_initialized():

@@ -12,24 +12,28 @@
 // in tensor memory, and the epilogue warps add it into fp32 registers scaled
 // by 2^(e_token + e_weight):
 //   acc[row, t] += 2^(ex[t, kb] + ew[row / 128, kb]) * partial_kb[row, t]
-// The weights are the MMA's M operand (128 rows per CTA) and up to 32 of a
-// slot's tokens its N, so the accumulator of a unit lives in registers (one
-// weight row per thread, 32 token columns).
+// The weights are the MMA's M operand (two 128-row MMAs per K step, 256 rows
+// and one 32 KB TMA box per stage) and up to 64 of a slot's tokens its N (one
+// weight pass serves them all; a second token group would stream the weights
+// from DRAM again), so the accumulators of a unit live in registers: each
+// epilogue thread owns two weight rows and 32 token columns.
 //   MM1 + SwiGLU: unit = (slot, 128 features f, token group); A = gate rows
 //                 f..f+127 and the same up rows (one 3-D TMA box), two MMAs
 //                 per K step; the epilogue forms h = silu(gate) * up and
 //                 quantises it per token over its 128 features (one group),
 //                 writing codes and the scale byte for the down projection.
-//   MM2:          unit = (slot, 128 output rows, token group); bf16 output.
+//   MM2:          unit = (slot, 256 output rows, token group): two MMAs per K
+//                 step on the two 128-row halves; bf16 output.
 // With few tokens per slot (decode) the weight stream is the whole cost, and
 // FP8 weights halve it.
 //
-// Roles (192 threads, one CTA per SM):
+// Roles (320 threads, one CTA per SM):
 //   warp 0    TMA producer: weight box + token box per stage
 //   warp 1    TMEM allocation; lane 0 issues the MMAs and commits (stage free,
-//             partial ready); partials ping-pong between two TMEM buffers
-//   warps 2-5 epilogue: per k-block tcgen05.ld of the partial(s), release,
-//             scale and accumulate; per unit SwiGLU + quantisation or bf16 out
+//             partial ready); partials rotate through four TMEM buffers
+//   warps 2-9 epilogue, two warps per TMEM lane quarter (token columns 0-31 and
+//             32-63): per k-block tcgen05.ld of the partials, release, scale and
+//             accumulate; per unit SwiGLU + quantisation or bf16 out
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets
 // MOE_DEV_TIMEOUT, the other roles stop at their next wait, TMEM is freed and
 // the kernel returns.
@@ -45,29 +49,31 @@ namespace {
 using namespace tc;
 
 constexpr int BK = 128;     // fp8 values per k-block = one 128-byte swizzle row = one scale group
-constexpr int NT = 32;      // tokens per unit
-constexpr int THREADS = 192;
+constexpr int NT = 64;      // tokens per unit
+constexpr int CT = 32;      // token columns per epilogue warp
+constexpr int THREADS = 320;
+constexpr int NPB = 4;      // TMEM partial buffers: the MMAs run up to 4 k-blocks ahead of the epilogue
 
 template <bool SWIGLU>
 struct F8Cfg {
-  static constexpr int A_ROWS = SWIGLU ? 256 : 128;  // gate + up, or down rows
+  static constexpr int A_ROWS = 256;  // 128 gate + 128 up rows, or 256 down rows
   static constexpr int A_BYTES = A_ROWS * BK;
   static constexpr int B_BYTES = NT * BK;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = SWIGLU ? 5 : 9;
-  static constexpr int PCOLS = SWIGLU ? 2 * NT : NT;  // partial columns per buffer
+  static constexpr int STAGES = 5;
+  static constexpr int PCOLS = 2 * NT;  // partial columns per buffer (two MMAs)
 };
 
 struct F8Smem {
-  uint64_t full[9];
-  uint64_t empty[9];
-  uint64_t pfull[2];
-  uint64_t pempty[2];
+  uint64_t full[5];
+  uint64_t empty[5];
+  uint64_t pfull[NPB];
+  uint64_t pempty[NPB];
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t total_units;
   int32_t warp_sums[THREADS / 32];
-  float wmax[4][NT];                 // per-warp token maxima of h
+  float wmax[2][4][CT];              // per epilogue warp: token maxima of h
   int32_t pref[MOE_MAX_SLOTS + 1];   // unit prefix over the slot range
   int32_t row0[MOE_MAX_SLOTS];
   int32_t rows[MOE_MAX_SLOTS];
@@ -88,12 +94,18 @@ struct F8Params {
   const uint8_t* xscale;   // [cap, K / 128] token scale bytes
   const uint8_t* wscale;   // weight scale bytes [P, rows / 128, K / 128]
   int wscale_rows;         // rows / 128 per slot: 2I/128 (MM1) or H/128 (MM2)
-  int up_block;            // MM1: I / 128 (first up block)
+  int blk_mul, blk_off;    // weight blocks of tile t: t*blk_mul and t*blk_mul + blk_off
   int out_ld;
   uint8_t* hq;             // MM1: h codes [cap, I]
   uint8_t* hscale;         // MM1: h scale bytes [cap, I / 128]
   __nv_bfloat16* y;        // MM2: [cap, H]
   uint32_t* status;
+};
+
+// Token-row tensor maps with boxes of 16, 32, 48 and 64 rows (N = 16 .. 64).
+struct TokMaps {
+  CUtensorMap m[NT / 16];
+  __host__ __device__ const CUtensorMap& operator[](int i) const { return m[i]; }
 };
 
 __host__ __device__ __forceinline__ int32_t token_groups(int32_t rows) {
@@ -130,8 +142,8 @@ __device__ __forceinline__ F8Unit decode_unit(const F8Smem& L, int nslots, int u
 
 template <bool SWIGLU>
 __global__ void __launch_bounds__(THREADS, 1)
-    ffn_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB16,
-                   const __grid_constant__ CUtensorMap tmB32, const F8Params p) {
+    ffn_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ TokMaps tmB,
+                   const F8Params p) {
   using C = F8Cfg<SWIGLU>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -169,9 +181,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(smem_u32(&L.full[i]), 1);   // the producer's expect_tx
         mbar_init(smem_u32(&L.empty[i]), 1);  // the MMA commit
       }
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < NPB; ++i) {
         mbar_init(smem_u32(&L.pfull[i]), 1);   // the MMA commit
-        mbar_init(smem_u32(&L.pempty[i]), 4);  // every epilogue warp
+        mbar_init(smem_u32(&L.pempty[i]), 8);  // every epilogue warp
       }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -209,7 +221,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const F8Unit un = decode_unit(L, p.nslots, u);
       const int32_t slot = p.slot_lo + un.slot;
-      const CUtensorMap* bmap = un.N == 16 ? &tmB16 : &tmB32;
+      const CUtensorMap* bmap = &tmB[(un.N >> 4) - 1];
       const uint32_t tx = (uint32_t)(C::A_BYTES + un.N * BK);
       bool ok = true;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
@@ -227,7 +239,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (SWIGLU)
             tma_load_3d<1>(sa, &tmA, kc, un.tile * 128, 2 * slot, full, pol_w);
           else
-            tma_load_2d<1>(sa, &tmA, kc, slot * p.wrows_per_slot + un.tile * 128, full, pol_w);
+            tma_load_2d<1>(sa, &tmA, kc, slot * p.wrows_per_slot + un.tile * 256, full, pol_w);
           tma_load_2d<1>(sb, bmap, kc, un.tok0, full, pol_tok);
         }
         __syncwarp();
@@ -247,7 +259,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
-        const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
+        const uint32_t pb = it % NPB, pph = (it / NPB) & 1u;
         if (!wait_bar(smem_u32(&L.full[st]), ph, abort_flag, p.status) ||
             !wait_bar(smem_u32(&L.pempty[pb]), pph ^ 1u, abort_flag, p.status)) {
           ok = false;
@@ -263,7 +275,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {  // +32 bytes per K=32 step in the swizzle row
             mma_e4m3(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk != 0);
-            if (SWIGLU) mma_e4m3(d + NT, adesc_up + 2 * kk, bdesc + 2 * kk, idesc, kk != 0);
+            mma_e4m3(d + NT, adesc_up + 2 * kk, bdesc + 2 * kk, idesc, kk != 0);
           }
           commit<1>(smem_u32(&L.empty[st]));
           commit<1>(smem_u32(&L.pfull[pb]));
@@ -274,33 +286,36 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 = weight rows of the tile
-    const uint32_t lanes = tmem_base + ((uint32_t)(q * 32) << 16);
+    const int q = warp & 3;          // TMEM lanes 32q .. 32q+31 = weight rows of the tile
+    const int cg = (warp - 2) >> 2;  // token columns 32cg .. 32cg+31 of the unit
+    const uint32_t lanes = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(cg * CT);
+    const uint32_t bar_id = 1u + (uint32_t)cg;  // the four warps of this column group
     uint32_t it = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const F8Unit un = decode_unit(L, p.nslots, u);
       const int32_t slot = p.slot_lo + un.slot;
-      // scale bytes, loaded one k-block ahead: lane j holds token j's byte,
+      const int t0 = cg * CT;  // first token of this warp's columns
+      // scale bytes, loaded one k-block ahead: lane j holds token t0 + j's byte,
       // every lane the weight blocks' bytes
-      const int64_t trow = (int64_t)un.tok0 + lane;
-      const bool tv = lane < un.ntok && trow < p.cap;
+      const int64_t trow = (int64_t)un.tok0 + t0 + lane;
+      const bool tv = t0 + lane < un.ntok && trow < p.cap;
       const uint8_t* xs_row = p.xscale + (tv ? trow : 0) * p.num_kb;
-      const int64_t wb0 = (int64_t)slot * p.wscale_rows + un.tile;
+      const int64_t wb0 = (int64_t)slot * p.wscale_rows + un.tile * p.blk_mul;
       const uint8_t* ws0 = p.wscale + wb0 * p.num_kb;
-      const uint8_t* ws1 = p.wscale + (wb0 + p.up_block) * p.num_kb;
-      uint32_t nx = tv ? xs_row[0] : 127u, nw0 = ws0[0], nw1 = SWIGLU ? ws1[0] : 127u;
-      float acc0[NT], acc1[NT];
+      const uint8_t* ws1 = p.wscale + (wb0 + p.blk_off) * p.num_kb;
+      uint32_t nx = tv ? xs_row[0] : 127u, nw0 = ws0[0], nw1 = ws1[0];
+      float acc0[CT], acc1[CT];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) acc0[j] = acc1[j] = 0.0f;
+      for (int j = 0; j < CT; ++j) acc0[j] = acc1[j] = 0.0f;
       bool ok = true;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const uint32_t ex = nx, ew0 = nw0, ew1 = nw1;
         if (kb + 1 < p.num_kb) {
           nx = tv ? xs_row[kb + 1] : 127u;
           nw0 = ws0[kb + 1];
-          if (SWIGLU) nw1 = ws1[kb + 1];
+          nw1 = ws1[kb + 1];
         }
-        const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
+        const uint32_t pb = it % NPB, pph = (it / NPB) & 1u;
         if (!wait_bar(smem_u32(&L.pfull[pb]), pph, abort_flag, p.status)) {
           ok = false;
           it += p.num_kb - kb;
@@ -309,57 +324,62 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_after();
         uint32_t r0[32], r1[32];
         tmem_ld32(lanes + pb * C::PCOLS, r0);
-        if (SWIGLU) tmem_ld32(lanes + pb * C::PCOLS + NT, r1);
+        tmem_ld32(lanes + pb * C::PCOLS + NT, r1);
         tmem_wait_ld();
         fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&L.pempty[pb]));
         const float cx_mine = pow2i((int)ex - 127);
         const float cw0 = pow2i((int)ew0 - 127);
-        const float cw1 = SWIGLU ? pow2i((int)ew1 - 127) : 0.0f;
+        const float cw1 = pow2i((int)ew1 - 127);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
+        for (int j = 0; j < CT; ++j) {
           const float cx = __shfl_sync(0xffffffffu, cx_mine, j);
           acc0[j] = fmaf(__uint_as_float(r0[j]), cx * cw0, acc0[j]);
-          if (SWIGLU) acc1[j] = fmaf(__uint_as_float(r1[j]), cx * cw1, acc1[j]);
+          acc1[j] = fmaf(__uint_as_float(r1[j]), cx * cw1, acc1[j]);
         }
       }
-      if (SWIGLU) ok = named_all(1, 128, ok);  // the four warps leave together
+      if (SWIGLU) ok = named_all(bar_id, 128, ok);  // the group's four warps leave together
       if (!ok) break;
-      const int feat = un.tile * 128 + q * 32 + lane;
       if (SWIGLU) {
+        const int feat = un.tile * 128 + q * 32 + lane;
         // h = silu(gate) * up, then per token one scale over its 128 features
-        float m[NT];
+        float m[CT];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
+        for (int j = 0; j < CT; ++j) {
           acc0[j] = acc0[j] / (1.0f + expf(-acc0[j])) * acc1[j];
           m[j] = fabsf(acc0[j]);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
-          for (int j = 0; j < NT; ++j) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], off));
+          for (int j = 0; j < CT; ++j) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], off));
         if (lane == 0)
 #pragma unroll
-          for (int j = 0; j < NT; ++j) L.wmax[q][j] = m[j];
-        named_sync(1, 128);
+          for (int j = 0; j < CT; ++j) L.wmax[cg][q][j] = m[j];
+        named_sync(bar_id, 128);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const float amax = fmaxf(fmaxf(L.wmax[0][j], L.wmax[1][j]), fmaxf(L.wmax[2][j], L.wmax[3][j]));
+        for (int j = 0; j < CT; ++j) {
+          const float amax = fmaxf(fmaxf(L.wmax[cg][0][j], L.wmax[cg][1][j]),
+                                   fmaxf(L.wmax[cg][2][j], L.wmax[cg][3][j]));
           const int e = fp8_scale_exp(amax);
-          const int64_t row = (int64_t)un.tok0 + j;
-          if (j < un.ntok && row < p.cap) {
+          const int64_t row = (int64_t)un.tok0 + t0 + j;
+          if (t0 + j < un.ntok && row < p.cap) {
             p.hq[row * p.out_ld + feat] = (uint8_t)(e4m3x4(acc0[j] * pow2i(-e), 0.f, 0.f, 0.f) & 0xFFu);
             if (q == 0 && lane == 0)
               p.hscale[row * (p.out_ld / 128) + un.tile] = (uint8_t)(e + 127);
           }
         }
-        named_sync(1, 128);  // the maxima are read before the next unit writes them
+        named_sync(bar_id, 128);  // the maxima are read before the next unit writes them
       } else {
+        const int feat = un.tile * 256 + q * 32 + lane;  // and feat + 128 (second half)
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const int64_t row = (int64_t)un.tok0 + j;
-          if (j < un.ntok && row < p.cap) p.y[row * p.out_ld + feat] = __float2bfloat16_rn(acc0[j]);
+        for (int j = 0; j < CT; ++j) {
+          const int64_t row = (int64_t)un.tok0 + t0 + j;
+          if (t0 + j < un.ntok && row < p.cap) {
+            p.y[row * p.out_ld + feat] = __float2bfloat16_rn(acc0[j]);
+            p.y[row * p.out_ld + feat + 128] = __float2bfloat16_rn(acc1[j]);
+          }
         }
       }
     }
@@ -411,13 +431,14 @@ template <bool SWIGLU>
 moe_status run_f8(const F8Args& a, cudaStream_t s) {
   int max_ctas = 0;
   if (!f8_setup<SWIGLU>(&max_ctas)) return MOE_ERR_CUDA;
-  CUtensorMap mA, mB16, mB32;
+  CUtensorMap mA;
+  TokMaps mB;
   const uint8_t* tok = SWIGLU ? a.xq : a.hq;
   const uint64_t K = SWIGLU ? (uint64_t)a.H : (uint64_t)a.I;
-  const bool ok = (SWIGLU ? make_map_u8_gate_up(&mA, a.wguq, a.H, a.I, a.P, 128)
-                          : make_map_u8(&mA, a.wdq, a.I, (uint64_t)a.P * a.H, 128)) &&
-                  make_map_u8(&mB16, tok, K, (uint64_t)a.cap, 16) &&
-                  make_map_u8(&mB32, tok, K, (uint64_t)a.cap, 32);
+  bool ok = SWIGLU ? make_map_u8_gate_up(&mA, a.wguq, a.H, a.I, a.P, 128)
+                   : make_map_u8(&mA, a.wdq, a.I, (uint64_t)a.P * a.H, 256);
+  for (int i = 0; i < NT / 16 && ok; ++i)
+    ok = make_map_u8(&mB.m[i], tok, K, (uint64_t)a.cap, 16u * (i + 1));
   if (!ok) return MOE_ERR_CUDA;
   F8Params p;
   p.offsets = a.offsets;
@@ -425,13 +446,14 @@ moe_status run_f8(const F8Args& a, cudaStream_t s) {
   p.nslots = a.slot_hi - a.slot_lo;
   p.cap = a.cap;
   p.num_kb = (int)(K / BK);
-  p.n_tiles = SWIGLU ? a.I / 128 : a.H / 128;
+  p.n_tiles = SWIGLU ? a.I / 128 : a.H / 256;
   p.wrows_per_slot = a.H;
   p.K = (int)K;
   p.xscale = SWIGLU ? a.xscale : a.hs;
   p.wscale = SWIGLU ? a.wgus : a.wds;
   p.wscale_rows = SWIGLU ? 2 * a.I / 128 : a.H / 128;
-  p.up_block = SWIGLU ? a.I / 128 : 0;
+  p.blk_mul = SWIGLU ? 1 : 2;
+  p.blk_off = SWIGLU ? a.I / 128 : 1;
   p.out_ld = SWIGLU ? a.I : a.H;
   p.hq = a.hq;
   p.hscale = a.hs;
@@ -440,7 +462,7 @@ moe_status run_f8(const F8Args& a, cudaStream_t s) {
   // upper bound of units (device-side counts unknown here)
   const int64_t bound = (a.cap / NT + p.nslots) * (int64_t)p.n_tiles;
   const int grid = (int)(bound < max_ctas ? bound : max_ctas);
-  ffn_fp8_kernel<SWIGLU><<<grid, THREADS, f8_smem_bytes<SWIGLU>(), s>>>(mA, mB16, mB32, p);
+  ffn_fp8_kernel<SWIGLU><<<grid, THREADS, f8_smem_bytes<SWIGLU>(), s>>>(mA, mB, p);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -466,7 +488,7 @@ extern "C" moe_status moe_grouped_ffn_fp8(const uint8_t* d_sorted_q,
                                           void* d_out_sorted, void* d_ws, size_t ws_bytes,
                                           uint32_t* d_status, void* stream) {
   if (P < 1 || P > MOE_MAX_SLOTS || slot_lo < 0 || slot_hi > P || slot_lo > slot_hi || cap < 0 ||
-      cap > INT32_MAX || H < 128 || H % 128 != 0 || I < 128 || I % 128 != 0)
+      cap > INT32_MAX || H < 256 || H % 256 != 0 || I < 128 || I % 128 != 0)
     return MOE_ERR_INVALID_ARG;
   if ((int64_t)P * H > INT32_MAX || (int64_t)2 * P * I > INT32_MAX) return MOE_ERR_INVALID_ARG;
   if (cap == 0 || slot_lo == slot_hi) return MOE_OK;

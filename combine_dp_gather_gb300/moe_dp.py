@@ -338,7 +338,10 @@ class MoeLayer:
 
     Buffers are sized once for `max_rows` global rows; `forward` runs
     gather -> route -> dispatch -> grouped FFN -> combine -> scatter on the
-    current stream without a host synchronisation."""
+    current stream without a host synchronisation.  With fp8=True (bf16 layer)
+    the expert weights are quantised once here (e4m3, 128 x 128 blocks), the
+    dispatch quantises the permuted rows per token group and the grouped FFN
+    runs on FP8 operands."""
 
     def __init__(self, *, R: int, H: int, E: int, k: int, I: int, w_gate_up: torch.Tensor,
                  w_down: torch.Tensor, max_rows: int, mode: int = MOE_PAD_SUM,
@@ -346,7 +349,7 @@ class MoeLayer:
                  align: int = 1, l2p: Optional[torch.Tensor] = None,
                  nrep: Optional[torch.Tensor] = None, slot_range=None,
                  norm_gamma: Optional[torch.Tensor] = None, norm_eps: float = 1e-6,
-                 n_shared: int = 0):
+                 n_shared: int = 0, fp8: bool = False):
         dev = w_gate_up.device
         self.R, self.H, self.E, self.k, self.I = R, H, E, k, I
         self.P = w_gate_up.shape[0]
@@ -381,14 +384,24 @@ class MoeLayer:
         self.offsets_P = torch.empty(self.P + 1, **i32)
         self.perm = torch.empty(self.cap, **i32)
         self.inv = torch.empty(max_rows, self.kk, **i32)
-        self.xs = torch.empty(self.cap, H, device=dev, dtype=self.dtype)
+        self.fp8 = fp8
+        if fp8:
+            if self.dtype != torch.bfloat16:
+                raise ValueError("the FP8 path takes a bf16 layer")
+            self.w_fp8 = quantize_expert_weights_fp8(w_gate_up, w_down)
+            self.xs = None
+            self.xq = torch.empty(self.cap, H, device=dev, dtype=torch.uint8)
+            self.xq_scales = torch.empty(self.cap, H // 128, device=dev, dtype=torch.uint8)
+        else:
+            self.xs = torch.empty(self.cap, H, device=dev, dtype=self.dtype)
         self.ys = torch.empty(self.cap, H, device=dev, dtype=self.dtype)
         self.yg = torch.empty(max_rows, H, device=dev, dtype=self.dtype)
         self.ws_dispatch = torch.empty(max(moe_dispatch_ws_bytes(max_rows, self.kk,
                                                                  E + n_shared), 16),
                                        device=dev, dtype=torch.uint8)
-        self.ws_ffn = torch.empty(max(moe_grouped_ffn_ws_bytes(self.cap, I, self.dtype), 16),
-                                  device=dev, dtype=torch.uint8)
+        ws_ffn = (moe_grouped_ffn_fp8_ws_bytes(self.cap, I) if fp8
+                  else moe_grouped_ffn_ws_bytes(self.cap, I, self.dtype))
+        self.ws_ffn = torch.empty(max(ws_ffn, 16), device=dev, dtype=torch.uint8)
         self.rows = 0
 
     def set_counts(self, counts: Sequence[int]) -> int:
@@ -436,11 +449,20 @@ class MoeLayer:
         moe_route_topk(lg, self.k, self.renormalize, self.d_counts, self.d_offsets, ids, w, st,
                        stream, n_shared=self.n_shared)
         ev("route")
-        moe_dispatch(xg, ids, self.E + self.n_shared, self.P, self.counts_P, self.offsets_P, self.perm, inv,
-                     self.xs, self.ws_dispatch, self.l2p, self.nrep, self.align, st, stream)
-        ev("dispatch")
-        moe_grouped_ffn(self.xs, self.offsets_P, self.wgu, self.wd, self.ys, self.ws_ffn,
-                        self.slot_range[0], self.slot_range[1], st, stream)
+        E_all = self.E + self.n_shared
+        if self.fp8:
+            moe_dispatch_fp8(xg, ids, E_all, self.P, self.counts_P, self.offsets_P, self.perm,
+                             inv, self.xq, self.xq_scales, self.ws_dispatch, self.l2p, self.nrep,
+                             self.align, st, stream)
+            ev("dispatch")
+            moe_grouped_ffn_fp8(self.xq, self.xq_scales, self.offsets_P, self.w_fp8, self.ys,
+                                self.ws_ffn, self.slot_range[0], self.slot_range[1], st, stream)
+        else:
+            moe_dispatch(xg, ids, E_all, self.P, self.counts_P, self.offsets_P, self.perm, inv,
+                         self.xs, self.ws_dispatch, self.l2p, self.nrep, self.align, st, stream)
+            ev("dispatch")
+            moe_grouped_ffn(self.xs, self.offsets_P, self.wgu, self.wd, self.ys, self.ws_ffn,
+                            self.slot_range[0], self.slot_range[1], st, stream)
         ev("ffn")
         moe_combine(self.ys, inv, w, yg, st, stream)
         ev("combine")

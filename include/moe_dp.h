@@ -345,7 +345,8 @@ size_t moe_grouped_ffn_fp8_ws_bytes(int64_t cap, int I);
  *   d_w_gate_up_q [P, 2I, H], d_w_gate_up_scales [P, 2I/128, H/128]
  *   d_w_down_q [P, H, I], d_w_down_scales [P, H/128, I/128]
  *   d_out_sorted  device bf16 [cap, H] out (rows of the slot range)
- * H and I multiples of 128; sm_103 only (else MOE_ERR_UNSUPPORTED). */
+ * H a multiple of 256, I a multiple of 128; sm_103 only (else
+ * MOE_ERR_UNSUPPORTED). */
 moe_status moe_grouped_ffn_fp8(const uint8_t* d_sorted_q, const uint8_t* d_sorted_scales,
                                const int32_t* d_offsets_P, int P, int slot_lo, int slot_hi,
                                int64_t cap, const uint8_t* d_w_gate_up_q,

@@ -178,3 +178,86 @@ def test_grouped_ffn_fp8_dsv3_width(md, orc):
     got = as_f32(to_np(ys)).astype(np.float64)
     assert_close(got[:n], ref[:n], BF16_ATOL, BF16_RTOL, "grouped FFN fp8, DSV3 width")
     assert rel_fro(got[:n], ref[:n]) < 1e-2
+
+
+# ------------------------------------------------------------------ whole layer
+def _layer_fp8_check(md, orc, spec, sample=None):
+    from combine_dp_gather_gb300 import synth
+    x_loc = synth.hidden_states(spec, DEV)
+    lg_loc = synth.router_logits(spec, DEV)
+    wgu, wd = synth.expert_weights(spec, None, DEV)
+    offs, rows = md.moe_dp_layout(spec.counts, spec.mode, spec.static_bound, spec.tokens_per_req)
+    layer = md.MoeLayer(R=spec.R, H=spec.H, E=spec.E, k=spec.k, I=spec.I, w_gate_up=wgu,
+                        w_down=wd, max_rows=max(rows, 1), mode=spec.mode,
+                        renormalize=spec.renormalize, n_shared=spec.n_shared, fp8=True)
+    out = [torch.empty(c, spec.H, device=DEV, dtype=wgu.dtype) for c in spec.counts]
+    layer.forward(x_loc, lg_loc, out, counts=spec.counts)
+    assert _status(layer.status) == 0
+    offs_o, rows_o = orc.dp_layout(spec.counts, spec.mode, 0, 1)
+    valid = orc.valid_rows(spec.counts, offs_o, rows_o)
+    xg_o = orc.dp_gather([to_np(t) for t in x_loc], spec.counts, offs_o, rows_o)
+    lg_o = orc.dp_gather([to_np(t) for t in lg_loc], spec.counts, offs_o, rows_o)
+    ids_o, w_o = orc.route_topk(lg_o, spec.k, spec.renormalize, valid, spec.n_shared)
+    kk = spec.k + spec.n_shared
+    assert np.array_equal(to_np(layer.ids[:rows]), ids_o)
+    c_o, o_o, p_o, i_o = orc.dispatch(ids_o, spec.E + spec.n_shared, layer.P, None, None, 1,
+                                      layer.cap)
+    n = int(o_o[-1])
+    assert np.array_equal(to_np(layer.offsets_P), o_o)
+    assert np.array_equal(to_np(layer.inv[:rows]), i_o)
+    x_f = as_f32(xg_o)
+    q_o, s_o = orc.quant_groups(x_f)                     # every global row, then permuted
+    assert np.array_equal(to_np(layer.xq[:n]), q_o[p_o[:n]])
+    assert np.array_equal(to_np(layer.xq_scales[:n]), s_o[p_o[:n]])
+    real = np.nonzero(valid)[0]
+    toks = real if sample is None else np.unique(np.concatenate(
+        [real[:1], real[-1:], np.random.default_rng(0).choice(real, size=min(sample, len(real)),
+                                                             replace=False)]))
+    slot_of = np.searchsorted(o_o, np.arange(n), side="right") - 1
+    need = {}
+    for g in toks:
+        for j in range(kk):
+            need.setdefault(int(slot_of[i_o[g, j]]), []).append((int(g), j))
+    guq, gus, dq, ds = layer.w_fp8
+    y_ref = {}
+    for s, pairs in need.items():
+        wq = orc.quant_blocks(as_f32(to_np(wgu[s])))
+        dq_o = orc.quant_blocks(as_f32(to_np(wd[s])))
+        assert np.array_equal(to_np(guq[s]), wq[0]) and np.array_equal(to_np(gus[s]), wq[1])
+        assert np.array_equal(to_np(dq[s]), dq_o[0]) and np.array_equal(to_np(ds[s]), dq_o[1])
+        rows_s = [g for g, _ in pairs]
+        ys_s = orc.expert_ffn_fp8(q_o[rows_s], s_o[rows_s], *wq, *dq_o)
+        for (g, j), y in zip(pairs, ys_s):
+            y_ref[(g, j)] = y
+    yg = as_f32(to_np(layer.yg[:rows]))
+    for g in toks:
+        ref = np.zeros(spec.H)
+        for j in range(kk):
+            y = y_ref[(int(g), j)]
+            assert_close(as_f32(to_np(layer.ys[int(i_o[g, j])])), y, BF16_ATOL, BF16_RTOL,
+                         f"fp8 expert out row {g} j {j}")
+            ref += w_o[g, j] * y
+        assert_close(yg[g], ref, BF16_ATOL, BF16_RTOL, f"fp8 combined row {g}")
+    assert not yg[valid == 0].any()
+    got = np.concatenate([as_f32(to_np(t)) for t in out])
+    assert np.array_equal(got, yg[valid == 1])
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_layer_fp8_tiny_all_rows(md, orc, mode):
+    from combine_dp_gather_gb300 import synth
+    spec = synth.LayerSpec("tiny_fp8", [16, 0, 140, 8, 1], mode, H=512, E=16, k=4, I=256,
+                           dtype="bf16", w_std=0.05, zipf_s=1.1)
+    _layer_fp8_check(md, orc, spec)
+
+
+def test_layer_fp8_dsv3_decode(md, orc):
+    from combine_dp_gather_gb300 import synth
+    _layer_fp8_check(md, orc, synth.spec_decode(seed=0), sample=6)
+
+
+def test_layer_fp8_with_shared_expert(md, orc):
+    from combine_dp_gather_gb300 import synth
+    spec = synth.LayerSpec("tiny_fp8_shared", [16, 0, 140, 8, 1], 1, H=512, E=16, k=4, I=256,
+                           dtype="bf16", w_std=0.05, zipf_s=1.1, n_shared=1)
+    _layer_fp8_check(md, orc, spec)
