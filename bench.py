@@ -70,6 +70,8 @@ FFN_TRAFFIC = {
                "bytes": 5581868544},
     "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "b7099fd4b3c2faf1",
                 "bytes": 25903843328},
+    "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
+                   "sha256_16": "6dbc846840f68bbc", "bytes": 2796148480},
 }
 
 
