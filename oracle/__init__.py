@@ -90,6 +90,7 @@ def _load():
             "orc_quant_blocks": (None, [P, i64, ctypes.c_int, P, P]),
             "orc_expert_ffn_fp8": (None, [P, P, i64, ctypes.c_int, ctypes.c_int, P, P, P, P,
                                           P]),
+            "orc_router_logits": (None, [P, i64, ctypes.c_int, P, ctypes.c_int, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -380,3 +381,16 @@ def grouped_ffn_fp8(xq, xe, offsets, wq, slot_lo: int = 0, slot_hi: int | None =
         if b > a:
             ys[a:b] = expert_ffn_fp8(xq[a:b], xe[a:b], *wq(s))
     return ys
+
+
+# ---------------------------------------------------------------- router GEMM
+def router_logits(x, w) -> np.ndarray:
+    """Gate projection: x [rows, H] f32, w [E, H] f32 -> logits [rows, E] f64."""
+    x, w = _c(x, np.float32), _c(w, np.float32)
+    rows, H = x.shape
+    E = w.shape[0]
+    assert w.shape == (E, H)
+    out = np.empty((rows, E), np.float64)
+    if rows:
+        _load().orc_router_logits(_p(x), rows, H, _p(w), E, _p(out))
+    return out

@@ -637,3 +637,20 @@ void orc_expert_ffn_fp8(const uint8_t *xq, const uint8_t *xe, int64_t n, int H, 
     free(ae);
   }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Router GEMM.  [P1] section "Two-batch Overlap" lists the MoE operations   */
+/* op_gate then op_select_experts: the gate projects each token's hidden     */
+/* state onto the experts and top-k selection follows.  Reading: a linear    */
+/* gate without bias, logits[g, e] = sum_h x[g, h] * w[e, h] (w [E, H]),     */
+/* h ascending; selection is orc_route_topk on these logits.                */
+/* Parity: pinned (numpy matmul).                                            */
+/* ------------------------------------------------------------------------ */
+void orc_router_logits(const float *x, int64_t rows, int H, const float *w, int E, double *logits) {
+  for (int64_t g = 0; g < rows; ++g)
+    for (int e = 0; e < E; ++e) {
+      double s = 0.0;
+      for (int h = 0; h < H; ++h) s += (double)x[g * H + h] * (double)w[(int64_t)e * H + h];
+      logits[g * E + e] = s;
+    }
+}

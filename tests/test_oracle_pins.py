@@ -669,3 +669,18 @@ def test_ffn_fp8_matches_numpy_on_dequantised_operands(orc):
     dense = orc.expert_ffn(x.astype(np.float32), wgu.astype(np.float32), wd.astype(np.float32))
     rel = np.linalg.norm(y - dense) / np.linalg.norm(dense)
     assert rel < 0.1, rel
+
+
+# ----------------------------------------------------------------- router GEMM
+def test_router_logits_match_numpy_and_feed_topk(orc):
+    rng = np.random.default_rng(10)
+    x = rng.standard_normal((7, 96)).astype(np.float32)
+    w = rng.standard_normal((12, 96)).astype(np.float32)
+    lg = orc.router_logits(x, w)
+    np.testing.assert_allclose(lg, x.astype(np.float64) @ w.astype(np.float64).T, rtol=1e-12,
+                               atol=1e-12)
+    # a one-hot gate row selects its expert: logits = x . w_e, so w_e = x's own row wins
+    w2 = np.zeros((5, 96), np.float32)
+    w2[3] = x[0]
+    ids, _ = orc.route_topk(orc.router_logits(x[:1], w2), 1, True, np.ones(1, np.uint8))
+    assert ids.tolist() == [[3]]
