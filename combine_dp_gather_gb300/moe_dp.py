@@ -60,6 +60,9 @@ _SIGS = {
     "moe_dispatch_fp8": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _I, _I, _I64, _P, _P,
                               _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "moe_grouped_ffn_fp8_ws_bytes": (_SZ, [_I64, _I]),
+    "moe_route_gemm_ws_bytes": (_SZ, [_I64, _I, _I, _I]),
+    "moe_route_gemm_topk": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P,
+                                 _SZ, _P, _P]),
     "moe_grouped_ffn_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I64, _P, _P, _P, _P, _I, _I, _P, _P,
                                  _SZ, _P, _P]),
 }
@@ -235,6 +238,24 @@ def moe_dispatch_noalloc(x: Optional[torch.Tensor], ids: torch.Tensor, E: int, P
     _check("moe_dispatch_noalloc", lib().moe_dispatch_noalloc(
         _ptr(x), _ptr(ids), rows, k, H, dt, E, P, _ptr(l2p), _ptr(nrep), X, align,
         perm.numel(), _ptr(counts_P), _ptr(offsets_P), _ptr(perm), _ptr(inv), _ptr(sorted_out),
+        _ptr(d_status), _stream(stream)))
+
+
+def moe_route_gemm_ws_bytes(rows: int, H: int, E: int, k: int) -> int:
+    return int(lib().moe_route_gemm_ws_bytes(rows, H, E, k))
+
+
+def moe_route_gemm_topk(x: torch.Tensor, w_router: torch.Tensor, k: int, renormalize: bool,
+                        d_counts, d_offsets, ids: torch.Tensor, w: torch.Tensor,
+                        ws: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
+                        d_status=None, stream=None, n_shared: int = 0):
+    """Gate GEMM (x [rows, H] . w_router [E, H]^T, bf16) fused ahead of top-k."""
+    rows, H = x.shape
+    E = w_router.shape[0]
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check("moe_route_gemm_topk", lib().moe_route_gemm_topk(
+        _ptr(x), _ptr(w_router), rows, H, E, k, int(renormalize), n_shared, _ptr(d_counts),
+        _ptr(d_offsets), d_counts.numel(), _ptr(ids), _ptr(w), _ptr(logits), _ptr(ws), nbytes,
         _ptr(d_status), _stream(stream)))
 
 
