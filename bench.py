@@ -43,15 +43,21 @@ UNIT = "tokens/s"
 L2_NOTE = "inputs larger than L2: every step streams the touched experts' weights from HBM"
 
 def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
-                      fp8: bool = False) -> int:
+                      fp8: bool = False, router_gemm: bool = False, sms: int = 152) -> int:
     """Kernel launches of one layer step: gather (hidden states and logits), route,
     dispatch (one CTA-wide kernel for <= 16384 routed pairs whose tables fit 48 KB, else
     histogram + scan + rank; then the row copy; + the alignment pad kernel when
     align > 1, plus the FP8 rows' pad kernel on the FP8 path), grouped FFN (MM1+SwiGLU
-    and MM2), combine, scatter."""
+    and MM2), combine, scatter.  With the router gate GEMM the logits gather goes and
+    routing is one fused kernel (>= sms/4 row tiles and k <= 8) or split GEMM + sum +
+    top-k."""
     small = rows * k <= 16384 and 4 * (33 * E + 3 * P + 1) <= 48 * 1024
     dispatch = (1 if small else 3) + 1 + (1 + (1 if fp8 else 0) if align > 1 else 0)
-    return 2 + 1 + dispatch + 2 + 1 + 1
+    gather, route = 2, 1
+    if router_gemm:
+        gather = 1
+        route = 1 if (k <= 8 and 4 * ((rows + 127) // 128) >= sms) else 3
+    return gather + route + dispatch + 2 + 1 + 1
 
 
 def ffn_kernel(cap: int, P: int, fp8: bool = False) -> str:
@@ -102,6 +108,9 @@ def parse():
                     help="shared experts, always selected with weight 1 (0 = none)")
     ap.add_argument("--boundary", default="plain", choices=["plain", "addnorm"],
                     help="addnorm: residual add + RMSNorm fused into the hidden-state gather")
+    ap.add_argument("--router", default="logits", choices=["logits", "gemm"],
+                    help="gemm: router logits from the gate GEMM (W_r N(0, 1/H) plus the "
+                         "workload's Zipf bias) fused ahead of top-k instead of given logits")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 dispatch and grouped FFN (e4m3, UE8M0 scales per 128-token group "
                          "and 128x128 weight block); layer input and output stay bf16")
@@ -248,13 +257,17 @@ def run_native(args, rank, world, local_rank):
     lg_loc = synth.router_logits(spec, dev)
     wgu, wd = synth.expert_weights(spec, p2l, dev)
     offs, rows = md.moe_dp_layout(spec.counts, spec.mode, spec.static_bound, spec.tokens_per_req)
+    gate_w = gate_b = gate_np = None
+    if args.router == "gemm":
+        gate_w, gate_b = synth.router_gate(spec, dev)
+        gate_np = gate_to_host(gate_w, gate_b)
     layer = md.MoeLayer(
         R=spec.R, H=spec.H, E=spec.E, k=spec.k, I=spec.I, w_gate_up=wgu, w_down=wd,
         max_rows=max(rows, 1), mode=spec.mode, static_bound=spec.static_bound,
         tokens_per_req=spec.tokens_per_req, renormalize=spec.renormalize, align=spec.align,
         l2p=None if l2p_np is None else torch.from_numpy(l2p_np).to(dev),
         nrep=None if nrep_np is None else torch.from_numpy(nrep_np).to(dev),
-        n_shared=spec.n_shared, fp8=args.fp8)
+        n_shared=spec.n_shared, fp8=args.fp8, router_weight=gate_w, router_bias=gate_b)
     out = [torch.empty(c, spec.H, device=dev, dtype=wgu.dtype) for c in spec.counts]
     res_loc = None
     if args.boundary == "addnorm":
@@ -339,10 +352,12 @@ def run_native(args, rank, world, local_rank):
         # and outputs let the next step's host->device copy and the previous step's
         # device->host read run on copy streams while this step computes.
         hx = [t.cpu().pin_memory() for t in x_loc]
-        hl = [t.cpu().pin_memory() for t in lg_loc]
+        # with the gate GEMM the logits are computed on the device, not an input
+        hl = [t.cpu().pin_memory() for t in lg_loc] if args.router == "logits" else []
         ho = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out] for _ in range(2)]
         dx = [[torch.empty_like(t) for t in x_loc] for _ in range(2)]
-        dl = [[torch.empty_like(t) for t in lg_loc] for _ in range(2)]
+        dl = [[torch.empty_like(t) for t in lg_loc] if args.router == "logits" else lg_loc
+              for _ in range(2)]
         dout = [[torch.empty_like(t) for t in out] for _ in range(2)]
         comp = torch.cuda.current_stream()
         s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
@@ -425,17 +440,19 @@ def run_native(args, rank, world, local_rank):
                 e2e=e2e, rows=rows, touched=touched,
                 launches=launches_per_step(max(rows, 1), spec.k + spec.n_shared,
                                            spec.E + spec.n_shared, layer.P, layer.cap,
-                                           spec.align, args.fp8),
-                inputs=(x_loc, lg_loc, wgu, wd, l2p_np, nrep_np))
+                                           spec.align, args.fp8, args.router == "gemm",
+                                           torch.cuda.get_device_properties(dev).multi_processor_count),
+                inputs=(x_loc, lg_loc, wgu, wd, l2p_np, nrep_np), gate=gate_np)
 
 
 # ------------------------------------------------------------------ oracle (CPU)
-def oracle_sample_step(spec, n_tokens, x_loc, lg_loc, wgu, wd, l2p, nrep, fp8=False):
+def oracle_sample_step(spec, n_tokens, x_loc, lg_loc, wgu, wd, l2p, nrep, fp8=False, gate=None):
     """One oracle pass over the first n_tokens tokens of the workload (replica
     order, MAX/SUM/static layout of the truncated counts).  With fp8 the permuted
     rows are quantised (timed) and the experts run on FP8 operands (weight
-    quantisation is preparation, not timed).  Returns (seconds of oracle compute,
-    cpu seconds)."""
+    quantisation is preparation, not timed).  With gate = (W_r, bias) the router
+    logits come from the oracle's gate projection (timed) instead of the given
+    logits.  Returns (seconds of oracle compute, cpu seconds)."""
     import oracle
     counts, left = [], n_tokens
     for c in spec.counts:
@@ -453,7 +470,12 @@ def oracle_sample_step(spec, n_tokens, x_loc, lg_loc, wgu, wd, l2p, nrep, fp8=Fa
     offs, rows = oracle.dp_layout(counts, spec.mode, spec.static_bound, spec.tokens_per_req)
     valid = oracle.valid_rows(counts, offs, rows)
     xg = oracle.dp_gather(xs, counts, offs, rows)
-    lg = oracle.dp_gather(lgs, counts, offs, rows)
+    if gate is None:
+        lg = oracle.dp_gather(lgs, counts, offs, rows)
+    else:
+        lg = oracle.router_logits(xg, gate[0])
+        if gate[1] is not None:
+            lg = lg + gate[1][None, :]
     ids, w = oracle.route_topk(lg, spec.k, spec.renormalize, valid, spec.n_shared)
     cnt, o, perm, inv = oracle.dispatch(ids, spec.E + spec.n_shared, spec.slots, l2p, nrep,
                                         spec.align)
@@ -494,13 +516,20 @@ def oracle_inputs(spec):
     return x_loc, lg_loc, wgu, wd, l2p, nrep
 
 
-def cpu_baseline(spec, budget_s=20.0, inputs=None, fp8=False):
+def gate_to_host(w, b):
+    """Gate weights as exact float32 host arrays for the oracle (bias may be None)."""
+    import oracle
+    wb = w.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return oracle.bf16_bits_to_f32(wb), (None if b is None else b.cpu().numpy().astype(np.float64))
+
+
+def cpu_baseline(spec, budget_s=20.0, inputs=None, fp8=False, gate=None):
     import oracle
     oracle.build()
     x_loc, lg_loc, wgu, wd, l2p, nrep = inputs or oracle_inputs(spec)
-    wall1, _ = oracle_sample_step(spec, 1, x_loc, lg_loc, wgu, wd, l2p, nrep, fp8)
+    wall1, _ = oracle_sample_step(spec, 1, x_loc, lg_loc, wgu, wd, l2p, nrep, fp8, gate)
     n = int(max(1, min(spec.T, budget_s / max(wall1, 1e-3))))
-    wall, cpu = oracle_sample_step(spec, n, x_loc, lg_loc, wgu, wd, l2p, nrep, fp8)
+    wall, cpu = oracle_sample_step(spec, n, x_loc, lg_loc, wgu, wd, l2p, nrep, fp8, gate)
     ffn = "FP8 (e4m3) SwiGLU FFN in fp64" if fp8 else "fp64 SwiGLU FFN"
     return {"value": round(n / wall, 3), "unit": UNIT, "cores": round(cpu / wall, 2),
             "kind": "oracle",
@@ -516,14 +545,15 @@ def run_reference(args, rank, world):
     import oracle
     oracle.build()
     inputs = oracle_inputs(spec)
-    wall1, _ = oracle_sample_step(spec, 1, *inputs, args.fp8)
+    gate = gate_to_host(*synth.router_gate(spec, "cpu")) if args.router == "gemm" else None
+    wall1, _ = oracle_sample_step(spec, 1, *inputs, args.fp8, gate)
     budget = 120.0
     n = int(max(1, min(spec.T, budget / (args.steps + args.warmup) / max(wall1, 1e-3))))
     for _ in range(args.warmup):
-        oracle_sample_step(spec, n, *inputs, args.fp8)
+        oracle_sample_step(spec, n, *inputs, args.fp8, gate)
     walls, cpus = [], []
     for _ in range(args.steps):
-        w, c = oracle_sample_step(spec, n, *inputs, args.fp8)
+        w, c = oracle_sample_step(spec, n, *inputs, args.fp8, gate)
         walls.append(w)
         cpus.append(c)
     tot = sum(walls)
@@ -588,6 +618,8 @@ def main():
             "dtype": "fp8-e4m3" if args.fp8 else spec.dtype, "data": "synthetic",
             "config": dict(synth.describe(spec), global_rows=r["rows"], l2=L2_NOTE, **r["extra"],
                            boundary=args.boundary, shared_experts=spec.n_shared,
+                           router=("gate GEMM fused ahead of top-k, W_r N(0, 1/H) plus the Zipf "
+                                   "bias" if args.router == "gemm" else "given logits"),
                            fp8=("e4m3 codes, UE8M0 scales per 128-token group and 128x128 "
                                 "weight block; bf16 layer input/output") if args.fp8 else None,
                            parallelism=f"{world} independent replica(s), one per GPU",
@@ -603,7 +635,8 @@ def main():
                            "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                            "ms_per_step": round(agg["e2e_ms_max"] / e["steps"], 4)}
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(spec, inputs=r["inputs"], fp8=args.fp8)
+            line["cpu_baseline"] = cpu_baseline(spec, inputs=r["inputs"], fp8=args.fp8,
+                                                gate=r["gate"])
         print(json.dumps(line), flush=True)
     finally:
         if world > 1 and torch.distributed.is_initialized():

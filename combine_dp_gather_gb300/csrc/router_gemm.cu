@@ -2,8 +2,10 @@
 //
 // SGLang chapter 17, section "Two-batch Overlap": the MoE operations run
 // op_gate and then op_select_experts: the gate projects each token's hidden
-// state onto the experts (here logits[g, e] = sum_h x[g, h] * W_r[e, h], a
-// bias-free linear gate, bf16 operands, fp32 accumulation) and the top-k
+// state onto the experts (here logits[g, e] = sum_h x[g, h] * W_r[e, h] + b[e],
+// a linear gate with an optional per-expert bias, bf16 operands, fp32
+// accumulation; section "推理时怎么“选副本”": expert selection takes the router
+// logits together with a per-expert correction bias) and the top-k
 // selection follows (moe_route_topk's rule: k largest logits, equal logits
 // lower id first, softmax weights over the k or over all experts).
 //
@@ -49,6 +51,7 @@ struct RSmem {
   int32_t abort_flag;
   int32_t off[MOE_MAX_REPLICAS + 1];
   int32_t cnt[MOE_MAX_REPLICAS];
+  float bias[256];
 };
 constexpr size_t r_smem_bytes() { return 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(RSmem); }
 
@@ -63,6 +66,7 @@ struct RParams {
   float* w;
   float* logits;   // fused: optional [rows, E] copy of the logits
   float* partial;  // split: [ks][rows][E]
+  const float* bias;  // [E] or null
   uint32_t* status;
 };
 
@@ -99,11 +103,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int tile = blockIdx.x, ks = blockIdx.y;
   const int kb0 = ks * p.kb_per;
   const int kb1 = kb0 + p.kb_per < p.num_kb ? kb0 + p.kb_per : p.num_kb;
-  if (K > 0)
+  if (K > 0) {
     for (int i = threadIdx.x; i <= p.R; i += THREADS) {
       L.off[i] = p.offsets[i];
       if (i < p.R) L.cnt[i] = p.counts[i];
     }
+    for (int e = threadIdx.x; e < p.E; e += THREADS) L.bias[e] = p.bias != nullptr ? p.bias[e] : 0.0f;
+  }
   if (threadIdx.x == 0) {
     L.abort_flag = 0;
     for (int i = 0; i < STAGES; ++i) {
@@ -218,7 +224,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float v = __uint_as_float(r[i]);
+            const float v = __uint_as_float(r[i]) + L.bias[32 * c + i];
+            r[i] = __float_as_uint(v);
             topk_insert<KK>(tv, ti, v, 32 * c + i);
             if (!p.renorm) {
               if (v > m) {
@@ -277,10 +284,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) tmem_dealloc<1>(tmem_base);
 }
 
-// logits[i] = sum over ks ascending of partial[ks][i] (float4 per thread).
+// logits[i] = sum over ks ascending of partial[ks][i], then + bias[e]
+// (float4 per thread; E is a multiple of 4).
 __global__ void __launch_bounds__(256)
-    router_reduce_kernel(const float4* __restrict__ partial, int64_t n4, int ks,
-                         float4* __restrict__ logits) {
+    router_reduce_kernel(const float4* __restrict__ partial, int64_t n4, int ks, int E,
+                         const float* __restrict__ bias, float4* __restrict__ logits) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
     float4 a = partial[i];
@@ -290,6 +298,13 @@ __global__ void __launch_bounds__(256)
       a.y += b.y;
       a.z += b.z;
       a.w += b.w;
+    }
+    if (bias != nullptr) {
+      const int e = (int)((i * 4) % E);
+      a.x += bias[e];
+      a.y += bias[e + 1];
+      a.z += bias[e + 2];
+      a.w += bias[e + 3];
     }
     logits[i] = a;
   }
@@ -349,8 +364,9 @@ extern "C" size_t moe_route_gemm_ws_bytes(int64_t rows, int H, int E, int k) {
   return pl.fused ? 0 : split_ws(rows, E, pl.ks);
 }
 
-extern "C" moe_status moe_route_gemm_topk(const void* d_x, const void* d_w_router, int64_t rows,
-                                          int H, int E, int k, int renormalize, int n_shared,
+extern "C" moe_status moe_route_gemm_topk(const void* d_x, const void* d_w_router,
+                                          const float* d_bias, int64_t rows, int H, int E, int k,
+                                          int renormalize, int n_shared,
                                           const int32_t* d_counts, const int32_t* d_offsets,
                                           int R, int32_t* d_ids, float* d_w, float* d_logits,
                                           void* d_ws, size_t ws_bytes, uint32_t* d_status,
@@ -394,6 +410,7 @@ extern "C" moe_status moe_route_gemm_topk(const void* d_x, const void* d_w_route
   p.w = d_w;
   p.logits = d_logits;
   p.partial = static_cast<float*>(d_ws);
+  p.bias = d_bias;
   p.status = d_status;
   cudaStream_t s = as_stream(stream);
   const unsigned tiles = (unsigned)((rows + BM - 1) / BM);
@@ -420,7 +437,7 @@ extern "C" moe_status moe_route_gemm_topk(const void* d_x, const void* d_w_route
   int64_t blocks = (n4 + 255) / 256;
   const int64_t lim = (int64_t)num_sms() * 8;
   router_reduce_kernel<<<(unsigned)(blocks < lim ? blocks : lim), 256, 0, s>>>(
-      static_cast<const float4*>(d_ws), n4, pl.ks, reinterpret_cast<float4*>(logits));
+      static_cast<const float4*>(d_ws), n4, pl.ks, E, d_bias, reinterpret_cast<float4*>(logits));
   if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
   return moe_route_topk_shared(logits, rows, E, k, renormalize, n_shared, d_counts, d_offsets, R,
                                d_ids, d_w, d_status, stream);

@@ -61,8 +61,8 @@ _SIGS = {
                               _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "moe_grouped_ffn_fp8_ws_bytes": (_SZ, [_I64, _I]),
     "moe_route_gemm_ws_bytes": (_SZ, [_I64, _I, _I, _I]),
-    "moe_route_gemm_topk": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P,
-                                 _SZ, _P, _P]),
+    "moe_route_gemm_topk": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P,
+                                 _P, _SZ, _P, _P]),
     "moe_grouped_ffn_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I64, _P, _P, _P, _P, _I, _I, _P, _P,
                                  _SZ, _P, _P]),
 }
@@ -248,13 +248,15 @@ def moe_route_gemm_ws_bytes(rows: int, H: int, E: int, k: int) -> int:
 def moe_route_gemm_topk(x: torch.Tensor, w_router: torch.Tensor, k: int, renormalize: bool,
                         d_counts, d_offsets, ids: torch.Tensor, w: torch.Tensor,
                         ws: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
-                        d_status=None, stream=None, n_shared: int = 0):
-    """Gate GEMM (x [rows, H] . w_router [E, H]^T, bf16) fused ahead of top-k."""
+                        d_status=None, stream=None, n_shared: int = 0,
+                        bias: Optional[torch.Tensor] = None):
+    """Gate GEMM (x [rows, H] . w_router [E, H]^T + bias, bf16) fused ahead of top-k."""
     rows, H = x.shape
     E = w_router.shape[0]
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check("moe_route_gemm_topk", lib().moe_route_gemm_topk(
-        _ptr(x), _ptr(w_router), rows, H, E, k, int(renormalize), n_shared, _ptr(d_counts),
+        _ptr(x), _ptr(w_router), _ptr(bias), rows, H, E, k, int(renormalize), n_shared,
+        _ptr(d_counts),
         _ptr(d_offsets), d_counts.numel(), _ptr(ids), _ptr(w), _ptr(logits), _ptr(ws), nbytes,
         _ptr(d_status), _stream(stream)))
 
@@ -359,7 +361,10 @@ class MoeLayer:
 
     Buffers are sized once for `max_rows` global rows; `forward` runs
     gather -> route -> dispatch -> grouped FFN -> combine -> scatter on the
-    current stream without a host synchronisation.  With fp8=True (bf16 layer)
+    current stream without a host synchronisation.  With router_weight [E, H]
+    (bf16) the router logits are computed from the gathered hidden states by the
+    gate GEMM fused ahead of top-k instead of being gathered from the replicas.
+    With fp8=True (bf16 layer)
     the expert weights are quantised once here (e4m3, 128 x 128 blocks), the
     dispatch quantises the permuted rows per token group and the grouped FFN
     runs on FP8 operands."""
@@ -370,7 +375,9 @@ class MoeLayer:
                  align: int = 1, l2p: Optional[torch.Tensor] = None,
                  nrep: Optional[torch.Tensor] = None, slot_range=None,
                  norm_gamma: Optional[torch.Tensor] = None, norm_eps: float = 1e-6,
-                 n_shared: int = 0, fp8: bool = False):
+                 n_shared: int = 0, fp8: bool = False,
+                 router_weight: Optional[torch.Tensor] = None,
+                 router_bias: Optional[torch.Tensor] = None):
         dev = w_gate_up.device
         self.R, self.H, self.E, self.k, self.I = R, H, E, k, I
         self.P = w_gate_up.shape[0]
@@ -423,6 +430,12 @@ class MoeLayer:
         ws_ffn = (moe_grouped_ffn_fp8_ws_bytes(self.cap, I) if fp8
                   else moe_grouped_ffn_ws_bytes(self.cap, I, self.dtype))
         self.ws_ffn = torch.empty(max(ws_ffn, 16), device=dev, dtype=torch.uint8)
+        self.router_weight, self.router_bias = router_weight, router_bias
+        if router_weight is not None:
+            if router_weight.shape != (E, H) or router_weight.dtype != torch.bfloat16:
+                raise ValueError("router_weight must be bf16 [E, H]")
+            self.ws_router = torch.empty(max(moe_route_gemm_ws_bytes(max_rows, H, E, k), 16),
+                                         device=dev, dtype=torch.uint8)
         self.rows = 0
 
     def set_counts(self, counts: Sequence[int]) -> int:
@@ -465,10 +478,16 @@ class MoeLayer:
                                       self.d_counts, self.d_offsets, xg, st, stream)
         else:
             moe_dp_gather(local_x, self.d_counts, self.d_offsets, xg, st, stream)
-        moe_dp_gather(local_logits, self.d_counts, self.d_offsets, lg, st, stream)
+        if self.router_weight is None:
+            moe_dp_gather(local_logits, self.d_counts, self.d_offsets, lg, st, stream)
         ev("gather")
-        moe_route_topk(lg, self.k, self.renormalize, self.d_counts, self.d_offsets, ids, w, st,
-                       stream, n_shared=self.n_shared)
+        if self.router_weight is None:
+            moe_route_topk(lg, self.k, self.renormalize, self.d_counts, self.d_offsets, ids, w,
+                           st, stream, n_shared=self.n_shared)
+        else:
+            moe_route_gemm_topk(xg, self.router_weight, self.k, self.renormalize, self.d_counts,
+                                self.d_offsets, ids, w, self.ws_router, None, st, stream,
+                                n_shared=self.n_shared, bias=self.router_bias)
         ev("route")
         E_all = self.E + self.n_shared
         if self.fp8:

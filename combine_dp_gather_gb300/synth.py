@@ -159,6 +159,19 @@ def router_logits(spec: LayerSpec, device="cpu") -> List[torch.Tensor]:
     return list(torch.split(lg, spec.counts, dim=0))
 
 
+def router_gate(spec: LayerSpec, device="cpu"):
+    """Gate weights [E, H] bf16, N(0, 1/H), and the optional Zipf bias [E] fp32: the
+    gate of hidden states N(0,1) then gives logits N(0,1) plus the same popularity
+    bias as router_logits."""
+    g = _gen(device, spec.seed * 1000 + 7)
+    w = torch.randn(spec.E, spec.H, generator=g, device=device, dtype=torch.float32)
+    w = (w / spec.H ** 0.5).to(torch.bfloat16)
+    b = None
+    if spec.zipf_s is not None:
+        b = torch.from_numpy(zipf_bias(spec.E, spec.zipf_s, spec.seed)).to(device)
+    return w, b
+
+
 def expert_weights_logical(spec: LayerSpec, e: int, device="cpu"):
     """Weights of logical expert e: (wgu [2I, H], wd [H, I]) in the layer dtype.
     Gate rows 0..I-1, up rows I..2I-1; each expert has its own seed so any

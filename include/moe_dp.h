@@ -187,12 +187,15 @@ moe_status moe_route_topk(const float* d_logits, int64_t rows, int E, int k, int
 
 /* Router gate GEMM fused ahead of top-k.  [P1] section "Two-batch Overlap"
  * lists op_gate then op_select_experts: the gate projects each token onto the
- * experts and top-k selection follows.  Here the gate is bias-free:
- *   logits[g, e] = sum_h x[g, h] * W_r[e, h]   (bf16 operands, fp32 sums)
+ * experts and top-k selection follows; section "推理时怎么“选副本”": expert
+ * selection takes the router logits together with a per-expert correction
+ * bias.  Here:
+ *   logits[g, e] = sum_h x[g, h] * W_r[e, h] + b[e]   (bf16 operands, fp32 sums)
  * and the selection, weights, pad rows and shared experts are exactly those
  * of moe_route_topk_shared on these logits.
  *   d_x         device bf16 [rows, H], the gathered rows (16-byte aligned)
  *   d_w_router  device bf16 [E, H]; E a multiple of 32 up to 256; H of 64
+ *   d_bias      device float32 [E] per-expert bias, or NULL (none)
  *   d_logits    device float32 [rows, E] out, or NULL (not needed)
  *   d_ws        workspace of moe_route_gemm_ws_bytes(rows, H, E, k) bytes
  *               (0 when the fused path runs; may then be NULL)
@@ -201,8 +204,8 @@ moe_status moe_route_topk(const float* d_logits, int64_t rows, int E, int k, int
  * a fixed order before the top-k kernel (the result does not depend on
  * scheduling).  sm_103 only. */
 size_t moe_route_gemm_ws_bytes(int64_t rows, int H, int E, int k);
-moe_status moe_route_gemm_topk(const void* d_x, const void* d_w_router, int64_t rows, int H,
-                               int E, int k, int renormalize, int n_shared,
+moe_status moe_route_gemm_topk(const void* d_x, const void* d_w_router, const float* d_bias,
+                               int64_t rows, int H, int E, int k, int renormalize, int n_shared,
                                const int32_t* d_counts, const int32_t* d_offsets, int R,
                                int32_t* d_ids, float* d_w, float* d_logits, void* d_ws,
                                size_t ws_bytes, uint32_t* d_status, void* stream);
