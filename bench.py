@@ -72,12 +72,12 @@ def ffn_kernel(cap: int, P: int, fp8: bool = False) -> str:
 # step of the default workload (ncu, --clock-control none), valid while the kernel's
 # sources hash to the recorded SHA-256 prefix; any other source reports traffic null.
 FFN_TRAFFIC = {
-    "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "ffc89c55dbd49c95",
-               "bytes": 5581868544},
-    "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "b7099fd4b3c2faf1",
-                "bytes": 25903843328},
+    "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "55f0dffc52932a6f",
+               "bytes": 5582279168},
+    "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "cc5ff3093b6f5983",
+                "bytes": 25887725312},
     "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
-                   "sha256_16": "6dbc846840f68bbc", "bytes": 2796148480},
+                   "sha256_16": "6dbc846840f68bbc", "bytes": 2795898368},
 }
 
 
