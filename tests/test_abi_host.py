@@ -208,3 +208,77 @@ def test_status_strings(md):
     for code in range(8):
         assert md.lib().moe_status_string(code).decode() != "unknown status"
     assert md.lib().moe_status_string(99).decode() == "unknown status"
+
+
+def test_fp8_entries_reject_bad_args(md):
+    L = md.lib()
+    E_ARG, E_UNS, E_CAP = md.MOE_ERR_INVALID_ARG, md.MOE_ERR_UNSUPPORTED, md.MOE_ERR_CAPACITY
+    assert L.moe_quantize_fp8_groups(FAKE, 4, 100, 1, FAKE, FAKE, NULL) == E_ARG   # K % 128
+    assert L.moe_quantize_fp8_groups(FAKE, 4, 256, 7, FAKE, FAKE, NULL) == E_UNS   # dtype
+    assert L.moe_quantize_fp8_groups(MISAL, 4, 256, 1, FAKE, FAKE, NULL) == E_ARG
+    assert L.moe_quantize_fp8_groups(FAKE, 4, 256, 1, FAKE, NULL, NULL) == E_ARG
+    assert L.moe_quantize_fp8_groups(NULL, 0, 256, 1, NULL, NULL, NULL) == md.MOE_OK
+    assert L.moe_quantize_fp8_blocks(FAKE, 100, 256, 1, FAKE, FAKE, NULL) == E_ARG  # R % 128
+    assert L.moe_quantize_fp8_blocks(FAKE, 128, 64, 1, FAKE, FAKE, NULL) == E_ARG
+    assert L.moe_quantize_fp8_blocks(FAKE, 128, 256, 1, MISAL, FAKE, NULL) == E_ARG
+
+    def disp(**kw):
+        a = dict(g=FAKE, ids=FAKE, rows=16, k=2, H=256, dt=1, E=8, P=8, l2p=NULL, nrep=NULL,
+                 X=0, align=1, cap=32, cnt=FAKE, off=FAKE, perm=FAKE, inv=FAKE, q=FAKE, s=FAKE,
+                 ws=FAKE, wsb=1 << 20)
+        a.update(kw)
+        return L.moe_dispatch_fp8(a["g"], a["ids"], a["rows"], a["k"], a["H"], a["dt"], a["E"],
+                                  a["P"], a["l2p"], a["nrep"], a["X"], a["align"], a["cap"],
+                                  a["cnt"], a["off"], a["perm"], a["inv"], a["q"], a["s"],
+                                  a["ws"], a["wsb"], NULL, NULL)
+
+    assert disp(H=192) == E_ARG                # H % 128
+    assert disp(q=NULL) == E_ARG
+    assert disp(q=MISAL) == E_ARG
+    assert disp(g=NULL) == E_ARG
+    assert disp(dt=5) == E_UNS
+    assert disp(P=9) == E_ARG                  # the index checks of moe_dispatch apply
+    assert disp(wsb=0) == E_CAP
+
+    def ffn(**kw):
+        a = dict(xq=FAKE, xs=FAKE, off=FAKE, P=8, lo=0, hi=8, cap=64, gq=FAKE, gs=FAKE, dq=FAKE,
+                 ds=FAKE, H=512, I=256, ys=FAKE, ws=FAKE, wsb=1 << 30)
+        a.update(kw)
+        return L.moe_grouped_ffn_fp8(a["xq"], a["xs"], a["off"], a["P"], a["lo"], a["hi"],
+                                     a["cap"], a["gq"], a["gs"], a["dq"], a["ds"], a["H"], a["I"],
+                                     a["ys"], a["ws"], a["wsb"], NULL, NULL)
+
+    assert ffn(H=384) == E_ARG                 # H % 256
+    assert ffn(I=192) == E_ARG                 # I % 128
+    assert ffn(hi=9) == E_ARG
+    assert ffn(gs=NULL) == E_ARG
+    assert ffn(gq=MISAL) == E_ARG
+    assert ffn(wsb=16) == E_CAP
+    assert ffn(cap=0) == md.MOE_OK             # nothing to do
+    assert L.moe_grouped_ffn_fp8_ws_bytes(64, 256) >= 64 * 256 + 64 * 2
+    assert L.moe_grouped_ffn_fp8_ws_bytes(64, 100) == 0
+
+
+def test_router_gemm_rejects_bad_args(md):
+    L = md.lib()
+    E_ARG = md.MOE_ERR_INVALID_ARG
+
+    def call(**kw):
+        a = dict(x=FAKE, wr=FAKE, b=NULL, rows=16, H=512, E=64, k=4, rn=1, ns=0, cnt=FAKE,
+                 off=FAKE, R=2, ids=FAKE, w=FAKE, lg=NULL, ws=FAKE, wsb=1 << 30)
+        a.update(kw)
+        return L.moe_route_gemm_topk(a["x"], a["wr"], a["b"], a["rows"], a["H"], a["E"], a["k"],
+                                     a["rn"], a["ns"], a["cnt"], a["off"], a["R"], a["ids"],
+                                     a["w"], a["lg"], a["ws"], a["wsb"], NULL, NULL)
+
+    assert call(E=48) == E_ARG                 # E a multiple of 32
+    assert call(E=512) == E_ARG                # at most 256
+    assert call(H=100) == E_ARG                # H a multiple of 64
+    assert call(k=65) == E_ARG                 # k <= E
+    assert call(k=30, ns=3) == E_ARG           # k + n_shared <= 32
+    assert call(x=MISAL) == E_ARG
+    assert call(lg=MISAL) == E_ARG
+    assert call(wr=NULL) == E_ARG
+    assert call(R=0) == E_ARG
+    assert call(rows=0) == md.MOE_OK
+    assert L.moe_route_gemm_ws_bytes(16, 512, 48, 4) == 0
