@@ -34,9 +34,11 @@
 //
 // TMEM holds two 256-column fp32 accumulators per SM.  A unit of N <= 256
 // tokens takes one (the next unit's MMAs overlap its epilogue), a unit of
-// 256 < N <= 320 takes both; the epilogue frees each buffer as soon as it has
-// read it.  Token rows past the slot's end are computed from whatever follows
-// and never stored; rows past the buffer read as zero.
+// 256 < N <= 320 takes both: its first 256 tokens in the second, its tail in
+// the first, which the epilogue reads and frees first, so the next unit's MMAs
+// (which start in that buffer) overlap the rest of the epilogue.  Token rows
+// past the slot's end are computed from whatever follows and never stored;
+// rows past the buffer read as zero.
 //
 // Roles (320 threads, one CTA per SM, clusters of two):
 //   warp 0    TMA producer (both CTAs): one weight box (128 rows) and one
@@ -297,7 +299,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                                    abort_flag, p.status))
           break;
         fence_after();
-        const uint32_t d0 = tmem_base + buf0 * ACC_COLS, d1 = tmem_base + buf1 * ACC_COLS;
+        // a two-buffer unit keeps its first 256 tokens in its second buffer and
+        // the rest in its first, which the epilogue reads (and frees) first
+        const uint32_t d0 = tmem_base + (nbuf == 2 ? buf1 : buf0) * ACC_COLS;
+        const uint32_t d1 = tmem_base + buf0 * ACC_COLS;
         const uint32_t id0 = idesc_bf16(256, un.N0);
         const uint32_t id1 = idesc_bf16(256, un.N1 ? un.N1 : 16);
         const uint32_t boff1 = (uint32_t)(un.N0 >> 1) * BK * 2;
@@ -354,17 +359,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       fence_after();
       const uint32_t lanes = tmem_base + ((uint32_t)(q * 32) << 16);
-      // chunk c = 32 accumulator columns: the first nch0 of buffer 0, then buffer 1
-      const int nch0 = (un.N0 + 31) >> 5, nch = nch0 + ((un.N1 + 31) >> 5);
-      auto chunk_buf = [&](int c) { return c < nch0 ? 0 : 1; };
-      auto chunk_col = [&](int c) { return 32 * (c < nch0 ? c : c - nch0); };
+      // chunk c = 32 accumulator columns.  Two-buffer unit: the first ntail
+      // chunks are the second MMA's (tail tokens, buffer buf0), then the first
+      // MMA's (buffer buf1); one-buffer unit: the first MMA's, buffer buf0.
+      const int ntail = nbuf == 2 ? (un.N1 + 31) >> 5 : 0;
+      const int nch = ntail + ((un.N0 + 31) >> 5);
+      const uint32_t bmain = nbuf == 2 ? buf1 : buf0;
+      auto chunk_buf = [&](int c) { return c < ntail ? 1 : 0; };  // which MMA (col_token)
+      auto chunk_col = [&](int c) { return 32 * (c < ntail ? c : c - ntail); };
       auto chunk_addr = [&](int c) {
-        return lanes + (c < nch0 ? buf0 : buf1) * ACC_COLS + (uint32_t)chunk_col(c);
+        return lanes + (c < ntail ? buf0 : bmain) * ACC_COLS + (uint32_t)chunk_col(c);
       };
-      // buffer 0 goes back to the MMA issuer once this warp has no chunk of it left
+      // the tail buffer goes back to the MMA issuer once this warp has no chunk
+      // of it left (the next unit's MMAs start in it)
       bool freed0 = false;
       auto free_buf0 = [&](int next_chunk) {
-        if (nbuf == 2 && !freed0 && next_chunk >= nch0) {
+        if (nbuf == 2 && !freed0 && next_chunk >= ntail) {
           freed0 = true;
           fence_before();
           __syncwarp();
