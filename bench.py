@@ -111,6 +111,12 @@ def parse():
     ap.add_argument("--router", default="logits", choices=["logits", "gemm"],
                     help="gemm: router logits from the gate GEMM (W_r N(0, 1/H) plus the "
                          "workload's Zipf bias) fused ahead of top-k instead of given logits")
+    ap.add_argument("--stage-every", type=int, default=10,
+                    help="record the per-stage CUDA events on every n-th timed step (the events "
+                         "themselves cost ~2 us each on the device)")
+    ap.add_argument("--exec", default="graph", choices=["graph", "eager"],
+                    help="graph: each step is a replay of a CUDA graph of the layer (all its "
+                         "kernels; captured before the timed region); eager: stream launches")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 dispatch and grouped FFN (e4m3, UE8M0 scales per 128-token group "
                          "and 128x128 weight block); layer input and output stay bf16")
@@ -214,11 +220,13 @@ class ClockSampler:
 class StepEvents:
     """CUDA events recorded on the launching stream at each stage boundary."""
 
-    def __init__(self):
+    def __init__(self, external: bool = False):
         self.marks = []
+        self.external = external
 
     def mark(self, name):
-        e = torch.cuda.Event(enable_timing=True)
+        # external: recorded as a node when the step is captured into a CUDA graph
+        e = torch.cuda.Event(enable_timing=True, external=self.external)
         e.record()
         self.marks.append((name, e))
 
@@ -284,7 +292,17 @@ def run_native(args, rank, world, local_rank):
         raise RuntimeError(f"device status {int(layer.status.item()):#x} after warm-up")
 
     # ---- timed region: K steps, inputs resident in HBM
-    evs = [StepEvents() for _ in range(args.steps)]
+    every = max(1, args.stage_every)
+    use_graph = args.exec == "graph"
+    evs = [StepEvents(external=use_graph) if i % every == 0 else None
+           for i in range(args.steps)]
+    graphs = None
+    if use_graph:
+        graphs = [layer.capture(x_loc, lg_loc, out, local_residual=res_loc, timings=evs[i])
+                  for i in range(args.steps)]
+        for g in graphs:       # a graph's first launch also uploads it: keep that untimed
+            g.replay()
+        torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -293,7 +311,10 @@ def run_native(args, rank, world, local_rank):
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
         for i in range(args.steps):
-            layer.forward(x_loc, lg_loc, out, timings=evs[i], local_residual=res_loc)
+            if graphs is not None:
+                graphs[i].replay()
+            else:
+                layer.forward(x_loc, lg_loc, out, timings=evs[i], local_residual=res_loc)
         t1.record()
         torch.cuda.synchronize()
     if world > 1:
@@ -302,6 +323,8 @@ def run_native(args, rank, world, local_rank):
     clocks = clk.summary()
     stage = {}
     for e in evs:
+        if e is None:
+            continue
         for k, v in e.durations().items():
             stage.setdefault(k, []).append(v)
     stage_ms = {k: statistics.mean(v) for k, v in stage.items()}
@@ -374,11 +397,23 @@ def run_native(args, rank, world, local_rank):
                     a.copy_(h, non_blocking=True)
                 h2d_done[b].record(s_h2d)
 
+        # graph execution: one graph per buffer set; each step stages its counts
+        # (the same host->device copy as an eager step) and replays
+        for b in range(2):  # capture warms up on these buffers: give them real rows
+            for a, t in zip(dx[b] + (dl[b] if args.router == "logits" else []),
+                            x_loc + (lg_loc if args.router == "logits" else [])):
+                a.copy_(t)
+        e2e_graphs = ([layer.capture(dx[b], dl[b], dout[b], local_residual=res_loc)
+                       for b in range(2)] if use_graph else None)
+
         def step(i, n):
             b = i % 2
             comp.wait_event(h2d_done[b])
             comp.wait_event(d2h_done[b])  # dout[b] was read back
-            layer.forward(dx[b], dl[b], dout[b], counts=spec.counts, local_residual=res_loc)
+            if e2e_graphs is not None:
+                e2e_graphs[b].replay(spec.counts)
+            else:
+                layer.forward(dx[b], dl[b], dout[b], counts=spec.counts, local_residual=res_loc)
             fwd_done[b].record(comp)
             if i + 1 < n:
                 h2d(1 - b)
@@ -620,6 +655,9 @@ def main():
                            boundary=args.boundary, shared_experts=spec.n_shared,
                            router=("gate GEMM fused ahead of top-k, W_r N(0, 1/H) plus the Zipf "
                                    "bias" if args.router == "gemm" else "given logits"),
+                           execution=("CUDA graph of the layer step, replayed" if args.exec == "graph"
+                                      else "stream launches"),
+                           stage_events=f"every {max(1, args.stage_every)}th timed step",
                            fp8=("e4m3 codes, UE8M0 scales per 128-token group and 128x128 "
                                 "weight block; bf16 layer input/output") if args.fp8 else None,
                            parallelism=f"{world} independent replica(s), one per GPU",

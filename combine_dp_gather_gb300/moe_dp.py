@@ -456,6 +456,14 @@ class MoeLayer:
         self.rows = rows
         return rows
 
+    def capture(self, local_x: Sequence[torch.Tensor], local_logits: Sequence[torch.Tensor],
+                out: Sequence[torch.Tensor],
+                local_residual: Optional[Sequence[torch.Tensor]] = None,
+                timings=None) -> "LayerGraph":
+        """Capture one step for the current counts layout (set_counts first) as a CUDA
+        graph; see LayerGraph."""
+        return LayerGraph(self, local_x, local_logits, out, local_residual, timings)
+
     def forward(self, local_x: Sequence[torch.Tensor], local_logits: Sequence[torch.Tensor],
                 out: Sequence[torch.Tensor], counts: Optional[Sequence[int]] = None,
                 stream=None, timings=None,
@@ -509,3 +517,37 @@ class MoeLayer:
         moe_dp_scatter(yg, self.d_counts, self.d_offsets, out, st, stream)
         ev("scatter")
         return out
+
+
+class LayerGraph:
+    """One MoeLayer step captured as a CUDA graph: the layer's kernels replay with
+    one launch, reading the replica counts and offsets from device memory.
+
+    A replay uses the tensors given at capture (the same replica inputs, outputs
+    and residuals) and the global row count of the layout at capture: replay(counts)
+    stages new counts on the device and requires the same row count (always true
+    under a static bound, where every step has identical kernel grids)."""
+
+    def __init__(self, layer: MoeLayer, local_x, local_logits, out, local_residual=None,
+                 timings=None):
+        if layer.rows == 0:
+            raise MoeError("LayerGraph", MOE_ERR_INVALID_ARG)
+        self.layer, self.rows = layer, layer.rows
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):      # one eager step first: host-side setup runs once
+            layer.forward(local_x, local_logits, out, local_residual=local_residual)
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            layer.forward(local_x, local_logits, out, local_residual=local_residual,
+                          timings=timings)
+
+    def replay(self, counts: Optional[Sequence[int]] = None):
+        if counts is not None:
+            _, rows = moe_dp_layout(counts, self.layer.mode, self.layer.static_bound,
+                                    self.layer.tpr)
+            if rows != self.rows:
+                raise MoeError("LayerGraph.replay", MOE_ERR_INVALID_ARG)
+            self.layer.set_counts(counts)
+        self.graph.replay()
