@@ -77,7 +77,7 @@ FFN_TRAFFIC = {
     "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "eb3b415fed33a4c0",
                 "bytes": 25820602368},
     "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
-                   "sha256_16": "6dbc846840f68bbc", "bytes": 2795898368},
+                   "sha256_16": "04f40fea5296bdc1", "bytes": 2794673664},
 }
 
 

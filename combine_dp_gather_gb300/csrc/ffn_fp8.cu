@@ -34,6 +34,13 @@
 //   warps 2-9 epilogue, two warps per TMEM lane quarter (token columns 0-31 and
 //             32-63): per k-block tcgen05.ld of the partials, release, scale and
 //             accumulate; per unit SwiGLU + quantisation or bf16 out
+// The epilogue's per-k-block work sets the pace once the weight stream is fast
+// enough, so it is kept small: a warp whose columns hold no token of the unit
+// only releases the buffer; the others scale only the columns that hold tokens
+// (in groups of 8), with packed fp32x2 FMAs.  A k-block's factor
+// 2^(e_token + e_weight) depends on the token and on which 128-row half of the
+// tile a row is in, not on the row, so each lane forms its token's two factors
+// once and the warp reads them back from shared memory as broadcasts.
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets
 // MOE_DEV_TIMEOUT, the other roles stop at their next wait, TMEM is freed and
 // the kernel returns.
@@ -53,6 +60,35 @@ constexpr int NT = 64;      // tokens per unit
 constexpr int CT = 32;      // token columns per epilogue warp
 constexpr int THREADS = 320;
 constexpr int NPB = 4;      // TMEM partial buffers: the MMAs run up to 4 k-blocks ahead of the epilogue
+
+// tcgen05.wait::ld that also names the destination registers of the load it
+// waits for, so the compiler cannot move a use of them above the wait.
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// (a0, a1) += (x0, x1) * (f[0], f[1]) as one packed fp32x2 FMA (each lane rounded
+// as fmaf); f is a shared-memory pair at the same address in every lane.
+__device__ __forceinline__ void fma2_shared(float& a0, float& a1, uint32_t x0, uint32_t x1,
+                                            const float* f) {
+  uint64_t a, x, g;
+  asm volatile("ld.shared.b64 %0, [%1];"
+               : "=l"(g)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(f)))
+               : "memory");
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(x0), "r"(x1));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x), "l"(g));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
+}
 
 template <bool SWIGLU>
 struct F8Cfg {
@@ -74,6 +110,7 @@ struct F8Smem {
   int32_t total_units;
   int32_t warp_sums[THREADS / 32];
   float wmax[2][4][CT];              // per epilogue warp: token maxima of h
+  alignas(16) float fac[8][2][CT];   // per epilogue warp: this k-block's token factors
   int32_t pref[MOE_MAX_SLOTS + 1];   // unit prefix over the slot range
   int32_t row0[MOE_MAX_SLOTS];
   int32_t rows[MOE_MAX_SLOTS];
@@ -290,11 +327,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int cg = (warp - 2) >> 2;  // token columns 32cg .. 32cg+31 of the unit
     const uint32_t lanes = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(cg * CT);
     const uint32_t bar_id = 1u + (uint32_t)cg;  // the four warps of this column group
+    float* fac0 = L.fac[warp - 2][0];  // factors of the first half (gate rows / rows 0-127)
+    float* fac1 = L.fac[warp - 2][1];  // and of the second (up rows / rows 128-255)
     uint32_t it = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const F8Unit un = decode_unit(L, p.nslots, u);
       const int32_t slot = p.slot_lo + un.slot;
       const int t0 = cg * CT;  // first token of this warp's columns
+      const bool act = t0 < un.ntok;
+      const int ncol = un.ntok - t0;  // columns of this warp that hold tokens (if act)
       // scale bytes, loaded one k-block ahead: lane j holds token t0 + j's byte,
       // every lane the weight blocks' bytes
       const int64_t trow = (int64_t)un.tok0 + t0 + lane;
@@ -322,22 +363,36 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         fence_after();
-        uint32_t r0[32], r1[32];
-        tmem_ld32(lanes + pb * C::PCOLS, r0);
-        tmem_ld32(lanes + pb * C::PCOLS + NT, r1);
-        tmem_wait_ld();
+        if (!act) {  // no token of the unit in this warp's columns
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&L.pempty[pb]));
+          continue;
+        }
+        const float cx_mine = pow2i((int)ex - 127);
+        uint32_t r[32];
+        tmem_ld32(lanes + pb * C::PCOLS, r);
+        __syncwarp();  // the previous k-block's factors have been read
+        fac0[lane] = cx_mine * pow2i((int)ew0 - 127);
+        fac1[lane] = cx_mine * pow2i((int)ew1 - 127);
+        __syncwarp();
+        tmem_wait_ld_regs(r);
+#pragma unroll
+        for (int g = 0; g < CT; g += 8)
+          if (g < ncol)
+#pragma unroll
+            for (int j = g; j < g + 8; j += 2)
+              fma2_shared(acc0[j], acc0[j + 1], r[j], r[j + 1], &fac0[j]);
+        tmem_ld32(lanes + pb * C::PCOLS + NT, r);
+        tmem_wait_ld_regs(r);
         fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&L.pempty[pb]));
-        const float cx_mine = pow2i((int)ex - 127);
-        const float cw0 = pow2i((int)ew0 - 127);
-        const float cw1 = pow2i((int)ew1 - 127);
 #pragma unroll
-        for (int j = 0; j < CT; ++j) {
-          const float cx = __shfl_sync(0xffffffffu, cx_mine, j);
-          acc0[j] = fmaf(__uint_as_float(r0[j]), cx * cw0, acc0[j]);
-          acc1[j] = fmaf(__uint_as_float(r1[j]), cx * cw1, acc1[j]);
-        }
+        for (int g = 0; g < CT; g += 8)
+          if (g < ncol)
+#pragma unroll
+            for (int j = g; j < g + 8; j += 2)
+              fma2_shared(acc1[j], acc1[j + 1], r[j], r[j + 1], &fac1[j]);
       }
       if (SWIGLU) ok = named_all(bar_id, 128, ok);  // the group's four warps leave together
       if (!ok) break;

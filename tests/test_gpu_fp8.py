@@ -133,14 +133,15 @@ def _dev_u8(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
-@pytest.mark.parametrize("counts,lo,hi", [
-    ([0, 1, 15, 16, 17, 31, 32, 33, 64, 100], 0, 10),
-    ([5, 0, 40, 3], 1, 3),
-    ([1] * 6, 0, 6)])
-def test_grouped_ffn_fp8(md, orc, counts, lo, hi):
-    """Token groups of 32 per unit: N = 16 or 32, ragged groups, several groups per slot,
-    empty slots, slot ranges; rows outside the range untouched."""
-    H, I = 512, 256
+@pytest.mark.parametrize("counts,lo,hi,H,I", [
+    ([0, 1, 15, 16, 17, 31, 32, 33, 64, 100], 0, 10, 512, 256),
+    ([5, 0, 40, 3], 1, 3, 512, 256),
+    ([1] * 6, 0, 6, 512, 256),
+    ([7, 70, 0, 33], 0, 4, 768, 640)])   # 6 and 5 k-blocks per unit
+def test_grouped_ffn_fp8(md, orc, counts, lo, hi, H, I):
+    """Token groups of up to 64 per unit: N = 16 .. 64, ragged groups, several groups per
+    slot, empty slots, slot ranges; rows outside the range untouched; K / 128 = 2, 4, 5
+    and 6 k-blocks per unit."""
     offsets, cap, xq, xe, wgu, wd = _fp8_inputs(orc, counts, H, I, seed=sum(counts) + lo)
     P = len(counts)
     w_fp8 = (_dev_u8(np.stack([w[0] for w in wgu])), _dev_u8(np.stack([w[1] for w in wgu])),
