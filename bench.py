@@ -395,10 +395,12 @@ def run_native(args, rank, world, local_rank):
                     a.copy_(h, non_blocking=True)
                 for a, h in zip(dl[b], hl):
                     a.copy_(h, non_blocking=True)
+                if e2e_graphs is not None:  # the step's counts travel with its inputs
+                    e2e_graphs[b].stage(spec.counts, stream=s_h2d)
                 h2d_done[b].record(s_h2d)
 
-        # graph execution: one graph per buffer set; each step stages its counts
-        # (the same host->device copy as an eager step) and replays
+        # graph execution: one graph per buffer set, each with its own counts/offsets
+        # buffer that the copy stream fills together with the step's inputs
         for b in range(2):  # capture warms up on these buffers: give them real rows
             for a, t in zip(dx[b] + (dl[b] if args.router == "logits" else []),
                             x_loc + (lg_loc if args.router == "logits" else [])):
@@ -411,7 +413,7 @@ def run_native(args, rank, world, local_rank):
             comp.wait_event(h2d_done[b])
             comp.wait_event(d2h_done[b])  # dout[b] was read back
             if e2e_graphs is not None:
-                e2e_graphs[b].replay(spec.counts)
+                e2e_graphs[b].replay()
             else:
                 layer.forward(dx[b], dl[b], dout[b], counts=spec.counts, local_residual=res_loc)
             fwd_done[b].record(comp)

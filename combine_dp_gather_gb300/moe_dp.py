@@ -393,16 +393,10 @@ class MoeLayer:
         self.max_rows = max_rows
         self.cap = moe_dispatch_cap_bound(max_rows, k + n_shared, self.P, align)
         i32 = dict(device=dev, dtype=torch.int32)
-        self.d_counts = torch.zeros(R, **i32)
-        self.d_offsets = torch.zeros(R + 1, **i32)
-        # ring of pinned staging buffers for the per-step counts/offsets copy, so
-        # the host only waits when it laps a copy still in flight
-        self._meta_ring = [torch.zeros(2 * R + 1, dtype=torch.int32, pin_memory=True)
-                           for _ in range(4)]
-        self._meta_done = [torch.cuda.Event() for _ in range(4)]
-        for ev in self._meta_done:
-            ev.record()
-        self._meta_i = 0
+        # counts [R] and offsets [R + 1] side by side: one host->device copy per step
+        self.d_meta = torch.zeros(2 * R + 1, **i32)
+        self.d_counts, self.d_offsets = self.d_meta[:R], self.d_meta[R:]
+        self._stage = _MetaStager(R)
         self.status = torch.zeros(1, **i32)
         self.xg = torch.empty(max_rows, H, device=dev, dtype=self.dtype)
         self.logits_g = torch.empty(max_rows, E, device=dev, dtype=torch.float32)
@@ -440,19 +434,12 @@ class MoeLayer:
 
     def set_counts(self, counts: Sequence[int]) -> int:
         """Host layout for this step's replica counts; stages counts and offsets on
-        the device (one pinned H2D copy).  Returns the global row count."""
+        the device (one pinned H2D copy on the current stream).  Returns the global
+        row count."""
         offsets, rows = moe_dp_layout(counts, self.mode, self.static_bound, self.tpr)
         if rows > self.max_rows:
             raise MoeError("MoeLayer.set_counts", MOE_ERR_CAPACITY)
-        i = self._meta_i
-        self._meta_i = (i + 1) % len(self._meta_ring)
-        self._meta_done[i].synchronize()  # the copy that last used this buffer has run
-        h = self._meta_ring[i]
-        h[: self.R] = torch.tensor(list(counts), dtype=torch.int32)
-        h[self.R:] = torch.tensor(offsets, dtype=torch.int32)
-        self.d_counts.copy_(h[: self.R], non_blocking=True)
-        self.d_offsets.copy_(h[self.R:], non_blocking=True)
-        self._meta_done[i].record()
+        self._stage(counts, offsets, self.d_meta, None)
         self.rows = rows
         return rows
 
@@ -519,35 +506,78 @@ class MoeLayer:
         return out
 
 
+class _MetaStager:
+    """Ring of pinned staging buffers for the per-step counts/offsets copy, so the
+    host only waits when it laps a copy still in flight."""
+
+    def __init__(self, R: int, depth: int = 4):
+        self.R = R
+        self.ring = [torch.zeros(2 * R + 1, dtype=torch.int32, pin_memory=True)
+                     for _ in range(depth)]
+        self.done = [torch.cuda.Event() for _ in range(depth)]
+        for ev in self.done:
+            ev.record()
+        self.i = 0
+
+    def __call__(self, counts, offsets, d_meta: torch.Tensor, stream):
+        i = self.i
+        self.i = (i + 1) % len(self.ring)
+        self.done[i].synchronize()  # the copy that last used this buffer has run
+        h = self.ring[i]
+        h[: self.R] = torch.tensor(list(counts), dtype=torch.int32)
+        h[self.R:] = torch.tensor(offsets, dtype=torch.int32)
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            d_meta.copy_(h, non_blocking=True)
+            self.done[i].record(s)
+
+
 class LayerGraph:
     """One MoeLayer step captured as a CUDA graph: the layer's kernels replay with
-    one launch, reading the replica counts and offsets from device memory.
+    one launch, reading the replica counts and offsets from a device buffer of the
+    graph's own.
 
     A replay uses the tensors given at capture (the same replica inputs, outputs
-    and residuals) and the global row count of the layout at capture: replay(counts)
-    stages new counts on the device and requires the same row count (always true
-    under a static bound, where every step has identical kernel grids)."""
+    and residuals) and the global row count of the layout at capture.  stage(counts,
+    stream) copies a step's counts and offsets into the graph's buffer on any stream
+    (e.g. the copy stream that brings the step's inputs, so the compute stream sees
+    no copy between replays); replay(counts) stages on the current stream and
+    replays.  New counts must give the same row count (always true under a static
+    bound, where every step has identical kernel grids)."""
 
     def __init__(self, layer: MoeLayer, local_x, local_logits, out, local_residual=None,
                  timings=None):
         if layer.rows == 0:
             raise MoeError("LayerGraph", MOE_ERR_INVALID_ARG)
         self.layer, self.rows = layer, layer.rows
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):      # one eager step first: host-side setup runs once
-            layer.forward(local_x, local_logits, out, local_residual=local_residual)
-        torch.cuda.current_stream().wait_stream(side)
-        self.graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.graph):
-            layer.forward(local_x, local_logits, out, local_residual=local_residual,
-                          timings=timings)
+        self.d_meta = layer.d_meta.clone()       # the layer's current layout
+        self._stage = _MetaStager(layer.R)
+        saved = layer.d_meta, layer.d_counts, layer.d_offsets
+        layer.d_meta = self.d_meta
+        layer.d_counts, layer.d_offsets = self.d_meta[: layer.R], self.d_meta[layer.R:]
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):  # one eager step first: host-side setup runs once
+                layer.forward(local_x, local_logits, out, local_residual=local_residual)
+            torch.cuda.current_stream().wait_stream(side)
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph):
+                layer.forward(local_x, local_logits, out, local_residual=local_residual,
+                              timings=timings)
+        finally:
+            layer.d_meta, layer.d_counts, layer.d_offsets = saved
+
+    def stage(self, counts: Sequence[int], stream=None):
+        """Copy this step's counts and offsets into the graph's buffer on `stream`
+        (default: the current stream); order the replay after it."""
+        L = self.layer
+        offsets, rows = moe_dp_layout(counts, L.mode, L.static_bound, L.tpr)
+        if rows != self.rows:
+            raise MoeError("LayerGraph.stage", MOE_ERR_INVALID_ARG)
+        self._stage(counts, offsets, self.d_meta, stream)
 
     def replay(self, counts: Optional[Sequence[int]] = None):
         if counts is not None:
-            _, rows = moe_dp_layout(counts, self.layer.mode, self.layer.static_bound,
-                                    self.layer.tpr)
-            if rows != self.rows:
-                raise MoeError("LayerGraph.replay", MOE_ERR_INVALID_ARG)
-            self.layer.set_counts(counts)
+            self.stage(counts)
         self.graph.replay()

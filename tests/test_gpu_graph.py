@@ -68,3 +68,15 @@ def test_graph_replay_matches_eager(md, fp8):
         assert np.array_equal(to_np(a[:c]), to_np(b[:c]))
     with pytest.raises(md.MoeError):
         g.replay([20, 3, 139, 0, 7])      # 5 x 139 rows: another layout
+    # counts staged on another stream, the replay ordered after it
+    counts3 = [140, 0, 0, 1, 99]
+    layer.forward(bx, bl, eager, counts=counts3)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g.stage(counts3, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    for a, b, c in zip(bo, eager, counts3):
+        assert np.array_equal(to_np(a[:c]), to_np(b[:c]))
