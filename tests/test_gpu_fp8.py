@@ -9,7 +9,8 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import BF16_ATOL, BF16_RTOL, as_f32, assert_close, rel_fro, to_np
+from gpu_util import (BF16_ATOL, BF16_RTOL, as_f32, assert_close, graph_replay_matches_eager,
+                      rel_fro, to_np)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -242,6 +243,7 @@ def _layer_fp8_check(md, orc, spec, sample=None):
     assert not yg[valid == 0].any()
     got = np.concatenate([as_f32(to_np(t)) for t in out])
     assert np.array_equal(got, yg[valid == 1])
+    graph_replay_matches_eager(layer, x_loc, lg_loc, out)
 
 
 @pytest.mark.parametrize("mode", [0, 1])

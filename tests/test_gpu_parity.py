@@ -16,7 +16,7 @@ import torch
 import oracle as orc_mod
 from combine_dp_gather_gb300 import synth
 from gpu_util import (BF16_ATOL, BF16_RTOL, F32_ATOL, F32_RTOL, W_ATOL, W_RTOL, as_f32,
-                      assert_close, rel_fro, to_np)
+                      assert_close, graph_replay_matches_eager, rel_fro, to_np)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -498,12 +498,16 @@ def test_layer_dsv3_decode_full_size(md, orc):
     spec = synth.spec_decode(seed=0)
     res = _layer_gpu(md, spec)
     _check_layer(md, orc, spec, *res, sample=10)
+    layer, out, x_loc, lg_loc = res[:4]
+    graph_replay_matches_eager(layer, x_loc, lg_loc, out)
 
 
 def test_layer_dsv3_prefill_full_size(md, orc):
     spec = synth.spec_prefill()
     res = _layer_gpu(md, spec)
     _check_layer(md, orc, spec, *res, sample=6)
+    layer, out, x_loc, lg_loc = res[:4]
+    graph_replay_matches_eager(layer, x_loc, lg_loc, out)
 
 
 @pytest.mark.parametrize("mix,tpr,mode", [("mix0", 1, 0), ("mix1", 4, 1), ("mix2", 4, 2),
