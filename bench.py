@@ -74,8 +74,8 @@ def ffn_kernel(cap: int, P: int, fp8: bool = False) -> str:
 FFN_TRAFFIC = {
     "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "55f0dffc52932a6f",
                "bytes": 5582279168},
-    "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "eb3b415fed33a4c0",
-                "bytes": 25820602368},
+    "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "8c030af9768dcdcc",
+                "bytes": 25841341184},
     "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
                    "sha256_16": "04f40fea5296bdc1", "bytes": 2794673664},
 }

@@ -32,13 +32,17 @@
 // (in a hand-over buffer already read) and writes token rows with 16-byte
 // stores (h and ys stay [tokens, features]).
 //
-// TMEM holds two 256-column fp32 accumulators per SM.  A unit of N <= 256
-// tokens takes one (the next unit's MMAs overlap its epilogue), a unit of
-// 256 < N <= 320 takes both: its first 256 tokens in the second, its tail in
-// the first, which the epilogue reads and frees first, so the next unit's MMAs
-// (which start in that buffer) overlap the rest of the epilogue.  Token rows
-// past the slot's end are computed from whatever follows and never stored;
-// rows past the buffer read as zero.
+// TMEM (512 fp32 columns per SM) is two halves of 256 columns, each a "head"
+// (its first 64 columns) and a "rest".  Units alternate halves: unit s puts
+// its first N0 <= 256 tokens in half s % 2 and its tail (N1 <= 64 tokens) in
+// the head of the other half.  The epilogue reads the tail, then the main
+// part from its first column, and hands each of the three regions back as
+// soon as its warps have loaded their last chunk of it; the next unit needs
+// only its own half (the rest was freed a unit ago, the head holds this
+// unit's tail) and the head of this unit's half for its tail, so its MMAs
+// start after the first few chunks of this epilogue instead of all of it.
+// Token rows past the slot's end are computed from whatever follows and never
+// stored; rows past the buffer read as zero.
 //
 // Roles (320 threads, one CTA per SM, clusters of two):
 //   warp 0    TMA producer (both CTAs): one weight box (128 rows) and one
@@ -70,7 +74,8 @@ constexpr int B_BYTES = B_ROWS * BK * 2;        // 20 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 36 KB
 constexpr int STAGES = 5;
 constexpr int THREADS = 320;
-constexpr int ACC_COLS = 256;                   // one accumulator buffer
+constexpr int HALF_COLS = 256;                  // one TMEM half: a unit's main accumulator
+constexpr int HEAD_COLS = 64;                   // head of a half: the other half's unit's tail
 constexpr int EPI_WARPS = 8;                    // two per TMEM lane quarter
 constexpr int XCH_BYTES = 32 * 32 * 4;          // per epilogue warp: 32 lanes x 32 fp32
 constexpr int NUM_BOXES = B_ROWS / 8;           // token boxes of 8, 16, ..., 160 rows
@@ -98,8 +103,8 @@ struct SwapParams {
 struct SmemLayout {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t tmem_full[2];
-  uint64_t tmem_empty[2];
+  uint64_t tmem_full[2];    // per unit parity: the unit's MMAs are done
+  uint64_t tmem_empty[4];   // per TMEM region (head 0, rest 0, head 1, rest 1): drained
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t total_units;
@@ -205,10 +210,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(smem_u32(&L.full[i]), 1);   // leader: its producer's expect_tx
         mbar_init(smem_u32(&L.empty[i]), 1);  // the leader's MMA commit
       }
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(smem_u32(&L.tmem_full[i]), 1);
+      for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&L.tmem_full[i]), 1);
+      for (int i = 0; i < 4; ++i)
         mbar_init(smem_u32(&L.tmem_empty[i]), 2 * EPI_WARPS);  // every epilogue warp of the pair
-      }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) tmem_alloc<2>(smem_u32(&L.tmem_base));  // whole warp, both CTAs
@@ -287,22 +291,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader CTA)
     if (leader) {
-      uint32_t it = 0, bseq = 0;
-      for (int u = cid; u < total; u += ncl) {
+      uint32_t it = 0, seq = 0;
+      uint32_t uses[4] = {0, 0, 0, 0};  // earlier uses of each TMEM region
+      for (int u = cid; u < total; u += ncl, ++seq) {
         const SUnit un = decode_unit(L, p.nslots, u);
-        const uint32_t nbuf = un.N1 ? 2u : 1u;
-        const uint32_t buf0 = bseq & 1u, buf1 = (bseq + 1) & 1u;
-        if (!wait_bar(smem_u32(&L.tmem_empty[buf0]), ((bseq >> 1) & 1u) ^ 1u, abort_flag,
-                      p.status))
-          break;
-        if (nbuf == 2 && !wait_bar(smem_u32(&L.tmem_empty[buf1]), (((bseq + 1) >> 1) & 1u) ^ 1u,
-                                   abort_flag, p.status))
-          break;
+        const uint32_t hm = seq & 1u;  // the unit's half; its tail goes to the other head
+        // this half's head and rest, and for a tail the other half's head
+        auto take = [&](uint32_t r) {
+          const bool got = wait_bar(smem_u32(&L.tmem_empty[r]), (uses[r] & 1u) ^ 1u, abort_flag,
+                                    p.status);
+          ++uses[r];
+          return got;
+        };
+        if (!take(2 * hm) || !take(2 * hm + 1) || (un.N1 && !take(2 * (hm ^ 1u)))) break;
         fence_after();
-        // a two-buffer unit keeps its first 256 tokens in its second buffer and
-        // the rest in its first, which the epilogue reads (and frees) first
-        const uint32_t d0 = tmem_base + (nbuf == 2 ? buf1 : buf0) * ACC_COLS;
-        const uint32_t d1 = tmem_base + buf0 * ACC_COLS;
+        const uint32_t d0 = tmem_base + hm * HALF_COLS;
+        const uint32_t d1 = tmem_base + (hm ^ 1u) * HALF_COLS;
         const uint32_t id0 = idesc_bf16(256, un.N0);
         const uint32_t id1 = idesc_bf16(256, un.N1 ? un.N1 : 16);
         const uint32_t boff1 = (uint32_t)(un.N0 >> 1) * BK * 2;
@@ -329,12 +333,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           __syncwarp();
         }
         if (!ok) break;
-        if (lane == 0) {
-          commit<2>(smem_u32(&L.tmem_full[buf0]));
-          if (nbuf == 2) commit<2>(smem_u32(&L.tmem_full[buf1]));
-        }
+        if (lane == 0) commit<2>(smem_u32(&L.tmem_full[hm]));
         __syncwarp();
-        bseq += nbuf;
       }
     }
   } else {
@@ -345,41 +345,44 @@ __global__ void __launch_bounds__(THREADS, 1)
     float* xmine = xch + e * (XCH_BYTES / 4);
     float* xpeer = xch + e_peer * (XCH_BYTES / 4);
     const uint32_t bar_id = 1u + (uint32_t)(q & 1) + 2u * (uint32_t)grp;  // lanes q and q ^ 2
-    uint32_t bseq = 0;
-    for (int u = cid; u < total; u += ncl) {
+    uint32_t seq = 0;
+    for (int u = cid; u < total; u += ncl, ++seq) {
       const SUnit un = decode_unit(L, p.nslots, u);
-      const uint32_t nbuf = un.N1 ? 2u : 1u;
-      const uint32_t buf0 = bseq & 1u, buf1 = (bseq + 1) & 1u;
-      bool ok = wait_bar(smem_u32(&L.tmem_full[buf0]), (bseq >> 1) & 1u, abort_flag, p.status);
-      if (ok && nbuf == 2)
-        ok = wait_bar(smem_u32(&L.tmem_full[buf1]), ((bseq + 1) >> 1) & 1u, abort_flag, p.status);
+      const uint32_t hm = seq & 1u;  // the unit's half; its tail is in the other head
+      bool ok = wait_bar(smem_u32(&L.tmem_full[hm]), (seq >> 1) & 1u, abort_flag, p.status);
       // the gate and up warps of a feature range leave together, or the one
       // still in the chunk loop would wait for its partner forever
       if (SWIGLU) ok = named_all(bar_id, 64, ok);
       if (!ok) break;
       fence_after();
       const uint32_t lanes = tmem_base + ((uint32_t)(q * 32) << 16);
-      // chunk c = 32 accumulator columns.  Two-buffer unit: the first ntail
-      // chunks are the second MMA's (tail tokens, buffer buf0), then the first
-      // MMA's (buffer buf1); one-buffer unit: the first MMA's, buffer buf0.
-      const int ntail = nbuf == 2 ? (un.N1 + 31) >> 5 : 0;
-      const int nch = ntail + ((un.N0 + 31) >> 5);
-      const uint32_t bmain = nbuf == 2 ? buf1 : buf0;
+      // chunk c = 32 accumulator columns: first the ntail chunks of the tail
+      // (second MMA, head of the other half), then the main part's (first MMA,
+      // this unit's half) from its first column
+      const int ntail = (un.N1 + 31) >> 5;
+      const int nmain = (un.N0 + 31) >> 5;
+      const int nch = ntail + nmain;
       auto chunk_buf = [&](int c) { return c < ntail ? 1 : 0; };  // which MMA (col_token)
       auto chunk_col = [&](int c) { return 32 * (c < ntail ? c : c - ntail); };
       auto chunk_addr = [&](int c) {
-        return lanes + (c < ntail ? buf0 : bmain) * ACC_COLS + (uint32_t)chunk_col(c);
+        return lanes + (c < ntail ? hm ^ 1u : hm) * HALF_COLS + (uint32_t)chunk_col(c);
       };
-      // the tail buffer goes back to the MMA issuer once this warp has no chunk
-      // of it left (the next unit's MMAs start in it)
-      bool freed0 = false;
-      auto free_buf0 = [&](int next_chunk) {
-        if (nbuf == 2 && !freed0 && next_chunk >= ntail) {
-          freed0 = true;
-          fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&L.tmem_empty[buf0]), 0));
-        }
+      // regions of this unit in chunk order: tail (other head), head, rest of
+      // this half; each goes back to the MMA issuer once this warp has loaded
+      // its last chunk of it (the regions the MMA issuer waited on)
+      const int head_end = ntail + (nmain < HEAD_COLS / 32 ? nmain : HEAD_COLS / 32);
+      auto r_end = [&](int i) { return i == 0 ? ntail : (i == 1 ? head_end : nch); };
+      auto r_id = [&](int i) { return i == 0 ? 2 * (hm ^ 1u) : 2 * hm + (uint32_t)(i - 1); };
+      int freed = un.N1 ? 0 : 1;  // regions 0 .. freed-1 handed back (no tail: none to hand)
+      auto release = [&](int next_chunk) {
+        const int from = freed;
+        while (freed < 3 && next_chunk >= r_end(freed)) ++freed;
+        if (freed == from) return;
+        fence_before();
+        __syncwarp();
+        if (lane == 0)
+          for (int i = from; i < freed; ++i)
+            mbar_arrive_cluster(map_to_rank(smem_u32(&L.tmem_empty[r_id(i)]), 0));
       };
       // 32 columns x 32 features of this warp -> token rows of `out`, 16-byte
       // stores through a staging tile (`wstg`, a hand-over buffer no longer read)
@@ -409,7 +412,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(chunk_addr(c), v0);
           if (has2) tmem_ld32(chunk_addr(c + 1), v1);
           tmem_wait_ld();
-          free_buf0(c + 4);
+          release(c + 4);
           // the gate warp computes chunk c, the up warp chunk c + 1; each hands
           // the other the values it lacks
           if (is_gate) {
@@ -443,20 +446,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint32_t v[32];
           tmem_ld32(chunk_addr(c), v);
           tmem_wait_ld();
-          free_buf0(c + 2);
+          release(c + 2);
           float y[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(v[j]);
           store_block(y, c, feat, reinterpret_cast<__nv_bfloat16*>(xmine));
         }
       }
-      fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (!freed0) mbar_arrive_cluster(map_to_rank(smem_u32(&L.tmem_empty[buf0]), 0));
-        if (nbuf == 2) mbar_arrive_cluster(map_to_rank(smem_u32(&L.tmem_empty[buf1]), 0));
-      }
-      bseq += nbuf;
+      release(nch);  // whatever this warp had no chunk of
     }
   }
 
