@@ -52,6 +52,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     combine_kernel(const uint4* __restrict__ ys, const int32_t* __restrict__ inv,
                    const float* __restrict__ w, int64_t rows, int k, int vpr, int64_t cap,
                    uint4* __restrict__ out, uint32_t* status) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   constexpr int EPV = BF16 ? 8 : 4;  // elements per 16-byte vector
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
@@ -147,11 +149,11 @@ extern "C" moe_status moe_combine(const void* d_out_sorted, const int32_t* d_inv
   int grid = (int)(want < lim ? want : lim);
   cudaStream_t s = as_stream(stream);
   if (dtype == MOE_BF16)
-    combine_kernel<true><<<grid, kWarps * 32, 0, s>>>(
+    launch(combine_kernel<true>, grid, kWarps * 32, 0, s,
         static_cast<const uint4*>(d_out_sorted), d_inv, d_w, rows, k, vpr, cap,
         static_cast<uint4*>(d_global_out), d_status);
   else
-    combine_kernel<false><<<grid, kWarps * 32, 0, s>>>(
+    launch(combine_kernel<false>, grid, kWarps * 32, 0, s,
         static_cast<const uint4*>(d_out_sorted), d_inv, d_w, rows, k, vpr, cap,
         static_cast<uint4*>(d_global_out), d_status);
   return launch_status();

@@ -22,6 +22,44 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 int num_sms();  // cached per device (host.cpp)
 
+// Programmatic dependent launch: every kernel of the library is launched with
+// programmatic stream serialization, so its launch may overlap the end of the
+// kernel before it on the stream.  Each kernel starts with grid_dep_wait(),
+// which returns once the earlier kernels on the stream have completed and
+// their memory is visible, before it touches global memory; it then calls
+// grid_dep_launch() so that the next kernel can start launching.  MOE_PDL=0
+// in the environment turns the overlap off (plain stream order).
+bool pdl_enabled();  // host.cpp
+
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+inline void set_pdl_attr(cudaLaunchAttribute& a) {
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+}
+
+// kernel<<<grid, block, smem, stream>>>(args...) with the dependent-launch
+// attribute; the result is also left for cudaGetLastError.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                   cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  set_pdl_attr(attr[0]);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Replica pointer table passed by value as a kernel argument.
 struct ReplicaPtrs {
   const void* p[MOE_MAX_REPLICAS];

@@ -36,6 +36,8 @@ inline int64_t n_chunks(int64_t pairs) { return (pairs + kChunk - 1) / kChunk; }
 __global__ void __launch_bounds__(256)
     dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t pairs, int E,
                          int32_t* __restrict__ hist, uint32_t* status) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   extern __shared__ int32_t s_h[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_h[e] = 0;
   __syncthreads();
@@ -85,6 +87,8 @@ __global__ void __launch_bounds__(1024)
                          const int32_t* __restrict__ l2p, const int32_t* __restrict__ nrep, int X,
                          int align, int64_t cap, int32_t* __restrict__ counts_P,
                          int32_t* __restrict__ offsets_P, uint32_t* status) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   __shared__ int32_t s_cnt[MOE_MAX_SLOTS];    // per logical expert
   __shared__ int32_t s_slot[MOE_MAX_SLOTS];   // per physical slot
   __shared__ int32_t s_claim[MOE_MAX_SLOTS];
@@ -211,6 +215,8 @@ __global__ void __launch_bounds__(32)
                          const int32_t* __restrict__ offsets_P, int64_t cap,
                          int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                          int stage_map, uint32_t* status) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   extern __shared__ int32_t smem[];
   int32_t* s_run = smem;               // [E]  running count (starts at the chunk base)
   int32_t* s_off = s_run + E;          // [P + 1]
@@ -255,6 +261,8 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
                           int X, int align, int64_t cap, int32_t* __restrict__ counts_P,
                           int32_t* __restrict__ offsets_P, int32_t* __restrict__ perm,
                           int32_t* __restrict__ inv, uint32_t* status) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   extern __shared__ int32_t smem[];
   int32_t* s_hist = smem;                           // [kSmallWarps][E]
   int32_t* s_off = s_hist + kSmallWarps * E;        // [P + 1]
@@ -361,6 +369,8 @@ constexpr int kSegVecs = 32 * kCopyUnroll;  // vectors per warp segment of a row
 __global__ void __launch_bounds__(kCopyWarps * 32)
     dispatch_copy_kernel(const uint4* __restrict__ xg, const int32_t* __restrict__ inv,
                          int64_t rows, int k, int vpr, int64_t cap, uint4* __restrict__ xs) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t)blockIdx.x * kCopyWarps + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kCopyWarps;
@@ -396,6 +406,8 @@ __global__ void __launch_bounds__(256)
     dispatch_pad_kernel(const int32_t* __restrict__ counts_P, const int32_t* __restrict__ offsets_P,
                         int P, int vpr, int64_t cap, int32_t* __restrict__ perm,
                         uint4* __restrict__ xs) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   const int s = blockIdx.x;
   if (s >= P) return;
   int64_t a = (int64_t)offsets_P[s] + counts_P[s];
@@ -456,21 +468,21 @@ extern "C" moe_status moe_dispatch(const void* d_global, const int32_t* d_ids, i
       sizeof(int32_t) * ((size_t)kSmallWarps * E + (P + 1) + 2 * (size_t)P + E);
   if (pairs <= kSmallPairs && small_smem <= kSmallSmemBytes) {
     const size_t smem = small_smem;
-    dispatch_small_kernel<<<1, kSmallWarps * 32, smem, s>>>(
+    launch(dispatch_small_kernel, 1, kSmallWarps * 32, smem, s,
         d_ids, pairs, k, E, P, d_l2p, d_nrep, X, align, cap, d_counts_P, d_offsets_P, d_perm,
         d_inv, d_status);
   } else if (chunks == 0) {
-    dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, 0, E, P, d_l2p, d_nrep, X, align, cap,
+    launch(dispatch_scan_kernel, 1, 1024, 0, s, hist, 0, E, P, d_l2p, d_nrep, X, align, cap,
                                             d_counts_P, d_offsets_P, d_status);
   } else {
-    dispatch_hist_kernel<<<(unsigned)chunks, 256, E * sizeof(int32_t), s>>>(d_ids, pairs, E, hist,
+    launch(dispatch_hist_kernel, (unsigned)chunks, 256, E * sizeof(int32_t), s, d_ids, pairs, E, hist,
                                                                             d_status);
-    dispatch_scan_kernel<<<1, 1024, 0, s>>>(hist, chunks, E, P, d_l2p, d_nrep, X, align, cap,
+    launch(dispatch_scan_kernel, 1, 1024, 0, s, hist, chunks, E, P, d_l2p, d_nrep, X, align, cap,
                                             d_counts_P, d_offsets_P, d_status);
     // replica tables staged in shared memory when they fit (else read from global)
     const int stage_map = d_l2p != nullptr && (int64_t)E * X <= 4096;
     const size_t smem = sizeof(int32_t) * (E + (P + 1) + (stage_map ? E + (size_t)E * X : 0));
-    dispatch_rank_kernel<<<(unsigned)chunks, 32, smem, s>>>(d_ids, pairs, k, E, hist, d_l2p,
+    launch(dispatch_rank_kernel, (unsigned)chunks, 32, smem, s, d_ids, pairs, k, E, hist, d_l2p,
                                                            d_nrep, X, P, d_offsets_P, cap, d_perm,
                                                            d_inv, stage_map, d_status);
   }
@@ -478,12 +490,12 @@ extern "C" moe_status moe_dispatch(const void* d_global, const int32_t* d_ids, i
     const int64_t items = rows * ((vpr + kSegVecs - 1) / kSegVecs);
     int64_t want = (items + kCopyWarps - 1) / kCopyWarps;
     int64_t lim = (int64_t)num_sms() * 8;
-    dispatch_copy_kernel<<<(unsigned)(want < lim ? want : lim), kCopyWarps * 32, 0, s>>>(
+    launch(dispatch_copy_kernel, (unsigned)(want < lim ? want : lim), kCopyWarps * 32, 0, s,
         static_cast<const uint4*>(d_global), d_inv, rows, k, vpr, cap,
         static_cast<uint4*>(d_sorted));
   }
   if (align > 1) {
-    dispatch_pad_kernel<<<P, 256, 0, s>>>(d_counts_P, d_offsets_P, P, vpr, cap, d_perm,
+    launch(dispatch_pad_kernel, P, 256, 0, s, d_counts_P, d_offsets_P, P, vpr, cap, d_perm,
                                           move_rows ? static_cast<uint4*>(d_sorted) : nullptr);
   }
   return launch_status();

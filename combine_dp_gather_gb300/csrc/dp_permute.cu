@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     dp_gather_kernel(ReplicaPtrs src, const int32_t* __restrict__ counts,
                      const int32_t* __restrict__ offsets, int R, int64_t rows, int vpr,
                      uint4* __restrict__ global, uint32_t* status) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   __shared__ int32_t s_off[MOE_MAX_REPLICAS + 1];
   __shared__ int32_t s_cnt[MOE_MAX_REPLICAS];
   for (int i = threadIdx.x; i <= R; i += blockDim.x) {
@@ -87,6 +89,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     dp_scatter_kernel(const uint4* __restrict__ global, const int32_t* __restrict__ counts,
                       const int32_t* __restrict__ offsets, int R, int64_t rows, int vpr,
                       ReplicaPtrs dst, uint32_t* status) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   __shared__ int32_t s_off[MOE_MAX_REPLICAS + 1];
   __shared__ int32_t s_cnt[MOE_MAX_REPLICAS];
   for (int i = threadIdx.x; i <= R; i += blockDim.x) {
@@ -168,6 +172,8 @@ __global__ void __launch_bounds__(kNormThreads)
                                  const int32_t* __restrict__ counts,
                                  const int32_t* __restrict__ offsets, int R, int64_t rows, int H,
                                  int vpr, uint4* __restrict__ global, uint32_t* status) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   constexpr int EPV = BF16 ? 8 : 4;
   __shared__ int32_t s_off[MOE_MAX_REPLICAS + 1];
   __shared__ int32_t s_cnt[MOE_MAX_REPLICAS];
@@ -276,7 +282,7 @@ extern "C" moe_status moe_dp_gather(const void* const* local, const int32_t* d_c
     ptrs.p[r] = local[r];
   }
   const int vpr = (int)((int64_t)H * dtype_bytes(dtype) / 16);
-  dp_gather_kernel<<<grid_for_rows(rows, vpr), kWarps * 32, 0, as_stream(stream)>>>(
+  launch(dp_gather_kernel, grid_for_rows(rows, vpr), kWarps * 32, 0, as_stream(stream),
       ptrs, d_counts, d_offsets, R, rows, vpr, static_cast<uint4*>(d_global), d_status);
   return launch_status();
 }
@@ -305,11 +311,11 @@ extern "C" moe_status moe_dp_gather_add_rmsnorm(const void* const* local_hidden,
   const int64_t lim = (int64_t)num_sms() * 8;
   const int grid = (int)(rows < lim ? rows : lim);
   if (dtype == MOE_BF16)
-    dp_gather_add_rmsnorm_kernel<true><<<grid, kNormThreads, 0, as_stream(stream)>>>(
+    launch(dp_gather_add_rmsnorm_kernel<true>, grid, kNormThreads, 0, as_stream(stream),
         hp, rp, static_cast<const uint4*>(d_gamma), eps, d_counts, d_offsets, R, rows, H, vpr,
         static_cast<uint4*>(d_global), d_status);
   else
-    dp_gather_add_rmsnorm_kernel<false><<<grid, kNormThreads, 0, as_stream(stream)>>>(
+    launch(dp_gather_add_rmsnorm_kernel<false>, grid, kNormThreads, 0, as_stream(stream),
         hp, rp, static_cast<const uint4*>(d_gamma), eps, d_counts, d_offsets, R, rows, H, vpr,
         static_cast<uint4*>(d_global), d_status);
   return launch_status();
@@ -328,7 +334,7 @@ extern "C" moe_status moe_dp_scatter(const void* d_global, const int32_t* d_coun
     ptrs.p[r] = local[r];
   }
   const int vpr = (int)((int64_t)H * dtype_bytes(dtype) / 16);
-  dp_scatter_kernel<<<grid_for_rows(rows, vpr), kWarps * 32, 0, as_stream(stream)>>>(
+  launch(dp_scatter_kernel, grid_for_rows(rows, vpr), kWarps * 32, 0, as_stream(stream),
       static_cast<const uint4*>(d_global), d_counts, d_offsets, R, rows, vpr, ptrs, d_status);
   return launch_status();
 }

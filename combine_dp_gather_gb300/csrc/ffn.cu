@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(TS * 8)
     ffn1_f32_kernel(const float* __restrict__ xs, const int32_t* __restrict__ offsets, int lo,
                     int hi, int64_t cap, const float* __restrict__ wgu, int H, int I,
                     float* __restrict__ h) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   const int64_t r0 = (int64_t)blockIdx.y * TS;
   const int i = blockIdx.x * TS + (threadIdx.x & (TS - 1));
   const int64_t begin = offsets[lo], end = offsets[hi] < cap ? offsets[hi] : cap;
@@ -54,6 +56,8 @@ __global__ void __launch_bounds__(TS * 8)
     ffn2_f32_kernel(const float* __restrict__ h, const int32_t* __restrict__ offsets, int lo,
                     int hi, int64_t cap, const float* __restrict__ wd, int H, int I,
                     float* __restrict__ ys) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   const int64_t r0 = (int64_t)blockIdx.y * TS;
   const int o = blockIdx.x * TS + (threadIdx.x & (TS - 1));
   const int64_t begin = offsets[lo], end = offsets[hi] < cap ? offsets[hi] : cap;
@@ -75,11 +79,11 @@ moe_status launch_ffn_simt_f32(const FfnArgs& a, cudaStream_t s) {
   if (a.slot_hi <= a.slot_lo || a.cap <= 0) return MOE_OK;
   dim3 block(TS * 8);
   dim3 g1((a.I + TS - 1) / TS, (unsigned)((a.cap + TS - 1) / TS));
-  ffn1_f32_kernel<<<g1, block, 0, s>>>(static_cast<const float*>(a.xs), a.offsets, a.slot_lo,
+  launch(ffn1_f32_kernel, g1, block, 0, s, static_cast<const float*>(a.xs), a.offsets, a.slot_lo,
                                        a.slot_hi, a.cap, static_cast<const float*>(a.wgu), a.H,
                                        a.I, static_cast<float*>(a.h));
   dim3 g2((a.H + TS - 1) / TS, (unsigned)((a.cap + TS - 1) / TS));
-  ffn2_f32_kernel<<<g2, block, 0, s>>>(static_cast<const float*>(a.h), a.offsets, a.slot_lo,
+  launch(ffn2_f32_kernel, g2, block, 0, s, static_cast<const float*>(a.h), a.offsets, a.slot_lo,
                                        a.slot_hi, a.cap, static_cast<const float*>(a.wd), a.H,
                                        a.I, static_cast<float*>(a.ys));
   return launch_status();

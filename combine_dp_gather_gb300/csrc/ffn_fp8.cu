@@ -181,6 +181,8 @@ template <bool SWIGLU>
 __global__ void __launch_bounds__(THREADS, 1)
     ffn_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ TokMaps tmB,
                    const F8Params p) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   using C = F8Cfg<SWIGLU>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -517,7 +519,7 @@ moe_status run_f8(const F8Args& a, cudaStream_t s) {
   // upper bound of units (device-side counts unknown here)
   const int64_t bound = (a.cap / NT + p.nslots) * (int64_t)p.n_tiles;
   const int grid = (int)(bound < max_ctas ? bound : max_ctas);
-  ffn_fp8_kernel<SWIGLU><<<grid, THREADS, f8_smem_bytes<SWIGLU>(), s>>>(mA, mB, p);
+  launch(ffn_fp8_kernel<SWIGLU>, grid, THREADS, f8_smem_bytes<SWIGLU>(), s, mA, mB, p);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -124,6 +124,8 @@ template <bool SWIGLU>
 __global__ void __launch_bounds__(THREADS, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const TcParams p) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stage_base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -400,9 +402,9 @@ moe_status run_ffn(const FfnArgs& a, const CUtensorMap& mA, const CUtensorMap& m
   const int64_t bound = m_bound * p.n_tiles;
   const int grid = (int)(bound < max_ctas ? bound : max_ctas);
   if (gemm1)
-    ffn_tc_kernel<true><<<grid, THREADS, smem_bytes(), s>>>(mA, mB, p);
+    launch(ffn_tc_kernel<true>, grid, THREADS, smem_bytes(), s, mA, mB, p);
   else
-    ffn_tc_kernel<false><<<grid, THREADS, smem_bytes(), s>>>(mA, mB, p);
+    launch(ffn_tc_kernel<false>, grid, THREADS, smem_bytes(), s, mA, mB, p);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -171,6 +171,8 @@ __device__ __forceinline__ int col_token(const SUnit& un, int buf, int col) {
 template <bool SWIGLU>
 __global__ void __launch_bounds__(THREADS, 1)
     ffn_swap_kernel(const __grid_constant__ Maps maps, const SwapParams p) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stage_base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -480,6 +482,12 @@ cudaLaunchConfig_t launch_cfg(int clusters, cudaStream_t s, cudaLaunchAttribute*
   cfg.numAttrs = 1;
   return cfg;
 }
+cudaLaunchConfig_t launch_cfg_pdl(int clusters, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = launch_cfg(clusters, s, attr);
+  set_pdl_attr(attr[1]);
+  cfg.numAttrs = 2;
+  return cfg;
+}
 
 // Per device: raise the dynamic shared-memory limit and find how many pairs
 // fit at once (the persistent grid must be fully resident).
@@ -540,8 +548,8 @@ moe_status run_swap(const FfnArgs& a, const Maps& m, bool gemm1, cudaStream_t s)
   // upper bound of units (device-side counts unknown here)
   const int64_t bound = (a.cap / NMAX + p.nslots) * (int64_t)p.n_tiles;
   const int clusters = (int)(bound < max_clusters ? bound : max_clusters);
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = launch_cfg(clusters, s, attr);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = launch_cfg_pdl(clusters, s, attr);
   const cudaError_t e = gemm1 ? cudaLaunchKernelEx(&cfg, ffn_swap_kernel<true>, m, p)
                               : cudaLaunchKernelEx(&cfg, ffn_swap_kernel<false>, m, p);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

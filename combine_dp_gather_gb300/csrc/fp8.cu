@@ -65,6 +65,8 @@ template <bool BF16>
 __global__ void __launch_bounds__(kWarps * 32)
     quant_groups_kernel(const void* __restrict__ x, int64_t n, int K, uint8_t* __restrict__ q,
                         uint8_t* __restrict__ scales) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   const int lane = threadIdx.x & 31;
   const int segs = (K + kSeg - 1) / kSeg;
   const int64_t items = n * segs;
@@ -97,6 +99,8 @@ template <bool BF16>
 __global__ void __launch_bounds__(256)
     quant_blocks_kernel(const void* __restrict__ w, int K, uint8_t* __restrict__ q,
                         uint8_t* __restrict__ scales) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   __shared__ float wmax[8];
   const int br = blockIdx.y, bc = blockIdx.x, t = threadIdx.x;
   const int64_t r = (int64_t)br * 128 + (t >> 1);
@@ -144,6 +148,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     dispatch_copy_fp8_kernel(const void* __restrict__ xg, const int32_t* __restrict__ inv,
                              int64_t rows, int k, int H, int64_t cap, uint8_t* __restrict__ xq,
                              uint8_t* __restrict__ xscale) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   const int lane = threadIdx.x & 31;
   const int segs = (H + kSeg - 1) / kSeg;
   const int64_t items = rows * segs;
@@ -180,6 +186,8 @@ __global__ void __launch_bounds__(256)
     dispatch_pad_fp8_kernel(const int32_t* __restrict__ counts_P,
                             const int32_t* __restrict__ offsets_P, int P, int H, int64_t cap,
                             uint8_t* __restrict__ xq, uint8_t* __restrict__ xscale) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   const int s = blockIdx.x;
   if (s >= P) return;
   int64_t a = (int64_t)offsets_P[s] + counts_P[s];
@@ -214,9 +222,9 @@ extern "C" moe_status moe_quantize_fp8_groups(const void* d_x, int64_t n, int K,
   cudaStream_t s = as_stream(stream);
   const int64_t items = n * ((K + kSeg - 1) / kSeg);
   if (dtype == MOE_BF16)
-    quant_groups_kernel<true><<<grid_for(items), kWarps * 32, 0, s>>>(d_x, n, K, d_q, d_scales);
+    launch(quant_groups_kernel<true>, grid_for(items), kWarps * 32, 0, s, d_x, n, K, d_q, d_scales);
   else
-    quant_groups_kernel<false><<<grid_for(items), kWarps * 32, 0, s>>>(d_x, n, K, d_q, d_scales);
+    launch(quant_groups_kernel<false>, grid_for(items), kWarps * 32, 0, s, d_x, n, K, d_q, d_scales);
   return launch_status();
 }
 
@@ -231,9 +239,9 @@ extern "C" moe_status moe_quantize_fp8_blocks(const void* d_w, int64_t R, int K,
   cudaStream_t s = as_stream(stream);
   dim3 grid((unsigned)(K / 128), (unsigned)(R / 128));
   if (dtype == MOE_BF16)
-    quant_blocks_kernel<true><<<grid, 256, 0, s>>>(d_w, K, d_q, d_scales);
+    launch(quant_blocks_kernel<true>, grid, 256, 0, s, d_w, K, d_q, d_scales);
   else
-    quant_blocks_kernel<false><<<grid, 256, 0, s>>>(d_w, K, d_q, d_scales);
+    launch(quant_blocks_kernel<false>, grid, 256, 0, s, d_w, K, d_q, d_scales);
   return launch_status();
 }
 
@@ -258,14 +266,14 @@ extern "C" moe_status moe_dispatch_fp8(const void* d_global, const int32_t* d_id
   if (rows > 0) {
     const int64_t items = rows * ((H + kSeg - 1) / kSeg);
     if (dtype == MOE_BF16)
-      dispatch_copy_fp8_kernel<true><<<grid_for(items), kWarps * 32, 0, s>>>(
+      launch(dispatch_copy_fp8_kernel<true>, grid_for(items), kWarps * 32, 0, s,
           d_global, d_inv, rows, k, H, cap, d_sorted_q, d_sorted_scales);
     else
-      dispatch_copy_fp8_kernel<false><<<grid_for(items), kWarps * 32, 0, s>>>(
+      launch(dispatch_copy_fp8_kernel<false>, grid_for(items), kWarps * 32, 0, s,
           d_global, d_inv, rows, k, H, cap, d_sorted_q, d_sorted_scales);
   }
   if (align > 1 && cap > 0)
-    dispatch_pad_fp8_kernel<<<P, 256, 0, s>>>(d_counts_P, d_offsets_P, P, H, cap, d_sorted_q,
+    launch(dispatch_pad_fp8_kernel, P, 256, 0, s, d_counts_P, d_offsets_P, P, H, cap, d_sorted_q,
                                               d_sorted_scales);
   return launch_status();
 }

@@ -5,10 +5,19 @@
 #include <limits.h>
 #include <mutex>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "moe_dp.h"
 
 namespace moe {
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_PDL");
+    return !(v != nullptr && v[0] == '0' && v[1] == 0);
+  }();
+  return on;
+}
 
 int num_sms() {
   static std::mutex mu;

@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(kWarps * 32)
                       int n_shared, const int32_t* __restrict__ counts,
                       const int32_t* __restrict__ offsets, int R, int32_t* __restrict__ ids,
                       float* __restrict__ w, uint32_t* status) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   const int kk = k + n_shared;  // row stride of ids / w
   __shared__ int32_t s_off[MOE_MAX_REPLICAS + 1];
   __shared__ int32_t s_cnt[MOE_MAX_REPLICAS];
@@ -129,7 +131,7 @@ void launch_route(const float* logits, int64_t rows, int E, int k, int renorm, i
   int64_t want = (rows + kWarps - 1) / kWarps;
   int64_t cap = (int64_t)num_sms() * 8;
   int grid = (int)(want < cap ? want : cap);
-  route_topk_kernel<EPL><<<grid, kWarps * 32, 0, s>>>(logits, rows, E, k, renorm, n_shared,
+  launch(route_topk_kernel<EPL>, grid, kWarps * 32, 0, s, logits, rows, E, k, renorm, n_shared,
                                                      counts, offsets, R, ids, w, status);
 }
 

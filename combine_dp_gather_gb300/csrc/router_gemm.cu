@@ -95,6 +95,8 @@ template <int K>
 __global__ void __launch_bounds__(THREADS, 1)
     router_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const RParams p) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stage_base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -289,6 +291,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 __global__ void __launch_bounds__(256)
     router_reduce_kernel(const float4* __restrict__ partial, int64_t n4, int ks, int E,
                          const float* __restrict__ bias, float4* __restrict__ logits) {
+  grid_dep_wait();    // earlier kernels on the stream are complete
+  grid_dep_launch();  // the next kernel may start its launch
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
     float4 a = partial[i];
@@ -419,7 +423,7 @@ extern "C" moe_status moe_route_gemm_topk(const void* d_x, const void* d_w_route
     switch (k) {
 #define MOE_CASE(K)                                                                  \
   case K:                                                                            \
-    router_gemm_kernel<K><<<dim3(tiles, 1), THREADS, smem, s>>>(mA, mB, p); \
+    launch(router_gemm_kernel<K>, dim3(tiles, 1), THREADS, smem, s, mA, mB, p); \
     break;
       MOE_CASE(1) MOE_CASE(2) MOE_CASE(3) MOE_CASE(4) MOE_CASE(5) MOE_CASE(6) MOE_CASE(7)
       MOE_CASE(8)
@@ -429,14 +433,14 @@ extern "C" moe_status moe_route_gemm_topk(const void* d_x, const void* d_w_route
     }
     return launch_status();
   }
-  router_gemm_kernel<0><<<dim3(tiles, (unsigned)pl.ks), THREADS, smem, s>>>(mA, mB, p);
+  launch(router_gemm_kernel<0>, dim3(tiles, (unsigned)pl.ks), THREADS, smem, s, mA, mB, p);
   float* logits = d_logits != nullptr
                       ? d_logits
                       : static_cast<float*>(d_ws) + (size_t)pl.ks * (size_t)rows * E;
   const int64_t n4 = rows * (int64_t)E / 4;
   int64_t blocks = (n4 + 255) / 256;
   const int64_t lim = (int64_t)num_sms() * 8;
-  router_reduce_kernel<<<(unsigned)(blocks < lim ? blocks : lim), 256, 0, s>>>(
+  launch(router_reduce_kernel, (unsigned)(blocks < lim ? blocks : lim), 256, 0, s,
       static_cast<const float4*>(d_ws), n4, pl.ks, E, d_bias, reinterpret_cast<float4*>(logits));
   if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
   return moe_route_topk_shared(logits, rows, E, k, renormalize, n_shared, d_counts, d_offsets, R,
