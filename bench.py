@@ -120,6 +120,9 @@ def parse():
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 dispatch and grouped FFN (e4m3, UE8M0 scales per 128-token group "
                          "and 128x128 weight block); layer input and output stay bf16")
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="host threads of the timed oracle (cpu_baseline and --impl reference); "
+                         "0 = every core")
     ap.add_argument("--tokens", type=int, default=None,
                     help="prefill token count (with --experts: many rows, few weights)")
     return ap.parse_args()
@@ -560,9 +563,10 @@ def gate_to_host(w, b):
     return oracle.bf16_bits_to_f32(wb), (None if b is None else b.cpu().numpy().astype(np.float64))
 
 
-def cpu_baseline(spec, budget_s=20.0, inputs=None, fp8=False, gate=None):
+def cpu_baseline(spec, budget_s=20.0, inputs=None, fp8=False, gate=None, threads=0):
     import oracle
     oracle.build()
+    oracle.set_threads(threads)
     x_loc, lg_loc, wgu, wd, l2p, nrep = inputs or oracle_inputs(spec)
     wall1, _ = oracle_sample_step(spec, 1, x_loc, lg_loc, wgu, wd, l2p, nrep, fp8, gate)
     n = int(max(1, min(spec.T, budget_s / max(wall1, 1e-3))))
@@ -581,6 +585,7 @@ def run_reference(args, rank, world):
     spec = make_spec(args.config, args.seed, args.experts, args.tokens)
     import oracle
     oracle.build()
+    oracle.set_threads(args.cpu_threads)
     inputs = oracle_inputs(spec)
     gate = gate_to_host(*synth.router_gate(spec, "cpu")) if args.router == "gemm" else None
     wall1, _ = oracle_sample_step(spec, 1, *inputs, args.fp8, gate)
@@ -676,7 +681,7 @@ def main():
                            "ms_per_step": round(agg["e2e_ms_max"] / e["steps"], 4)}
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(spec, inputs=r["inputs"], fp8=args.fp8,
-                                                gate=r["gate"])
+                                                gate=r["gate"], threads=args.cpu_threads)
         print(json.dumps(line), flush=True)
     finally:
         if world > 1 and torch.distributed.is_initialized():

@@ -70,6 +70,7 @@ def _load():
             "orc_dp_padding_mode": (ctypes.c_int, [P, ctypes.c_int, ctypes.c_int,
                                                    ctypes.c_int, ctypes.c_int]),
             "orc_valid_rows": (None, [P, P, ctypes.c_int, i64, P]),
+            "orc_set_threads": (None, [ctypes.c_int]),
             "orc_dp_gather": (None, [P, P, P, ctypes.c_int, i64, i64, P]),
             "orc_dp_scatter": (None, [P, P, P, ctypes.c_int, i64, P]),
             "orc_route_topk": (ctypes.c_int, [P, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -149,6 +150,11 @@ def dp_padding_mode(counts, gather_width: int, is_extend_in_batch: bool,
     counts = _c(counts, np.int32)
     return _load().orc_dp_padding_mode(_p(counts), len(counts), gather_width,
                                        int(is_extend_in_batch), int(max_len_with_idle))
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops (OpenMP); n < 1 keeps the default."""
+    _load().orc_set_threads(int(n))
 
 
 def valid_rows(counts, offsets, rows: int) -> np.ndarray:

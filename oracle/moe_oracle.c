@@ -23,6 +23,7 @@
  * tests/test_oracle_pins.py.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -653,4 +654,10 @@ void orc_router_logits(const float *x, int64_t rows, int H, const float *w, int 
       for (int h = 0; h < H; ++h) s += (double)x[g * H + h] * (double)w[(int64_t)e * H + h];
       logits[g * E + e] = s;
     }
+}
+
+/* Host threads the oracle's parallel loops use (the timed CPU baseline runs it
+ * once on every core and once on one).  n < 1 leaves the default. */
+void orc_set_threads(int n) {
+  if (n >= 1) omp_set_num_threads(n);
 }
