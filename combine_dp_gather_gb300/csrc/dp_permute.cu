@@ -47,10 +47,21 @@ __device__ __forceinline__ void copy_seg(const uint4* __restrict__ src, uint4* _
   }
 }
 
+// One row tensor of the gather: the replicas' pointers, 16-byte vectors per
+// row, the global buffer.  A plane with vpr == 0 is absent.
+struct GatherPlane {
+  ReplicaPtrs src;
+  int vpr;
+  uint4* global;
+};
+
+// Items are (global row, segment) over the segments of plane a then plane b,
+// so one launch gathers two row tensors of the same replicas (hidden states
+// and router logits) with the same per-row replica lookup.
 __global__ void __launch_bounds__(kWarps * 32)
-    dp_gather_kernel(ReplicaPtrs src, const int32_t* __restrict__ counts,
-                     const int32_t* __restrict__ offsets, int R, int64_t rows, int vpr,
-                     uint4* __restrict__ global, uint32_t* status) {
+    dp_gather_kernel(const __grid_constant__ GatherPlane a, const __grid_constant__ GatherPlane b,
+                     const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+                     int R, int64_t rows, uint32_t* status) {
   grid_dep_wait();    // earlier kernels on the stream are complete
   grid_dep_launch();  // the next kernel may start its launch
   __shared__ int32_t s_off[MOE_MAX_REPLICAS + 1];
@@ -63,11 +74,14 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarps;
-  const int segs = (vpr + kSegVecs - 1) / kSegVecs;
+  const int segs_a = (a.vpr + kSegVecs - 1) / kSegVecs;
+  const int segs = segs_a + (b.vpr + kSegVecs - 1) / kSegVecs;
   const int64_t items = rows * segs;
   for (int64_t w = warp0; w < items; w += nwarps) {
     const int64_t g = w / segs;
-    const int v0 = (int)(w - g * segs) * kSegVecs;
+    const int j = (int)(w - g * segs);
+    const GatherPlane& pl = j < segs_a ? a : b;
+    const int v0 = (j < segs_a ? j : j - segs_a) * kSegVecs;
     int r = find_segment(s_off, R, g);
     int64_t i = g - s_off[r];
     int64_t seg = (int64_t)s_off[r + 1] - s_off[r];
@@ -76,12 +90,13 @@ __global__ void __launch_bounds__(kWarps * 32)
       if (i == 0 && v0 == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
       c = seg;
     }
-    if (c > 0 && src.p[r] == nullptr) {
+    if (c > 0 && pl.src.p[r] == nullptr) {
       if (i == 0 && v0 == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
       c = 0;
     }
-    const uint4* from = (i >= 0 && i < c) ? static_cast<const uint4*>(src.p[r]) + i * vpr : nullptr;
-    copy_seg(from, global + g * vpr, v0, vpr, lane);
+    const uint4* from =
+        (i >= 0 && i < c) ? static_cast<const uint4*>(pl.src.p[r]) + i * pl.vpr : nullptr;
+    copy_seg(from, pl.global + g * pl.vpr, v0, pl.vpr, lane);
   }
 }
 
@@ -258,8 +273,21 @@ moe_status check_common(const int32_t* d_counts, const int32_t* d_offsets, int R
   return MOE_OK;
 }
 
-int grid_for_rows(int64_t rows, int vpr) {
-  const int64_t items = rows * ((vpr + kSegVecs - 1) / kSegVecs);
+bool make_plane(const void* const* local, int R, int H, int dtype, void* d_global,
+                GatherPlane* pl) {
+  if (local == nullptr) return false;
+  for (int r = 0; r < R; ++r) {
+    if (local[r] != nullptr && !aligned16(local[r])) return false;
+    pl->src.p[r] = local[r];
+  }
+  pl->vpr = (int)((int64_t)H * dtype_bytes(dtype) / 16);
+  pl->global = static_cast<uint4*>(d_global);
+  return true;
+}
+
+int grid_for_rows(int64_t rows, int vpr, int vpr2 = 0) {
+  const int64_t items =
+      rows * ((vpr + kSegVecs - 1) / kSegVecs + (vpr2 + kSegVecs - 1) / kSegVecs);
   int64_t want = (items + kWarps - 1) / kWarps;
   int64_t cap = (int64_t)num_sms() * 8;
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
@@ -275,15 +303,30 @@ extern "C" moe_status moe_dp_gather(const void* const* local, const int32_t* d_c
                                     int dtype, void* d_global, uint32_t* d_status, void* stream) {
   moe_status st = check_common(d_counts, d_offsets, R, rows, H, dtype, d_global);
   if (st != MOE_OK || rows == 0) return st;
-  if (local == nullptr) return MOE_ERR_INVALID_ARG;
-  ReplicaPtrs ptrs;
-  for (int r = 0; r < R; ++r) {
-    if (local[r] != nullptr && !aligned16(local[r])) return MOE_ERR_INVALID_ARG;
-    ptrs.p[r] = local[r];
-  }
-  const int vpr = (int)((int64_t)H * dtype_bytes(dtype) / 16);
-  launch(dp_gather_kernel, grid_for_rows(rows, vpr), kWarps * 32, 0, as_stream(stream),
-      ptrs, d_counts, d_offsets, R, rows, vpr, static_cast<uint4*>(d_global), d_status);
+  GatherPlane a, b;
+  if (!make_plane(local, R, H, dtype, d_global, &a)) return MOE_ERR_INVALID_ARG;
+  b.vpr = 0;
+  b.global = nullptr;
+  launch(dp_gather_kernel, grid_for_rows(rows, a.vpr), kWarps * 32, 0, as_stream(stream), a, b,
+         d_counts, d_offsets, R, rows, d_status);
+  return launch_status();
+}
+
+extern "C" moe_status moe_dp_gather2(const void* const* local_a, int H_a, int dtype_a,
+                                     void* d_global_a, const void* const* local_b, int H_b,
+                                     int dtype_b, void* d_global_b, const int32_t* d_counts,
+                                     const int32_t* d_offsets, int R, int64_t rows,
+                                     uint32_t* d_status, void* stream) {
+  moe_status st = check_common(d_counts, d_offsets, R, rows, H_a, dtype_a, d_global_a);
+  if (st != MOE_OK) return st;
+  st = check_common(d_counts, d_offsets, R, rows, H_b, dtype_b, d_global_b);
+  if (st != MOE_OK || rows == 0) return st;
+  GatherPlane a, b;
+  if (!make_plane(local_a, R, H_a, dtype_a, d_global_a, &a) ||
+      !make_plane(local_b, R, H_b, dtype_b, d_global_b, &b))
+    return MOE_ERR_INVALID_ARG;
+  launch(dp_gather_kernel, grid_for_rows(rows, a.vpr, b.vpr), kWarps * 32, 0, as_stream(stream),
+         a, b, d_counts, d_offsets, R, rows, d_status);
   return launch_status();
 }
 

@@ -50,6 +50,9 @@ _SIGS = {
                              _P]),
     "moe_combine": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I64, _P, _P, _P]),
     "moe_dp_scatter": (_I, [_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P]),
+    "moe_dp_gather2": (_I, [_P, _I, _I, _P, _P, _I, _I, _P, _P, _P, _I, _I64, _P, _P]),
+    "moe_combine_scatter": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I64, _P, _P, _I, _P, _P, _P,
+                                 _P]),
     "moe_route_topk_shared": (_I, [_P, _I64, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]),
     "moe_dp_gather_add_rmsnorm": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _I, _I64, _I, _I, _P,
                                        _P, _P]),
@@ -180,6 +183,21 @@ def moe_dp_gather(local: Sequence[torch.Tensor], d_counts, d_offsets, out: torch
     _check("moe_dp_gather", lib().moe_dp_gather(
         ctypes.cast(ptrs, _P), _ptr(d_counts), _ptr(d_offsets), R, out.shape[0], out.shape[1],
         dtype_code(out.dtype), _ptr(out), _ptr(d_status), _stream(stream)))
+
+
+def moe_dp_gather2(local_a: Sequence[torch.Tensor], local_b: Sequence[torch.Tensor], d_counts,
+                   d_offsets, out_a: torch.Tensor, out_b: torch.Tensor, d_status=None,
+                   stream=None):
+    """DP gather of two row tensors of the same replicas in one launch."""
+    R = len(local_a)
+    if len(local_b) != R or out_a.shape[0] != out_b.shape[0]:
+        raise MoeError("moe_dp_gather2", MOE_ERR_INVALID_ARG)
+    pa = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_a])
+    pb = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_b])
+    _check("moe_dp_gather2", lib().moe_dp_gather2(
+        ctypes.cast(pa, _P), out_a.shape[1], dtype_code(out_a.dtype), _ptr(out_a),
+        ctypes.cast(pb, _P), out_b.shape[1], dtype_code(out_b.dtype), _ptr(out_b),
+        _ptr(d_counts), _ptr(d_offsets), R, out_a.shape[0], _ptr(d_status), _stream(stream)))
 
 
 def moe_dp_gather_add_rmsnorm(local_hidden: Sequence[torch.Tensor],
@@ -345,6 +363,20 @@ def moe_combine(ys: torch.Tensor, inv: torch.Tensor, w: torch.Tensor, out: torch
         ys.shape[0], _ptr(out), _ptr(d_status), _stream(stream)))
 
 
+def moe_combine_scatter(ys: torch.Tensor, inv: torch.Tensor, w: torch.Tensor, d_counts, d_offsets,
+                        local: Sequence[torch.Tensor], global_out: Optional[torch.Tensor] = None,
+                        d_status=None, stream=None):
+    """moe_combine then moe_dp_scatter in one launch; global_out (optional) also
+    receives the combined global buffer."""
+    rows, k = inv.shape
+    R = len(local)
+    ptrs = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local])
+    _check("moe_combine_scatter", lib().moe_combine_scatter(
+        _ptr(ys), _ptr(inv), _ptr(w), rows, k, ys.shape[1], dtype_code(ys.dtype), ys.shape[0],
+        _ptr(d_counts), _ptr(d_offsets), R, ctypes.cast(ptrs, _P),
+        _ptr(global_out) if global_out is not None else None, _ptr(d_status), _stream(stream)))
+
+
 def moe_dp_scatter(global_buf: torch.Tensor, d_counts, d_offsets, local: Sequence[torch.Tensor],
                    d_status=None, stream=None):
     R = len(local)
@@ -361,7 +393,8 @@ class MoeLayer:
 
     Buffers are sized once for `max_rows` global rows; `forward` runs
     gather -> route -> dispatch -> grouped FFN -> combine -> scatter on the
-    current stream without a host synchronisation.  With router_weight [E, H]
+    current stream without a host synchronisation (the hidden-state and logits
+    gathers share one launch, and so do combine and scatter).  With router_weight [E, H]
     (bf16) the router logits are computed from the gathered hidden states by the
     gate GEMM fused ahead of top-k instead of being gathered from the replicas.
     With fp8=True (bf16 layer)
@@ -377,8 +410,11 @@ class MoeLayer:
                  norm_gamma: Optional[torch.Tensor] = None, norm_eps: float = 1e-6,
                  n_shared: int = 0, fp8: bool = False,
                  router_weight: Optional[torch.Tensor] = None,
-                 router_bias: Optional[torch.Tensor] = None):
+                 router_bias: Optional[torch.Tensor] = None, keep_global: bool = False):
         dev = w_gate_up.device
+        # keep_global: also write the combined global buffer (yg, pad rows zero);
+        # otherwise the combine writes the replicas' outputs only
+        self.keep_global = keep_global
         self.R, self.H, self.E, self.k, self.I = R, H, E, k, I
         self.P = w_gate_up.shape[0]
         self.dtype = w_gate_up.dtype
@@ -471,10 +507,13 @@ class MoeLayer:
                 raise ValueError("local_residual needs norm_gamma")
             moe_dp_gather_add_rmsnorm(local_x, local_residual, self.norm_gamma, self.norm_eps,
                                       self.d_counts, self.d_offsets, xg, st, stream)
+            if self.router_weight is None:
+                moe_dp_gather(local_logits, self.d_counts, self.d_offsets, lg, st, stream)
+        elif self.router_weight is None:  # hidden states and logits in one launch
+            moe_dp_gather2(local_x, local_logits, self.d_counts, self.d_offsets, xg, lg, st,
+                           stream)
         else:
             moe_dp_gather(local_x, self.d_counts, self.d_offsets, xg, st, stream)
-        if self.router_weight is None:
-            moe_dp_gather(local_logits, self.d_counts, self.d_offsets, lg, st, stream)
         ev("gather")
         if self.router_weight is None:
             moe_route_topk(lg, self.k, self.renormalize, self.d_counts, self.d_offsets, ids, w,
@@ -499,10 +538,9 @@ class MoeLayer:
             moe_grouped_ffn(self.xs, self.offsets_P, self.wgu, self.wd, self.ys, self.ws_ffn,
                             self.slot_range[0], self.slot_range[1], st, stream)
         ev("ffn")
-        moe_combine(self.ys, inv, w, yg, st, stream)
-        ev("combine")
-        moe_dp_scatter(yg, self.d_counts, self.d_offsets, out, st, stream)
-        ev("scatter")
+        moe_combine_scatter(self.ys, inv, w, self.d_counts, self.d_offsets, out,
+                            yg if self.keep_global else None, st, stream)
+        ev("combine_scatter")
         return out
 
 

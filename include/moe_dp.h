@@ -150,6 +150,16 @@ moe_status moe_dp_gather(const void* const* local, const int32_t* d_counts,
                          const int32_t* d_offsets, int R, int64_t rows, int H, int dtype,
                          void* d_global, uint32_t* d_status, void* stream);
 
+/* moe_dp_gather of two row tensors of the same replicas in one launch (e.g.
+ * the hidden states and the router logits of each token): tensor a is
+ * [counts[r], H_a] of dtype_a per replica into d_global_a [rows, H_a], tensor b
+ * likewise; counts, offsets, zero pad rows and error behaviour as
+ * moe_dp_gather, whose result each output equals bit for bit. */
+moe_status moe_dp_gather2(const void* const* local_a, int H_a, int dtype_a, void* d_global_a,
+                          const void* const* local_b, int H_b, int dtype_b, void* d_global_b,
+                          const int32_t* d_counts, const int32_t* d_offsets, int R, int64_t rows,
+                          uint32_t* d_status, void* stream);
+
 /* Residual add + RMSNorm fused ahead of the DP gather.  [P1] section
  * "边界判定的融合" (_reduce_update_read_dp_gather): the attention output is added
  * into the residual ("update", written back in place) and the FFN input is read
@@ -292,6 +302,19 @@ moe_status moe_combine(const void* d_out_sorted, const int32_t* d_inv, const flo
 moe_status moe_dp_scatter(const void* d_global, const int32_t* d_counts, const int32_t* d_offsets,
                           int R, int64_t rows, int H, int dtype, void* const* local,
                           uint32_t* d_status, void* stream);
+
+/* moe_combine followed by moe_dp_scatter in one launch: each combined row of
+ * replica r's segment (global row offsets[r] + i, i < counts[r]) is written
+ * straight to local[r] row i, bit for bit what the two calls produce.  With
+ * d_global_out non-NULL the combined global buffer [rows, H] (pad rows zero)
+ * is written as well; with NULL it is not, and pad rows are skipped.
+ *   arguments as moe_combine and moe_dp_scatter (local: HOST array of R device
+ *   pointers, local[r] [counts[r], H] out). */
+moe_status moe_combine_scatter(const void* d_out_sorted, const int32_t* d_inv, const float* d_w,
+                               int64_t rows, int k, int H, int dtype, int64_t cap,
+                               const int32_t* d_counts, const int32_t* d_offsets, int R,
+                               void* const* local, void* d_global_out, uint32_t* d_status,
+                               void* stream);
 
 /* Same as moe_dispatch, but allocates nothing and takes no workspace: the
  * per-chunk histograms live in a fixed device array inside the library.

@@ -120,6 +120,48 @@ def test_gather_scatter_reject_bad_args(md):
     assert L.moe_dp_scatter(FAKE, NULL, FAKE, 2, 8, 64, 1, two, NULL, NULL) == E_ARG
 
 
+def test_gather2_and_combine_scatter_reject_bad_args(md):
+    L = md.lib()
+    two = _ptrs(0x2000, 0x3000)
+    E_ARG, E_UNS = md.MOE_ERR_INVALID_ARG, md.MOE_ERR_UNSUPPORTED
+    ok = (two, 64, 1, FAKE, two, 256, 0, FAKE, FAKE, FAKE, 2, 8, NULL, NULL)
+
+    def g2(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return L.moe_dp_gather2(*a)
+    assert g2(a0=NULL) == E_ARG                      # no replica table for tensor a
+    assert g2(a4=NULL) == E_ARG                      # ... or for tensor b
+    assert g2(a4=_ptrs(0x2008, 0x3000)) == E_ARG     # misaligned replica row
+    assert g2(a1=7) == E_ARG                         # 14-byte rows
+    assert g2(a6=9) == E_UNS                         # unknown dtype of b
+    assert g2(a7=NULL) == E_ARG                      # no global buffer for b
+    assert g2(a3=MISAL) == E_ARG
+    assert g2(a8=NULL) == E_ARG                      # no counts
+    assert g2(a10=0) == E_ARG and g2(a10=300) == E_ARG
+    assert g2(a11=-1) == E_ARG
+    assert g2(a11=0) == md.MOE_OK                    # nothing to move, no launch
+
+    cs = (FAKE, FAKE, FAKE, 8, 2, 64, 1, 64, FAKE, FAKE, 2, two, NULL, NULL, NULL)
+
+    def c(**kw):
+        a = list(cs)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return L.moe_combine_scatter(*a)
+    assert c(a4=0) == E_ARG                          # k = 0
+    assert c(a5=4) == E_ARG                          # 8-byte rows
+    assert c(a6=3) == E_UNS
+    assert c(a1=NULL) == E_ARG and c(a2=NULL) == E_ARG
+    assert c(a8=NULL) == E_ARG and c(a9=NULL) == E_ARG
+    assert c(a10=0) == E_ARG and c(a10=300) == E_ARG
+    assert c(a11=NULL) == E_ARG                      # no replica table
+    assert c(a11=_ptrs(0x2008, 0x3000)) == E_ARG
+    assert c(a12=MISAL) == E_ARG                     # misaligned optional global buffer
+    assert c(a3=0) == md.MOE_OK
+
+
 def test_gather_add_rmsnorm_rejects_bad_args(md):
     L = md.lib()
     two = _ptrs(0x2000, 0x3000)

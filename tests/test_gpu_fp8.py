@@ -191,7 +191,8 @@ def _layer_fp8_check(md, orc, spec, sample=None):
     offs, rows = md.moe_dp_layout(spec.counts, spec.mode, spec.static_bound, spec.tokens_per_req)
     layer = md.MoeLayer(R=spec.R, H=spec.H, E=spec.E, k=spec.k, I=spec.I, w_gate_up=wgu,
                         w_down=wd, max_rows=max(rows, 1), mode=spec.mode,
-                        renormalize=spec.renormalize, n_shared=spec.n_shared, fp8=True)
+                        renormalize=spec.renormalize, n_shared=spec.n_shared, fp8=True,
+                        keep_global=True)
     out = [torch.empty(c, spec.H, device=DEV, dtype=wgu.dtype) for c in spec.counts]
     layer.forward(x_loc, lg_loc, out, counts=spec.counts)
     assert _status(layer.status) == 0

@@ -75,6 +75,29 @@ def test_gather_scatter_bitexact(md, orc, mode, dtype):
                            b.view(torch.int16) if dtype == torch.bfloat16 else b)
 
 
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_gather2_bitexact(md, orc, mode):
+    """Hidden states (bf16) and router logits (fp32) of the same replicas in one
+    launch: each output is the oracle's gather, bit for bit."""
+    rng = np.random.default_rng(30 + mode)
+    R, B, tpr, H, E = 12, 24, 1, 7168, 256
+    counts = [int(v) for v in rng.choice([0, 1, 5, 17, 24], size=R)]
+    counts[0] = 0
+    g = torch.Generator(device=DEV).manual_seed(31)
+    xs = [torch.randn(c, H, generator=g, device=DEV).to(torch.bfloat16) for c in counts]
+    ls = [torch.randn(c, E, generator=g, device=DEV) for c in counts]
+    offs, rows = md.moe_dp_layout(counts, mode, B, tpr)
+    offs_o, rows_o = orc.dp_layout(counts, mode, B, tpr)
+    d_c, d_o = dev_i32(counts), dev_i32(offs)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    xg = torch.full((rows, H), 3.0, device=DEV, dtype=torch.bfloat16)
+    lg = torch.full((rows, E), 3.0, device=DEV)
+    md.moe_dp_gather2(xs, ls, d_c, d_o, xg, lg, st)
+    assert status_of(st) == 0
+    assert np.array_equal(to_np(xg), orc.dp_gather([to_np(t) for t in xs], counts, offs_o, rows_o))
+    assert np.array_equal(to_np(lg), orc.dp_gather([to_np(t) for t in ls], counts, offs_o, rows_o))
+
+
 def test_gather_all_idle_and_bad_counts(md):
     counts = [0, 0, 0]
     offs, rows = md.moe_dp_layout(counts, 1)
@@ -376,6 +399,49 @@ def test_combine_random(md, orc, dtype):
     assert_close(as_f32(to_np(out)), ref, *tol, what="combine")
 
 
+@pytest.mark.parametrize("dtype,mode", [(torch.bfloat16, 1), (torch.bfloat16, 0),
+                                        (torch.float32, 2)])
+def test_combine_scatter(md, orc, dtype, mode):
+    """Combine fused with the DP scatter: the replicas' outputs are bit for bit those
+    of moe_combine followed by moe_dp_scatter (and within tolerance of the oracle's
+    combine + scatter); the optional global buffer equals moe_combine's."""
+    rng = np.random.default_rng(40 + mode)
+    counts = [int(v) for v in rng.choice([0, 3, 9, 24], size=10)]
+    counts[2] = 0
+    offs, rows = md.moe_dp_layout(counts, mode, 24, 1)
+    offs_o, rows_o = orc.dp_layout(counts, mode, 24, 1)
+    valid = orc.valid_rows(counts, offs_o, rows_o)
+    k, H, cap = 6, 1024 if dtype == torch.bfloat16 else 512, 1500
+    g = torch.Generator(device=DEV).manual_seed(41)
+    ys = torch.randn(cap, H, generator=g, device=DEV).to(dtype)
+    inv = torch.stack([torch.randperm(cap, generator=g, device=DEV)[:k] for _ in range(rows)])
+    inv = inv.to(torch.int32)
+    inv[torch.from_numpy(valid == 0).to(DEV)] = -1          # pad rows are not routed
+    w = torch.rand(rows, k, generator=g, device=DEV)
+    d_c, d_o = dev_i32(counts), dev_i32(offs)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ref_g = torch.empty(rows, H, device=DEV, dtype=dtype)
+    md.moe_combine(ys, inv, w, ref_g, st)
+    ref_l = [torch.full((c, H), 5.0, device=DEV, dtype=dtype) for c in counts]
+    md.moe_dp_scatter(ref_g, d_c, d_o, ref_l, st)
+    for keep in (False, True):
+        out = [torch.full((c, H), 7.0, device=DEV, dtype=dtype) for c in counts]
+        glob = torch.full((rows, H), 9.0, device=DEV, dtype=dtype) if keep else None
+        md.moe_combine_scatter(ys, inv, w, d_c, d_o, out, glob, st)
+        assert status_of(st) == 0
+        for a, b in zip(out, ref_l):
+            assert torch.equal(a.view(torch.int16) if dtype == torch.bfloat16 else a,
+                               b.view(torch.int16) if dtype == torch.bfloat16 else b)
+        if keep:
+            assert torch.equal(glob, ref_g)
+    yg_o = orc.combine(as_f32(to_np(ys)).astype(np.float64), to_np(inv),
+                       to_np(w).astype(np.float64))
+    loc_o = orc.dp_scatter(yg_o, counts, offs_o)
+    tol = (4e-3, 4e-3) if dtype == torch.bfloat16 else (1e-5, 1e-5)
+    for a, b in zip(out, loc_o):
+        assert_close(as_f32(to_np(a)), b, *tol, what="combine_scatter")
+
+
 # ------------------------------------------------------------------ whole layer
 def _layer_gpu(md, spec, l2p_np=None, nrep_np=None, p2l=None, ranges=None):
     x_loc = synth.hidden_states(spec, DEV)
@@ -388,7 +454,7 @@ def _layer_gpu(md, spec, l2p_np=None, nrep_np=None, p2l=None, ranges=None):
                         w_down=wd, max_rows=max(rows, 1), mode=spec.mode,
                         static_bound=spec.static_bound, tokens_per_req=spec.tokens_per_req,
                         renormalize=spec.renormalize, align=spec.align, l2p=l2p, nrep=nrep,
-                        n_shared=spec.n_shared)
+                        n_shared=spec.n_shared, keep_global=True)
     out = [torch.empty(c, spec.H, device=DEV, dtype=wgu.dtype) for c in spec.counts]
     layer.forward(x_loc, lg_loc, out, counts=spec.counts)
     if ranges is not None:          # re-run the FFN as one call per simulated EP rank
@@ -477,6 +543,16 @@ def test_layer_tiny_bf16_all_rows(md, orc, mode):
                            dtype="bf16", w_std=0.05, zipf_s=1.1)
     res = _layer_gpu(md, spec)
     _check_layer(md, orc, spec, *res)
+    # without the global output buffer (the default) the replicas get the same bits
+    layer, out, x_loc, lg_loc, wgu, wd, offs, rows = res
+    lean = md.MoeLayer(R=spec.R, H=spec.H, E=spec.E, k=spec.k, I=spec.I, w_gate_up=wgu,
+                       w_down=wd, max_rows=rows, mode=spec.mode)
+    out2 = [torch.full_like(t, 7.0) for t in out]
+    lean.forward(x_loc, lg_loc, out2, counts=spec.counts)
+    torch.cuda.synchronize()
+    assert int(lean.status.item()) == 0
+    for a, b in zip(out2, out):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
 @pytest.mark.parametrize("mode", [0, 1])

@@ -95,7 +95,7 @@ def test_layer_with_router_gate(md, orc):
     offs, rows = md.moe_dp_layout(spec.counts, spec.mode)
     layer = md.MoeLayer(R=spec.R, H=spec.H, E=spec.E, k=spec.k, I=spec.I, w_gate_up=wgu,
                         w_down=wd, max_rows=rows, mode=spec.mode, router_weight=gw,
-                        router_bias=gb)
+                        router_bias=gb, keep_global=True)
     out = [torch.empty(c, spec.H, device=DEV, dtype=torch.bfloat16) for c in spec.counts]
     layer.forward(x_loc, lg_loc, out, counts=spec.counts)
     torch.cuda.synchronize()
