@@ -468,35 +468,33 @@ extern "C" moe_status moe_dispatch(const void* d_global, const int32_t* d_ids, i
       sizeof(int32_t) * ((size_t)kSmallWarps * E + (P + 1) + 2 * (size_t)P + E);
   if (pairs <= kSmallPairs && small_smem <= kSmallSmemBytes) {
     const size_t smem = small_smem;
-    launch(dispatch_small_kernel, 1, kSmallWarps * 32, smem, s,
-        d_ids, pairs, k, E, P, d_l2p, d_nrep, X, align, cap, d_counts_P, d_offsets_P, d_perm,
-        d_inv, d_status);
+    launch(dispatch_small_kernel, 1, kSmallWarps * 32, smem, s, d_ids, pairs, k, E, P, d_l2p,
+           d_nrep, X, align, cap, d_counts_P, d_offsets_P, d_perm, d_inv, d_status);
   } else if (chunks == 0) {
     launch(dispatch_scan_kernel, 1, 1024, 0, s, hist, 0, E, P, d_l2p, d_nrep, X, align, cap,
-                                            d_counts_P, d_offsets_P, d_status);
+           d_counts_P, d_offsets_P, d_status);
   } else {
-    launch(dispatch_hist_kernel, (unsigned)chunks, 256, E * sizeof(int32_t), s, d_ids, pairs, E, hist,
-                                                                            d_status);
+    launch(dispatch_hist_kernel, (unsigned)chunks, 256, E * sizeof(int32_t), s, d_ids, pairs, E,
+           hist, d_status);
     launch(dispatch_scan_kernel, 1, 1024, 0, s, hist, chunks, E, P, d_l2p, d_nrep, X, align, cap,
-                                            d_counts_P, d_offsets_P, d_status);
+           d_counts_P, d_offsets_P, d_status);
     // replica tables staged in shared memory when they fit (else read from global)
     const int stage_map = d_l2p != nullptr && (int64_t)E * X <= 4096;
     const size_t smem = sizeof(int32_t) * (E + (P + 1) + (stage_map ? E + (size_t)E * X : 0));
     launch(dispatch_rank_kernel, (unsigned)chunks, 32, smem, s, d_ids, pairs, k, E, hist, d_l2p,
-                                                           d_nrep, X, P, d_offsets_P, cap, d_perm,
-                                                           d_inv, stage_map, d_status);
+           d_nrep, X, P, d_offsets_P, cap, d_perm, d_inv, stage_map, d_status);
   }
   if (move_rows && rows > 0) {
     const int64_t items = rows * ((vpr + kSegVecs - 1) / kSegVecs);
     int64_t want = (items + kCopyWarps - 1) / kCopyWarps;
     int64_t lim = (int64_t)num_sms() * 8;
     launch(dispatch_copy_kernel, (unsigned)(want < lim ? want : lim), kCopyWarps * 32, 0, s,
-        static_cast<const uint4*>(d_global), d_inv, rows, k, vpr, cap,
-        static_cast<uint4*>(d_sorted));
+           static_cast<const uint4*>(d_global), d_inv, rows, k, vpr, cap,
+           static_cast<uint4*>(d_sorted));
   }
   if (align > 1) {
     launch(dispatch_pad_kernel, P, 256, 0, s, d_counts_P, d_offsets_P, P, vpr, cap, d_perm,
-                                          move_rows ? static_cast<uint4*>(d_sorted) : nullptr);
+           move_rows ? static_cast<uint4*>(d_sorted) : nullptr);
   }
   return launch_status();
 }

@@ -325,8 +325,8 @@ extern "C" moe_status moe_dp_gather2(const void* const* local_a, int H_a, int dt
   if (!make_plane(local_a, R, H_a, dtype_a, d_global_a, &a) ||
       !make_plane(local_b, R, H_b, dtype_b, d_global_b, &b))
     return MOE_ERR_INVALID_ARG;
-  launch(dp_gather_kernel, grid_for_rows(rows, a.vpr, b.vpr), kWarps * 32, 0, as_stream(stream),
-         a, b, d_counts, d_offsets, R, rows, d_status);
+  launch(dp_gather_kernel, grid_for_rows(rows, a.vpr, b.vpr), kWarps * 32, 0, as_stream(stream), a,
+         b, d_counts, d_offsets, R, rows, d_status);
   return launch_status();
 }
 
@@ -354,13 +354,13 @@ extern "C" moe_status moe_dp_gather_add_rmsnorm(const void* const* local_hidden,
   const int64_t lim = (int64_t)num_sms() * 8;
   const int grid = (int)(rows < lim ? rows : lim);
   if (dtype == MOE_BF16)
-    launch(dp_gather_add_rmsnorm_kernel<true>, grid, kNormThreads, 0, as_stream(stream),
-        hp, rp, static_cast<const uint4*>(d_gamma), eps, d_counts, d_offsets, R, rows, H, vpr,
-        static_cast<uint4*>(d_global), d_status);
+    launch(dp_gather_add_rmsnorm_kernel<true>, grid, kNormThreads, 0, as_stream(stream), hp, rp,
+           static_cast<const uint4*>(d_gamma), eps, d_counts, d_offsets, R, rows, H, vpr,
+           static_cast<uint4*>(d_global), d_status);
   else
-    launch(dp_gather_add_rmsnorm_kernel<false>, grid, kNormThreads, 0, as_stream(stream),
-        hp, rp, static_cast<const uint4*>(d_gamma), eps, d_counts, d_offsets, R, rows, H, vpr,
-        static_cast<uint4*>(d_global), d_status);
+    launch(dp_gather_add_rmsnorm_kernel<false>, grid, kNormThreads, 0, as_stream(stream), hp, rp,
+           static_cast<const uint4*>(d_gamma), eps, d_counts, d_offsets, R, rows, H, vpr,
+           static_cast<uint4*>(d_global), d_status);
   return launch_status();
 }
 
@@ -378,6 +378,6 @@ extern "C" moe_status moe_dp_scatter(const void* d_global, const int32_t* d_coun
   }
   const int vpr = (int)((int64_t)H * dtype_bytes(dtype) / 16);
   launch(dp_scatter_kernel, grid_for_rows(rows, vpr), kWarps * 32, 0, as_stream(stream),
-      static_cast<const uint4*>(d_global), d_counts, d_offsets, R, rows, vpr, ptrs, d_status);
+         static_cast<const uint4*>(d_global), d_counts, d_offsets, R, rows, vpr, ptrs, d_status);
   return launch_status();
 }

@@ -80,12 +80,10 @@ moe_status launch_ffn_simt_f32(const FfnArgs& a, cudaStream_t s) {
   dim3 block(TS * 8);
   dim3 g1((a.I + TS - 1) / TS, (unsigned)((a.cap + TS - 1) / TS));
   launch(ffn1_f32_kernel, g1, block, 0, s, static_cast<const float*>(a.xs), a.offsets, a.slot_lo,
-                                       a.slot_hi, a.cap, static_cast<const float*>(a.wgu), a.H,
-                                       a.I, static_cast<float*>(a.h));
+         a.slot_hi, a.cap, static_cast<const float*>(a.wgu), a.H, a.I, static_cast<float*>(a.h));
   dim3 g2((a.H + TS - 1) / TS, (unsigned)((a.cap + TS - 1) / TS));
   launch(ffn2_f32_kernel, g2, block, 0, s, static_cast<const float*>(a.h), a.offsets, a.slot_lo,
-                                       a.slot_hi, a.cap, static_cast<const float*>(a.wd), a.H,
-                                       a.I, static_cast<float*>(a.ys));
+         a.slot_hi, a.cap, static_cast<const float*>(a.wd), a.H, a.I, static_cast<float*>(a.ys));
   return launch_status();
 }
 

@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(v[i]));
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  for (int off = 16; off > 0; off >>= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   if ((t & 31) == 0) wmax[t >> 5] = amax;
   __syncthreads();
   amax = wmax[0];
@@ -224,7 +225,8 @@ extern "C" moe_status moe_quantize_fp8_groups(const void* d_x, int64_t n, int K,
   if (dtype == MOE_BF16)
     launch(quant_groups_kernel<true>, grid_for(items), kWarps * 32, 0, s, d_x, n, K, d_q, d_scales);
   else
-    launch(quant_groups_kernel<false>, grid_for(items), kWarps * 32, 0, s, d_x, n, K, d_q, d_scales);
+    launch(quant_groups_kernel<false>, grid_for(items), kWarps * 32, 0, s, d_x, n, K, d_q,
+           d_scales);
   return launch_status();
 }
 
@@ -266,14 +268,14 @@ extern "C" moe_status moe_dispatch_fp8(const void* d_global, const int32_t* d_id
   if (rows > 0) {
     const int64_t items = rows * ((H + kSeg - 1) / kSeg);
     if (dtype == MOE_BF16)
-      launch(dispatch_copy_fp8_kernel<true>, grid_for(items), kWarps * 32, 0, s,
-          d_global, d_inv, rows, k, H, cap, d_sorted_q, d_sorted_scales);
+      launch(dispatch_copy_fp8_kernel<true>, grid_for(items), kWarps * 32, 0, s, d_global, d_inv,
+             rows, k, H, cap, d_sorted_q, d_sorted_scales);
     else
-      launch(dispatch_copy_fp8_kernel<false>, grid_for(items), kWarps * 32, 0, s,
-          d_global, d_inv, rows, k, H, cap, d_sorted_q, d_sorted_scales);
+      launch(dispatch_copy_fp8_kernel<false>, grid_for(items), kWarps * 32, 0, s, d_global, d_inv,
+             rows, k, H, cap, d_sorted_q, d_sorted_scales);
   }
   if (align > 1 && cap > 0)
     launch(dispatch_pad_fp8_kernel, P, 256, 0, s, d_counts_P, d_offsets_P, P, H, cap, d_sorted_q,
-                                              d_sorted_scales);
+           d_sorted_scales);
   return launch_status();
 }

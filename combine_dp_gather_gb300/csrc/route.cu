@@ -132,7 +132,7 @@ void launch_route(const float* logits, int64_t rows, int E, int k, int renorm, i
   int64_t cap = (int64_t)num_sms() * 8;
   int grid = (int)(want < cap ? want : cap);
   launch(route_topk_kernel<EPL>, grid, kWarps * 32, 0, s, logits, rows, E, k, renorm, n_shared,
-                                                     counts, offsets, R, ids, w, status);
+         counts, offsets, R, ids, w, status);
 }
 
 }  // namespace
@@ -156,17 +156,23 @@ extern "C" moe_status moe_route_topk_shared(const float* d_logits, int64_t rows,
   cudaStream_t s = as_stream(stream);
   const int ns = n_shared;
   if (E <= 32)
-    launch_route<1>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+    launch_route<1>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w,
+                     d_status, s);
   else if (E <= 64)
-    launch_route<2>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+    launch_route<2>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w,
+                     d_status, s);
   else if (E <= 128)
-    launch_route<4>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+    launch_route<4>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w,
+                     d_status, s);
   else if (E <= 256)
-    launch_route<8>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+    launch_route<8>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w,
+                     d_status, s);
   else if (E <= 512)
-    launch_route<16>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+    launch_route<16>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w,
+                      d_status, s);
   else
-    launch_route<32>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w, d_status, s);
+    launch_route<32>(d_logits, rows, E, k, renormalize, ns, d_counts, d_offsets, R, d_ids, d_w,
+                      d_status, s);
   return launch_status();
 }
 

@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       L.off[i] = p.offsets[i];
       if (i < p.R) L.cnt[i] = p.counts[i];
     }
-    for (int e = threadIdx.x; e < p.E; e += THREADS) L.bias[e] = p.bias != nullptr ? p.bias[e] : 0.0f;
+    for (int e = threadIdx.x; e < p.E; e += THREADS)
+      L.bias[e] = p.bias != nullptr ? p.bias[e] : 0.0f;
   }
   if (threadIdx.x == 0) {
     L.abort_flag = 0;
@@ -441,7 +442,7 @@ extern "C" moe_status moe_route_gemm_topk(const void* d_x, const void* d_w_route
   int64_t blocks = (n4 + 255) / 256;
   const int64_t lim = (int64_t)num_sms() * 8;
   launch(router_reduce_kernel, (unsigned)(blocks < lim ? blocks : lim), 256, 0, s,
-      static_cast<const float4*>(d_ws), n4, pl.ks, E, d_bias, reinterpret_cast<float4*>(logits));
+         static_cast<const float4*>(d_ws), n4, pl.ks, E, d_bias, reinterpret_cast<float4*>(logits));
   if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
   return moe_route_topk_shared(logits, rows, E, k, renormalize, n_shared, d_counts, d_offsets, R,
                                d_ids, d_w, d_status, stream);
