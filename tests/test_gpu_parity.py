@@ -115,6 +115,33 @@ def test_gather_all_idle_and_bad_counts(md):
     assert torch.equal(g.float(), torch.ones(8, 64, device=DEV))
 
 
+def test_fused_gather_and_combine_scatter_bad_counts_flag_without_fault(md):
+    """Device counts larger than their segment: both fused kernels set
+    MOE_DEV_BAD_COUNTS, copy or write only the rows that fit, and touch nothing
+    outside the buffers."""
+    local = [torch.ones(10, 64, device=DEV, dtype=torch.bfloat16) for _ in range(2)]
+    lgl = [torch.full((10, 32), 2.0, device=DEV) for _ in range(2)]
+    d_c, d_o = dev_i32([10, 10]), dev_i32([0, 4, 8])
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    xg = torch.full((8, 64), 7.0, device=DEV, dtype=torch.bfloat16)
+    lg = torch.full((8, 32), 7.0, device=DEV)
+    md.moe_dp_gather2(local, lgl, d_c, d_o, xg, lg, st)
+    assert status_of(st) & md.MOE_DEV_BAD_COUNTS
+    assert torch.equal(xg.float(), torch.ones(8, 64, device=DEV))
+    assert torch.equal(lg, torch.full((8, 32), 2.0, device=DEV))
+    # combine + scatter into replicas whose counts overflow their segments
+    ys = torch.ones(16, 64, device=DEV, dtype=torch.bfloat16)
+    inv = torch.arange(16, dtype=torch.int32, device=DEV).view(8, 2)
+    w = torch.full((8, 2), 0.5, device=DEV)
+    outs = [torch.full((10, 64), 3.0, device=DEV, dtype=torch.bfloat16) for _ in range(2)]
+    st.zero_()
+    md.moe_combine_scatter(ys, inv, w, d_c, d_o, outs, None, st)
+    assert status_of(st) & md.MOE_DEV_BAD_COUNTS
+    for o in outs:                      # the 4 rows of each segment, the rest untouched
+        assert torch.equal(o[:4].float(), torch.ones(4, 64, device=DEV))
+        assert torch.equal(o[4:].float(), torch.full((6, 64), 3.0, device=DEV))
+
+
 @pytest.mark.parametrize("dtype,H,mode", [(torch.bfloat16, 7168, 1), (torch.bfloat16, 512, 0),
                                           (torch.float32, 1024, 2)])
 def test_gather_add_rmsnorm(md, orc, dtype, H, mode):
