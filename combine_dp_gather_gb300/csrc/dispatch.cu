@@ -93,13 +93,20 @@ __global__ void __launch_bounds__(1024)
   __shared__ int32_t s_slot[MOE_MAX_SLOTS];   // per physical slot
   __shared__ int32_t s_claim[MOE_MAX_SLOTS];
   __shared__ int32_t s_warp[32];
-  // per-expert exclusive scan over chunks (in place: hist becomes chunk bases)
+  // per-expert exclusive scan over chunks (in place: hist becomes chunk bases),
+  // kScanBatch chunks' counts loaded together so their loads overlap
+  constexpr int kScanBatch = 16;
   for (int l = threadIdx.x; l < E; l += blockDim.x) {
     int32_t run = 0;
-    for (int64_t c = 0; c < chunks; ++c) {
-      int32_t t = hist[c * E + l];
-      hist[c * E + l] = run;
-      run += t;
+    for (int64_t c0 = 0; c0 < chunks; c0 += kScanBatch) {
+      int32_t t[kScanBatch];
+#pragma unroll
+      for (int i = 0; i < kScanBatch; ++i) t[i] = c0 + i < chunks ? hist[(c0 + i) * E + l] : 0;
+#pragma unroll
+      for (int i = 0; i < kScanBatch; ++i) {
+        if (c0 + i < chunks) hist[(c0 + i) * E + l] = run;
+        run += t[i];
+      }
     }
     s_cnt[l] = run;
   }
@@ -205,6 +212,25 @@ __device__ __forceinline__ void rank_segment(const int32_t (&idv)[STEPS], int64_
   }
 }
 
+// n words from global to shared memory by one warp, eight loads per lane in
+// flight at a time.
+__device__ __forceinline__ void stage_words(int32_t* dst, const int32_t* __restrict__ src, int n,
+                                            int lane) {
+  for (int e0 = 0; e0 < n; e0 += 8 * 32) {
+    int32_t v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = e0 + i * 32 + lane;
+      v[i] = e < n ? src[e] : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = e0 + i * 32 + lane;
+      if (e < n) dst[e] = v[i];
+    }
+  }
+}
+
 // One warp per chunk.  The chunk's base counts, the slot offsets and the
 // replica tables are staged in shared memory first, so the in-order ranking
 // touches only registers and shared memory.
@@ -231,13 +257,13 @@ __global__ void __launch_bounds__(32)
     idv[s] = q < pairs ? ids[q] : -1;
   }
   const int32_t* cb = chunk_base + (int64_t)blockIdx.x * E;
-  for (int e = lane; e < E; e += 32) s_run[e] = cb[e];
-  for (int e = lane; e <= P; e += 32) s_off[e] = offsets_P[e];
+  stage_words(s_run, cb, E, lane);
+  stage_words(s_off, offsets_P, P + 1, lane);
   const int32_t* m_l2p = l2p;
   const int32_t* m_nrep = nrep;
   if (l2p != nullptr && stage_map) {
-    for (int e = lane; e < E; e += 32) s_nrep[e] = nrep[e];
-    for (int e = lane; e < E * X; e += 32) s_l2p[e] = l2p[e];
+    stage_words(s_nrep, nrep, E, lane);
+    stage_words(s_l2p, l2p, E * X, lane);
     m_l2p = s_l2p;
     m_nrep = s_nrep;
   }
@@ -260,7 +286,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
                           const int32_t* __restrict__ l2p, const int32_t* __restrict__ nrep,
                           int X, int align, int64_t cap, int32_t* __restrict__ counts_P,
                           int32_t* __restrict__ offsets_P, int32_t* __restrict__ perm,
-                          int32_t* __restrict__ inv, uint32_t* status) {
+                          int32_t* __restrict__ inv, int stage_map, uint32_t* status) {
   grid_dep_wait();    // earlier kernels on the stream are complete
   grid_dep_launch();  // the next kernel may start its launch
   extern __shared__ int32_t smem[];
@@ -269,12 +295,23 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
   int32_t* s_slot = s_off + P + 1;                  // [P]
   int32_t* s_claim = s_slot + P;                    // [P]
   int32_t* s_cnt = s_claim + P;                     // [E]
+  int32_t* s_nrep = s_cnt + E;                      // [E]   (map staged only)
+  int32_t* s_l2p = s_nrep + E;                      // [E*X] (map staged only)
   __shared__ int32_t s_warp[32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) s_hist[i] = 0;
   for (int i = threadIdx.x; i < P; i += blockDim.x) {
     s_slot[i] = 0;
     s_claim[i] = 0;
+  }
+  // the replica tables, read by every rank step, from shared memory when they fit
+  const int32_t* m_l2p = l2p;
+  const int32_t* m_nrep = nrep;
+  if (l2p != nullptr && stage_map) {
+    for (int i = threadIdx.x; i < E; i += blockDim.x) s_nrep[i] = nrep[i];
+    for (int i = threadIdx.x; i < E * X; i += blockDim.x) s_l2p[i] = l2p[i];
+    m_l2p = s_l2p;
+    m_nrep = s_nrep;
   }
   // warp segments of whole 32-pair steps
   const int64_t seg = ((pairs + kSmallWarps - 1) / kSmallWarps + 31) / 32 * 32;
@@ -348,8 +385,8 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
     }
   }
   __syncthreads();
-  rank_segment<kSmallSteps>(idv, base, end, k, E, my_hist, l2p, nrep, X, P, s_off, cap, perm,
-                            inv, status);
+  rank_segment<kSmallSteps>(idv, base, end, k, E, my_hist, m_l2p, m_nrep, X, P, s_off, cap,
+                            perm, inv, status);
 }
 
 __device__ __forceinline__ uint4 ld_nc(const uint4* p) {
@@ -466,10 +503,12 @@ extern "C" moe_status moe_dispatch(const void* d_global, const int32_t* d_ids, i
   int32_t* hist = static_cast<int32_t*>(d_ws);
   const size_t small_smem =
       sizeof(int32_t) * ((size_t)kSmallWarps * E + (P + 1) + 2 * (size_t)P + E);
+  const size_t small_map = d_l2p != nullptr ? sizeof(int32_t) * ((size_t)E + (size_t)E * X) : 0;
   if (pairs <= kSmallPairs && small_smem <= kSmallSmemBytes) {
-    const size_t smem = small_smem;
+    const int stage = small_map > 0 && small_smem + small_map <= kSmallSmemBytes;
+    const size_t smem = small_smem + (stage ? small_map : 0);
     launch(dispatch_small_kernel, 1, kSmallWarps * 32, smem, s, d_ids, pairs, k, E, P, d_l2p,
-           d_nrep, X, align, cap, d_counts_P, d_offsets_P, d_perm, d_inv, d_status);
+           d_nrep, X, align, cap, d_counts_P, d_offsets_P, d_perm, d_inv, stage, d_status);
   } else if (chunks == 0) {
     launch(dispatch_scan_kernel, 1, 1024, 0, s, hist, 0, E, P, d_l2p, d_nrep, X, align, cap,
            d_counts_P, d_offsets_P, d_status);
