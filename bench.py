@@ -47,13 +47,13 @@ def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
                       addnorm: bool = False) -> int:
     """Kernel launches of one layer step: gather (hidden states and logits in one
     launch; two with the fused add + RMSNorm, whose kernel takes the hidden states
-    only), route, dispatch (one CTA-wide kernel for <= 16384 routed pairs whose tables
+    only), route, dispatch (one CTA-wide kernel for <= 8192 routed pairs whose tables
     fit 48 KB, else histogram + scan + rank; then the row copy; + the alignment pad
     kernel when align > 1, plus the FP8 rows' pad kernel on the FP8 path), grouped FFN
     (MM1+SwiGLU and MM2), combine with the DP scatter.  With the router gate GEMM the
     logits gather goes and routing is one fused kernel (>= sms/4 row tiles and k <= 8)
     or split GEMM + sum + top-k."""
-    small = rows * k <= 16384 and 4 * (33 * E + 3 * P + 1) <= 48 * 1024
+    small = rows * k <= 8192 and 4 * (33 * E + 3 * P + 1) <= 48 * 1024
     dispatch = (1 if small else 3) + 1 + (1 + (1 if fp8 else 0) if align > 1 else 0)
     gather, route = (2 if addnorm else 1), 1
     if router_gemm:

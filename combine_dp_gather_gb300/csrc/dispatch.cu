@@ -212,29 +212,15 @@ __device__ __forceinline__ void rank_segment(const int32_t (&idv)[STEPS], int64_
   }
 }
 
-// n words from global to shared memory by one warp, eight loads per lane in
-// flight at a time.
-__device__ __forceinline__ void stage_words(int32_t* dst, const int32_t* __restrict__ src, int n,
-                                            int lane) {
-  for (int e0 = 0; e0 < n; e0 += 8 * 32) {
-    int32_t v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = e0 + i * 32 + lane;
-      v[i] = e < n ? src[e] : 0;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = e0 + i * 32 + lane;
-      if (e < n) dst[e] = v[i];
-    }
-  }
-}
+// kRankWarps warps per chunk, each ranking a consecutive quarter of it: the
+// warps' per-expert counts (shared-memory histograms) give each warp its start
+// within the chunk's base counts, so the in-order ranking takes 8 steps per
+// warp instead of 32.  The slot offsets and the replica tables are staged in
+// shared memory first, so the ranking touches only registers and shared memory.
+constexpr int kRankWarps = 4;
+constexpr int kRankSteps = kChunk / 32 / kRankWarps;
 
-// One warp per chunk.  The chunk's base counts, the slot offsets and the
-// replica tables are staged in shared memory first, so the in-order ranking
-// touches only registers and shared memory.
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(kRankWarps * 32)
     dispatch_rank_kernel(const int32_t* __restrict__ ids, int64_t pairs, int k, int E,
                          const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ l2p,
                          const int32_t* __restrict__ nrep, int X, int P,
@@ -244,40 +230,62 @@ __global__ void __launch_bounds__(32)
   grid_dep_wait();    // earlier kernels on the stream are complete
   grid_dep_launch();  // the next kernel may start its launch
   extern __shared__ int32_t smem[];
-  int32_t* s_run = smem;               // [E]  running count (starts at the chunk base)
-  int32_t* s_off = s_run + E;          // [P + 1]
-  int32_t* s_nrep = s_off + P + 1;     // [E]   (map only)
-  int32_t* s_l2p = s_nrep + E;         // [E*X] (map only)
-  const int lane = threadIdx.x;
-  const int64_t base = (int64_t)blockIdx.x * kChunk;
-  int32_t idv[kChunk / 32];
+  int32_t* s_run = smem;                      // [kRankWarps][E] per-warp counts, then starts
+  int32_t* s_off = s_run + kRankWarps * E;    // [P + 1]
+  int32_t* s_nrep = s_off + P + 1;            // [E]   (map only)
+  int32_t* s_l2p = s_nrep + E;                // [E*X] (map only)
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t cbase = (int64_t)blockIdx.x * kChunk;
+  const int64_t cend = cbase + kChunk < pairs ? cbase + kChunk : pairs;
+  const int64_t base = cbase + (int64_t)wid * (kChunk / kRankWarps);
+  const int64_t wend = base + kChunk / kRankWarps;
+  const int64_t end = wend < cend ? wend : cend;  // may be <= base in the last chunk
+  int32_t idv[kRankSteps];
 #pragma unroll
-  for (int s = 0; s < kChunk / 32; ++s) {
+  for (int s = 0; s < kRankSteps; ++s) {
     const int64_t q = base + s * 32 + lane;
-    idv[s] = q < pairs ? ids[q] : -1;
+    idv[s] = q < end ? ids[q] : -1;
   }
-  const int32_t* cb = chunk_base + (int64_t)blockIdx.x * E;
-  stage_words(s_run, cb, E, lane);
-  stage_words(s_off, offsets_P, P + 1, lane);
+  for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) s_run[i] = 0;
+  for (int i = threadIdx.x; i <= P; i += blockDim.x) s_off[i] = offsets_P[i];
   const int32_t* m_l2p = l2p;
   const int32_t* m_nrep = nrep;
   if (l2p != nullptr && stage_map) {
-    stage_words(s_nrep, nrep, E, lane);
-    stage_words(s_l2p, l2p, E * X, lane);
+    for (int i = threadIdx.x; i < E; i += blockDim.x) s_nrep[i] = nrep[i];
+    for (int i = threadIdx.x; i < E * X; i += blockDim.x) s_l2p[i] = l2p[i];
     m_l2p = s_l2p;
     m_nrep = s_nrep;
   }
-  __syncwarp();
-  const int64_t end = base + kChunk < pairs ? base + kChunk : pairs;
-  rank_segment<kChunk / 32>(idv, base, end, k, E, s_run, m_l2p, m_nrep, X, P, s_off, cap, perm,
-                            inv, status);
+  __syncthreads();
+  int32_t* my_run = s_run + wid * E;
+#pragma unroll
+  for (int s = 0; s < kRankSteps; ++s) {
+    const int32_t l = idv[s];
+    if (l >= 0 && l < E) atomicAdd(&my_run[l], 1);
+  }
+  __syncthreads();
+  // each warp starts where the chunk's earlier warps end, from the chunk base
+  const int32_t* cb = chunk_base + (int64_t)blockIdx.x * E;
+  for (int l = threadIdx.x; l < E; l += blockDim.x) {
+    int32_t run = cb[l];
+#pragma unroll
+    for (int w = 0; w < kRankWarps; ++w) {
+      const int32_t t = s_run[w * E + l];
+      s_run[w * E + l] = run;
+      run += t;
+    }
+  }
+  __syncthreads();
+  rank_segment<kRankSteps>(idv, base, end, k, E, my_run, m_l2p, m_nrep, X, P, s_off, cap, perm,
+                           inv, status);
 }
 
 // Small problems (<= kSmallPairs routed pairs, tables within kSmallSmemBytes) in one CTA:
 // per-warp histograms, per-expert scan over warps, slot counts and aligned
 // offsets, then each warp ranks its own segment -- one launch instead of three.
 constexpr int kSmallWarps = 32;
-constexpr int kSmallSteps = 16;  // 32-pair steps per warp segment
+constexpr int kSmallSteps = 8;   // 32-pair steps per warp segment (above 8192 pairs the
+                                 // chunked kernels, four warps per 1024 pairs, are faster)
 constexpr int64_t kSmallPairs = (int64_t)kSmallWarps * kSmallSteps * 32;
 constexpr size_t kSmallSmemBytes = 48 * 1024;  // per-warp histograms + slot tables
 
@@ -519,9 +527,10 @@ extern "C" moe_status moe_dispatch(const void* d_global, const int32_t* d_ids, i
            d_counts_P, d_offsets_P, d_status);
     // replica tables staged in shared memory when they fit (else read from global)
     const int stage_map = d_l2p != nullptr && (int64_t)E * X <= 4096;
-    const size_t smem = sizeof(int32_t) * (E + (P + 1) + (stage_map ? E + (size_t)E * X : 0));
-    launch(dispatch_rank_kernel, (unsigned)chunks, 32, smem, s, d_ids, pairs, k, E, hist, d_l2p,
-           d_nrep, X, P, d_offsets_P, cap, d_perm, d_inv, stage_map, d_status);
+    const size_t smem = sizeof(int32_t) * ((size_t)kRankWarps * E + (P + 1) +
+                                           (stage_map ? E + (size_t)E * X : 0));
+    launch(dispatch_rank_kernel, (unsigned)chunks, kRankWarps * 32, smem, s, d_ids, pairs, k, E,
+           hist, d_l2p, d_nrep, X, P, d_offsets_P, cap, d_perm, d_inv, stage_map, d_status);
   }
   if (move_rows && rows > 0) {
     const int64_t items = rows * ((vpr + kSegVecs - 1) / kSegVecs);

@@ -200,13 +200,15 @@ def _distinct_ids(rows, k, E, seed, pad_every=7):
 
 @pytest.mark.parametrize("rows,E,use_map,align", [
     (3001, 64, False, 1), (3001, 64, False, 128), (3001, 64, True, 1), (3001, 64, True, 4),
-    (500, 64, False, 1), (500, 64, True, 4), (1900, 256, True, 1), (2048, 256, False, 1),
+    (500, 64, False, 1), (500, 64, True, 4), (1900, 256, True, 1), (1024, 256, False, 1),
+    (2048, 256, False, 1),
     (8192, 256, False, 1), (9001, 64, True, 4), (2047, 300, False, 1), (2047, 400, False, 1),
     (1, 64, False, 1)])
 def test_dispatch_bitexact(md, orc, rows, E, use_map, align):
-    """rows x 8 pairs: <= 16384 whose per-warp tables fit 48 KB (E <= ~340) runs the
-    one-CTA path (2048 rows is exactly the pair limit); more pairs (3001 rows: 24 chunks
-    of 1024 + a ragged tail) or E = 400 run the chunked histogram / scan / rank path."""
+    """rows x 8 pairs: <= 8192 whose per-warp tables fit 48 KB (E <= ~340) runs the
+    one-CTA path (1024 rows is exactly the pair limit); more pairs (1900 rows: 15 chunks
+    of 1024 + a ragged tail) or E = 400 run the chunked histogram / scan / rank path
+    (four warps per chunk)."""
     k, H = 8, 512
     l2p = nrep = None
     P = E
