@@ -26,9 +26,8 @@
 // slot whatever the slot's row count.
 //
 // Roles (192 threads, one CTA per SM):
-//   warp 0    TMA producer: A box of 64 x 16, 32, 64 or 128 rows (the tile's
-//             rows rounded up; decode slots hold a few tokens) and two B boxes
-//             64x128 (the weight tile) per stage, 128-byte swizzle; 4-stage ring
+//   warp 0    TMA producer: A box 64x128 (rows) and two B boxes 64x128 (the
+//             weight tile) per stage, 128-byte swizzle; 4-stage ring
 //   warp 1    TMEM allocation (512 columns: two 128x256 fp32 accumulators);
 //             lane 0 issues the MMAs (M=128, N=256, K=16, bf16 -> fp32) and
 //             tcgen05.commit to release stages and publish accumulators
@@ -84,16 +83,6 @@ struct SmemLayout {
 };
 constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemLayout); }
 
-// Token-tile maps with boxes of 16, 32, 64 and 128 rows: a tile loads only the
-// rows its slot has (rounded up to the next box), the rest of the 128-row A
-// tile keeps older data and computes rows that are never stored.
-struct AMaps {
-  CUtensorMap m[4];
-};
-__device__ __forceinline__ int a_box_index(int32_t rows) {
-  return rows <= 16 ? 0 : rows <= 32 ? 1 : rows <= 64 ? 2 : 3;
-}
-
 struct TcParams {
   const int32_t* offsets;
   int slot_lo, nslots;
@@ -133,7 +122,7 @@ __device__ __forceinline__ Unit decode_unit(const SmemLayout& L, int nslots, int
 
 template <bool SWIGLU>
 __global__ void __launch_bounds__(THREADS, 1)
-    ffn_tc_kernel(const __grid_constant__ AMaps tmA, const __grid_constant__ CUtensorMap tmB,
+    ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const TcParams p) {
   grid_dep_wait();    // earlier kernels on the stream are complete
   grid_dep_launch();  // the next kernel may start its launch
@@ -210,11 +199,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ producer
     const uint64_t pol_act = policy_evict_last();
     const uint64_t pol_w = policy_evict_first();
-    if (lane < 4)
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA.m[lane]))
-                   : "memory");
-    if (lane == 0)
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
     uint32_t it = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit un = decode_unit(L, p.nslots, u);
@@ -222,9 +210,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int32_t row0 = L.row_base[un.slot] + un.mt * BM;
       const int32_t brow1 = slot * p.b_rows_per_slot + un.n * p.b_tile_step;
       const int32_t brow2 = brow1 + p.b_second;
-      const int abox = a_box_index(L.row_end[un.slot] - row0);
-      const CUtensorMap* amap = &tmA.m[abox];
-      const uint32_t tx = (uint32_t)((16 << abox) * BK * 2 + B_BYTES);
       bool ok = true;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
@@ -236,8 +221,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t full = smem_u32(&L.full[st]);
           const uint32_t sa = smem_u32(stage_base + (size_t)st * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
-          mbar_arrive_expect_tx(full, tx);
-          tma_load_2d<1>(sa, amap, kb * BK, row0, full, pol_act);
+          mbar_arrive_expect_tx(full, STAGE_BYTES);
+          tma_load_2d<1>(sa, &tmA, kb * BK, row0, full, pol_act);
           tma_load_2d<1>(sb, &tmB, kb * BK, brow1, full, pol_w);
           tma_load_2d<1>(sb + B_BOX_BYTES, &tmB, kb * BK, brow2, full, pol_w);
         }
@@ -382,7 +367,7 @@ bool device_setup(int* max_ctas) {
 }
 
 // One launch of MM1 + SwiGLU (gemm1) or MM2.
-moe_status run_ffn(const FfnArgs& a, const AMaps& mA, const CUtensorMap& mB, bool gemm1,
+moe_status run_ffn(const FfnArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, bool gemm1,
                    cudaStream_t s) {
   const int nslots = a.slot_hi - a.slot_lo;
   int max_ctas = 0;
@@ -431,14 +416,12 @@ moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   // rows per slot the sorted buffer can hold on average, over the whole layer
   const int64_t rows_per_slot = a.cap / (a.P > 0 ? a.P : 1);
   if (rows_per_slot >= kPairRowsPerSlot) return launch_ffn_tc_swap(a, s);
-  AMaps mA1, mA2;
-  CUtensorMap mB1, mB2;
-  bool ok = make_map(&mB1, a.wgu, (uint64_t)a.H, (uint64_t)a.P * 2 * a.I, 128) &&
-            make_map(&mB2, a.wd, (uint64_t)a.I, (uint64_t)a.P * a.H, 128);
-  for (int i = 0; i < 4 && ok; ++i)
-    ok = make_map(&mA1.m[i], a.xs, (uint64_t)a.H, (uint64_t)a.cap, 16u << i) &&
-         make_map(&mA2.m[i], a.h, (uint64_t)a.I, (uint64_t)a.cap, 16u << i);
-  if (!ok) return MOE_ERR_CUDA;
+  CUtensorMap mA1, mB1, mA2, mB2;
+  if (!make_map(&mA1, a.xs, (uint64_t)a.H, (uint64_t)a.cap, 128) ||
+      !make_map(&mB1, a.wgu, (uint64_t)a.H, (uint64_t)a.P * 2 * a.I, 128) ||
+      !make_map(&mA2, a.h, (uint64_t)a.I, (uint64_t)a.cap, 128) ||
+      !make_map(&mB2, a.wd, (uint64_t)a.I, (uint64_t)a.P * a.H, 128))
+    return MOE_ERR_CUDA;
   moe_status st = run_ffn(a, mA1, mB1, true, s);
   if (st != MOE_OK) return st;
   return run_ffn(a, mA2, mB2, false, s);
