@@ -34,10 +34,11 @@
 //   warps 2-9 epilogue, two warps per TMEM lane quarter (token columns 0-31 and
 //             32-63): per k-block tcgen05.ld of the partials, release, scale and
 //             accumulate; per unit SwiGLU + quantisation or bf16 out
-// The epilogue's per-k-block work sets the pace once the weight stream is fast
-// enough, so it is kept small: a warp whose columns hold no token of the unit
-// only releases the buffer; the others scale only the columns that hold tokens
-// (in groups of 8), with packed fp32x2 FMAs.  A k-block's factor
+// The epilogue's work sets the pace once the weight stream is fast enough, so it
+// is kept small: a warp whose columns hold no token of the unit only releases
+// the buffer; the others scale only the columns that hold tokens (in groups of
+// 8), with packed fp32x2 FMAs, and at the unit's end apply SwiGLU (fast exp and
+// divide) and the per-token quantisation to those columns only.  A k-block's factor
 // 2^(e_token + e_weight) depends on the token and on which 128-row half of the
 // tile a row is in, not on the row, so each lane forms its token's two factors
 // once and the warp reads them back from shared memory as broadcasts.
@@ -400,23 +401,31 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       if (SWIGLU) {
         const int feat = un.tile * 128 + q * 32 + lane;
-        // h = silu(gate) * up, then per token one scale over its 128 features
+        // h = silu(gate) * up, then per token one scale over its 128 features; only
+        // the column groups of 8 that hold tokens are computed
         float m[CT];
 #pragma unroll
-        for (int j = 0; j < CT; ++j) {
-          acc0[j] = acc0[j] / (1.0f + expf(-acc0[j])) * acc1[j];
-          m[j] = fabsf(acc0[j]);
+        for (int g = 0; g < CT; g += 8) {
+          if (g < ncol) {
+#pragma unroll
+            for (int j = g; j < g + 8; ++j) {
+              acc0[j] = __fdividef(acc0[j], 1.0f + __expf(-acc0[j])) * acc1[j];
+              m[j] = fabsf(acc0[j]);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+              for (int j = g; j < g + 8; ++j)
+                m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], off));
+            if (lane == 0)
+#pragma unroll
+              for (int j = g; j < g + 8; ++j) L.wmax[cg][q][j] = m[j];
+          }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-          for (int j = 0; j < CT; ++j) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], off));
-        if (lane == 0)
-#pragma unroll
-          for (int j = 0; j < CT; ++j) L.wmax[cg][q][j] = m[j];
         named_sync(bar_id, 128);
 #pragma unroll
         for (int j = 0; j < CT; ++j) {
+          if (j >= ncol) continue;
           const float amax = fmaxf(fmaxf(L.wmax[cg][0][j], L.wmax[cg][1][j]),
                                    fmaxf(L.wmax[cg][2][j], L.wmax[cg][3][j]));
           const int e = fp8_scale_exp(amax);
@@ -432,6 +441,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int feat = un.tile * 256 + q * 32 + lane;  // and feat + 128 (second half)
 #pragma unroll
         for (int j = 0; j < CT; ++j) {
+          if (j >= ncol) continue;
           const int64_t row = (int64_t)un.tok0 + t0 + j;
           if (t0 + j < un.ntok && row < p.cap) {
             p.y[row * p.out_ld + feat] = __float2bfloat16_rn(acc0[j]);
