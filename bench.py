@@ -79,7 +79,7 @@ FFN_TRAFFIC = {
     "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "205258ea68ec00af",
                 "bytes": 25761555200},
     "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
-                   "sha256_16": "35e34b6af376f95c", "bytes": 2794181632},
+                   "sha256_16": "932c697b75c2c4a4", "bytes": 2804173568},
 }
 
 
