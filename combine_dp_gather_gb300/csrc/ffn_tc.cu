@@ -32,8 +32,10 @@
 //             lane 0 issues the MMAs (M=128, N=256, K=16, bf16 -> fp32) and
 //             tcgen05.commit to release stages and publish accumulators
 //   warps 2-5 epilogue: tcgen05.ld 32 columns at a time from the warp's TMEM
-//             lane quarter, activation, bf16 pack, 64-byte row stores; one
-//             arrival per warp on the "accumulator free" barrier
+//             lane quarter, activation (fast exp and divide), bf16 pack, 64-byte
+//             row stores; a warp whose 32 rows lie past the slot's end (most of
+//             them at decode) skips straight to its arrival on the
+//             "accumulator free" barrier
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets
 // MOE_DEV_TIMEOUT, the other roles stop at their next wait, TMEM is freed and
 // the kernel returns.
@@ -283,7 +285,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool valid = row < row_end && row < p.cap;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
       __nv_bfloat16* orow = p.out + row * p.out_ld + (int64_t)un.n * p.out_tile_cols;
-      if (SWIGLU) {
+      // a warp whose 32 rows all lie past the slot's end has nothing to store
+      const bool any = row0 + quad * 32 < row_end && row0 + quad * 32 < p.cap;
+      if (!any) {
+      } else if (SWIGLU) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
           uint32_t g[32], v[32];
@@ -295,8 +300,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int e = 0; e < 16; ++e) {
             float g0 = __uint_as_float(g[2 * e]), g1 = __uint_as_float(g[2 * e + 1]);
             float u0 = __uint_as_float(v[2 * e]), u1 = __uint_as_float(v[2 * e + 1]);
-            float h0 = g0 / (1.0f + expf(-g0)) * u0;
-            float h1 = g1 / (1.0f + expf(-g1)) * u1;
+            float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+            float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
             pk[e] = pack_bf16x2(h0, h1);
           }
           if (valid) {
