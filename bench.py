@@ -74,8 +74,8 @@ def ffn_kernel(cap: int, P: int, fp8: bool = False) -> str:
 # step of the default workload (ncu, --clock-control none), valid while the kernel's
 # sources hash to the recorded SHA-256 prefix; any other source reports traffic null.
 FFN_TRAFFIC = {
-    "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "5f023d538f4b9739",
-               "bytes": 5581367808},
+    "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "10e862941fb51ca1",
+               "bytes": 5582041088},
     "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "205258ea68ec00af",
                 "bytes": 25761555200},
     "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
