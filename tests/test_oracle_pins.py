@@ -332,6 +332,28 @@ def test_ffn_matches_numpy(orc, n, H, I):
     assert np.allclose(y, ref, rtol=1e-12, atol=1e-13)
 
 
+def test_grouped_ffn_runs_each_slot_through_its_own_expert(orc):
+    """Slot s's rows [offsets[s], offsets[s+1]) go through expert s (against the numpy
+    SwiGLU), an empty slot is skipped, and rows of slots outside [lo, hi) are left NaN."""
+    rng = np.random.default_rng(21)
+    H, I = 24, 8
+    counts = [3, 0, 5, 2, 4]
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    xs = rng.standard_normal((int(offsets[-1]), H)).astype(np.float32)
+    wgu = (0.3 * rng.standard_normal((5, 2 * I, H))).astype(np.float32)
+    wd = (0.3 * rng.standard_normal((5, H, I))).astype(np.float32)
+    ys = orc.grouped_ffn(xs, offsets, wgu, wd, 1, 4)
+    for s in range(5):
+        a, b = int(offsets[s]), int(offsets[s + 1])
+        if 1 <= s < 4:
+            assert np.allclose(ys[a:b], numpy_swiglu(xs[a:b], wgu[s], wd[s]), rtol=1e-12,
+                               atol=1e-13)
+        else:
+            assert np.isnan(ys[a:b]).all()
+    # a slot read with another slot's weights would show: experts differ
+    assert not np.allclose(ys[3:8], numpy_swiglu(xs[3:8], wgu[3], wd[3]))
+
+
 def test_ffn_special_cases(orc):
     rng = np.random.default_rng(11)
     x = rng.standard_normal((4, 16)).astype(np.float32)
@@ -669,6 +691,26 @@ def test_ffn_fp8_matches_numpy_on_dequantised_operands(orc):
     dense = orc.expert_ffn(x.astype(np.float32), wgu.astype(np.float32), wd.astype(np.float32))
     rel = np.linalg.norm(y - dense) / np.linalg.norm(dense)
     assert rel < 0.1, rel
+
+
+def test_grouped_ffn_fp8_runs_each_slot_through_its_own_expert(orc):
+    """FP8 grouped FFN: every slot against the dense numpy evaluation on its own
+    dequantised operands; rows outside the slot range stay NaN."""
+    rng = np.random.default_rng(22)
+    H, I = 256, 128
+    counts = [2, 3, 0, 1]
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    xq, xe = orc.quant_groups(rng.standard_normal((int(offsets[-1]), H)))
+    ws = [(*orc.quant_blocks(0.05 * rng.standard_normal((2 * I, H))),
+           *orc.quant_blocks(0.05 * rng.standard_normal((H, I)))) for _ in counts]
+    ys = orc.grouped_ffn_fp8(xq, xe, offsets, lambda s: ws[s], 0, 3)
+    for s in range(4):
+        a, b = int(offsets[s]), int(offsets[s + 1])
+        if s < 3 and b > a:
+            ref = _fp8_ffn_numpy(xq[a:b], xe[a:b], *ws[s])
+            np.testing.assert_allclose(ys[a:b], ref, rtol=1e-9, atol=1e-12)
+        elif b > a:
+            assert np.isnan(ys[a:b]).all()
 
 
 # ----------------------------------------------------------------- router GEMM
