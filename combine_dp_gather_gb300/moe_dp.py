@@ -467,6 +467,7 @@ class MoeLayer:
             self.ws_router = torch.empty(max(moe_route_gemm_ws_bytes(max_rows, H, E, k), 16),
                                          device=dev, dtype=torch.uint8)
         self.rows = 0
+        self.counts = [0] * R
 
     def set_counts(self, counts: Sequence[int]) -> int:
         """Host layout for this step's replica counts; stages counts and offsets on
@@ -477,7 +478,21 @@ class MoeLayer:
             raise MoeError("MoeLayer.set_counts", MOE_ERR_CAPACITY)
         self._stage(counts, offsets, self.d_meta, None)
         self.rows = rows
+        self.counts = [int(c) for c in counts]
         return rows
+
+    def check_inputs(self, local_x, local_logits, out, local_residual=None,
+                     counts: Optional[Sequence[int]] = None):
+        """Host-side check of the replica tensors against the counts (the current
+        layout's by default): raises MoeError instead of letting a kernel read or write
+        past a replica's rows."""
+        counts = self.counts if counts is None else counts
+        _check_replicas("MoeLayer inputs", counts, local_x, self.H, self.dtype)
+        _check_replicas("MoeLayer outputs", counts, out, self.H, self.dtype)
+        if self.router_weight is None:
+            _check_replicas("MoeLayer logits", counts, local_logits, self.E, torch.float32)
+        if local_residual is not None:
+            _check_replicas("MoeLayer residual", counts, local_residual, self.H, self.dtype)
 
     def capture(self, local_x: Sequence[torch.Tensor], local_logits: Sequence[torch.Tensor],
                 out: Sequence[torch.Tensor],
@@ -496,6 +511,7 @@ class MoeLayer:
         RMSNorm of the updated residual is what gets gathered and routed."""
         if counts is not None:
             self.set_counts(counts)
+        self.check_inputs(local_x, local_logits, out, local_residual)
         rows = self.rows
         st = self.status
         xg, lg = self.xg[:rows], self.logits_g[:rows]
@@ -544,6 +560,19 @@ class MoeLayer:
         return out
 
 
+def _check_replicas(what: str, counts: Sequence[int], tensors, width: int, dtype):
+    """The kernels see plain pointers: every replica tensor must be a contiguous CUDA
+    [>= counts[r], width] array of `dtype`, or rows past its end would be touched."""
+    if tensors is None or len(tensors) != len(counts):
+        raise MoeError(what, MOE_ERR_INVALID_ARG)
+    for c, t in zip(counts, tensors):
+        if c == 0:
+            continue
+        if (not t.is_cuda or t.dtype != dtype or t.dim() != 2 or t.shape[1] != width or
+                t.shape[0] < c or not t.is_contiguous()):
+            raise MoeError(what, MOE_ERR_INVALID_ARG)
+
+
 class _MetaStager:
     """Ring of pinned staging buffers for the per-step counts/offsets copy, so the
     host only waits when it laps a copy still in flight."""
@@ -588,6 +617,7 @@ class LayerGraph:
         if layer.rows == 0:
             raise MoeError("LayerGraph", MOE_ERR_INVALID_ARG)
         self.layer, self.rows = layer, layer.rows
+        self.tensors = (local_x, local_logits, out, local_residual)
         self.d_meta = layer.d_meta.clone()       # the layer's current layout
         self._stage = _MetaStager(layer.R)
         saved = layer.d_meta, layer.d_counts, layer.d_offsets
@@ -613,6 +643,7 @@ class LayerGraph:
         offsets, rows = moe_dp_layout(counts, L.mode, L.static_bound, L.tpr)
         if rows != self.rows:
             raise MoeError("LayerGraph.stage", MOE_ERR_INVALID_ARG)
+        L.check_inputs(*self.tensors, counts=counts)   # the captured tensors hold the rows
         self._stage(counts, offsets, self.d_meta, stream)
 
     def replay(self, counts: Optional[Sequence[int]] = None):

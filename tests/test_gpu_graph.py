@@ -80,3 +80,32 @@ def test_graph_replay_matches_eager(md, fp8):
     assert int(layer.status.item()) == 0
     for a, b, c in zip(bo, eager, counts3):
         assert np.array_equal(to_np(a[:c]), to_np(b[:c]))
+
+
+def test_short_replica_tensors_are_rejected_on_the_host(md):
+    """The kernels only see pointers: a replica tensor with fewer rows than its count
+    (or the wrong width or dtype) is refused before anything is launched, in forward
+    and when a graph stages new counts."""
+    from combine_dp_gather_gb300 import synth
+    spec = synth.LayerSpec("tiny_check", [16, 0, 40], 1, H=512, E=16, k=4, I=256,
+                           dtype="bf16", w_std=0.05)
+    x = synth.hidden_states(spec, DEV)
+    lg = synth.router_logits(spec, DEV)
+    wgu, wd = synth.expert_weights(spec, None, DEV)
+    layer = md.MoeLayer(R=spec.R, H=spec.H, E=spec.E, k=spec.k, I=spec.I, w_gate_up=wgu,
+                        w_down=wd, max_rows=3 * 40, mode=spec.mode)
+    out = [torch.empty(c, spec.H, device=DEV, dtype=torch.bfloat16) for c in spec.counts]
+    short = [x[0], x[1], x[2][:39]]
+    with pytest.raises(md.MoeError):
+        layer.forward(short, lg, out, counts=spec.counts)
+    with pytest.raises(md.MoeError):
+        layer.forward(x, [t.to(torch.bfloat16) for t in lg], out, counts=spec.counts)
+    with pytest.raises(md.MoeError):
+        layer.forward(x, lg, out[:2], counts=spec.counts)
+    layer.forward(x, lg, out, counts=spec.counts)        # the right tensors pass
+    g = layer.capture(x, lg, out)
+    with pytest.raises(md.MoeError):
+        g.replay([40, 0, 16])                            # replica 0 holds 16 rows only
+    g.replay([16, 0, 40])
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
