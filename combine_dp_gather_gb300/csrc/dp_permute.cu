@@ -182,11 +182,13 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 
 template <bool BF16>
 __global__ void __launch_bounds__(kNormThreads)
-    dp_gather_add_rmsnorm_kernel(ReplicaPtrs hidden, ReplicaPtrs residual,
+    dp_gather_add_rmsnorm_kernel(const __grid_constant__ ReplicaPtrs hidden,
+                                 const __grid_constant__ ReplicaPtrs residual,
                                  const uint4* __restrict__ gamma, float eps,
                                  const int32_t* __restrict__ counts,
                                  const int32_t* __restrict__ offsets, int R, int64_t rows, int H,
-                                 int vpr, uint4* __restrict__ global, uint32_t* status) {
+                                 int vpr, uint4* __restrict__ global,
+                                 const __grid_constant__ GatherPlane side, uint32_t* status) {
   grid_dep_wait();    // earlier kernels on the stream are complete
   grid_dep_launch();  // the next kernel may start its launch
   constexpr int EPV = BF16 ? 8 : 4;
@@ -213,6 +215,15 @@ __global__ void __launch_bounds__(kNormThreads)
       c = 0;
     }
     uint4* dst = global + g * vpr;
+    // the side plane (router logits) of the same row: copied, or zero for a pad row
+    if (side.vpr > 0) {
+      const bool real = i >= 0 && i < c;
+      const bool have = real && side.src.p[r] != nullptr;
+      if (real && !have && i == 0 && threadIdx.x == 0) flag(status, MOE_DEV_BAD_COUNTS);
+      const uint4* srow = have ? static_cast<const uint4*>(side.src.p[r]) + i * side.vpr : nullptr;
+      for (int v = threadIdx.x; v < side.vpr; v += blockDim.x)
+        side.global[g * side.vpr + v] = srow != nullptr ? ld_nc(srow + v) : make_uint4(0, 0, 0, 0);
+    }
     if (!(i >= 0 && i < c)) {  // pad row (block-uniform)
       for (int v = threadIdx.x; v < vpr; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
       continue;
@@ -330,14 +341,13 @@ extern "C" moe_status moe_dp_gather2(const void* const* local_a, int H_a, int dt
   return launch_status();
 }
 
-extern "C" moe_status moe_dp_gather_add_rmsnorm(const void* const* local_hidden,
-                                                void* const* local_residual, const void* d_gamma,
-                                                float eps, const int32_t* d_counts,
-                                                const int32_t* d_offsets, int R, int64_t rows,
-                                                int H, int dtype, void* d_global,
-                                                uint32_t* d_status, void* stream) {
-  moe_status st = check_common(d_counts, d_offsets, R, rows, H, dtype, d_global);
-  if (st != MOE_OK || rows == 0) return st;
+namespace moe {
+namespace {
+moe_status gather_add_rmsnorm(const void* const* local_hidden, void* const* local_residual,
+                              const void* d_gamma, float eps, const GatherPlane& side,
+                              const int32_t* d_counts, const int32_t* d_offsets, int R,
+                              int64_t rows, int H, int dtype, void* d_global, uint32_t* d_status,
+                              void* stream) {
   if (local_hidden == nullptr || local_residual == nullptr || d_gamma == nullptr ||
       !aligned16(d_gamma) || !(eps >= 0.f))
     return MOE_ERR_INVALID_ARG;
@@ -356,12 +366,47 @@ extern "C" moe_status moe_dp_gather_add_rmsnorm(const void* const* local_hidden,
   if (dtype == MOE_BF16)
     launch(dp_gather_add_rmsnorm_kernel<true>, grid, kNormThreads, 0, as_stream(stream), hp, rp,
            static_cast<const uint4*>(d_gamma), eps, d_counts, d_offsets, R, rows, H, vpr,
-           static_cast<uint4*>(d_global), d_status);
+           static_cast<uint4*>(d_global), side, d_status);
   else
     launch(dp_gather_add_rmsnorm_kernel<false>, grid, kNormThreads, 0, as_stream(stream), hp, rp,
            static_cast<const uint4*>(d_gamma), eps, d_counts, d_offsets, R, rows, H, vpr,
-           static_cast<uint4*>(d_global), d_status);
+           static_cast<uint4*>(d_global), side, d_status);
   return launch_status();
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_dp_gather_add_rmsnorm(const void* const* local_hidden,
+                                                void* const* local_residual, const void* d_gamma,
+                                                float eps, const int32_t* d_counts,
+                                                const int32_t* d_offsets, int R, int64_t rows,
+                                                int H, int dtype, void* d_global,
+                                                uint32_t* d_status, void* stream) {
+  moe_status st = check_common(d_counts, d_offsets, R, rows, H, dtype, d_global);
+  if (st != MOE_OK || rows == 0) return st;
+  GatherPlane none;
+  none.vpr = 0;
+  none.global = nullptr;
+  return gather_add_rmsnorm(local_hidden, local_residual, d_gamma, eps, none, d_counts, d_offsets,
+                            R, rows, H, dtype, d_global, d_status, stream);
+}
+
+extern "C" moe_status moe_dp_gather_add_rmsnorm2(const void* const* local_hidden,
+                                                 void* const* local_residual, const void* d_gamma,
+                                                 float eps, const void* const* local_b, int H_b,
+                                                 int dtype_b, void* d_global_b,
+                                                 const int32_t* d_counts, const int32_t* d_offsets,
+                                                 int R, int64_t rows, int H, int dtype,
+                                                 void* d_global, uint32_t* d_status,
+                                                 void* stream) {
+  moe_status st = check_common(d_counts, d_offsets, R, rows, H, dtype, d_global);
+  if (st != MOE_OK) return st;
+  st = check_common(d_counts, d_offsets, R, rows, H_b, dtype_b, d_global_b);
+  if (st != MOE_OK || rows == 0) return st;
+  GatherPlane side;
+  if (!make_plane(local_b, R, H_b, dtype_b, d_global_b, &side)) return MOE_ERR_INVALID_ARG;
+  return gather_add_rmsnorm(local_hidden, local_residual, d_gamma, eps, side, d_counts, d_offsets,
+                            R, rows, H, dtype, d_global, d_status, stream);
 }
 
 extern "C" moe_status moe_dp_scatter(const void* d_global, const int32_t* d_counts,

@@ -56,6 +56,8 @@ _SIGS = {
     "moe_route_topk_shared": (_I, [_P, _I64, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]),
     "moe_dp_gather_add_rmsnorm": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _I, _I64, _I, _I, _P,
                                        _P, _P]),
+    "moe_dp_gather_add_rmsnorm2": (_I, [_P, _P, _P, ctypes.c_float, _P, _I, _I, _P, _P, _P, _I,
+                                        _I64, _I, _I, _P, _P, _P]),
     "moe_dispatch_noalloc": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _I, _I, _I64, _P,
                                   _P, _P, _P, _P, _P, _P]),
     "moe_quantize_fp8_groups": (_I, [_P, _I64, _I, _I, _P, _P, _P]),
@@ -203,15 +205,28 @@ def moe_dp_gather2(local_a: Sequence[torch.Tensor], local_b: Sequence[torch.Tens
 def moe_dp_gather_add_rmsnorm(local_hidden: Sequence[torch.Tensor],
                               local_residual: Sequence[torch.Tensor], gamma: torch.Tensor,
                               eps: float, d_counts, d_offsets, out: torch.Tensor, d_status=None,
-                              stream=None):
-    """Residual add (in place) + RMSNorm + DP gather of the normed rows."""
+                              stream=None, local_b: Optional[Sequence[torch.Tensor]] = None,
+                              out_b: Optional[torch.Tensor] = None):
+    """Residual add (in place) + RMSNorm + DP gather of the normed rows; with
+    local_b / out_b a second row tensor (the router logits) is gathered plainly in
+    the same launch."""
     R = len(local_hidden)
     hp = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_hidden])
     rp = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_residual])
-    _check("moe_dp_gather_add_rmsnorm", lib().moe_dp_gather_add_rmsnorm(
-        ctypes.cast(hp, _P), ctypes.cast(rp, _P), _ptr(gamma), float(eps), _ptr(d_counts),
-        _ptr(d_offsets), R, out.shape[0], out.shape[1], dtype_code(out.dtype), _ptr(out),
-        _ptr(d_status), _stream(stream)))
+    if local_b is None:
+        _check("moe_dp_gather_add_rmsnorm", lib().moe_dp_gather_add_rmsnorm(
+            ctypes.cast(hp, _P), ctypes.cast(rp, _P), _ptr(gamma), float(eps), _ptr(d_counts),
+            _ptr(d_offsets), R, out.shape[0], out.shape[1], dtype_code(out.dtype), _ptr(out),
+            _ptr(d_status), _stream(stream)))
+        return
+    if out_b is None or len(local_b) != R or out_b.shape[0] != out.shape[0]:
+        raise MoeError("moe_dp_gather_add_rmsnorm2", MOE_ERR_INVALID_ARG)
+    bp = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_b])
+    _check("moe_dp_gather_add_rmsnorm2", lib().moe_dp_gather_add_rmsnorm2(
+        ctypes.cast(hp, _P), ctypes.cast(rp, _P), _ptr(gamma), float(eps), ctypes.cast(bp, _P),
+        out_b.shape[1], dtype_code(out_b.dtype), _ptr(out_b), _ptr(d_counts), _ptr(d_offsets),
+        R, out.shape[0], out.shape[1], dtype_code(out.dtype), _ptr(out), _ptr(d_status),
+        _stream(stream)))
 
 
 def moe_route_topk(logits: torch.Tensor, k: int, renormalize: bool, d_counts, d_offsets,
@@ -521,10 +536,11 @@ class MoeLayer:
         if local_residual is not None:
             if self.norm_gamma is None:
                 raise ValueError("local_residual needs norm_gamma")
+            gathered = self.router_weight is None  # the logits ride in the same launch
             moe_dp_gather_add_rmsnorm(local_x, local_residual, self.norm_gamma, self.norm_eps,
-                                      self.d_counts, self.d_offsets, xg, st, stream)
-            if self.router_weight is None:
-                moe_dp_gather(local_logits, self.d_counts, self.d_offsets, lg, st, stream)
+                                      self.d_counts, self.d_offsets, xg, st, stream,
+                                      local_b=local_logits if gathered else None,
+                                      out_b=lg if gathered else None)
         elif self.router_weight is None:  # hidden states and logits in one launch
             moe_dp_gather2(local_x, local_logits, self.d_counts, self.d_offsets, xg, lg, st,
                            stream)

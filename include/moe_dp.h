@@ -181,6 +181,20 @@ moe_status moe_dp_gather_add_rmsnorm(const void* const* local_hidden, void* cons
                                      const int32_t* d_offsets, int R, int64_t rows, int H,
                                      int dtype, void* d_global, uint32_t* d_status, void* stream);
 
+/* moe_dp_gather_add_rmsnorm plus the plain gather of a second row tensor of the
+ * same replicas in the same launch (e.g. the router logits of each token):
+ * local_b[r] is [counts[r], H_b] of dtype_b, gathered into d_global_b
+ * [rows, H_b] bit for bit as moe_dp_gather would; the first tensor is added,
+ * normed and gathered as moe_dp_gather_add_rmsnorm.  Argument checks and error
+ * behaviour are those of the two entry points. */
+moe_status moe_dp_gather_add_rmsnorm2(const void* const* local_hidden,
+                                      void* const* local_residual, const void* d_gamma, float eps,
+                                      const void* const* local_b, int H_b, int dtype_b,
+                                      void* d_global_b, const int32_t* d_counts,
+                                      const int32_t* d_offsets, int R, int64_t rows, int H,
+                                      int dtype, void* d_global, uint32_t* d_status,
+                                      void* stream);
+
 /* Top-k routing of every real row of the global buffer.  [P1] names the
  * result TopKOutput{topk_ids, topk_weights} (sections "normal dispatch 的调用链"
  * and "Two-batch Overlap"); the scoring is softmax routing: the k largest

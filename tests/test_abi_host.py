@@ -177,6 +177,22 @@ def test_gather_add_rmsnorm_rejects_bad_args(md):
                                        FAKE, NULL, NULL) == E_UNS          # 32 KB rows
     assert L.moe_dp_gather_add_rmsnorm(two, two, MISAL, f(1e-6), FAKE, FAKE, 2, 8, 64, 1, FAKE,
                                        NULL, NULL) == E_ARG
+    g2 = L.moe_dp_gather_add_rmsnorm2
+    # the side plane: rows of whole 16-byte vectors, aligned pointers, a known dtype
+    assert g2(two, two, FAKE, f(1e-6), two, 6, 0, FAKE, FAKE, FAKE, 2, 8, 64, 1, FAKE, NULL,
+              NULL) == E_ARG                                              # 24-byte rows
+    assert g2(two, two, FAKE, f(1e-6), _ptrs(0x2000, 0x3008), 8, 0, FAKE, FAKE, FAKE, 2, 8, 64,
+              1, FAKE, NULL, NULL) == E_ARG                               # misaligned replica
+    assert g2(two, two, FAKE, f(1e-6), NULL, 8, 0, FAKE, FAKE, FAKE, 2, 8, 64, 1, FAKE, NULL,
+              NULL) == E_ARG                                              # no pointer array
+    assert g2(two, two, FAKE, f(1e-6), two, 8, 0, MISAL, FAKE, FAKE, 2, 8, 64, 1, FAKE, NULL,
+              NULL) == E_ARG                                              # misaligned output
+    assert g2(two, two, FAKE, f(1e-6), two, 8, 9, FAKE, FAKE, FAKE, 2, 8, 64, 1, FAKE, NULL,
+              NULL) == E_UNS                                              # unknown dtype
+    assert g2(two, two, NULL, f(1e-6), two, 8, 0, FAKE, FAKE, FAKE, 2, 8, 64, 1, FAKE, NULL,
+              NULL) == E_ARG                                              # no gamma
+    assert g2(two, two, FAKE, f(1e-6), two, 8, 0, FAKE, FAKE, FAKE, 2, 0, 64, 1, FAKE, NULL,
+              NULL) == md.MOE_OK                                          # no rows: no-op
 
 
 def test_route_rejects_bad_args(md):

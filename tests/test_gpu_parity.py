@@ -142,9 +142,13 @@ def test_fused_gather_and_combine_scatter_bad_counts_flag_without_fault(md):
         assert torch.equal(o[4:].float(), torch.full((6, 64), 3.0, device=DEV))
 
 
-@pytest.mark.parametrize("dtype,H,mode", [(torch.bfloat16, 7168, 1), (torch.bfloat16, 512, 0),
-                                          (torch.float32, 1024, 2)])
-def test_gather_add_rmsnorm(md, orc, dtype, H, mode):
+@pytest.mark.parametrize("dtype,H,mode,E", [(torch.bfloat16, 7168, 1, 0),
+                                            (torch.bfloat16, 7168, 1, 256),
+                                            (torch.bfloat16, 512, 0, 0),
+                                            (torch.float32, 1024, 2, 36)])
+def test_gather_add_rmsnorm(md, orc, dtype, H, mode, E):
+    """E > 0: the router logits [count, E] float32 ride in the same launch and must
+    equal the plain gather's output bit for bit (zero pad rows)."""
     counts = [5, 0, 33, 1, 17]
     offs, rows = md.moe_dp_layout(counts, mode, 40, 1)
     g = torch.Generator(device=DEV).manual_seed(H + mode)
@@ -154,7 +158,16 @@ def test_gather_add_rmsnorm(md, orc, dtype, H, mode):
     res0 = [t.clone() for t in res]
     out = torch.full((rows, H), 3.0, device=DEV, dtype=dtype)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    md.moe_dp_gather_add_rmsnorm(hid, res, gamma, 1e-6, dev_i32(counts), dev_i32(offs), out, st)
+    if E:
+        lg = [torch.randn(c, E, generator=g, device=DEV) for c in counts]
+        lg_out = torch.full((rows, E), 3.0, device=DEV)
+        md.moe_dp_gather_add_rmsnorm(hid, res, gamma, 1e-6, dev_i32(counts), dev_i32(offs), out,
+                                     st, local_b=lg, out_b=lg_out)
+        assert np.array_equal(to_np(lg_out), orc.dp_gather([to_np(t) for t in lg], counts,
+                                                           np.array(offs, np.int32), rows))
+    else:
+        md.moe_dp_gather_add_rmsnorm(hid, res, gamma, 1e-6, dev_i32(counts), dev_i32(offs), out,
+                                     st)
     assert status_of(st) == 0
     bf = dtype == torch.bfloat16
     f32 = lambda t: as_f32(to_np(t))
@@ -639,5 +652,65 @@ def test_layer_align128_and_determinism(md, orc):
     first = [t.clone() for t in out]
     layer.forward(rest[0], rest[1], out)
     torch.cuda.synchronize()
+    for a, b in zip(first, out):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_layer_addnorm_boundary(md, orc, mode):
+    """The residual add + RMSNorm boundary (the logits gathered in the same launch):
+    residuals are updated exactly as the oracle's add, the normed rows are within one
+    rounding of the oracle's norm, the logits are gathered bit for bit, and the rest
+    of the step equals a plain layer fed the normed rows (checked against the oracle),
+    bit for bit, in eager mode and under graph replay."""
+    spec = synth.LayerSpec("addnorm", [16, 0, 140, 8, 1], mode, H=512, E=16, k=4, I=256,
+                           dtype="bf16", w_std=0.05, zipf_s=1.1)
+    x_loc = synth.hidden_states(spec, DEV)
+    lg_loc = synth.router_logits(spec, DEV)
+    wgu, wd = synth.expert_weights(spec, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(77 + mode)
+    res = [torch.randn(c, spec.H, generator=g, device=DEV).to(torch.bfloat16)
+           for c in spec.counts]
+    res0 = [t.clone() for t in res]
+    gamma = (1 + 0.1 * torch.randn(spec.H, generator=g, device=DEV)).to(torch.bfloat16)
+    offs, rows = md.moe_dp_layout(spec.counts, spec.mode)
+    layer = md.MoeLayer(R=spec.R, H=spec.H, E=spec.E, k=spec.k, I=spec.I, w_gate_up=wgu,
+                        w_down=wd, max_rows=rows, mode=spec.mode, keep_global=True,
+                        norm_gamma=gamma, norm_eps=1e-6)
+    out = [torch.empty(c, spec.H, device=DEV, dtype=torch.bfloat16) for c in spec.counts]
+    layer.forward(x_loc, lg_loc, out, counts=spec.counts, local_residual=res)
+    assert status_of(layer.status) == 0
+    f32 = lambda t: as_f32(to_np(t))
+    xg = layer.xg[:rows].clone()
+    for r, c in enumerate(spec.counts):
+        r_new, y_r = orc.add_rmsnorm(f32(x_loc[r]), f32(res0[r]), f32(gamma), 1e-6, True)
+        assert np.array_equal(f32(res[r]), r_new)
+        assert_close(f32(xg[offs[r]: offs[r] + c]).astype(np.float64), y_r, 1e-6, 8e-3,
+                     "normed rows")
+    assert np.array_equal(to_np(layer.logits_g[:rows]),
+                          orc.dp_gather([to_np(t) for t in lg_loc], spec.counts,
+                                        np.array(offs, np.int32), rows))
+    # the rest of the step: a plain layer on the normed rows gives the same bits
+    normed = [xg[offs[r]: offs[r] + c].clone() for r, c in enumerate(spec.counts)]
+    plain = md.MoeLayer(R=spec.R, H=spec.H, E=spec.E, k=spec.k, I=spec.I, w_gate_up=wgu,
+                        w_down=wd, max_rows=rows, mode=spec.mode, keep_global=True)
+    out2 = [torch.full_like(t, 7.0) for t in out]
+    plain.forward(normed, lg_loc, out2, counts=spec.counts)
+    assert status_of(plain.status) == 0
+    for a, b in zip(out2, out):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    _check_layer(md, orc, spec, plain, out2, normed, lg_loc, wgu, wd, offs, rows)
+    # a graph replay from the same residuals repeats the step bit for bit
+    for t, t0 in zip(res, res0):
+        t.copy_(t0)
+    graph = layer.capture(x_loc, lg_loc, out, local_residual=res)
+    for t, t0 in zip(res, res0):     # capture's warm-up ran the step once
+        t.copy_(t0)
+    first = [t.clone() for t in out]
+    for t in out:
+        t.fill_(7.0)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert status_of(layer.status) == 0
     for a, b in zip(first, out):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
