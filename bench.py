@@ -48,7 +48,8 @@ def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
     launch, the fused add + RMSNorm included), route, dispatch (one CTA-wide kernel for <= 8192 routed pairs whose tables
     fit 48 KB, else histogram + scan + rank; then the row copy; + the alignment pad
     kernel when align > 1, plus the FP8 rows' pad kernel on the FP8 path), grouped FFN
-    (MM1+SwiGLU and MM2), combine with the DP scatter.  With the router gate GEMM the
+    (MM1+SwiGLU and MM2; one persistent launch for both on FP8), combine with the DP
+    scatter.  With the router gate GEMM the
     logits gather goes and routing is one fused kernel (>= sms/4 row tiles and k <= 8)
     or split GEMM + sum + top-k."""
     small = rows * k <= 8192 and 4 * (33 * E + 3 * P + 1) <= 48 * 1024
@@ -57,7 +58,7 @@ def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
     if router_gemm:
         gather = 1
         route = 1 if (k <= 8 and 4 * ((rows + 127) // 128) >= sms) else 3
-    return gather + route + dispatch + 2 + 1
+    return gather + route + dispatch + (1 if fp8 else 2) + 1
 
 
 def ffn_kernel(cap: int, P: int, fp8: bool = False) -> str:
@@ -360,8 +361,10 @@ def run_native(args, rank, world, local_rank):
                 "unit": "TFLOP/s", "frac": round(achieved / tc_peak, 4)}
     tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12
     roof.update({"traffic": ffn_traffic(args),
-                 "kernel": f"moe_grouped_ffn ({ffn_kernel(layer.cap, layer.P, args.fp8)} MM1+SwiGLU "
-                           "and MM2 launches)",
+                 "kernel": (f"moe_grouped_ffn_fp8 ({ffn_kernel(layer.cap, layer.P, True)}: "
+                            "MM1+SwiGLU and MM2 in one persistent launch)" if args.fp8 else
+                            f"moe_grouped_ffn ({ffn_kernel(layer.cap, layer.P)} MM1+SwiGLU "
+                            "and MM2 launches)"),
                  "tflops": round(tflops, 1),
                  "frac_of_bf16_peak": round(tflops / pk["bf16_tflops"], 4),
                  "frac_of_bf16_sustained": (round(tflops / pk["bf16_tflops_sustained"], 4)

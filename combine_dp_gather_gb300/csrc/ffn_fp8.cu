@@ -91,7 +91,6 @@ __device__ __forceinline__ void fma2_shared(float& a0, float& a1, uint32_t x0, u
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
 }
 
-template <bool SWIGLU>
 struct F8Cfg {
   static constexpr int A_ROWS = 256;  // 128 gate + 128 up rows, or 256 down rows
   static constexpr int A_BYTES = A_ROWS * BK;
@@ -100,43 +99,58 @@ struct F8Cfg {
   static constexpr int STAGES = 5;
   static constexpr int PCOLS = 2 * NT;  // partial columns per buffer (two MMAs)
 };
+constexpr int UQ = 4;  // claimed units in flight between the producer and the other roles
+
+// Scheduler words at the end of the workspace (int32): the unit ticket, the
+// CTAs that have finished, a reserved word, then per slot of the call the
+// MM1 units finished (counted once per epilogue column group).
+constexpr int kTicket = 0, kDone = 1, kReady = 3;
+constexpr int kSyncWords = kReady + MOE_MAX_SLOTS;
 
 struct F8Smem {
-  uint64_t full[5];
-  uint64_t empty[5];
+  uint64_t full[F8Cfg::STAGES];
+  uint64_t empty[F8Cfg::STAGES];
   uint64_t pfull[NPB];
   uint64_t pempty[NPB];
+  uint64_t ufull[UQ];   // a claimed unit id is in uring
+  uint64_t uempty[UQ];  // the MMA warp and the eight epilogue warps have read it
+  int32_t uring[UQ];
   uint32_t tmem_base;
   int32_t abort_flag;
-  int32_t total_units;
+  int32_t last_cta;
+  int32_t total1, total;
   int32_t warp_sums[THREADS / 32];
   float wmax[2][4][CT];              // per epilogue warp: token maxima of h
   alignas(16) float fac[8][2][CT];   // per epilogue warp: this k-block's token factors
-  int32_t pref[MOE_MAX_SLOTS + 1];   // unit prefix over the slot range
+  int32_t pref[MOE_MAX_SLOTS + 1];   // token-group prefix over the slot range
   int32_t row0[MOE_MAX_SLOTS];
   int32_t rows[MOE_MAX_SLOTS];
 };
-template <bool SWIGLU>
 constexpr size_t f8_smem_bytes() {
-  return 1024 + (size_t)F8Cfg<SWIGLU>::STAGES * F8Cfg<SWIGLU>::STAGE_BYTES + sizeof(F8Smem);
+  return 1024 + (size_t)F8Cfg::STAGES * F8Cfg::STAGE_BYTES + sizeof(F8Smem);
 }
+
+// One of the two GEMMs: MM1 (gate/up + SwiGLU, K = H) or MM2 (down, K = I).
+struct F8Phase {
+  int num_kb;              // K / 128
+  int n_tiles;             // weight tiles per slot (128 features of gate + up, or 256 rows)
+  int out_ld;              // output row length: I (h codes) or H (y)
+  int wscale_rows;         // weight scale rows per slot: 2I/128 or H/128
+  int blk_mul, blk_off;    // weight blocks of tile t: t*blk_mul and t*blk_mul + blk_off
+  const uint8_t* xscale;   // token scale bytes [cap, K / 128]
+  const uint8_t* wscale;   // weight scale bytes [P, wscale_rows, K / 128]
+};
 
 struct F8Params {
   const int32_t* offsets;
   int slot_lo, nslots;
   int64_t cap;
-  int num_kb;          // K / 128
-  int n_tiles;         // 128-row weight tiles per slot
-  int wrows_per_slot;  // MM2: H
-  int K;               // reduction length (H for MM1, I for MM2)
-  const uint8_t* xscale;   // [cap, K / 128] token scale bytes
-  const uint8_t* wscale;   // weight scale bytes [P, rows / 128, K / 128]
-  int wscale_rows;         // rows / 128 per slot: 2I/128 (MM1) or H/128 (MM2)
-  int blk_mul, blk_off;    // weight blocks of tile t: t*blk_mul and t*blk_mul + blk_off
-  int out_ld;
-  uint8_t* hq;             // MM1: h codes [cap, I]
-  uint8_t* hscale;         // MM1: h scale bytes [cap, I / 128]
-  __nv_bfloat16* y;        // MM2: [cap, H]
+  int H;
+  F8Phase ph[2];
+  uint8_t* hq;             // h codes [cap, I]
+  uint8_t* hscale;         // h scale bytes [cap, I / 128]
+  __nv_bfloat16* y;        // [cap, H]
+  int32_t* sync;           // scheduler words
   uint32_t* status;
 };
 
@@ -151,23 +165,29 @@ __host__ __device__ __forceinline__ int32_t token_groups(int32_t rows) {
 }
 
 struct F8Unit {
+  int ph;    // 0: MM1 + SwiGLU, 1: MM2
   int slot, tile;
   int32_t tok0, ntok;
   int N;  // MMA width: tokens rounded up to 16
 };
-__device__ __forceinline__ F8Unit decode_unit(const F8Smem& L, int nslots, int u) {
-  int lo = 0, hi = nslots - 1;
-  while (lo < hi) {  // largest s with pref[s] <= u
+// Unit u of the call: MM1 units first (slot-major, then tile, then token
+// group), then the MM2 units in the same order.
+__device__ __forceinline__ F8Unit decode_unit(const F8Smem& L, const F8Params& p, int u) {
+  F8Unit r;
+  r.ph = u >= L.total1 ? 1 : 0;
+  const int v = r.ph ? u - L.total1 : u;
+  const int nt = p.ph[r.ph].n_tiles;
+  int lo = 0, hi = p.nslots - 1;
+  while (lo < hi) {  // largest s with pref[s] * nt <= v
     const int mid = (lo + hi + 1) >> 1;
-    if (L.pref[mid] <= u)
+    if (L.pref[mid] * nt <= v)
       lo = mid;
     else
       hi = mid - 1;
   }
-  const int local = u - L.pref[lo];
+  const int local = v - L.pref[lo] * nt;
   const int32_t T = L.rows[lo];
   const int32_t g = token_groups(T);
-  F8Unit r;
   r.slot = lo;
   r.tile = local / g;
   const int32_t grp = local % g;
@@ -178,13 +198,54 @@ __device__ __forceinline__ F8Unit decode_unit(const F8Smem& L, int nslots, int u
   return r;
 }
 
-template <bool SWIGLU>
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* a) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(int32_t* a, int32_t v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+// Generic-proxy writes and async-proxy (TMA) reads of global memory ordered.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Bounded wait of a whole warp until *ctr >= target (acquire); warp-uniform.
+__device__ bool wait_count(const int32_t* ctr, int32_t target, volatile int32_t* abort_flag,
+                           uint32_t* status) {
+  if (__all_sync(0xffffffffu, ld_acquire_gpu(ctr) >= target)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(100);
+    if (__all_sync(0xffffffffu, ld_acquire_gpu(ctr) >= target)) return true;
+    if ((i & 63u) == 0) {
+      bool stop = *abort_flag != 0;
+      if (!stop && globaltimer_ns() - t0 > kTimeoutNs) {
+        if ((threadIdx.x & 31) == 0) {
+          flag(status, MOE_DEV_TIMEOUT);
+          *abort_flag = 1;
+        }
+        stop = true;
+      }
+      if (__any_sync(0xffffffffu, stop)) return false;
+    }
+  }
+}
+
+// Both GEMMs of the grouped FFN in one persistent launch.  A CTA claims units
+// from a global ticket: all MM1 units, then all MM2 units; an MM2 unit of a
+// slot first waits until that slot's MM1 units have written h.  Every ticket
+// below an MM2 ticket is an MM1 unit held by a running CTA, and an MM1 unit
+// waits on nothing, so the waits always end.  The claim order balances the two
+// GEMMs' unequal units over the SMs (a CTA that finishes its last MM1 unit early
+// goes on with MM2 units).
 __global__ void __launch_bounds__(THREADS, 1)
-    ffn_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ TokMaps tmB,
+    ffn_fp8_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ TokMaps tmB1,
+                   const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ TokMaps tmB2,
                    const F8Params p) {
   grid_dep_wait();    // earlier kernels on the stream are complete
   grid_dep_launch();  // the next kernel may start its launch
-  using C = F8Cfg<SWIGLU>;
+  using C = F8Cfg;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stage_base = reinterpret_cast<uint8_t*>(
@@ -192,7 +253,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   F8Smem& L = *reinterpret_cast<F8Smem*>(stage_base + (size_t)STAGES * C::STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- unit table: token groups per slot, exclusive prefix of units
+  // ---- slot table: token groups per slot, exclusive prefix
   {
     const int per = (p.nslots + THREADS - 1) / THREADS;
     const int s0 = threadIdx.x * per;
@@ -205,7 +266,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (rows < 0) rows = 0;
         L.row0[s] = o0;
         L.rows[s] = rows;
-        local += token_groups(rows) * p.n_tiles;
+        local += token_groups(rows);
       }
     }
     int32_t x = local;
@@ -225,6 +286,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(smem_u32(&L.pfull[i]), 1);   // the MMA commit
         mbar_init(smem_u32(&L.pempty[i]), 8);  // every epilogue warp
       }
+      for (int i = 0; i < UQ; ++i) {
+        mbar_init(smem_u32(&L.ufull[i]), 1);   // the producer
+        mbar_init(smem_u32(&L.uempty[i]), 9);  // the MMA warp + eight epilogue warps
+      }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) tmem_alloc<1>(smem_u32(&L.tmem_base));
@@ -236,35 +301,56 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int s = s0 + i;
       if (s < p.nslots) {
         L.pref[s] = run;
-        run += token_groups(L.rows[s]) * p.n_tiles;
+        run += token_groups(L.rows[s]);
       }
     }
     if (threadIdx.x == THREADS - 1) {
       int32_t tot = 0;
       for (int w = 0; w < THREADS / 32; ++w) tot += L.warp_sums[w];
       L.pref[p.nslots] = tot;
-      L.total_units = tot;
+      L.total1 = tot * p.ph[0].n_tiles;
+      L.total = tot * (p.ph[0].n_tiles + p.ph[1].n_tiles);
     }
     fence_before();
     __syncthreads();
     fence_after();
   }
-  const int total = L.total_units;
+  const int total = L.total;
   const uint32_t tmem_base = L.tmem_base;
   volatile int32_t* abort_flag = &L.abort_flag;
+  int32_t* ready = p.sync + kReady;
+  const int32_t ready_per_group = 2 * p.ph[0].n_tiles;  // column groups x MM1 tiles
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol_tok = policy_evict_last();
     const uint64_t pol_w = policy_evict_first();
     uint32_t it = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const F8Unit un = decode_unit(L, p.nslots, u);
+    for (uint32_t q = 0;; ++q) {
+      const uint32_t rs = q % UQ, rph = (q / UQ) & 1u;
+      if (!wait_bar(smem_u32(&L.uempty[rs]), rph ^ 1u, abort_flag, p.status)) break;
+      int u = 0;
+      if (lane == 0) {
+        u = atomicAdd(p.sync + kTicket, 1);
+        if (u < 0 || u >= total) u = -1;  // no unit left
+        L.uring[rs] = u;
+        mbar_arrive(smem_u32(&L.ufull[rs]));
+      }
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u < 0) break;
+      const F8Unit un = decode_unit(L, p, u);
+      if (un.ph == 1) {  // h of the slot written by the MM1 units (any CTA)
+        if (!wait_count(ready + un.slot, ready_per_group * token_groups(L.rows[un.slot]),
+                        abort_flag, p.status))
+          break;
+        fence_proxy_async_global();
+      }
       const int32_t slot = p.slot_lo + un.slot;
-      const CUtensorMap* bmap = &tmB[(un.N >> 4) - 1];
+      const CUtensorMap* bmap = un.ph ? &tmB2[(un.N >> 4) - 1] : &tmB1[(un.N >> 4) - 1];
       const uint32_t tx = (uint32_t)(C::A_BYTES + un.N * BK);
+      const int num_kb = p.ph[un.ph].num_kb;
       bool ok = true;
-      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
         if (!wait_bar(smem_u32(&L.empty[st]), ph ^ 1u, abort_flag, p.status)) {
           ok = false;
@@ -276,10 +362,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t sb = sa + C::A_BYTES;
           const int32_t kc = kb * BK;
           mbar_arrive_expect_tx(full, tx);
-          if (SWIGLU)
-            tma_load_3d<1>(sa, &tmA, kc, un.tile * 128, 2 * slot, full, pol_w);
+          if (un.ph == 0)
+            tma_load_3d<1>(sa, &tmA1, kc, un.tile * 128, 2 * slot, full, pol_w);
           else
-            tma_load_2d<1>(sa, &tmA, kc, slot * p.wrows_per_slot + un.tile * 256, full, pol_w);
+            tma_load_2d<1>(sa, &tmA2, kc, slot * p.H + un.tile * 256, full, pol_w);
           tma_load_2d<1>(sb, bmap, kc, un.tok0, full, pol_tok);
         }
         __syncwarp();
@@ -293,11 +379,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     uint32_t it = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const F8Unit un = decode_unit(L, p.nslots, u);
+    for (uint32_t q = 0;; ++q) {
+      const uint32_t rs = q % UQ, rph = (q / UQ) & 1u;
+      if (!wait_bar(smem_u32(&L.ufull[rs]), rph, abort_flag, p.status)) break;
+      const int u = L.uring[rs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&L.uempty[rs]));
+      if (u < 0) break;
+      const F8Unit un = decode_unit(L, p, u);
       const uint32_t idesc = idesc_e4m3(128, un.N);
+      const int num_kb = p.ph[un.ph].num_kb;
       bool ok = true;
-      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
         const uint32_t pb = it % NPB, pph = (it / NPB) & 1u;
         if (!wait_bar(smem_u32(&L.full[st]), ph, abort_flag, p.status) ||
@@ -333,8 +426,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     float* fac0 = L.fac[warp - 2][0];  // factors of the first half (gate rows / rows 0-127)
     float* fac1 = L.fac[warp - 2][1];  // and of the second (up rows / rows 128-255)
     uint32_t it = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const F8Unit un = decode_unit(L, p.nslots, u);
+    for (uint32_t qu = 0;; ++qu) {
+      const uint32_t rs = qu % UQ, rph = (qu / UQ) & 1u;
+      bool ok = wait_bar(smem_u32(&L.ufull[rs]), rph, abort_flag, p.status);
+      const int u = ok ? L.uring[rs] : -1;
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(smem_u32(&L.uempty[rs]));
+      F8Unit un{};
+      if (ok && u >= 0) {
+        un = decode_unit(L, p, u);
+        if (un.ph == 1)  // the scale bytes of h are read below
+          ok = wait_count(ready + un.slot, ready_per_group * token_groups(L.rows[un.slot]),
+                          abort_flag, p.status);
+      }
+      // the column group's four warps go on, or stop, together (named barriers below)
+      ok = named_all(bar_id, 128, ok);
+      if (!ok || u < 0) break;
+      const bool swiglu = un.ph == 0;
+      const F8Phase& P = p.ph[un.ph];
       const int32_t slot = p.slot_lo + un.slot;
       const int t0 = cg * CT;  // first token of this warp's columns
       const bool act = t0 < un.ntok;
@@ -343,18 +452,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       // every lane the weight blocks' bytes
       const int64_t trow = (int64_t)un.tok0 + t0 + lane;
       const bool tv = t0 + lane < un.ntok && trow < p.cap;
-      const uint8_t* xs_row = p.xscale + (tv ? trow : 0) * p.num_kb;
-      const int64_t wb0 = (int64_t)slot * p.wscale_rows + un.tile * p.blk_mul;
-      const uint8_t* ws0 = p.wscale + wb0 * p.num_kb;
-      const uint8_t* ws1 = p.wscale + (wb0 + p.blk_off) * p.num_kb;
+      const uint8_t* xs_row = P.xscale + (tv ? trow : 0) * P.num_kb;
+      const int64_t wb0 = (int64_t)slot * P.wscale_rows + un.tile * P.blk_mul;
+      const uint8_t* ws0 = P.wscale + wb0 * P.num_kb;
+      const uint8_t* ws1 = P.wscale + (wb0 + P.blk_off) * P.num_kb;
       uint32_t nx = tv ? xs_row[0] : 127u, nw0 = ws0[0], nw1 = ws1[0];
       float acc0[CT], acc1[CT];
 #pragma unroll
       for (int j = 0; j < CT; ++j) acc0[j] = acc1[j] = 0.0f;
-      bool ok = true;
-      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+      for (int kb = 0; kb < P.num_kb; ++kb, ++it) {
         const uint32_t ex = nx, ew0 = nw0, ew1 = nw1;
-        if (kb + 1 < p.num_kb) {
+        if (kb + 1 < P.num_kb) {
           nx = tv ? xs_row[kb + 1] : 127u;
           nw0 = ws0[kb + 1];
           nw1 = ws1[kb + 1];
@@ -362,7 +470,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t pb = it % NPB, pph = (it / NPB) & 1u;
         if (!wait_bar(smem_u32(&L.pfull[pb]), pph, abort_flag, p.status)) {
           ok = false;
-          it += p.num_kb - kb;
+          it += P.num_kb - kb;
           break;
         }
         fence_after();
@@ -397,9 +505,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = g; j < g + 8; j += 2)
               fma2_shared(acc1[j], acc1[j + 1], r[j], r[j + 1], &fac1[j]);
       }
-      if (SWIGLU) ok = named_all(bar_id, 128, ok);  // the group's four warps leave together
+      ok = named_all(bar_id, 128, ok);  // the group's four warps leave together
       if (!ok) break;
-      if (SWIGLU) {
+      if (swiglu) {
         const int feat = un.tile * 128 + q * 32 + lane;
         // h = silu(gate) * up, then per token one scale over its 128 features; only
         // the column groups of 8 that hold tokens are computed
@@ -431,12 +539,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int e = fp8_scale_exp(amax);
           const int64_t row = (int64_t)un.tok0 + t0 + j;
           if (t0 + j < un.ntok && row < p.cap) {
-            p.hq[row * p.out_ld + feat] = (uint8_t)(e4m3x4(acc0[j] * pow2i(-e), 0.f, 0.f, 0.f) & 0xFFu);
+            p.hq[row * P.out_ld + feat] = (uint8_t)(e4m3x4(acc0[j] * pow2i(-e), 0.f, 0.f, 0.f) & 0xFFu);
             if (q == 0 && lane == 0)
-              p.hscale[row * (p.out_ld / 128) + un.tile] = (uint8_t)(e + 127);
+              p.hscale[row * (P.out_ld / 128) + un.tile] = (uint8_t)(e + 127);
           }
         }
-        named_sync(bar_id, 128);  // the maxima are read before the next unit writes them
+        // h of this column group is published: visible at gpu scope (and to the
+        // TMA loads of MM2 units) before the slot's count goes up
+        __threadfence();
+        fence_proxy_async_global();
+        named_sync(bar_id, 128);  // also: the maxima are read before the next unit writes them
+        if (q == 0 && lane == 0) red_release_gpu_add(ready + un.slot, 1);
       } else {
         const int feat = un.tile * 256 + q * 32 + lane;  // and feat + 128 (second half)
 #pragma unroll
@@ -444,8 +557,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (j >= ncol) continue;
           const int64_t row = (int64_t)un.tok0 + t0 + j;
           if (t0 + j < un.ntok && row < p.cap) {
-            p.y[row * p.out_ld + feat] = __float2bfloat16_rn(acc0[j]);
-            p.y[row * p.out_ld + feat + 128] = __float2bfloat16_rn(acc1[j]);
+            p.y[row * P.out_ld + feat] = __float2bfloat16_rn(acc0[j]);
+            p.y[row * P.out_ld + feat + 128] = __float2bfloat16_rn(acc1[j]);
           }
         }
       }
@@ -456,10 +569,36 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   fence_after();
   if (warp == 1) tmem_dealloc<1>(tmem_base);
+  // The last CTA out checks the scheduler words against this call's units and
+  // clears them for the next call.  Every other CTA has made its last claim and
+  // count before adding itself to kDone.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    L.last_cta = atomicAdd(p.sync + kDone, 1) == (int)gridDim.x - 1;
+    __threadfence();
+  }
+  __syncthreads();
+  if (L.last_cta) {
+    const bool timed_out =
+        p.status != nullptr && (ld_acquire_gpu(reinterpret_cast<const int32_t*>(p.status)) &
+                                (int32_t)MOE_DEV_TIMEOUT) != 0;
+    bool bad = false;
+    for (int s = threadIdx.x; s < p.nslots; s += THREADS) {
+      if (ld_acquire_gpu(ready + s) != ready_per_group * token_groups(L.rows[s])) bad = true;
+      ready[s] = 0;
+    }
+    if (threadIdx.x == 0) {
+      // each CTA's producer claimed every unit ticket once and one ticket past the end
+      if (ld_acquire_gpu(p.sync + kTicket) != total + (int)gridDim.x) bad = true;
+      p.sync[kTicket] = 0;
+      p.sync[kDone] = 0;
+    }
+    if (bad && !timed_out) flag(p.status, MOE_DEV_BAD_WORKSPACE);
+    __threadfence();
+  }
 }
 
 // ------------------------------------------------------------- host side
-template <bool SWIGLU>
 bool f8_setup(int* max_ctas) {
   static std::mutex mu;
   static int ctas[64] = {0};
@@ -467,13 +606,13 @@ bool f8_setup(int* max_ctas) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   std::lock_guard<std::mutex> lock(mu);
   if (ctas[dev] == 0) {
-    const int bytes = (int)f8_smem_bytes<SWIGLU>();
-    if (cudaFuncSetAttribute(ffn_fp8_kernel<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const int bytes = (int)f8_smem_bytes();
+    if (cudaFuncSetAttribute(ffn_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              bytes) != cudaSuccess)
       return false;
     int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, ffn_fp8_kernel<SWIGLU>, THREADS,
-                                                      bytes) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, ffn_fp8_kernel, THREADS, bytes) !=
+            cudaSuccess ||
         b < 1)
       return false;
     ctas[dev] = b * num_sms();
@@ -491,49 +630,61 @@ struct F8Args {
   int H, I;
   uint8_t *hq, *hs;
   __nv_bfloat16* y;
+  int32_t* sync;
   uint32_t* status;
 };
 
-template <bool SWIGLU>
 moe_status run_f8(const F8Args& a, cudaStream_t s) {
   int max_ctas = 0;
-  if (!f8_setup<SWIGLU>(&max_ctas)) return MOE_ERR_CUDA;
-  CUtensorMap mA;
-  TokMaps mB;
-  const uint8_t* tok = SWIGLU ? a.xq : a.hq;
-  const uint64_t K = SWIGLU ? (uint64_t)a.H : (uint64_t)a.I;
-  bool ok = SWIGLU ? make_map_u8_gate_up(&mA, a.wguq, a.H, a.I, a.P, 128)
-                   : make_map_u8(&mA, a.wdq, a.I, (uint64_t)a.P * a.H, 256);
+  if (!f8_setup(&max_ctas)) return MOE_ERR_CUDA;
+  CUtensorMap mA1, mA2;
+  TokMaps mB1, mB2;
+  bool ok = make_map_u8_gate_up(&mA1, a.wguq, a.H, a.I, a.P, 128) &&
+            make_map_u8(&mA2, a.wdq, a.I, (uint64_t)a.P * a.H, 256);
   for (int i = 0; i < NT / 16 && ok; ++i)
-    ok = make_map_u8(&mB.m[i], tok, K, (uint64_t)a.cap, 16u * (i + 1));
+    ok = make_map_u8(&mB1.m[i], a.xq, a.H, (uint64_t)a.cap, 16u * (i + 1)) &&
+         make_map_u8(&mB2.m[i], a.hq, a.I, (uint64_t)a.cap, 16u * (i + 1));
   if (!ok) return MOE_ERR_CUDA;
   F8Params p;
   p.offsets = a.offsets;
   p.slot_lo = a.slot_lo;
   p.nslots = a.slot_hi - a.slot_lo;
   p.cap = a.cap;
-  p.num_kb = (int)(K / BK);
-  p.n_tiles = SWIGLU ? a.I / 128 : a.H / 256;
-  p.wrows_per_slot = a.H;
-  p.K = (int)K;
-  p.xscale = SWIGLU ? a.xscale : a.hs;
-  p.wscale = SWIGLU ? a.wgus : a.wds;
-  p.wscale_rows = SWIGLU ? 2 * a.I / 128 : a.H / 128;
-  p.blk_mul = SWIGLU ? 1 : 2;
-  p.blk_off = SWIGLU ? a.I / 128 : 1;
-  p.out_ld = SWIGLU ? a.I : a.H;
+  p.H = a.H;
+  F8Phase& m1 = p.ph[0];
+  m1.num_kb = a.H / BK;
+  m1.n_tiles = a.I / 128;
+  m1.out_ld = a.I;
+  m1.wscale_rows = 2 * a.I / 128;
+  m1.blk_mul = 1;
+  m1.blk_off = a.I / 128;
+  m1.xscale = a.xscale;
+  m1.wscale = a.wgus;
+  F8Phase& m2 = p.ph[1];
+  m2.num_kb = a.I / BK;
+  m2.n_tiles = a.H / 256;
+  m2.out_ld = a.H;
+  m2.wscale_rows = a.H / 128;
+  m2.blk_mul = 2;
+  m2.blk_off = 1;
+  m2.xscale = a.hs;
+  m2.wscale = a.wds;
   p.hq = a.hq;
   p.hscale = a.hs;
   p.y = a.y;
+  p.sync = a.sync;
   p.status = a.status;
   // upper bound of units (device-side counts unknown here)
-  const int64_t bound = (a.cap / NT + p.nslots) * (int64_t)p.n_tiles;
+  const int64_t bound = (a.cap / NT + p.nslots) * (int64_t)(m1.n_tiles + m2.n_tiles);
   const int grid = (int)(bound < max_ctas ? bound : max_ctas);
-  launch(ffn_fp8_kernel<SWIGLU>, grid, THREADS, f8_smem_bytes<SWIGLU>(), s, mA, mB, p);
+  launch(ffn_fp8_kernel, grid, THREADS, f8_smem_bytes(), s, mA1, mB1, mA2, mB2, p);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 size_t hscale_offset(int64_t cap, int I) { return ((size_t)cap * I + 255) & ~(size_t)255; }
+size_t sync_offset(int64_t cap, int I) {
+  return (hscale_offset(cap, I) + (size_t)cap * (I / 128) + 255) & ~(size_t)255;
+}
 
 }  // namespace
 }  // namespace moe
@@ -542,7 +693,7 @@ using namespace moe;
 
 extern "C" size_t moe_grouped_ffn_fp8_ws_bytes(int64_t cap, int I) {
   if (cap < 0 || I < 128 || I % 128 != 0) return 0;
-  return hscale_offset(cap, I) + (size_t)cap * (I / 128);
+  return sync_offset(cap, I) + sizeof(int32_t) * kSyncWords;
 }
 
 extern "C" moe_status moe_grouped_ffn_fp8(const uint8_t* d_sorted_q,
@@ -590,9 +741,7 @@ extern "C" moe_status moe_grouped_ffn_fp8(const uint8_t* d_sorted_q,
   a.hq = static_cast<uint8_t*>(d_ws);
   a.hs = static_cast<uint8_t*>(d_ws) + hscale_offset(cap, I);
   a.y = static_cast<__nv_bfloat16*>(d_out_sorted);
+  a.sync = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(d_ws) + sync_offset(cap, I));
   a.status = d_status;
-  cudaStream_t s = as_stream(stream);
-  moe_status st = run_f8<true>(a, s);
-  if (st != MOE_OK) return st;
-  return run_f8<false>(a, s);
+  return run_f8(a, as_stream(stream));
 }

@@ -25,7 +25,7 @@ MOE_ERR_DEVICE_INPUT, MOE_ERR_TIMEOUT, MOE_ERR_CUDA, MOE_ERR_UNSUPPORTED = 4, 5,
 MOE_PAD_SUM, MOE_PAD_MAX, MOE_PAD_STATIC = 0, 1, 2
 MOE_F32, MOE_BF16 = 0, 1
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_MAP, MOE_DEV_CAPACITY = 0x1, 0x2, 0x4
-MOE_DEV_TIMEOUT, MOE_DEV_BAD_COUNTS = 0x8, 0x10
+MOE_DEV_TIMEOUT, MOE_DEV_BAD_COUNTS, MOE_DEV_BAD_WORKSPACE = 0x8, 0x10, 0x20
 
 _lock = threading.Lock()
 _lib = None
@@ -474,7 +474,8 @@ class MoeLayer:
                                        device=dev, dtype=torch.uint8)
         ws_ffn = (moe_grouped_ffn_fp8_ws_bytes(self.cap, I) if fp8
                   else moe_grouped_ffn_ws_bytes(self.cap, I, self.dtype))
-        self.ws_ffn = torch.empty(max(ws_ffn, 16), device=dev, dtype=torch.uint8)
+        # zero-filled: the FP8 FFN's scheduler words start at zero
+        self.ws_ffn = torch.zeros(max(ws_ffn, 16), device=dev, dtype=torch.uint8)
         self.router_weight, self.router_bias = router_weight, router_bias
         if router_weight is not None:
             if router_weight.shape != (E, H) or router_weight.dtype != torch.bfloat16:

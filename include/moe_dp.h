@@ -79,6 +79,8 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 #define MOE_DEV_TIMEOUT 0x8u       /* a bounded device wait gave up */
 #define MOE_DEV_BAD_COUNTS 0x10u   /* a replica count exceeds its segment, or an
                                       index points outside its buffer */
+#define MOE_DEV_BAD_WORKSPACE 0x20u /* a grouped-FFN workspace's scheduler words were
+                                        not zero at the call (they are cleared) */
 
 #define MOE_MAX_REPLICAS 256 /* R limit (replica pointers travel as kernel arguments) */
 #define MOE_MAX_SLOTS 1024   /* P limit of the grouped FFN's tile scheduler */
@@ -395,7 +397,11 @@ moe_status moe_dispatch_fp8(const void* d_global, const int32_t* d_ids, int64_t 
                             void* d_ws, size_t ws_bytes, uint32_t* d_status, void* stream);
 
 /* Workspace of moe_grouped_ffn_fp8: the FP8 SwiGLU activation (codes and
- * scale bytes) of cap rows. */
+ * scale bytes) of cap rows, then the scheduler's words: the last
+ * 4 * (3 + MOE_MAX_SLOTS) bytes.  They must be zero before the first call on a
+ * workspace (e.g. a zero-filled allocation); every call leaves them zero.  A
+ * call that finds them otherwise sets MOE_DEV_BAD_WORKSPACE (its output is then
+ * not valid) and clears them.  One call at a time per workspace. */
 size_t moe_grouped_ffn_fp8_ws_bytes(int64_t cap, int I);
 
 /* Grouped SwiGLU FFN on FP8 operands (moe_grouped_ffn's computation): per
@@ -408,7 +414,9 @@ size_t moe_grouped_ffn_fp8_ws_bytes(int64_t cap, int I);
  *   d_w_down_q [P, H, I], d_w_down_scales [P, H/128, I/128]
  *   d_out_sorted  device bf16 [cap, H] out (rows of the slot range)
  * H a multiple of 256, I a multiple of 128; sm_103 only (else
- * MOE_ERR_UNSUPPORTED). */
+ * MOE_ERR_UNSUPPORTED).  Both GEMMs run in one launch: CTAs claim the MM1 units
+ * and then the MM2 units in order, and an MM2 unit waits (bounded, else
+ * MOE_DEV_TIMEOUT) until its slot's h is written. */
 moe_status moe_grouped_ffn_fp8(const uint8_t* d_sorted_q, const uint8_t* d_sorted_scales,
                                const int32_t* d_offsets_P, int P, int slot_lo, int slot_hi,
                                int64_t cap, const uint8_t* d_w_gate_up_q,

@@ -149,7 +149,7 @@ def test_grouped_ffn_fp8(md, orc, counts, lo, hi, H, I):
              _dev_u8(np.stack([w[0] for w in wd])), _dev_u8(np.stack([w[1] for w in wd])))
     sentinel = 1232.0
     ys = torch.full((cap, H), sentinel, device=DEV, dtype=torch.bfloat16)
-    ws = torch.empty(md.moe_grouped_ffn_fp8_ws_bytes(cap, I), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(md.moe_grouped_ffn_fp8_ws_bytes(cap, I), dtype=torch.uint8, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     md.moe_grouped_ffn_fp8(_dev_u8(xq), _dev_u8(xe), torch.from_numpy(offsets).to(DEV), w_fp8, ys,
                            ws, lo, hi, d_status=st)
@@ -170,7 +170,7 @@ def test_grouped_ffn_fp8_dsv3_width(md, orc):
     w_fp8 = (_dev_u8(np.stack([w[0] for w in wgu])), _dev_u8(np.stack([w[1] for w in wgu])),
              _dev_u8(np.stack([w[0] for w in wd])), _dev_u8(np.stack([w[1] for w in wd])))
     ys = torch.zeros((cap, H), device=DEV, dtype=torch.bfloat16)
-    ws = torch.empty(md.moe_grouped_ffn_fp8_ws_bytes(cap, I), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(md.moe_grouped_ffn_fp8_ws_bytes(cap, I), dtype=torch.uint8, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     md.moe_grouped_ffn_fp8(_dev_u8(xq), _dev_u8(xe), torch.from_numpy(offsets).to(DEV), w_fp8, ys,
                            ws, d_status=st)
@@ -180,6 +180,35 @@ def test_grouped_ffn_fp8_dsv3_width(md, orc):
     got = as_f32(to_np(ys)).astype(np.float64)
     assert_close(got[:n], ref[:n], BF16_ATOL, BF16_RTOL, "grouped FFN fp8, DSV3 width")
     assert rel_fro(got[:n], ref[:n]) < 1e-2
+
+
+def test_grouped_ffn_fp8_stale_workspace_flagged_and_cleared(md, orc):
+    """The scheduler words at the end of the workspace start at zero and every call
+    leaves them zero.  A call that finds a stale unit ticket claims no unit, sets
+    MOE_DEV_BAD_WORKSPACE and clears the words; the next call on the same workspace
+    is correct."""
+    counts = [7, 70, 0, 33]
+    H, I = 512, 256
+    offsets, cap, xq, xe, wgu, wd = _fp8_inputs(orc, counts, H, I, seed=11)
+    w_fp8 = (_dev_u8(np.stack([w[0] for w in wgu])), _dev_u8(np.stack([w[1] for w in wgu])),
+             _dev_u8(np.stack([w[0] for w in wd])), _dev_u8(np.stack([w[1] for w in wd])))
+    ws = torch.zeros(md.moe_grouped_ffn_fp8_ws_bytes(cap, I), dtype=torch.uint8, device=DEV)
+    words = ws[-4 * (3 + 1024):].view(torch.int32)        # ticket, done, reserved, per slot
+    words[0] = 1 << 30
+    ys = torch.zeros((cap, H), device=DEV, dtype=torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    args = (_dev_u8(xq), _dev_u8(xe), torch.from_numpy(offsets).to(DEV), w_fp8, ys, ws)
+    md.moe_grouped_ffn_fp8(*args, d_status=st)
+    assert _status(st) == md.MOE_DEV_BAD_WORKSPACE
+    assert not words.any()
+    st.zero_()
+    md.moe_grouped_ffn_fp8(*args, d_status=st)
+    assert _status(st) == 0
+    assert not words.any()
+    n = int(offsets[-1])
+    ref = orc.grouped_ffn_fp8(xq, xe, offsets, lambda s: (*wgu[s], *wd[s]))
+    got = as_f32(to_np(ys)).astype(np.float64)
+    assert_close(got[:n], ref[:n], BF16_ATOL, BF16_RTOL, "grouped FFN fp8 after clearing")
 
 
 # ------------------------------------------------------------------ whole layer
