@@ -27,13 +27,16 @@
 // With few tokens per slot (decode) the weight stream is the whole cost, and
 // FP8 weights halve it.
 //
-// Roles (320 threads, one CTA per SM):
+// Roles (352 threads, one CTA per SM):
 //   warp 0    TMA producer: weight box + token box per stage
 //   warp 1    TMEM allocation; lane 0 issues the MMAs and commits (stage free,
 //             partial ready); partials rotate through four TMEM buffers
 //   warps 2-9 epilogue, two warps per TMEM lane quarter (token columns 0-31 and
 //             32-63): per k-block tcgen05.ld of the partials, release, scale and
 //             accumulate; per unit SwiGLU + quantisation or bf16 out
+//   warp 10   publisher: makes each MM1 unit's h visible to the other CTAs (a
+//             gpu-scope fence, which waits for the stores) and counts it for its
+//             slot, off the epilogue's path
 // The epilogue's work sets the pace once the weight stream is fast enough, so it
 // is kept small: a warp whose columns hold no token of the unit only releases
 // the buffer; the others scale only the columns that hold tokens (in groups of
@@ -59,7 +62,7 @@ using namespace tc;
 constexpr int BK = 128;     // fp8 values per k-block = one 128-byte swizzle row = one scale group
 constexpr int NT = 64;      // tokens per unit
 constexpr int CT = 32;      // token columns per epilogue warp
-constexpr int THREADS = 320;
+constexpr int THREADS = 352;
 constexpr int NPB = 4;      // TMEM partial buffers: the MMAs run up to 4 k-blocks ahead of the epilogue
 
 // tcgen05.wait::ld that also names the destination registers of the load it
@@ -115,6 +118,7 @@ struct F8Smem {
   uint64_t ufull[UQ];   // a claimed unit id is in uring
   uint64_t uempty[UQ];  // the MMA warp and the eight epilogue warps have read it
   int32_t uring[UQ];
+  int32_t h_stored;     // epilogue warps that have stored an MM1 unit's h (8 per unit)
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t last_cta;
@@ -210,14 +214,26 @@ __device__ __forceinline__ void red_release_gpu_add(int32_t* a, int32_t v) {
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+__device__ __forceinline__ int32_t ld_acquire_cta(const int32_t* a) {
+  int32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(a)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_cta_add(int32_t* a, int32_t v) {
+  asm volatile("red.release.cta.shared::cta.add.s32 [%0], %1;" ::"r"(smem_u32(a)), "r"(v)
+               : "memory");
+}
 // Bounded wait of a whole warp until *ctr >= target (acquire); warp-uniform.
-__device__ bool wait_count(const int32_t* ctr, int32_t target, volatile int32_t* abort_flag,
-                           uint32_t* status) {
-  if (__all_sync(0xffffffffu, ld_acquire_gpu(ctr) >= target)) return true;
+template <bool SHARED>
+__device__ bool wait_count_t(const int32_t* ctr, int32_t target, volatile int32_t* abort_flag,
+                             uint32_t* status) {
+  if (__all_sync(0xffffffffu, (SHARED ? ld_acquire_cta(ctr) : ld_acquire_gpu(ctr)) >= target))
+    return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    __nanosleep(100);
-    if (__all_sync(0xffffffffu, ld_acquire_gpu(ctr) >= target)) return true;
+    if (!SHARED) __nanosleep(100);
+    if (__all_sync(0xffffffffu, (SHARED ? ld_acquire_cta(ctr) : ld_acquire_gpu(ctr)) >= target))
+      return true;
     if ((i & 63u) == 0) {
       bool stop = *abort_flag != 0;
       if (!stop && globaltimer_ns() - t0 > kTimeoutNs) {
@@ -230,6 +246,15 @@ __device__ bool wait_count(const int32_t* ctr, int32_t target, volatile int32_t*
       if (__any_sync(0xffffffffu, stop)) return false;
     }
   }
+}
+// a global counter written by other CTAs / a shared counter of this CTA
+__device__ __forceinline__ bool wait_count(const int32_t* ctr, int32_t target,
+                                           volatile int32_t* abort_flag, uint32_t* status) {
+  return wait_count_t<false>(ctr, target, abort_flag, status);
+}
+__device__ __forceinline__ bool wait_count_cta(const int32_t* ctr, int32_t target,
+                                               volatile int32_t* abort_flag, uint32_t* status) {
+  return wait_count_t<true>(ctr, target, abort_flag, status);
 }
 
 // Both GEMMs of the grouped FFN in one persistent launch.  A CTA claims units
@@ -278,6 +303,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 31) L.warp_sums[warp] = x;
     if (threadIdx.x == 0) {
       L.abort_flag = 0;
+      L.h_stored = 0;
       for (int i = 0; i < STAGES; ++i) {
         mbar_init(smem_u32(&L.full[i]), 1);   // the producer's expect_tx
         mbar_init(smem_u32(&L.empty[i]), 1);  // the MMA commit
@@ -288,7 +314,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       for (int i = 0; i < UQ; ++i) {
         mbar_init(smem_u32(&L.ufull[i]), 1);   // the producer
-        mbar_init(smem_u32(&L.uempty[i]), 9);  // the MMA warp + eight epilogue warps
+        mbar_init(smem_u32(&L.uempty[i]), 10);  // MMA, eight epilogue and the publisher warp
       }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -319,7 +345,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem_base = L.tmem_base;
   volatile int32_t* abort_flag = &L.abort_flag;
   int32_t* ready = p.sync + kReady;
-  const int32_t ready_per_group = 2 * p.ph[0].n_tiles;  // column groups x MM1 tiles
+  const int32_t ready_per_group = p.ph[0].n_tiles;  // MM1 units per token group
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -417,7 +443,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!ok) break;
     }
-  } else {
+  } else if (warp < 10) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;          // TMEM lanes 32q .. 32q+31 = weight rows of the tile
     const int cg = (warp - 2) >> 2;  // token columns 32cg .. 32cg+31 of the unit
@@ -544,12 +570,11 @@ __global__ void __launch_bounds__(THREADS, 1)
               p.hscale[row * (P.out_ld / 128) + un.tile] = (uint8_t)(e + 127);
           }
         }
-        // h of this column group is published: visible at gpu scope (and to the
-        // TMA loads of MM2 units) before the slot's count goes up
-        __threadfence();
-        fence_proxy_async_global();
-        named_sync(bar_id, 128);  // also: the maxima are read before the next unit writes them
-        if (q == 0 && lane == 0) red_release_gpu_add(ready + un.slot, 1);
+        // this warp's h is stored; the publisher warp makes it visible to the MM2
+        // units of other CTAs
+        __syncwarp();
+        if (lane == 0) red_release_cta_add(&L.h_stored, 1);
+        named_sync(bar_id, 128);  // the maxima are read before the next unit writes them
       } else {
         const int feat = un.tile * 256 + q * 32 + lane;  // and feat + 128 (second half)
 #pragma unroll
@@ -562,6 +587,29 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
+    }
+  }
+
+  else {
+    // ------------------------------------------------------------ publisher
+    int32_t mm1_units = 0;
+    for (uint32_t qu = 0;; ++qu) {
+      const uint32_t rs = qu % UQ, rph = (qu / UQ) & 1u;
+      if (!wait_bar(smem_u32(&L.ufull[rs]), rph, abort_flag, p.status)) break;
+      const int u = L.uring[rs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&L.uempty[rs]));
+      if (u < 0) break;
+      if (u >= L.total1) continue;  // an MM2 unit publishes nothing
+      const F8Unit un = decode_unit(L, p, u);
+      ++mm1_units;
+      if (!wait_count_cta(&L.h_stored, 8 * mm1_units, abort_flag, p.status)) break;
+      if (lane == 0) {
+        __threadfence();              // the eight warps' h stores, at gpu scope
+        fence_proxy_async_global();   // and for the TMA loads that read them
+        red_release_gpu_add(ready + un.slot, 1);
+      }
+      __syncwarp();
     }
   }
 
