@@ -69,8 +69,8 @@ def ffn_kernel(cap: int, P: int, fp8: bool = False) -> str:
         return "ffn_fp8_kernel"
     return "ffn_swap_kernel" if cap // max(P, 1) >= 192 else "ffn_tc_kernel"
 
-# dram__bytes_read.sum + dram__bytes_write.sum of the two grouped-FFN launches of one
-# step of the default workload (ncu, --clock-control none), valid while the kernel's
+# dram__bytes_read.sum + dram__bytes_write.sum of the grouped-FFN launches (two in bf16,
+# one on FP8) of one step of the workload (ncu, --clock-control none), valid while the kernel's
 # sources hash to the recorded SHA-256 prefix; any other source reports traffic null.
 FFN_TRAFFIC = {
     "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "10e862941fb51ca1",
@@ -78,7 +78,7 @@ FFN_TRAFFIC = {
     "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "205258ea68ec00af",
                 "bytes": 25761555200},
     "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
-                   "sha256_16": "932c697b75c2c4a4", "bytes": 2804173568},
+                   "sha256_16": "48d55c67d6dd9ef4", "bytes": 2789277440},
 }
 
 
