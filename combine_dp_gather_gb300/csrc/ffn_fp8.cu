@@ -27,6 +27,14 @@
 // With few tokens per slot (decode) the weight stream is the whole cost, and
 // FP8 weights halve it.
 //
+// Both GEMMs run in one persistent launch.  The producer of each CTA claims the
+// next unit from a ticket in the workspace (all MM1 units of the call, then all
+// MM2 units, each in slot order) and hands it to the other roles through a
+// four-entry ring in shared memory.  An SM that finishes its last MM1 unit early
+// goes on with MM2 units, so neither GEMM leaves a partly empty last round of
+// SMs.  An MM2 unit reads h, so its producer (and its epilogue, which reads the
+// scale bytes) first waits until every MM1 unit of the slot has been counted.
+//
 // Roles (352 threads, one CTA per SM):
 //   warp 0    TMA producer: weight box + token box per stage
 //   warp 1    TMEM allocation; lane 0 issues the MMAs and commits (stage free,
@@ -45,9 +53,9 @@
 // 2^(e_token + e_weight) depends on the token and on which 128-row half of the
 // tile a row is in, not on the row, so each lane forms its token's two factors
 // once and the warp reads them back from shared memory as broadcasts.
-// Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets
-// MOE_DEV_TIMEOUT, the other roles stop at their next wait, TMEM is freed and
-// the kernel returns.
+// Every wait (mbarriers and slot counts) is bounded (globaltimer); on expiry
+// the kernel sets MOE_DEV_TIMEOUT, the other roles stop at their next wait,
+// TMEM is freed and the kernel returns.
 #include <mutex>
 
 #include "common.cuh"

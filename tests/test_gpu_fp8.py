@@ -211,6 +211,36 @@ def test_grouped_ffn_fp8_stale_workspace_flagged_and_cleared(md, orc):
     assert_close(got[:n], ref[:n], BF16_ATOL, BF16_RTOL, "grouped FFN fp8 after clearing")
 
 
+def test_grouped_ffn_fp8_slot_wait_times_out_and_recovers(md, orc):
+    """An MM2 unit waits, with a time limit, until its slot's MM1 units are counted.
+    A slot count planted far below zero never reaches its target: the waiting CTAs
+    give up after the limit (about 2 s), the call sets MOE_DEV_TIMEOUT (not
+    MOE_DEV_BAD_WORKSPACE), the device stays usable, the scheduler words are
+    cleared, and the next call on the same workspace is correct."""
+    counts = [7, 70, 0, 33]
+    H, I = 512, 256
+    offsets, cap, xq, xe, wgu, wd = _fp8_inputs(orc, counts, H, I, seed=12)
+    w_fp8 = (_dev_u8(np.stack([w[0] for w in wgu])), _dev_u8(np.stack([w[1] for w in wgu])),
+             _dev_u8(np.stack([w[0] for w in wd])), _dev_u8(np.stack([w[1] for w in wd])))
+    ws = torch.zeros(md.moe_grouped_ffn_fp8_ws_bytes(cap, I), dtype=torch.uint8, device=DEV)
+    words = ws[-4 * (3 + 1024):].view(torch.int32)        # ticket, done, reserved, per slot
+    words[3 + 1] = -(1 << 20)                              # slot 1 (70 tokens)
+    ys = torch.zeros((cap, H), device=DEV, dtype=torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    args = (_dev_u8(xq), _dev_u8(xe), torch.from_numpy(offsets).to(DEV), w_fp8, ys, ws)
+    md.moe_grouped_ffn_fp8(*args, d_status=st)
+    code = _status(st)
+    assert code & md.MOE_DEV_TIMEOUT and not code & md.MOE_DEV_BAD_WORKSPACE
+    assert not words.any()
+    st.zero_()
+    md.moe_grouped_ffn_fp8(*args, d_status=st)
+    assert _status(st) == 0
+    n = int(offsets[-1])
+    ref = orc.grouped_ffn_fp8(xq, xe, offsets, lambda s: (*wgu[s], *wd[s]))
+    got = as_f32(to_np(ys)).astype(np.float64)
+    assert_close(got[:n], ref[:n], BF16_ATOL, BF16_RTOL, "grouped FFN fp8 after the timeout")
+
+
 # ------------------------------------------------------------------ whole layer
 def _layer_fp8_check(md, orc, spec, sample=None):
     from combine_dp_gather_gb300 import synth
