@@ -77,6 +77,8 @@ FFN_TRAFFIC = {
                "bytes": 5582041088},
     "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "205258ea68ec00af",
                 "bytes": 25761555200},
+    "eplb": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "10e862941fb51ca1",
+             "bytes": 12737062656},
     "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
                    "sha256_16": "48d55c67d6dd9ef4", "bytes": 2789277440},
 }
