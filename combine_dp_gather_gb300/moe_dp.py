@@ -344,10 +344,20 @@ def moe_grouped_ffn_fp8_ws_bytes(cap: int, I: int) -> int:
     return int(lib().moe_grouped_ffn_fp8_ws_bytes(cap, I))
 
 
+def fp8_ffn_workspace(cap: int, I: int, device="cuda") -> torch.Tensor:
+    """A workspace for moe_grouped_ffn_fp8: zero-filled, as its scheduler words (the
+    last bytes) must be zero before the first call; every call leaves them zero."""
+    n = moe_grouped_ffn_fp8_ws_bytes(cap, I)
+    if n == 0:
+        raise MoeError("moe_grouped_ffn_fp8_ws_bytes", MOE_ERR_INVALID_ARG)
+    return torch.zeros(n, device=device, dtype=torch.uint8)
+
+
 def moe_grouped_ffn_fp8(xq: torch.Tensor, x_scales: torch.Tensor, offsets_P: torch.Tensor,
                         w_fp8, ys: torch.Tensor, ws: torch.Tensor, slot_lo: int = 0,
                         slot_hi: Optional[int] = None, d_status=None, stream=None):
-    """w_fp8 = quantize_expert_weights_fp8(...); ys bf16 [cap, H] out."""
+    """w_fp8 = quantize_expert_weights_fp8(...); ys bf16 [cap, H] out; ws from
+    fp8_ffn_workspace (zero-filled scheduler words, left zero by every call)."""
     guq, gus, dq, ds = w_fp8
     P, I2, H = guq.shape
     slot_hi = P if slot_hi is None else slot_hi
@@ -474,8 +484,8 @@ class MoeLayer:
                                        device=dev, dtype=torch.uint8)
         ws_ffn = (moe_grouped_ffn_fp8_ws_bytes(self.cap, I) if fp8
                   else moe_grouped_ffn_ws_bytes(self.cap, I, self.dtype))
-        # zero-filled: the FP8 FFN's scheduler words start at zero
-        self.ws_ffn = torch.zeros(max(ws_ffn, 16), device=dev, dtype=torch.uint8)
+        self.ws_ffn = (fp8_ffn_workspace(self.cap, I, dev) if fp8 else
+                       torch.empty(max(ws_ffn, 16), device=dev, dtype=torch.uint8))
         self.router_weight, self.router_bias = router_weight, router_bias
         if router_weight is not None:
             if router_weight.shape != (E, H) or router_weight.dtype != torch.bfloat16:

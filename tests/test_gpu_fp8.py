@@ -149,7 +149,7 @@ def test_grouped_ffn_fp8(md, orc, counts, lo, hi, H, I):
              _dev_u8(np.stack([w[0] for w in wd])), _dev_u8(np.stack([w[1] for w in wd])))
     sentinel = 1232.0
     ys = torch.full((cap, H), sentinel, device=DEV, dtype=torch.bfloat16)
-    ws = torch.zeros(md.moe_grouped_ffn_fp8_ws_bytes(cap, I), dtype=torch.uint8, device=DEV)
+    ws = md.fp8_ffn_workspace(cap, I, DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     md.moe_grouped_ffn_fp8(_dev_u8(xq), _dev_u8(xe), torch.from_numpy(offsets).to(DEV), w_fp8, ys,
                            ws, lo, hi, d_status=st)
@@ -170,7 +170,7 @@ def test_grouped_ffn_fp8_dsv3_width(md, orc):
     w_fp8 = (_dev_u8(np.stack([w[0] for w in wgu])), _dev_u8(np.stack([w[1] for w in wgu])),
              _dev_u8(np.stack([w[0] for w in wd])), _dev_u8(np.stack([w[1] for w in wd])))
     ys = torch.zeros((cap, H), device=DEV, dtype=torch.bfloat16)
-    ws = torch.zeros(md.moe_grouped_ffn_fp8_ws_bytes(cap, I), dtype=torch.uint8, device=DEV)
+    ws = md.fp8_ffn_workspace(cap, I, DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     md.moe_grouped_ffn_fp8(_dev_u8(xq), _dev_u8(xe), torch.from_numpy(offsets).to(DEV), w_fp8, ys,
                            ws, d_status=st)
@@ -192,7 +192,7 @@ def test_grouped_ffn_fp8_stale_workspace_flagged_and_cleared(md, orc):
     offsets, cap, xq, xe, wgu, wd = _fp8_inputs(orc, counts, H, I, seed=11)
     w_fp8 = (_dev_u8(np.stack([w[0] for w in wgu])), _dev_u8(np.stack([w[1] for w in wgu])),
              _dev_u8(np.stack([w[0] for w in wd])), _dev_u8(np.stack([w[1] for w in wd])))
-    ws = torch.zeros(md.moe_grouped_ffn_fp8_ws_bytes(cap, I), dtype=torch.uint8, device=DEV)
+    ws = md.fp8_ffn_workspace(cap, I, DEV)
     words = ws[-4 * (3 + 1024):].view(torch.int32)        # ticket, done, reserved, per slot
     words[0] = 1 << 30
     ys = torch.zeros((cap, H), device=DEV, dtype=torch.bfloat16)
@@ -222,7 +222,7 @@ def test_grouped_ffn_fp8_slot_wait_times_out_and_recovers(md, orc):
     offsets, cap, xq, xe, wgu, wd = _fp8_inputs(orc, counts, H, I, seed=12)
     w_fp8 = (_dev_u8(np.stack([w[0] for w in wgu])), _dev_u8(np.stack([w[1] for w in wgu])),
              _dev_u8(np.stack([w[0] for w in wd])), _dev_u8(np.stack([w[1] for w in wd])))
-    ws = torch.zeros(md.moe_grouped_ffn_fp8_ws_bytes(cap, I), dtype=torch.uint8, device=DEV)
+    ws = md.fp8_ffn_workspace(cap, I, DEV)
     words = ws[-4 * (3 + 1024):].view(torch.int32)        # ticket, done, reserved, per slot
     words[3 + 1] = -(1 << 20)                              # slot 1 (70 tokens)
     ys = torch.zeros((cap, H), device=DEV, dtype=torch.bfloat16)
