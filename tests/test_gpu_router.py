@@ -124,3 +124,54 @@ def test_layer_with_router_gate(md, orc):
             y = orc.expert_ffn(x_f[r:r + 1], as_f32(to_np(wgu[e])), as_f32(to_np(wd[e])))[0]
             ref += w_o[r, j] * y
         assert_close(yg[r], ref, 2e-2, 1e-2, f"gate layer row {r}")
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_layer_all_options_together(md, fp8):
+    """The fused boundary (residual add + RMSNorm), the router gate GEMM with its bias
+    and (optionally) the FP8 experts in one layer: the step equals, bit for bit, a
+    layer with the gate GEMM (and FP8) fed the rows the fused boundary normed; the
+    residual holds the exact sum; a graph replay repeats the step."""
+    from combine_dp_gather_gb300 import synth
+    spec = synth.LayerSpec("all_opts", [16, 0, 140, 8, 1], 1, H=512, E=32, k=4, I=256,
+                           dtype="bf16", w_std=0.05, zipf_s=1.1)
+    x_loc = synth.hidden_states(spec, DEV)
+    lg_loc = synth.router_logits(spec, DEV)          # ignored by the gate path
+    wgu, wd = synth.expert_weights(spec, None, DEV)
+    gw, gb = synth.router_gate(spec, DEV)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    res = [torch.randn(c, spec.H, generator=g, device=DEV).to(torch.bfloat16)
+           for c in spec.counts]
+    res0 = [t.clone() for t in res]
+    gamma = (1 + 0.1 * torch.randn(spec.H, generator=g, device=DEV)).to(torch.bfloat16)
+    offs, rows = md.moe_dp_layout(spec.counts, spec.mode)
+    common = dict(R=spec.R, H=spec.H, E=spec.E, k=spec.k, I=spec.I, w_gate_up=wgu, w_down=wd,
+                  max_rows=rows, mode=spec.mode, router_weight=gw, router_bias=gb, fp8=fp8)
+    layer = md.MoeLayer(norm_gamma=gamma, norm_eps=1e-6, **common)
+    out = [torch.empty(c, spec.H, device=DEV, dtype=torch.bfloat16) for c in spec.counts]
+    layer.forward(x_loc, lg_loc, out, counts=spec.counts, local_residual=res)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    for a, b, h in zip(res, res0, x_loc):
+        assert torch.equal(a, (b.float() + h.float()).to(torch.bfloat16))
+    normed = [layer.xg[offs[r]: offs[r] + c].clone() for r, c in enumerate(spec.counts)]
+    plain = md.MoeLayer(**common)
+    out2 = [torch.full_like(t, 7.0) for t in out]
+    plain.forward(normed, lg_loc, out2, counts=spec.counts)
+    torch.cuda.synchronize()
+    assert int(plain.status.item()) == 0
+    for a, b in zip(out2, out):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for t, t0 in zip(res, res0):
+        t.copy_(t0)
+    graph = layer.capture(x_loc, lg_loc, out, local_residual=res)
+    for t, t0 in zip(res, res0):      # the capture's warm-up ran the step once
+        t.copy_(t0)
+    first = [t.clone() for t in out]
+    for t in out:
+        t.fill_(7.0)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    for a, b in zip(first, out):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
