@@ -373,7 +373,7 @@ def run_native(args, rank, world, local_rank):
                                             if pk.get("bf16_tflops_sustained") else None),
                  "peak_source": pk["source"],
                  "algorithmic_bytes": int(ffn_bytes), "algorithmic_flops": int(ffn_flops),
-                 "touched_slots": touched, "ms_per_launch_pair": round(ffn_ms, 4)})
+                 "touched_slots": touched, "ffn_ms_per_step": round(ffn_ms, 4)})
 
     # ---- e2e: same calls, inputs from pinned host memory, outputs back to host
     e2e = None
