@@ -182,6 +182,45 @@ def test_grouped_ffn_fp8_dsv3_width(md, orc):
     assert rel_fro(got[:n], ref[:n]) < 1e-2
 
 
+def test_grouped_ffn_fp8_max_slots_and_ep_ranges(md, orc):
+    """MOE_MAX_SLOTS (1024) slots, tokens in a scattered few (the first and last
+    included, one with two token groups): one call over all slots matches the oracle,
+    and sixteen calls over 64-slot ranges (as EP ranks would) on the same workspace
+    give the same bits."""
+    P, H, I = 1024, 256, 128
+    rng = np.random.default_rng(21)
+    counts = [0] * P
+    for s_ in [0, 1, 77, 300, 511, 512, 640, 1000, 1023]:
+        counts[s_] = int(rng.integers(1, 40))
+    counts[512] = 90
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    cap = int(offsets[-1]) + 24
+    x = rng.standard_normal((cap, H)).astype(np.float32)
+    xq, xe = orc.quant_groups(x)
+    wgu1 = orc.quant_blocks(rng.standard_normal((2 * I, H)) * 0.05)
+    wd1 = orc.quant_blocks(rng.standard_normal((H, I)) * 0.05)
+    wgu2 = orc.quant_blocks(rng.standard_normal((2 * I, H)) * 0.05)
+    wd2 = orc.quant_blocks(rng.standard_normal((H, I)) * 0.05)
+    pick = lambda s_: (wgu1, wd1) if s_ % 2 == 0 else (wgu2, wd2)     # two weight sets
+    w_fp8 = tuple(_dev_u8(np.stack([pick(s_)[j][i] for s_ in range(P)]))
+                  for j, i in [(0, 0), (0, 1), (1, 0), (1, 1)])
+    ws = md.fp8_ffn_workspace(cap, I, DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    args = (_dev_u8(xq), _dev_u8(xe), torch.from_numpy(offsets).to(DEV), w_fp8)
+    ys_a = torch.zeros((cap, H), device=DEV, dtype=torch.bfloat16)
+    md.moe_grouped_ffn_fp8(*args, ys_a, ws, d_status=st)
+    assert _status(st) == 0
+    ys_b = torch.zeros((cap, H), device=DEV, dtype=torch.bfloat16)
+    for lo in range(0, P, 64):
+        md.moe_grouped_ffn_fp8(*args, ys_b, ws, lo, lo + 64, d_status=st)
+    assert _status(st) == 0
+    n = int(offsets[-1])
+    assert torch.equal(ys_a[:n].view(torch.int16), ys_b[:n].view(torch.int16))
+    ref = orc.grouped_ffn_fp8(xq, xe, offsets, lambda s_: (*pick(s_)[0], *pick(s_)[1]))
+    got = as_f32(to_np(ys_a)).astype(np.float64)
+    assert_close(got[:n], ref[:n], BF16_ATOL, BF16_RTOL, "grouped FFN fp8, 1024 slots")
+
+
 def test_grouped_ffn_fp8_stale_workspace_flagged_and_cleared(md, orc):
     """The scheduler words at the end of the workspace start at zero and every call
     leaves them zero.  A call that finds a stale unit ticket claims no unit, sets
