@@ -281,16 +281,18 @@ def test_grouped_ffn_fp8_slot_wait_times_out_and_recovers(md, orc):
 
 
 # ------------------------------------------------------------------ whole layer
-def _layer_fp8_check(md, orc, spec, sample=None):
+def _layer_fp8_check(md, orc, spec, sample=None, l2p_np=None, nrep_np=None, p2l=None):
     from combine_dp_gather_gb300 import synth
     x_loc = synth.hidden_states(spec, DEV)
     lg_loc = synth.router_logits(spec, DEV)
-    wgu, wd = synth.expert_weights(spec, None, DEV)
+    wgu, wd = synth.expert_weights(spec, p2l, DEV)
     offs, rows = md.moe_dp_layout(spec.counts, spec.mode, spec.static_bound, spec.tokens_per_req)
+    l2p = None if l2p_np is None else torch.from_numpy(l2p_np).to(DEV)
+    nrep = None if nrep_np is None else torch.from_numpy(nrep_np).to(DEV)
     layer = md.MoeLayer(R=spec.R, H=spec.H, E=spec.E, k=spec.k, I=spec.I, w_gate_up=wgu,
                         w_down=wd, max_rows=max(rows, 1), mode=spec.mode,
                         renormalize=spec.renormalize, n_shared=spec.n_shared, fp8=True,
-                        keep_global=True)
+                        keep_global=True, l2p=l2p, nrep=nrep)
     out = [torch.empty(c, spec.H, device=DEV, dtype=wgu.dtype) for c in spec.counts]
     layer.forward(x_loc, lg_loc, out, counts=spec.counts)
     assert _status(layer.status) == 0
@@ -301,8 +303,8 @@ def _layer_fp8_check(md, orc, spec, sample=None):
     ids_o, w_o = orc.route_topk(lg_o, spec.k, spec.renormalize, valid, spec.n_shared)
     kk = spec.k + spec.n_shared
     assert np.array_equal(to_np(layer.ids[:rows]), ids_o)
-    c_o, o_o, p_o, i_o = orc.dispatch(ids_o, spec.E + spec.n_shared, layer.P, None, None, 1,
-                                      layer.cap)
+    c_o, o_o, p_o, i_o = orc.dispatch(ids_o, spec.E + spec.n_shared, layer.P, l2p_np, nrep_np,
+                                      1, layer.cap)
     n = int(o_o[-1])
     assert np.array_equal(to_np(layer.offsets_P), o_o)
     assert np.array_equal(to_np(layer.inv[:rows]), i_o)
@@ -356,6 +358,22 @@ def test_layer_fp8_tiny_all_rows(md, orc, mode):
 def test_layer_fp8_dsv3_decode(md, orc):
     from combine_dp_gather_gb300 import synth
     _layer_fp8_check(md, orc, synth.spec_decode(seed=0), sample=6)
+
+
+def test_layer_fp8_eplb_full_size(md, orc):
+    """The EPLB workload on the FP8 path: 256 logical experts on 288 slots through the
+    map, hot slots with up to ~1000 rows (16 token groups per weight tile)."""
+    from combine_dp_gather_gb300 import synth
+    spec = synth.spec_eplb()
+    l2p, nrep, p2l = synth.make_map(spec)
+    _layer_fp8_check(md, orc, spec, sample=6, l2p_np=l2p, nrep_np=nrep, p2l=p2l)
+
+
+def test_layer_fp8_prefill_full_size(md, orc):
+    """The prefill workload (8192 tokens, ~256 rows per slot: four token groups per
+    weight tile) on the FP8 path."""
+    from combine_dp_gather_gb300 import synth
+    _layer_fp8_check(md, orc, synth.spec_prefill(), sample=4)
 
 
 def test_layer_fp8_with_shared_expert(md, orc):
