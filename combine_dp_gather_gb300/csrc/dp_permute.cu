@@ -12,7 +12,12 @@
 // at once (one memory round trip per segment); replica pointers travel by
 // value in the kernel arguments, counts and offsets are read once per block
 // into shared memory.
+//
+// The gather can also route its rows on the way (moe_dp_gather_route): one
+// warp per global row takes the top-k of the row's router logits straight from
+// its replica (route_row.cuh), so the routing needs no launch of its own.
 #include "common.cuh"
+#include "route_row.cuh"
 
 namespace moe {
 namespace {
@@ -55,13 +60,25 @@ struct GatherPlane {
   uint4* global;
 };
 
+// Routing of the gathered rows from the replicas' router logits (float32
+// [counts[r], E] per replica) into ids / w [rows, k + n_shared].
+struct RoutePlan {
+  ReplicaPtrs src;
+  int E, k, n_shared, renorm;
+  int32_t* ids;
+  float* w;
+};
+
 // Items are (global row, segment) over the segments of plane a then plane b,
 // so one launch gathers two row tensors of the same replicas (hidden states
-// and router logits) with the same per-row replica lookup.
+// and router logits) with the same per-row replica lookup.  With EPL > 0 the
+// first `rows` items are the rows' routing (one warp each; EPL experts per lane).
+template <int EPL>
 __global__ void __launch_bounds__(kWarps * 32)
     dp_gather_kernel(const __grid_constant__ GatherPlane a, const __grid_constant__ GatherPlane b,
-                     const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
-                     int R, int64_t rows, uint32_t* status) {
+                     const __grid_constant__ RoutePlan rt, const int32_t* __restrict__ counts,
+                     const int32_t* __restrict__ offsets, int R, int64_t rows,
+                     uint32_t* status) {
   grid_dep_wait();    // earlier kernels on the stream are complete
   grid_dep_launch();  // the next kernel may start its launch
   __shared__ int32_t s_off[MOE_MAX_REPLICAS + 1];
@@ -76,10 +93,35 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int64_t nwarps = (int64_t)gridDim.x * kWarps;
   const int segs_a = (a.vpr + kSegVecs - 1) / kSegVecs;
   const int segs = segs_a + (b.vpr + kSegVecs - 1) / kSegVecs;
-  const int64_t items = rows * segs;
+  const int64_t route_items = EPL > 0 ? rows : 0;
+  const int64_t items = route_items + rows * segs;
   for (int64_t w = warp0; w < items; w += nwarps) {
-    const int64_t g = w / segs;
-    const int j = (int)(w - g * segs);
+    if (EPL > 0 && w < route_items) {
+      const int64_t g = w;
+      const int r = find_segment(s_off, R, g);
+      const int64_t i = g - s_off[r];
+      const int64_t seg = (int64_t)s_off[r + 1] - s_off[r];
+      int64_t c = s_cnt[r];
+      if (c > seg) {
+        if (i == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
+        c = seg;
+      }
+      if (c > 0 && rt.src.p[r] == nullptr) {
+        if (i == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
+        c = 0;
+      }
+      const int kk = rt.k + rt.n_shared;
+      if (i >= 0 && i < c)
+        route_row<(EPL > 0 ? EPL : 1)>(static_cast<const float*>(rt.src.p[r]) + i * rt.E, rt.E,
+                                       rt.k, rt.n_shared, rt.renorm, rt.ids + g * kk,
+                                       rt.w + g * kk, lane);
+      else
+        route_pad_row(kk, rt.ids + g * kk, rt.w + g * kk, lane);
+      continue;
+    }
+    const int64_t wi = w - route_items;
+    const int64_t g = wi / segs;
+    const int j = (int)(wi - g * segs);
     const GatherPlane& pl = j < segs_a ? a : b;
     const int v0 = (j < segs_a ? j : j - segs_a) * kSegVecs;
     int r = find_segment(s_off, R, g);
@@ -296,12 +338,16 @@ bool make_plane(const void* const* local, int R, int H, int dtype, void* d_globa
   return true;
 }
 
-int grid_for_rows(int64_t rows, int vpr, int vpr2 = 0) {
-  const int64_t items =
-      rows * ((vpr + kSegVecs - 1) / kSegVecs + (vpr2 + kSegVecs - 1) / kSegVecs);
+int segments(int vpr) { return (vpr + kSegVecs - 1) / kSegVecs; }
+
+int grid_for_items(int64_t items) {
   int64_t want = (items + kWarps - 1) / kWarps;
   int64_t cap = (int64_t)num_sms() * 8;
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+int grid_for_rows(int64_t rows, int vpr, int vpr2 = 0) {
+  return grid_for_items(rows * (segments(vpr) + segments(vpr2)));
 }
 
 }  // namespace
@@ -318,8 +364,8 @@ extern "C" moe_status moe_dp_gather(const void* const* local, const int32_t* d_c
   if (!make_plane(local, R, H, dtype, d_global, &a)) return MOE_ERR_INVALID_ARG;
   b.vpr = 0;
   b.global = nullptr;
-  launch(dp_gather_kernel, grid_for_rows(rows, a.vpr), kWarps * 32, 0, as_stream(stream), a, b,
-         d_counts, d_offsets, R, rows, d_status);
+  launch(dp_gather_kernel<0>, grid_for_rows(rows, a.vpr), kWarps * 32, 0, as_stream(stream), a,
+         b, RoutePlan{}, d_counts, d_offsets, R, rows, d_status);
   return launch_status();
 }
 
@@ -336,8 +382,77 @@ extern "C" moe_status moe_dp_gather2(const void* const* local_a, int H_a, int dt
   if (!make_plane(local_a, R, H_a, dtype_a, d_global_a, &a) ||
       !make_plane(local_b, R, H_b, dtype_b, d_global_b, &b))
     return MOE_ERR_INVALID_ARG;
-  launch(dp_gather_kernel, grid_for_rows(rows, a.vpr, b.vpr), kWarps * 32, 0, as_stream(stream), a,
-         b, d_counts, d_offsets, R, rows, d_status);
+  launch(dp_gather_kernel<0>, grid_for_rows(rows, a.vpr, b.vpr), kWarps * 32, 0,
+         as_stream(stream), a, b, RoutePlan{}, d_counts, d_offsets, R, rows, d_status);
+  return launch_status();
+}
+
+extern "C" moe_status moe_dp_gather_route(const void* const* local_x, int H, int dtype,
+                                          void* d_global_x, const void* const* local_logits, int E,
+                                          void* d_global_logits, int k, int renormalize,
+                                          int n_shared, const int32_t* d_counts,
+                                          const int32_t* d_offsets, int R, int64_t rows,
+                                          int32_t* d_ids, float* d_w, uint32_t* d_status,
+                                          void* stream) {
+  moe_status st = check_common(d_counts, d_offsets, R, rows, H, dtype, d_global_x);
+  if (st != MOE_OK) return st;
+  if (E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E || n_shared < 0 ||
+      k + n_shared > MOE_MAX_TOPK)
+    return MOE_ERR_INVALID_ARG;
+  if (d_global_logits != nullptr) {
+    st = check_common(d_counts, d_offsets, R, rows, E, MOE_F32, d_global_logits);
+    if (st != MOE_OK) return st;
+  }
+  if (rows == 0) return MOE_OK;
+  if (local_logits == nullptr || d_ids == nullptr || d_w == nullptr) return MOE_ERR_INVALID_ARG;
+  GatherPlane a, b;
+  if (!make_plane(local_x, R, H, dtype, d_global_x, &a)) return MOE_ERR_INVALID_ARG;
+  if (d_global_logits != nullptr) {
+    if (!make_plane(local_logits, R, E, MOE_F32, d_global_logits, &b)) return MOE_ERR_INVALID_ARG;
+  } else {
+    b.vpr = 0;
+    b.global = nullptr;
+  }
+  RoutePlan rt;
+  for (int r = 0; r < R; ++r) {
+    if (reinterpret_cast<uintptr_t>(local_logits[r]) % alignof(float) != 0)
+      return MOE_ERR_INVALID_ARG;
+    rt.src.p[r] = local_logits[r];
+  }
+  rt.E = E;
+  rt.k = k;
+  rt.n_shared = n_shared;
+  rt.renorm = renormalize != 0;
+  rt.ids = d_ids;
+  rt.w = d_w;
+  const int grid = grid_for_items(rows * (1 + segments(a.vpr) + segments(b.vpr)));
+  cudaStream_t s = as_stream(stream);
+  switch (route_epl(E)) {
+    case 1:
+      launch(dp_gather_kernel<1>, grid, kWarps * 32, 0, s, a, b, rt, d_counts, d_offsets, R, rows,
+             d_status);
+      break;
+    case 2:
+      launch(dp_gather_kernel<2>, grid, kWarps * 32, 0, s, a, b, rt, d_counts, d_offsets, R, rows,
+             d_status);
+      break;
+    case 4:
+      launch(dp_gather_kernel<4>, grid, kWarps * 32, 0, s, a, b, rt, d_counts, d_offsets, R, rows,
+             d_status);
+      break;
+    case 8:
+      launch(dp_gather_kernel<8>, grid, kWarps * 32, 0, s, a, b, rt, d_counts, d_offsets, R, rows,
+             d_status);
+      break;
+    case 16:
+      launch(dp_gather_kernel<16>, grid, kWarps * 32, 0, s, a, b, rt, d_counts, d_offsets, R,
+             rows, d_status);
+      break;
+    default:
+      launch(dp_gather_kernel<32>, grid, kWarps * 32, 0, s, a, b, rt, d_counts, d_offsets, R,
+             rows, d_status);
+      break;
+  }
   return launch_status();
 }
 

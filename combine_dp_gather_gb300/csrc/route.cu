@@ -13,13 +13,8 @@
 // of every real row with weight 1, so dispatch, the grouped FFN and combine
 // treat it as one more slot.
 //
-// Design: one warp per row.  Lane l holds experts l, l+32, ... (coalesced
-// 128-byte loads); k rounds of a warp arg-max on (logit desc, id asc) pick
-// the experts; lane j keeps the j-th pick; the weights use expf in float32
-// and sum in pick order.
-#include <float.h>
-
-#include "common.cuh"
+// Design: one warp per row (route_row.cuh).
+#include "route_row.cuh"
 
 namespace moe {
 namespace {
@@ -55,72 +50,10 @@ __global__ void __launch_bounds__(kWarps * 32)
       c = seg;
     }
     if (!(i >= 0 && i < c)) {
-      if (lane < kk) {
-        ids[g * kk + lane] = -1;
-        w[g * kk + lane] = 0.f;
-      }
+      route_pad_row(kk, ids + g * kk, w + g * kk, lane);
       continue;
     }
-    const float* lr = logits + g * E;
-    float v[EPL];
-#pragma unroll
-    for (int t = 0; t < EPL; ++t) {
-      int e = lane + 32 * t;
-      v[t] = e < E ? lr[e] : -FLT_MAX;
-    }
-    uint32_t taken = 0;
-    float my_val = 0.f;
-    int my_id = -1;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = INT32_MAX;
-#pragma unroll
-      for (int t = 0; t < EPL; ++t) {
-        int e = lane + 32 * t;
-        bool cand = e < E && !((taken >> t) & 1u);
-        if (cand && (v[t] > bv || (v[t] == bv && e < bi))) {
-          bv = v[t];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
-      if (lane == j) {
-        my_val = bv;
-        my_id = bi;
-      }
-    }
-    const float top = __shfl_sync(0xffffffffu, my_val, 0);
-    float ex = lane < k ? expf(my_val - top) : 0.f;
-    float denom = 0.f;
-    if (renorm) {
-      for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
-    } else {
-      float part = 0.f;
-#pragma unroll
-      for (int t = 0; t < EPL; ++t) {
-        int e = lane + 32 * t;
-        if (e < E) part += expf(v[t] - top);
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-      denom = part;
-    }
-    if (lane < k) {
-      ids[g * kk + lane] = my_id;
-      w[g * kk + lane] = ex / denom;
-    } else if (lane < kk) {  // shared experts: always selected, weight 1
-      ids[g * kk + lane] = E + (lane - k);
-      w[g * kk + lane] = 1.f;
-    }
+    route_row<EPL>(logits + g * E, E, k, n_shared, renorm, ids + g * kk, w + g * kk, lane);
   }
 }
 

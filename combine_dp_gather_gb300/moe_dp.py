@@ -56,6 +56,8 @@ _SIGS = {
     "moe_route_topk_shared": (_I, [_P, _I64, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]),
     "moe_dp_gather_add_rmsnorm": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _I, _I64, _I, _I, _P,
                                        _P, _P]),
+    "moe_dp_gather_route": (_I, [_P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _P, _P, _I, _I64, _P,
+                                 _P, _P, _P]),
     "moe_dp_gather_add_rmsnorm2": (_I, [_P, _P, _P, ctypes.c_float, _P, _I, _I, _P, _P, _P, _I,
                                         _I64, _I, _I, _P, _P, _P]),
     "moe_dispatch_noalloc": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _I, _I, _I64, _P,
@@ -200,6 +202,26 @@ def moe_dp_gather2(local_a: Sequence[torch.Tensor], local_b: Sequence[torch.Tens
         ctypes.cast(pa, _P), out_a.shape[1], dtype_code(out_a.dtype), _ptr(out_a),
         ctypes.cast(pb, _P), out_b.shape[1], dtype_code(out_b.dtype), _ptr(out_b),
         _ptr(d_counts), _ptr(d_offsets), R, out_a.shape[0], _ptr(d_status), _stream(stream)))
+
+
+def moe_dp_gather_route(local_x: Sequence[torch.Tensor], local_logits: Sequence[torch.Tensor],
+                        d_counts, d_offsets, out_x: torch.Tensor, k: int, renormalize: bool,
+                        ids: torch.Tensor, w: torch.Tensor, out_logits=None, n_shared: int = 0,
+                        d_status=None, stream=None):
+    """DP gather of the hidden states and top-k routing of the gathered rows (from
+    the replicas' float32 logits) in one launch; out_logits optionally receives the
+    gathered logits."""
+    R = len(local_x)
+    if len(local_logits) != R:
+        raise MoeError("moe_dp_gather_route", MOE_ERR_INVALID_ARG)
+    E = int(local_logits[0].shape[1]) if local_logits[0].dim() == 2 else 0
+    px = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_x])
+    pl = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_logits])
+    _check("moe_dp_gather_route", lib().moe_dp_gather_route(
+        ctypes.cast(px, _P), out_x.shape[1], dtype_code(out_x.dtype), _ptr(out_x),
+        ctypes.cast(pl, _P), E, _ptr(out_logits), k, int(renormalize), n_shared,
+        _ptr(d_counts), _ptr(d_offsets), R, out_x.shape[0], _ptr(ids), _ptr(w), _ptr(d_status),
+        _stream(stream)))
 
 
 def moe_dp_gather_add_rmsnorm(local_hidden: Sequence[torch.Tensor],
@@ -552,15 +574,16 @@ class MoeLayer:
                                       self.d_counts, self.d_offsets, xg, st, stream,
                                       local_b=local_logits if gathered else None,
                                       out_b=lg if gathered else None)
-        elif self.router_weight is None:  # hidden states and logits in one launch
-            moe_dp_gather2(local_x, local_logits, self.d_counts, self.d_offsets, xg, lg, st,
-                           stream)
+        elif self.router_weight is None:  # the gather routes its rows in the same launch
+            moe_dp_gather_route(local_x, local_logits, self.d_counts, self.d_offsets, xg, self.k,
+                                self.renormalize, ids, w, None, self.n_shared, st, stream)
         else:
             moe_dp_gather(local_x, self.d_counts, self.d_offsets, xg, st, stream)
         ev("gather")
         if self.router_weight is None:
-            moe_route_topk(lg, self.k, self.renormalize, self.d_counts, self.d_offsets, ids, w,
-                           st, stream, n_shared=self.n_shared)
+            if local_residual is not None:
+                moe_route_topk(lg, self.k, self.renormalize, self.d_counts, self.d_offsets, ids,
+                               w, st, stream, n_shared=self.n_shared)
         else:
             moe_route_gemm_topk(xg, self.router_weight, self.k, self.renormalize, self.d_counts,
                                 self.d_offsets, ids, w, self.ws_router, None, st, stream,

@@ -162,6 +162,23 @@ moe_status moe_dp_gather2(const void* const* local_a, int H_a, int dtype_a, void
                           const int32_t* d_counts, const int32_t* d_offsets, int R, int64_t rows,
                           uint32_t* d_status, void* stream);
 
+/* moe_dp_gather of the hidden states with the top-k routing of the gathered
+ * rows in the same launch: for every global row the result of moe_dp_gather
+ * (into d_global_x) and of moe_route_topk_shared on the row's router logits
+ * (into d_ids / d_w), both bit for bit.  The routing reads each real row's
+ * logits from its replica (local_logits[r] is float32 [counts[r], E]), so
+ * they need not be gathered; with d_global_logits != NULL they are also
+ * gathered there (float32 [rows, E], E a multiple of 4).
+ *   local_x, H, dtype, d_global_x   as moe_dp_gather
+ *   E, k, renormalize, n_shared     as moe_route_topk_shared
+ *   d_ids int32 / d_w float32 [rows, k + n_shared] out
+ * Argument checks and device errors are those of the two entry points. */
+moe_status moe_dp_gather_route(const void* const* local_x, int H, int dtype, void* d_global_x,
+                               const void* const* local_logits, int E, void* d_global_logits,
+                               int k, int renormalize, int n_shared, const int32_t* d_counts,
+                               const int32_t* d_offsets, int R, int64_t rows, int32_t* d_ids,
+                               float* d_w, uint32_t* d_status, void* stream);
+
 /* Residual add + RMSNorm fused ahead of the DP gather.  [P1] section
  * "边界判定的融合" (_reduce_update_read_dp_gather): the attention output is added
  * into the residual ("update", written back in place) and the FFN input is read

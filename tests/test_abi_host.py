@@ -162,6 +162,36 @@ def test_gather2_and_combine_scatter_reject_bad_args(md):
     assert c(a3=0) == md.MOE_OK
 
 
+def test_gather_route_rejects_bad_args(md):
+    L = md.lib()
+    two = _ptrs(0x2000, 0x3000)
+    E_ARG, E_UNS = md.MOE_ERR_INVALID_ARG, md.MOE_ERR_UNSUPPORTED
+
+    def call(**kw):
+        a = dict(lx=two, H=64, dt=1, gx=FAKE, ll=two, E=256, gl=NULL, k=8, rn=1, ns=0,
+                 cnt=FAKE, off=FAKE, R=2, rows=8, ids=FAKE, w=FAKE)
+        a.update(kw)
+        return L.moe_dp_gather_route(a["lx"], a["H"], a["dt"], a["gx"], a["ll"], a["E"],
+                                     a["gl"], a["k"], a["rn"], a["ns"], a["cnt"], a["off"],
+                                     a["R"], a["rows"], a["ids"], a["w"], NULL, NULL)
+
+    assert call(k=0) == E_ARG
+    assert call(k=300) == E_ARG                          # k > E
+    assert call(E=2000) == E_ARG                         # E > MOE_MAX_EXPERTS
+    assert call(ns=-1) == E_ARG
+    assert call(k=30, ns=3) == E_ARG                     # k + n_shared > MOE_MAX_TOPK
+    assert call(ll=NULL) == E_ARG
+    assert call(ids=NULL) == E_ARG
+    assert call(w=NULL) == E_ARG
+    assert call(ll=_ptrs(0x2000, 0x3002)) == E_ARG      # logits not float-aligned
+    assert call(gl=MISAL) == E_ARG                       # misaligned gathered logits
+    assert call(E=30, gl=FAKE) == E_ARG                  # 120-byte rows cannot be gathered
+    assert call(gx=MISAL) == E_ARG
+    assert call(H=3) == E_ARG                            # 6-byte rows
+    assert call(dt=7) == E_UNS
+    assert call(rows=0) == md.MOE_OK                     # nothing to do
+
+
 def test_gather_add_rmsnorm_rejects_bad_args(md):
     L = md.lib()
     two = _ptrs(0x2000, 0x3000)

@@ -203,6 +203,52 @@ def test_route_topk(md, orc, E, k, renorm):
     assert_close(to_np(w), w_o, W_ATOL, W_RTOL, "route weights")
 
 
+@pytest.mark.parametrize("E,k,n_shared,mode", [(256, 8, 0, 1), (256, 8, 1, 0), (8, 2, 0, 2),
+                                                (300, 6, 0, 1), (32, 32, 0, 0), (1024, 4, 2, 1),
+                                                (30, 3, 0, 1)])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_gather_route_bitexact(md, orc, E, k, n_shared, mode, renorm):
+    """The gather that routes its rows in the same launch equals moe_dp_gather2 +
+    moe_route_topk_shared bit for bit (hidden states, logits when gathered, ids and
+    weights), and the oracle's gather and top-k; E = 30 cannot gather its 120-byte
+    logit rows and routes without them."""
+    rng = np.random.default_rng(E + k + mode)
+    R, B, H = 9, 40, 512
+    counts = [int(v) for v in rng.choice([0, 1, 7, 33, 40], size=R)]
+    counts[1] = 0
+    g = torch.Generator(device=DEV).manual_seed(E * 3 + k)
+    xs = [torch.randn(c, H, generator=g, device=DEV).to(torch.bfloat16) for c in counts]
+    ls = [torch.randn(c, E, generator=g, device=DEV) for c in counts]
+    for t in ls:
+        t[::3] = torch.round(t[::3] * 2) / 2               # many exact ties
+    offs, rows = md.moe_dp_layout(counts, mode, B, 1)
+    offs_o, rows_o = orc.dp_layout(counts, mode, B, 1)
+    d_c, d_o = dev_i32(counts), dev_i32(offs)
+    kk = k + n_shared
+    gather_logits = E * 4 % 16 == 0
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    xg = torch.full((rows, H), 3.0, device=DEV, dtype=torch.bfloat16)
+    lg = torch.full((rows, E), 3.0, device=DEV) if gather_logits else None
+    ids = torch.full((rows, kk), -7, dtype=torch.int32, device=DEV)
+    w = torch.full((rows, kk), 9.0, device=DEV)
+    md.moe_dp_gather_route(xs, ls, d_c, d_o, xg, k, renorm, ids, w, lg, n_shared, st)
+    assert status_of(st) == 0
+    assert np.array_equal(to_np(xg), orc.dp_gather([to_np(t) for t in xs], counts, offs_o, rows_o))
+    lg_o = orc.dp_gather([to_np(t) for t in ls], counts, offs_o, rows_o)
+    if gather_logits:
+        assert np.array_equal(to_np(lg), lg_o)
+    valid = orc.valid_rows(counts, offs_o, rows_o)
+    ids_o, w_o = orc.route_topk(lg_o, k, renorm, valid, n_shared)
+    assert np.array_equal(to_np(ids), ids_o)
+    assert_close(to_np(w), w_o, W_ATOL, W_RTOL, "route weights")
+    # the same bits as the two separate kernels
+    ids2, w2 = torch.empty_like(ids), torch.empty_like(w)
+    md.moe_route_topk(torch.from_numpy(lg_o).to(DEV), k, renorm, d_c, d_o, ids2, w2, st,
+                      n_shared=n_shared)
+    assert status_of(st) == 0
+    assert torch.equal(ids, ids2) and torch.equal(w.view(torch.int32), w2.view(torch.int32))
+
+
 # ------------------------------------------------------------------ dispatch
 def _distinct_ids(rows, k, E, seed, pad_every=7):
     g = torch.Generator(device=DEV).manual_seed(seed)
