@@ -43,11 +43,9 @@ UNIT = "tokens/s"
 L2_NOTE = "inputs larger than L2: every step streams the touched experts' weights from HBM"
 
 def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
-                      fp8: bool = False, router_gemm: bool = False, sms: int = 152,
-                      addnorm: bool = False) -> int:
+                      fp8: bool = False, router_gemm: bool = False, sms: int = 152) -> int:
     """Kernel launches of one layer step: gather (with given logits it routes the rows
-    in the same launch; the fused add + RMSNorm gathers the logits and a routing
-    launch follows), dispatch (one CTA-wide kernel for <= 8192 routed pairs whose tables
+    in the same launch, the fused add + RMSNorm included), dispatch (one CTA-wide kernel for <= 8192 routed pairs whose tables
     fit 48 KB, else histogram + scan + rank; then the row copy; + the alignment pad
     kernel when align > 1, plus the FP8 rows' pad kernel on the FP8 path), grouped FFN
     (MM1+SwiGLU and MM2; one persistent launch for both on FP8), combine with the DP
@@ -56,7 +54,7 @@ def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
     or split GEMM + sum + top-k."""
     small = rows * k <= 8192 and 4 * (33 * E + 3 * P + 1) <= 48 * 1024
     dispatch = (1 if small else 3) + 1 + (1 + (1 if fp8 else 0) if align > 1 else 0)
-    gather, route = 1, (1 if addnorm else 0)
+    gather, route = 1, 0
     if router_gemm:
         gather = 1
         route = 1 if (k <= 8 and 4 * ((rows + 127) // 128) >= sms) else 3
@@ -488,8 +486,7 @@ def run_native(args, rank, world, local_rank):
                 launches=launches_per_step(max(rows, 1), spec.k + spec.n_shared,
                                            spec.E + spec.n_shared, layer.P, layer.cap,
                                            spec.align, args.fp8, args.router == "gemm",
-                                           torch.cuda.get_device_properties(dev).multi_processor_count,
-                                           args.boundary == "addnorm"),
+                                           torch.cuda.get_device_properties(dev).multi_processor_count),
                 inputs=(x_loc, lg_loc, wgu, wd, l2p_np, nrep_np), gate=gate_np)
 
 

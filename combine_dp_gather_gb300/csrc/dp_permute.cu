@@ -69,6 +69,24 @@ struct RoutePlan {
   float* w;
 };
 
+// Routing of global row g (row i of replica r, whose first c rows are real) by
+// one warp; rows of a replica without a logits pointer are flagged and padded.
+template <int EPL>
+__device__ __forceinline__ void route_global_row(const RoutePlan& rt, int r, int64_t i, int64_t c,
+                                                 int64_t g, int lane, uint32_t* status) {
+  const int kk = rt.k + rt.n_shared;
+  bool real = i >= 0 && i < c;
+  if (real && rt.src.p[r] == nullptr) {
+    if (i == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
+    real = false;
+  }
+  if (real)
+    route_row<(EPL > 0 ? EPL : 1)>(static_cast<const float*>(rt.src.p[r]) + i * rt.E, rt.E, rt.k,
+                                   rt.n_shared, rt.renorm, rt.ids + g * kk, rt.w + g * kk, lane);
+  else
+    route_pad_row(kk, rt.ids + g * kk, rt.w + g * kk, lane);
+}
+
 // Items are (global row, segment) over the segments of plane a then plane b,
 // so one launch gathers two row tensors of the same replicas (hidden states
 // and router logits) with the same per-row replica lookup.  With EPL > 0 the
@@ -106,17 +124,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         if (i == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
         c = seg;
       }
-      if (c > 0 && rt.src.p[r] == nullptr) {
-        if (i == 0 && lane == 0) flag(status, MOE_DEV_BAD_COUNTS);
-        c = 0;
-      }
-      const int kk = rt.k + rt.n_shared;
-      if (i >= 0 && i < c)
-        route_row<(EPL > 0 ? EPL : 1)>(static_cast<const float*>(rt.src.p[r]) + i * rt.E, rt.E,
-                                       rt.k, rt.n_shared, rt.renorm, rt.ids + g * kk,
-                                       rt.w + g * kk, lane);
-      else
-        route_pad_row(kk, rt.ids + g * kk, rt.w + g * kk, lane);
+      route_global_row<EPL>(rt, r, i, c, g, lane, status);
       continue;
     }
     const int64_t wi = w - route_items;
@@ -222,7 +230,7 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
   return r;
 }
 
-template <bool BF16>
+template <bool BF16, int EPL>
 __global__ void __launch_bounds__(kNormThreads)
     dp_gather_add_rmsnorm_kernel(const __grid_constant__ ReplicaPtrs hidden,
                                  const __grid_constant__ ReplicaPtrs residual,
@@ -230,7 +238,8 @@ __global__ void __launch_bounds__(kNormThreads)
                                  const int32_t* __restrict__ counts,
                                  const int32_t* __restrict__ offsets, int R, int64_t rows, int H,
                                  int vpr, uint4* __restrict__ global,
-                                 const __grid_constant__ GatherPlane side, uint32_t* status) {
+                                 const __grid_constant__ GatherPlane side,
+                                 const __grid_constant__ RoutePlan rt, uint32_t* status) {
   grid_dep_wait();    // earlier kernels on the stream are complete
   grid_dep_launch();  // the next kernel may start its launch
   constexpr int EPV = BF16 ? 8 : 4;
@@ -268,6 +277,7 @@ __global__ void __launch_bounds__(kNormThreads)
     }
     if (!(i >= 0 && i < c)) {  // pad row (block-uniform)
       for (int v = threadIdx.x; v < vpr; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
+      if (EPL > 0 && wid == kNormThreads / 32 - 1) route_global_row<EPL>(rt, r, i, c, g, lane, status);
       continue;
     }
     const uint4* hrow = static_cast<const uint4*>(hidden.p[r]) + i * vpr;
@@ -310,6 +320,8 @@ __global__ void __launch_bounds__(kNormThreads)
         dst[v] = pack8<BF16>(y);
       }
     }
+    // the row's routing by the last warp, from the replica's logits
+    if (EPL > 0 && wid == kNormThreads / 32 - 1) route_global_row<EPL>(rt, r, i, c, g, lane, status);
   }
 }
 
@@ -458,11 +470,47 @@ extern "C" moe_status moe_dp_gather_route(const void* const* local_x, int H, int
 
 namespace moe {
 namespace {
+template <bool BF16, int EPL>
+void launch_norm(int grid, cudaStream_t s, const ReplicaPtrs& hp, const ReplicaPtrs& rp,
+                 const void* d_gamma, float eps, const int32_t* d_counts, const int32_t* d_offsets,
+                 int R, int64_t rows, int H, int vpr, void* d_global, const GatherPlane& side,
+                 const RoutePlan& rt, uint32_t* d_status) {
+  launch(dp_gather_add_rmsnorm_kernel<BF16, EPL>, grid, kNormThreads, 0, s, hp, rp,
+         static_cast<const uint4*>(d_gamma), eps, d_counts, d_offsets, R, rows, H, vpr,
+         static_cast<uint4*>(d_global), side, rt, d_status);
+}
+
+template <bool BF16>
+void launch_norm_epl(int epl, int grid, cudaStream_t s, const ReplicaPtrs& hp,
+                     const ReplicaPtrs& rp, const void* d_gamma, float eps,
+                     const int32_t* d_counts, const int32_t* d_offsets, int R, int64_t rows, int H,
+                     int vpr, void* d_global, const GatherPlane& side, const RoutePlan& rt,
+                     uint32_t* d_status) {
+#define MOE_NORM_CASE(N)                                                                       \
+  case N:                                                                                      \
+    launch_norm<BF16, N>(grid, s, hp, rp, d_gamma, eps, d_counts, d_offsets, R, rows, H, vpr, \
+                         d_global, side, rt, d_status);                                        \
+    break;
+  switch (epl) {
+    MOE_NORM_CASE(0)
+    MOE_NORM_CASE(1)
+    MOE_NORM_CASE(2)
+    MOE_NORM_CASE(4)
+    MOE_NORM_CASE(8)
+    MOE_NORM_CASE(16)
+    default:
+      launch_norm<BF16, 32>(grid, s, hp, rp, d_gamma, eps, d_counts, d_offsets, R, rows, H, vpr,
+                            d_global, side, rt, d_status);
+      break;
+  }
+#undef MOE_NORM_CASE
+}
+
 moe_status gather_add_rmsnorm(const void* const* local_hidden, void* const* local_residual,
                               const void* d_gamma, float eps, const GatherPlane& side,
-                              const int32_t* d_counts, const int32_t* d_offsets, int R,
-                              int64_t rows, int H, int dtype, void* d_global, uint32_t* d_status,
-                              void* stream) {
+                              const RoutePlan* rt, const int32_t* d_counts,
+                              const int32_t* d_offsets, int R, int64_t rows, int H, int dtype,
+                              void* d_global, uint32_t* d_status, void* stream) {
   if (local_hidden == nullptr || local_residual == nullptr || d_gamma == nullptr ||
       !aligned16(d_gamma) || !(eps >= 0.f))
     return MOE_ERR_INVALID_ARG;
@@ -478,14 +526,15 @@ moe_status gather_add_rmsnorm(const void* const* local_hidden, void* const* loca
   }
   const int64_t lim = (int64_t)num_sms() * 8;
   const int grid = (int)(rows < lim ? rows : lim);
+  const int epl = rt != nullptr ? route_epl(rt->E) : 0;
+  const RoutePlan none{};
+  const RoutePlan& plan = rt != nullptr ? *rt : none;
   if (dtype == MOE_BF16)
-    launch(dp_gather_add_rmsnorm_kernel<true>, grid, kNormThreads, 0, as_stream(stream), hp, rp,
-           static_cast<const uint4*>(d_gamma), eps, d_counts, d_offsets, R, rows, H, vpr,
-           static_cast<uint4*>(d_global), side, d_status);
+    launch_norm_epl<true>(epl, grid, as_stream(stream), hp, rp, d_gamma, eps, d_counts, d_offsets,
+                          R, rows, H, vpr, d_global, side, plan, d_status);
   else
-    launch(dp_gather_add_rmsnorm_kernel<false>, grid, kNormThreads, 0, as_stream(stream), hp, rp,
-           static_cast<const uint4*>(d_gamma), eps, d_counts, d_offsets, R, rows, H, vpr,
-           static_cast<uint4*>(d_global), side, d_status);
+    launch_norm_epl<false>(epl, grid, as_stream(stream), hp, rp, d_gamma, eps, d_counts,
+                           d_offsets, R, rows, H, vpr, d_global, side, plan, d_status);
   return launch_status();
 }
 }  // namespace
@@ -502,8 +551,8 @@ extern "C" moe_status moe_dp_gather_add_rmsnorm(const void* const* local_hidden,
   GatherPlane none;
   none.vpr = 0;
   none.global = nullptr;
-  return gather_add_rmsnorm(local_hidden, local_residual, d_gamma, eps, none, d_counts, d_offsets,
-                            R, rows, H, dtype, d_global, d_status, stream);
+  return gather_add_rmsnorm(local_hidden, local_residual, d_gamma, eps, none, nullptr, d_counts,
+                            d_offsets, R, rows, H, dtype, d_global, d_status, stream);
 }
 
 extern "C" moe_status moe_dp_gather_add_rmsnorm2(const void* const* local_hidden,
@@ -520,8 +569,48 @@ extern "C" moe_status moe_dp_gather_add_rmsnorm2(const void* const* local_hidden
   if (st != MOE_OK || rows == 0) return st;
   GatherPlane side;
   if (!make_plane(local_b, R, H_b, dtype_b, d_global_b, &side)) return MOE_ERR_INVALID_ARG;
-  return gather_add_rmsnorm(local_hidden, local_residual, d_gamma, eps, side, d_counts, d_offsets,
-                            R, rows, H, dtype, d_global, d_status, stream);
+  return gather_add_rmsnorm(local_hidden, local_residual, d_gamma, eps, side, nullptr, d_counts,
+                            d_offsets, R, rows, H, dtype, d_global, d_status, stream);
+}
+
+extern "C" moe_status moe_dp_gather_add_rmsnorm_route(
+    const void* const* local_hidden, void* const* local_residual, const void* d_gamma, float eps,
+    const void* const* local_logits, int E, void* d_global_logits, int k, int renormalize,
+    int n_shared, int32_t* d_ids, float* d_w, const int32_t* d_counts, const int32_t* d_offsets,
+    int R, int64_t rows, int H, int dtype, void* d_global, uint32_t* d_status, void* stream) {
+  moe_status st = check_common(d_counts, d_offsets, R, rows, H, dtype, d_global);
+  if (st != MOE_OK) return st;
+  if (E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E || n_shared < 0 ||
+      k + n_shared > MOE_MAX_TOPK)
+    return MOE_ERR_INVALID_ARG;
+  if (d_global_logits != nullptr) {
+    st = check_common(d_counts, d_offsets, R, rows, E, MOE_F32, d_global_logits);
+    if (st != MOE_OK) return st;
+  }
+  if (rows == 0) return MOE_OK;
+  if (local_logits == nullptr || d_ids == nullptr || d_w == nullptr) return MOE_ERR_INVALID_ARG;
+  GatherPlane side;
+  if (d_global_logits != nullptr) {
+    if (!make_plane(local_logits, R, E, MOE_F32, d_global_logits, &side))
+      return MOE_ERR_INVALID_ARG;
+  } else {
+    side.vpr = 0;
+    side.global = nullptr;
+  }
+  RoutePlan rt;
+  for (int r = 0; r < R; ++r) {
+    if (reinterpret_cast<uintptr_t>(local_logits[r]) % alignof(float) != 0)
+      return MOE_ERR_INVALID_ARG;
+    rt.src.p[r] = local_logits[r];
+  }
+  rt.E = E;
+  rt.k = k;
+  rt.n_shared = n_shared;
+  rt.renorm = renormalize != 0;
+  rt.ids = d_ids;
+  rt.w = d_w;
+  return gather_add_rmsnorm(local_hidden, local_residual, d_gamma, eps, side, &rt, d_counts,
+                            d_offsets, R, rows, H, dtype, d_global, d_status, stream);
 }
 
 extern "C" moe_status moe_dp_scatter(const void* d_global, const int32_t* d_counts,

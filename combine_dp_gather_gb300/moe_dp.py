@@ -58,6 +58,8 @@ _SIGS = {
                                        _P, _P]),
     "moe_dp_gather_route": (_I, [_P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _P, _P, _I, _I64, _P,
                                  _P, _P, _P]),
+    "moe_dp_gather_add_rmsnorm_route": (_I, [_P, _P, _P, ctypes.c_float, _P, _I, _P, _I, _I, _I,
+                                             _P, _P, _P, _P, _I, _I64, _I, _I, _P, _P, _P]),
     "moe_dp_gather_add_rmsnorm2": (_I, [_P, _P, _P, ctypes.c_float, _P, _I, _I, _P, _P, _P, _I,
                                         _I64, _I, _I, _P, _P, _P]),
     "moe_dispatch_noalloc": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _I, _I, _I64, _P,
@@ -249,6 +251,28 @@ def moe_dp_gather_add_rmsnorm(local_hidden: Sequence[torch.Tensor],
         out_b.shape[1], dtype_code(out_b.dtype), _ptr(out_b), _ptr(d_counts), _ptr(d_offsets),
         R, out.shape[0], out.shape[1], dtype_code(out.dtype), _ptr(out), _ptr(d_status),
         _stream(stream)))
+
+
+def moe_dp_gather_add_rmsnorm_route(local_hidden: Sequence[torch.Tensor],
+                                    local_residual: Sequence[torch.Tensor], gamma: torch.Tensor,
+                                    eps: float, local_logits: Sequence[torch.Tensor], d_counts,
+                                    d_offsets, out: torch.Tensor, k: int, renormalize: bool,
+                                    ids: torch.Tensor, w: torch.Tensor, out_logits=None,
+                                    n_shared: int = 0, d_status=None, stream=None):
+    """Residual add (in place) + RMSNorm + DP gather of the normed rows, with the top-k
+    routing of every row from the replicas' float32 logits in the same launch."""
+    R = len(local_hidden)
+    if len(local_residual) != R or len(local_logits) != R:
+        raise MoeError("moe_dp_gather_add_rmsnorm_route", MOE_ERR_INVALID_ARG)
+    E = int(local_logits[0].shape[1]) if local_logits[0].dim() == 2 else 0
+    hp = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_hidden])
+    rp = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_residual])
+    lp = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_logits])
+    _check("moe_dp_gather_add_rmsnorm_route", lib().moe_dp_gather_add_rmsnorm_route(
+        ctypes.cast(hp, _P), ctypes.cast(rp, _P), _ptr(gamma), float(eps), ctypes.cast(lp, _P), E,
+        _ptr(out_logits), k, int(renormalize), n_shared, _ptr(ids), _ptr(w), _ptr(d_counts),
+        _ptr(d_offsets), R, out.shape[0], out.shape[1], dtype_code(out.dtype), _ptr(out),
+        _ptr(d_status), _stream(stream)))
 
 
 def moe_route_topk(logits: torch.Tensor, k: int, renormalize: bool, d_counts, d_offsets,
@@ -482,7 +506,6 @@ class MoeLayer:
         self._stage = _MetaStager(R)
         self.status = torch.zeros(1, **i32)
         self.xg = torch.empty(max_rows, H, device=dev, dtype=self.dtype)
-        self.logits_g = torch.empty(max_rows, E, device=dev, dtype=torch.float32)
         self.ids = torch.empty(max_rows, self.kk, **i32)
         self.w = torch.empty(max_rows, self.kk, device=dev, dtype=torch.float32)
         self.counts_P = torch.empty(self.P, **i32)
@@ -562,29 +585,29 @@ class MoeLayer:
         self.check_inputs(local_x, local_logits, out, local_residual)
         rows = self.rows
         st = self.status
-        xg, lg = self.xg[:rows], self.logits_g[:rows]
+        xg = self.xg[:rows]
         ids, w, inv, yg = self.ids[:rows], self.w[:rows], self.inv[:rows], self.yg[:rows]
         ev = timings.mark if timings is not None else (lambda name: None)
         ev("start")
         if local_residual is not None:
             if self.norm_gamma is None:
                 raise ValueError("local_residual needs norm_gamma")
-            gathered = self.router_weight is None  # the logits ride in the same launch
-            moe_dp_gather_add_rmsnorm(local_x, local_residual, self.norm_gamma, self.norm_eps,
-                                      self.d_counts, self.d_offsets, xg, st, stream,
-                                      local_b=local_logits if gathered else None,
-                                      out_b=lg if gathered else None)
+            if self.router_weight is None:  # the rows are routed in the same launch
+                moe_dp_gather_add_rmsnorm_route(local_x, local_residual, self.norm_gamma,
+                                                self.norm_eps, local_logits, self.d_counts,
+                                                self.d_offsets, xg, self.k, self.renormalize,
+                                                ids, w, None, self.n_shared, st, stream)
+            else:
+                moe_dp_gather_add_rmsnorm(local_x, local_residual, self.norm_gamma,
+                                          self.norm_eps, self.d_counts, self.d_offsets, xg, st,
+                                          stream)
         elif self.router_weight is None:  # the gather routes its rows in the same launch
             moe_dp_gather_route(local_x, local_logits, self.d_counts, self.d_offsets, xg, self.k,
                                 self.renormalize, ids, w, None, self.n_shared, st, stream)
         else:
             moe_dp_gather(local_x, self.d_counts, self.d_offsets, xg, st, stream)
         ev("gather")
-        if self.router_weight is None:
-            if local_residual is not None:
-                moe_route_topk(lg, self.k, self.renormalize, self.d_counts, self.d_offsets, ids,
-                               w, st, stream, n_shared=self.n_shared)
-        else:
+        if self.router_weight is not None:  # (given logits: routed by the gather)
             moe_route_gemm_topk(xg, self.router_weight, self.k, self.renormalize, self.d_counts,
                                 self.d_offsets, ids, w, self.ws_router, None, st, stream,
                                 n_shared=self.n_shared, bias=self.router_bias)

@@ -214,6 +214,20 @@ moe_status moe_dp_gather_add_rmsnorm2(const void* const* local_hidden,
                                       int dtype, void* d_global, uint32_t* d_status,
                                       void* stream);
 
+/* moe_dp_gather_add_rmsnorm with the top-k routing of every global row in the
+ * same launch: ids / w as moe_route_topk_shared computes them from each row's
+ * router logits, read from the row's replica (local_logits[r] float32
+ * [counts[r], E]); with d_global_logits != NULL the logits are also gathered
+ * there (E a multiple of 4).  Checks and errors as the two entry points. */
+moe_status moe_dp_gather_add_rmsnorm_route(const void* const* local_hidden,
+                                           void* const* local_residual, const void* d_gamma,
+                                           float eps, const void* const* local_logits, int E,
+                                           void* d_global_logits, int k, int renormalize,
+                                           int n_shared, int32_t* d_ids, float* d_w,
+                                           const int32_t* d_counts, const int32_t* d_offsets,
+                                           int R, int64_t rows, int H, int dtype, void* d_global,
+                                           uint32_t* d_status, void* stream);
+
 /* Top-k routing of every real row of the global buffer.  [P1] names the
  * result TopKOutput{topk_ids, topk_weights} (sections "normal dispatch 的调用链"
  * and "Two-batch Overlap"); the scoring is softmax routing: the k largest

@@ -192,6 +192,33 @@ def test_gather_route_rejects_bad_args(md):
     assert call(rows=0) == md.MOE_OK                     # nothing to do
 
 
+def test_gather_add_rmsnorm_route_rejects_bad_args(md):
+    L = md.lib()
+    two = _ptrs(0x2000, 0x3000)
+    E_ARG = md.MOE_ERR_INVALID_ARG
+    f = ctypes.c_float
+
+    def call(**kw):
+        a = dict(gm=FAKE, eps=f(1e-6), ll=two, E=256, gl=NULL, k=8, rn=1, ns=0, ids=FAKE,
+                 w=FAKE, rows=8, H=64, dt=1, gx=FAKE)
+        a.update(kw)
+        return L.moe_dp_gather_add_rmsnorm_route(two, two, a["gm"], a["eps"], a["ll"], a["E"],
+                                                 a["gl"], a["k"], a["rn"], a["ns"], a["ids"],
+                                                 a["w"], FAKE, FAKE, 2, a["rows"], a["H"],
+                                                 a["dt"], a["gx"], NULL, NULL)
+
+    assert call(gm=NULL) == E_ARG                        # no gamma
+    assert call(eps=f(-1.0)) == E_ARG
+    assert call(k=0) == E_ARG
+    assert call(k=30, ns=3) == E_ARG                     # k + n_shared > MOE_MAX_TOPK
+    assert call(ll=NULL) == E_ARG
+    assert call(ids=NULL) == E_ARG
+    assert call(ll=_ptrs(0x2000, 0x3002)) == E_ARG      # logits not float-aligned
+    assert call(E=30, gl=FAKE) == E_ARG                  # 120-byte rows cannot be gathered
+    assert call(H=16384) == md.MOE_ERR_UNSUPPORTED       # 32 KB rows
+    assert call(rows=0) == md.MOE_OK
+
+
 def test_gather_add_rmsnorm_rejects_bad_args(md):
     L = md.lib()
     two = _ptrs(0x2000, 0x3000)

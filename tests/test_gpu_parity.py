@@ -142,13 +142,15 @@ def test_fused_gather_and_combine_scatter_bad_counts_flag_without_fault(md):
         assert torch.equal(o[4:].float(), torch.full((6, 64), 3.0, device=DEV))
 
 
-@pytest.mark.parametrize("dtype,H,mode,E", [(torch.bfloat16, 7168, 1, 0),
-                                            (torch.bfloat16, 7168, 1, 256),
-                                            (torch.bfloat16, 512, 0, 0),
-                                            (torch.float32, 1024, 2, 36)])
-def test_gather_add_rmsnorm(md, orc, dtype, H, mode, E):
+@pytest.mark.parametrize("dtype,H,mode,E,route", [(torch.bfloat16, 7168, 1, 0, False),
+                                                  (torch.bfloat16, 7168, 1, 256, False),
+                                                  (torch.bfloat16, 7168, 1, 256, True),
+                                                  (torch.bfloat16, 512, 0, 0, False),
+                                                  (torch.float32, 1024, 2, 36, True)])
+def test_gather_add_rmsnorm(md, orc, dtype, H, mode, E, route):
     """E > 0: the router logits [count, E] float32 ride in the same launch and must
-    equal the plain gather's output bit for bit (zero pad rows)."""
+    equal the plain gather's output bit for bit (zero pad rows); with route the rows
+    are also routed (top-6 of E, one shared expert) as the oracle routes them."""
     counts = [5, 0, 33, 1, 17]
     offs, rows = md.moe_dp_layout(counts, mode, 40, 1)
     g = torch.Generator(device=DEV).manual_seed(H + mode)
@@ -161,10 +163,22 @@ def test_gather_add_rmsnorm(md, orc, dtype, H, mode, E):
     if E:
         lg = [torch.randn(c, E, generator=g, device=DEV) for c in counts]
         lg_out = torch.full((rows, E), 3.0, device=DEV)
-        md.moe_dp_gather_add_rmsnorm(hid, res, gamma, 1e-6, dev_i32(counts), dev_i32(offs), out,
-                                     st, local_b=lg, out_b=lg_out)
-        assert np.array_equal(to_np(lg_out), orc.dp_gather([to_np(t) for t in lg], counts,
-                                                           np.array(offs, np.int32), rows))
+        if route:
+            ids = torch.full((rows, 7), -7, dtype=torch.int32, device=DEV)
+            w = torch.full((rows, 7), 9.0, device=DEV)
+            md.moe_dp_gather_add_rmsnorm_route(hid, res, gamma, 1e-6, lg, dev_i32(counts),
+                                               dev_i32(offs), out, 6, True, ids, w, lg_out, 1,
+                                               st)
+        else:
+            md.moe_dp_gather_add_rmsnorm(hid, res, gamma, 1e-6, dev_i32(counts), dev_i32(offs),
+                                         out, st, local_b=lg, out_b=lg_out)
+        lg_o = orc.dp_gather([to_np(t) for t in lg], counts, np.array(offs, np.int32), rows)
+        assert np.array_equal(to_np(lg_out), lg_o)
+        if route:
+            valid_r = orc.valid_rows(counts, np.array(offs, np.int32), rows)
+            ids_o, w_o = orc.route_topk(lg_o, 6, True, valid_r, 1)
+            assert np.array_equal(to_np(ids), ids_o)
+            assert_close(to_np(w), w_o, W_ATOL, W_RTOL, "route weights")
     else:
         md.moe_dp_gather_add_rmsnorm(hid, res, gamma, 1e-6, dev_i32(counts), dev_i32(offs), out,
                                      st)
@@ -704,11 +718,11 @@ def test_layer_align128_and_determinism(md, orc):
 
 @pytest.mark.parametrize("mode", [0, 1])
 def test_layer_addnorm_boundary(md, orc, mode):
-    """The residual add + RMSNorm boundary (the logits gathered in the same launch):
+    """The residual add + RMSNorm boundary (the rows routed in the same launch):
     residuals are updated exactly as the oracle's add, the normed rows are within one
-    rounding of the oracle's norm, the logits are gathered bit for bit, and the rest
-    of the step equals a plain layer fed the normed rows (checked against the oracle),
-    bit for bit, in eager mode and under graph replay."""
+    rounding of the oracle's norm, the routing equals the oracle's, and the rest of the
+    step equals a plain layer fed the normed rows (checked against the oracle), bit
+    for bit, in eager mode and under graph replay."""
     spec = synth.LayerSpec("addnorm", [16, 0, 140, 8, 1], mode, H=512, E=16, k=4, I=256,
                            dtype="bf16", w_std=0.05, zipf_s=1.1)
     x_loc = synth.hidden_states(spec, DEV)
@@ -733,9 +747,11 @@ def test_layer_addnorm_boundary(md, orc, mode):
         assert np.array_equal(f32(res[r]), r_new)
         assert_close(f32(xg[offs[r]: offs[r] + c]).astype(np.float64), y_r, 1e-6, 8e-3,
                      "normed rows")
-    assert np.array_equal(to_np(layer.logits_g[:rows]),
-                          orc.dp_gather([to_np(t) for t in lg_loc], spec.counts,
-                                        np.array(offs, np.int32), rows))
+    valid = orc.valid_rows(spec.counts, np.array(offs, np.int32), rows)
+    lg_o = orc.dp_gather([to_np(t) for t in lg_loc], spec.counts, np.array(offs, np.int32), rows)
+    ids_o, w_o = orc.route_topk(lg_o, spec.k, True, valid)
+    assert np.array_equal(to_np(layer.ids[:rows]), ids_o)     # routed in the same launch
+    assert_close(to_np(layer.w[:rows]), w_o, W_ATOL, W_RTOL, "route weights")
     # the rest of the step: a plain layer on the normed rows gives the same bits
     normed = [xg[offs[r]: offs[r] + c].clone() for r, c in enumerate(spec.counts)]
     plain = md.MoeLayer(R=spec.R, H=spec.H, E=spec.E, k=spec.k, I=spec.I, w_gate_up=wgu,
