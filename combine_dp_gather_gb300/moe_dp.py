@@ -464,13 +464,13 @@ class MoeLayer:
 
     Buffers are sized once for `max_rows` global rows; `forward` runs
     gather -> route -> dispatch -> grouped FFN -> combine -> scatter on the
-    current stream without a host synchronisation (the hidden-state and logits
-    gathers share one launch, and so do combine and scatter).  With router_weight [E, H]
-    (bf16) the router logits are computed from the gathered hidden states by the
-    gate GEMM fused ahead of top-k instead of being gathered from the replicas.
-    With fp8=True (bf16 layer)
-    the expert weights are quantised once here (e4m3, 128 x 128 blocks), the
-    dispatch quantises the permuted rows per token group and the grouped FFN
+    current stream without a host synchronisation (the hidden-state gather routes
+    every row from its replica's logits in the same launch, with or without the fused
+    residual add + RMSNorm; combine and scatter share one launch).  With router_weight
+    [E, H] (bf16) the router logits are computed from the gathered hidden states by
+    the gate GEMM fused ahead of top-k instead.  With fp8=True (bf16 layer) the expert
+    weights are quantised once here (e4m3, 128 x 128 blocks), the dispatch quantises
+    the permuted rows per token group and the grouped FFN (one launch for both GEMMs)
     runs on FP8 operands."""
 
     def __init__(self, *, R: int, H: int, E: int, k: int, I: int, w_gate_up: torch.Tensor,
