@@ -61,3 +61,17 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_launch_counts_match_the_measured_steps():
+    """The bench's claimed launches per step, for the workloads whose counts were read
+    off CUDA-graph runs on the GPU (gpu_launches / steps): decode 6 (bf16) and 5 (FP8),
+    prefill 8 (chunked dispatch), decode with the split router GEMM 9."""
+    sys.path.insert(0, ROOT)
+    import bench
+    # decode: 440 global rows, top-8, 256 experts / slots, cap 3520 + 64
+    assert bench.launches_per_step(440, 8, 256, 256, 3584, 1) == 6
+    assert bench.launches_per_step(440, 8, 256, 256, 3584, 1, fp8=True) == 5
+    assert bench.launches_per_step(440, 8, 256, 256, 3584, 1, router_gemm=True) == 9
+    # prefill: 8192 rows x 8 pairs take the chunked dispatch (histogram, scan, rank, copy)
+    assert bench.launches_per_step(8192, 8, 256, 256, 65600, 1) == 8
