@@ -206,6 +206,18 @@ def moe_dp_gather2(local_a: Sequence[torch.Tensor], local_b: Sequence[torch.Tens
         _ptr(d_counts), _ptr(d_offsets), R, out_a.shape[0], _ptr(d_status), _stream(stream)))
 
 
+def _check_route_outputs(fn: str, rows: int, kk: int, ids, w, out_logits, E: int):
+    """The kernels write ids / w [rows, kk] (and the gathered logits [rows, E]): refuse
+    tensors of another shape or dtype before any launch."""
+    ok = (tuple(ids.shape) == (rows, kk) and ids.dtype == torch.int32 and ids.is_contiguous()
+          and tuple(w.shape) == (rows, kk) and w.dtype == torch.float32 and w.is_contiguous())
+    if out_logits is not None:
+        ok = ok and (tuple(out_logits.shape) == (rows, E) and out_logits.dtype == torch.float32
+                     and out_logits.is_contiguous())
+    if not ok:
+        raise MoeError(fn, MOE_ERR_INVALID_ARG)
+
+
 def moe_dp_gather_route(local_x: Sequence[torch.Tensor], local_logits: Sequence[torch.Tensor],
                         d_counts, d_offsets, out_x: torch.Tensor, k: int, renormalize: bool,
                         ids: torch.Tensor, w: torch.Tensor, out_logits=None, n_shared: int = 0,
@@ -217,6 +229,8 @@ def moe_dp_gather_route(local_x: Sequence[torch.Tensor], local_logits: Sequence[
     if len(local_logits) != R:
         raise MoeError("moe_dp_gather_route", MOE_ERR_INVALID_ARG)
     E = int(local_logits[0].shape[1]) if local_logits[0].dim() == 2 else 0
+    _check_route_outputs("moe_dp_gather_route", out_x.shape[0], k + n_shared, ids, w,
+                         out_logits, E)
     px = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_x])
     pl = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_logits])
     _check("moe_dp_gather_route", lib().moe_dp_gather_route(
@@ -265,6 +279,8 @@ def moe_dp_gather_add_rmsnorm_route(local_hidden: Sequence[torch.Tensor],
     if len(local_residual) != R or len(local_logits) != R:
         raise MoeError("moe_dp_gather_add_rmsnorm_route", MOE_ERR_INVALID_ARG)
     E = int(local_logits[0].shape[1]) if local_logits[0].dim() == 2 else 0
+    _check_route_outputs("moe_dp_gather_add_rmsnorm_route", out.shape[0], k + n_shared, ids, w,
+                         out_logits, E)
     hp = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_hidden])
     rp = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_residual])
     lp = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local_logits])

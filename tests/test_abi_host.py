@@ -162,6 +162,25 @@ def test_gather2_and_combine_scatter_reject_bad_args(md):
     assert c(a3=0) == md.MOE_OK
 
 
+def test_routing_gather_bindings_check_output_shapes(md):
+    """The bindings refuse ids / w / gathered-logit tensors the kernels would write past."""
+    import torch
+    xs = [torch.zeros(3, 64, dtype=torch.bfloat16), torch.zeros(0, 64, dtype=torch.bfloat16)]
+    ls = [torch.zeros(3, 32), torch.zeros(0, 32)]
+    out = torch.zeros(3, 64, dtype=torch.bfloat16)
+    good_ids, good_w = torch.zeros(3, 4, dtype=torch.int32), torch.zeros(3, 4)
+    bad = [(torch.zeros(3, 3, dtype=torch.int32), good_w, None),      # too few columns
+           (good_ids, torch.zeros(2, 4), None),                       # too few rows
+           (torch.zeros(3, 4, dtype=torch.int64), good_w, None),      # wrong dtype
+           (good_ids, good_w, torch.zeros(3, 16))]                    # logits narrower than E
+    for ids, w, lg in bad:
+        with pytest.raises(md.MoeError):
+            md.moe_dp_gather_route(xs, ls, None, None, out, 4, True, ids, w, lg)
+        with pytest.raises(md.MoeError):
+            md.moe_dp_gather_add_rmsnorm_route(xs, xs, torch.zeros(64), 1e-6, ls, None, None,
+                                               out, 4, True, ids, w, lg)
+
+
 def test_gather_route_rejects_bad_args(md):
     L = md.lib()
     two = _ptrs(0x2000, 0x3000)
