@@ -6,15 +6,20 @@
 A step is one pass of the whole hot path over one batch: DP gather (hidden
 states and router logits), top-k routing, dispatch, grouped SwiGLU expert FFN
 on the tensor cores, combine and DP scatter.  The default workload is the
-DeepSeek-V3-shaped decode layer: 8 DP replicas with seeded token counts in
-[0, 64] (one idle), MAX padding, hidden 7168, 256 experts, top-8, expert
-intermediate 2048, bf16 weights/activations with fp32 accumulation.
+DeepSeek-V3-shaped prefill layer, the largest single-GPU workload: T = 8192
+tokens of one request on one replica, hidden 7168, 256 experts with uniform
+popularity, top-8, expert intermediate 2048, bf16 weights/activations with
+fp32 accumulation.  `--config decode` runs the 8-replica decode layer (seeded
+token counts in [0, 64], one idle, MAX padding).
 
 Printed: one JSON line (rank 0).  `value` is tokens/s with inputs resident in
 HBM; `e2e` is the same metric through the same C-ABI calls with the step's
 inputs copied from pinned host buffers and its outputs copied back inside the
-timed region.  `roofline` reports the grouped FFN (the dominant call: two
-tcgen05 kernel launches that stream the expert weights) against the measured
+timed region.  `roofline` reports the grouped FFN (the dominant call: tcgen05
+kernels that stream the expert weights) against the measured bf16 tensor peak
+(burst and sustained) and against the HBM roofline at its arithmetic
+intensity, and, under `permutes`, the gather, dispatch and combine + scatter
+stages as algorithmic bytes over their live stage time against the measured
 HBM copy bandwidth.  N > 1 runs independent replicas, one per GPU (the layer
 has no cross-GPU exchange on this path), and reports the aggregate.
 """
@@ -98,7 +103,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--config", default="decode",
+    ap.add_argument("--config", default="prefill",
                     help="decode | prefill | eplb | tiny | pad_sweep[:mix:tokens_per_req:mode]")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -114,9 +119,10 @@ def parse():
     ap.add_argument("--router", default="logits", choices=["logits", "gemm"],
                     help="gemm: router logits from the gate GEMM (W_r N(0, 1/H) plus the "
                          "workload's Zipf bias) fused ahead of top-k instead of given logits")
-    ap.add_argument("--stage-every", type=int, default=10,
-                    help="record the per-stage CUDA events on every n-th timed step (the events "
-                         "themselves cost ~2 us each on the device)")
+    ap.add_argument("--stage-every", type=int, default=None,
+                    help="record the per-stage CUDA events on every n-th timed step (default: "
+                         "every step up to 50 steps, else enough steps for 50 samples; the "
+                         "events themselves cost ~2 us each on the device)")
     ap.add_argument("--exec", default="graph", choices=["graph", "eager"],
                     help="graph: each step is a replay of a CUDA graph of the layer (all its "
                          "kernels; captured before the timed region); eager: stream launches")
@@ -298,7 +304,7 @@ def run_native(args, rank, world, local_rank):
         raise RuntimeError(f"device status {int(layer.status.item()):#x} after warm-up")
 
     # ---- timed region: K steps, inputs resident in HBM
-    every = max(1, args.stage_every)
+    every = stage_every(args)
     use_graph = args.exec == "graph"
     evs = [StepEvents(external=use_graph) if i % every == 0 else None
            for i in range(args.steps)]
@@ -352,7 +358,8 @@ def run_native(args, rank, world, local_rank):
     pk = peaks()
     # an FP8 contraction takes the bf16 measured peak x 2 (the nominal fp8:bf16 ratio)
     tc_peak = pk["bf16_tflops"] * (2 if args.fp8 else 1)
-    hbm_bound = ffn_flops / (ffn_bytes) < (tc_peak * 1e12) / (pk["hbm_gbs"] * 1e9)
+    intensity = ffn_flops / ffn_bytes
+    hbm_bound = intensity < (tc_peak * 1e12) / (pk["hbm_gbs"] * 1e9)
     if hbm_bound:
         achieved = ffn_bytes / (ffn_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
@@ -362,6 +369,8 @@ def run_native(args, rank, world, local_rank):
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tc_peak,
                 "unit": "TFLOP/s", "frac": round(achieved / tc_peak, 4)}
     tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12
+    # attainable at this intensity: min(tensor peak, intensity x HBM bandwidth)
+    attainable = min(tc_peak, intensity * pk["hbm_gbs"] / 1e3)
     roof.update({"traffic": ffn_traffic(args),
                  "kernel": (f"moe_grouped_ffn_fp8 ({ffn_kernel(layer.cap, layer.P, True)}: "
                             "MM1+SwiGLU and MM2 in one persistent launch)" if args.fp8 else
@@ -371,9 +380,14 @@ def run_native(args, rank, world, local_rank):
                  "frac_of_bf16_peak": round(tflops / pk["bf16_tflops"], 4),
                  "frac_of_bf16_sustained": (round(tflops / pk["bf16_tflops_sustained"], 4)
                                             if pk.get("bf16_tflops_sustained") else None),
+                 "frac_of_hbm_roofline": round(tflops / attainable, 4),
+                 "intensity_flop_per_byte": round(intensity, 1),
+                 "target_frac_of_bf16_peak": None if args.fp8 else 0.60,
                  "peak_source": pk["source"],
                  "algorithmic_bytes": int(ffn_bytes), "algorithmic_flops": int(ffn_flops),
-                 "touched_slots": touched, "ffn_ms_per_step": round(ffn_ms, 4)})
+                 "touched_slots": touched, "ffn_ms_per_step": round(ffn_ms, 4),
+                 "ffn_samples": len(stage.get("ffn", [])),
+                 "permutes": permute_fractions(spec, rows, stage_ms, pk["hbm_gbs"], args.fp8)})
 
     # ---- e2e: same calls, inputs from pinned host memory, outputs back to host
     e2e = None
@@ -467,19 +481,15 @@ def run_native(args, rank, world, local_rank):
         # padding overhead: rows the global buffer carries that hold no token
         extra["wasted_row_fraction"] = round((rows - spec.T) / max(rows, 1), 4)
     if spec.P is not None and spec.P != spec.E:
-        ranges = synth.slot_ranges(spec.P, spec.n_ranges)
-        loads = [int(counts_P[a:b].sum()) for a, b in ranges]
+        loads = md.moe_range_loads(counts_P.tolist(), spec.n_ranges)
         # the same routing on the trivial layout (slot = logical id, E slots in
-        # n_ranges equal ranges): logical counts are the per-slot counts summed
-        # over each logical expert's replicas
-        logical = np.zeros(spec.E, np.int64)
-        np.add.at(logical, p2l, counts_P)
-        per = spec.E // spec.n_ranges
-        triv = [int(logical[r * per:(r + 1) * per].sum()) for r in range(spec.n_ranges)]
-        from combine_dp_gather_gb300 import moe_dp as _md
+        # n_ranges equal ranges): the per-slot counts summed over each logical
+        # expert's replicas
+        logical = md.moe_logical_counts(counts_P.tolist(), p2l.tolist(), spec.E)
+        triv = md.moe_range_loads(logical, spec.n_ranges)
         extra["range_loads"] = loads
-        extra["balancedness"] = round(_md.utilization_rate(loads), 4)
-        extra["balancedness_trivial_layout"] = round(_md.utilization_rate(triv), 4)
+        extra["balancedness"] = round(md.moe_balancedness(loads), 4)
+        extra["balancedness_trivial_layout"] = round(md.moe_balancedness(triv), 4)
     return dict(spec=spec, ms_total=ms_total, clocks=clocks, stage_ms=stage_ms, roof=roof,
                 extra=extra,
                 e2e=e2e, rows=rows, touched=touched,
@@ -488,6 +498,47 @@ def run_native(args, rank, world, local_rank):
                                            spec.align, args.fp8, args.router == "gemm",
                                            torch.cuda.get_device_properties(dev).multi_processor_count),
                 inputs=(x_loc, lg_loc, wgu, wd, l2p_np, nrep_np), gate=gate_np)
+
+
+def stage_every(args) -> int:
+    """Timed steps between two recordings of the stage events: every step up to 50
+    steps, else enough steps for 50 samples."""
+    if args.stage_every is not None:
+        return max(1, args.stage_every)
+    return max(1, args.steps // 50)
+
+
+def permute_fractions(spec, rows: int, stage_ms: dict, hbm_gbs: float, fp8: bool = False):
+    """Algorithmic bytes of the layer's row-moving stages over their live stage time
+    (CUDA events on the launching stream, launch gaps included), against the measured
+    HBM copy bandwidth.  T real tokens, `rows` global rows, kk routed slots per token,
+    b bytes per element:
+      gather (+ routing of every row): read T rows and write `rows` rows of H, read the
+        T rows' logits (E x 4 B), write ids and weights (kk x 8 B per row);
+      dispatch (stable sort + row copy): read T rows, write their T x kk copies, read
+        ids and write perm and inv (12 B per routed pair); on FP8 the copies are e4m3
+        codes plus one scale byte per 128 values;
+      combine + scatter: read the T x kk expert rows, write T rows, read inv and w
+        (8 B per routed pair)."""
+    b = 2 if spec.dtype == "bf16" else 4
+    kk, T, H, E = spec.k + spec.n_shared, spec.T, spec.H, spec.E
+    copy_row = H * (1 + 1 / 128) if fp8 else H * b
+    algo = {
+        "gather": T * H * b + rows * H * b + T * E * 4 + rows * kk * 8,
+        "dispatch": T * H * b + T * kk * copy_row + T * kk * 12,
+        "combine_scatter": T * kk * H * b + T * H * b + T * kk * 8,
+    }
+    out = {}
+    for name, nbytes in algo.items():
+        ms = stage_ms.get(name)
+        if not ms:
+            continue
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
+                     "achieved_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_gbs, 4)}
+    out["target_frac_of_hbm"] = 0.70
+    out["peak_gbs"] = hbm_gbs
+    return out
 
 
 # ------------------------------------------------------------------ oracle (CPU)
@@ -518,9 +569,7 @@ def oracle_sample_step(spec, n_tokens, x_loc, lg_loc, wgu, wd, l2p, nrep, fp8=Fa
     if gate is None:
         lg = oracle.dp_gather(lgs, counts, offs, rows)
     else:
-        lg = oracle.router_logits(xg, gate[0])
-        if gate[1] is not None:
-            lg = lg + gate[1][None, :]
+        lg = oracle.router_logits(xg, gate[0], gate[1])
     ids, w = oracle.route_topk(lg, spec.k, spec.renormalize, valid, spec.n_shared)
     cnt, o, perm, inv = oracle.dispatch(ids, spec.E + spec.n_shared, spec.slots, l2p, nrep,
                                         spec.align)
@@ -565,7 +614,7 @@ def gate_to_host(w, b):
     """Gate weights as exact float32 host arrays for the oracle (bias may be None)."""
     import oracle
     wb = w.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    return oracle.bf16_bits_to_f32(wb), (None if b is None else b.cpu().numpy().astype(np.float64))
+    return oracle.bf16_bits_to_f32(wb), (None if b is None else b.cpu().numpy().astype(np.float32))
 
 
 def cpu_baseline(spec, budget_s=20.0, inputs=None, fp8=False, gate=None, threads=0):
@@ -669,7 +718,7 @@ def main():
                                    "bias" if args.router == "gemm" else "given logits"),
                            execution=("CUDA graph of the layer step, replayed" if args.exec == "graph"
                                       else "stream launches"),
-                           stage_events=f"every {max(1, args.stage_every)}th timed step",
+                           stage_events=f"every {stage_every(args)}th timed step",
                            fp8=("e4m3 codes, UE8M0 scales per 128-token group and 128x128 "
                                 "weight block; bf16 layer input/output") if args.fp8 else None,
                            parallelism=f"{world} independent replica(s), one per GPU",

@@ -45,6 +45,35 @@ void* scratch_on_current_device(moe_status* st) {
   return addr[dev];
 }
 
+// moe_dispatch's own argument checks, applied before the scratch-size check so
+// that an invalid call returns what moe_dispatch returns for it, whatever its
+// size.
+moe_status check_dispatch_args(const void* d_global, const int32_t* d_ids, int64_t rows, int k,
+                               int H, int dtype, int E, int P, const int32_t* d_l2p,
+                               const int32_t* d_nrep, int X, int align, int64_t cap,
+                               const int32_t* d_counts_P, const int32_t* d_offsets_P,
+                               const int32_t* d_perm, const int32_t* d_inv,
+                               const void* d_sorted) {
+  if (d_counts_P == nullptr || d_offsets_P == nullptr ||
+      (rows > 0 && (d_ids == nullptr || d_inv == nullptr)) || (cap > 0 && d_perm == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (rows < 0 || k < 1 || k > MOE_MAX_TOPK || E < 1 || P < 1 || P > MOE_MAX_SLOTS ||
+      E > MOE_MAX_SLOTS || align < 1 || cap < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (rows * k > INT32_MAX || cap > INT32_MAX) return MOE_ERR_INVALID_ARG;
+  if ((d_l2p == nullptr) != (d_nrep == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (d_l2p == nullptr && P != E) return MOE_ERR_INVALID_ARG;
+  if (d_l2p != nullptr && X < 1) return MOE_ERR_INVALID_ARG;
+  if (rows > 0 && (d_global != nullptr || d_sorted != nullptr)) {
+    if (d_global == nullptr || d_sorted == nullptr || H < 1) return MOE_ERR_INVALID_ARG;
+    const int eb = moe::dtype_bytes(dtype);
+    if (eb == 0) return MOE_ERR_UNSUPPORTED;
+    if (((int64_t)H * eb) % 16 != 0 || !moe::aligned16(d_global) || !moe::aligned16(d_sorted))
+      return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" moe_status moe_dispatch_noalloc(const void* d_global, const int32_t* d_ids,
@@ -53,7 +82,10 @@ extern "C" moe_status moe_dispatch_noalloc(const void* d_global, const int32_t* 
                                            int align, int64_t cap, int32_t* d_counts_P,
                                            int32_t* d_offsets_P, int32_t* d_perm, int32_t* d_inv,
                                            void* d_sorted, uint32_t* d_status, void* stream) {
-  if (rows < 0 || k < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+  const moe_status bad = check_dispatch_args(d_global, d_ids, rows, k, H, dtype, E, P, d_l2p,
+                                             d_nrep, X, align, cap, d_counts_P, d_offsets_P,
+                                             d_perm, d_inv, d_sorted);
+  if (bad != MOE_OK) return bad;
   if (moe_dispatch_ws_bytes(rows, k, E) > (size_t)MOE_NOALLOC_SCRATCH_BYTES)
     return MOE_ERR_CAPACITY;  // rows * k pairs over E experts need more than the fixed scratch
   moe_status st = MOE_OK;

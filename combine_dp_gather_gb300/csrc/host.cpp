@@ -102,6 +102,49 @@ const char* moe_status_string(int status) {
   }
 }
 
+// SGLang chapter 17, section "不均衡的代价与冗余专家的思路" (compute_utilization_rate).
+double moe_balancedness(const int64_t* loads, int n) {
+  if (loads == nullptr || n < 1) return -1.0;
+  int64_t sum = 0, mx = 0;
+  for (int i = 0; i < n; ++i) {
+    if (loads[i] < 0) return -1.0;
+    sum += loads[i];
+    mx = loads[i] > mx ? loads[i] : mx;
+  }
+  const double mean = (double)sum / (double)n;
+  return (mean + 1e-5) / ((double)mx + 1e-5);
+}
+
+// SGLang chapter 17, section "逻辑与物理的两套映射": contiguous slot ranges per EP rank.
+moe_status moe_range_loads(const int32_t* counts, int n, int n_ranges, int64_t* loads) {
+  if (counts == nullptr || loads == nullptr || n < 1 || n_ranges < 1 || n % n_ranges != 0)
+    return MOE_ERR_INVALID_ARG;
+  const int per = n / n_ranges;
+  for (int r = 0; r < n_ranges; ++r) {
+    int64_t sum = 0;
+    for (int i = r * per; i < (r + 1) * per; ++i) {
+      if (counts[i] < 0) return MOE_ERR_INVALID_ARG;
+      sum += counts[i];
+    }
+    loads[r] = sum;
+  }
+  return MOE_OK;
+}
+
+// SGLang chapter 17, sections "逻辑与物理的两套映射" and "推理时怎么选副本":
+// per-slot counts summed over each logical expert's replicas.
+moe_status moe_logical_counts(const int32_t* counts_P, const int32_t* p2l, int P, int E,
+                              int64_t* counts_E) {
+  if (counts_P == nullptr || p2l == nullptr || counts_E == nullptr || P < 1 || E < 1)
+    return MOE_ERR_INVALID_ARG;
+  for (int e = 0; e < E; ++e) counts_E[e] = 0;
+  for (int s = 0; s < P; ++s) {
+    if (counts_P[s] < 0 || p2l[s] < 0 || p2l[s] >= E) return MOE_ERR_INVALID_ARG;
+    counts_E[p2l[s]] += counts_P[s];
+  }
+  return MOE_OK;
+}
+
 int64_t moe_dispatch_cap_bound(int64_t rows, int k, int P, int align) {
   if (rows < 0 || k < 1 || P < 1 || align < 1) return -1;
   return rows * k + (int64_t)P * (align - 1);

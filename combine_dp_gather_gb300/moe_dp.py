@@ -40,6 +40,9 @@ _SIGS = {
     "moe_dp_padding_mode": (_I, [_P, _I, _I, _I, _I]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_dispatch_cap_bound": (_I64, [_I64, _I, _I, _I]),
+    "moe_balancedness": (ctypes.c_double, [_P, _I]),
+    "moe_range_loads": (_I, [_P, _I, _I, _P]),
+    "moe_logical_counts": (_I, [_P, _P, _I, _I, _P]),
     "moe_dispatch_ws_bytes": (_SZ, [_I64, _I, _I]),
     "moe_grouped_ffn_ws_bytes": (_SZ, [_I64, _I, _I]),
     "moe_dp_gather": (_I, [_P, _P, _P, _I, _I64, _I, _I, _P, _P, _P]),
@@ -174,11 +177,33 @@ def moe_grouped_ffn_ws_bytes(cap: int, I: int, dtype: torch.dtype) -> int:
     return int(lib().moe_grouped_ffn_ws_bytes(cap, I, dtype_code(dtype)))
 
 
-def utilization_rate(per_range_counts: Sequence[float]) -> float:
-    """Balancedness (mean + 1e-5) / (max + 1e-5) of per-rank token counts (SGLang
-    chapter 17, section "不均衡的代价与冗余专家的思路", compute_utilization_rate)."""
-    vals = [float(v) for v in per_range_counts]
-    return (sum(vals) / len(vals) + 1e-5) / (max(vals) + 1e-5)
+def moe_balancedness(loads: Sequence[int]) -> float:
+    """Balancedness of per-rank token loads (host helper of the C ABI)."""
+    arr = (ctypes.c_int64 * len(loads))(*[int(v) for v in loads])
+    v = float(lib().moe_balancedness(ctypes.cast(arr, _P), len(loads)))
+    if v < 0:
+        raise MoeError("moe_balancedness", MOE_ERR_INVALID_ARG)
+    return v
+
+
+def moe_range_loads(counts: Sequence[int], n_ranges: int) -> List[int]:
+    """Token loads of n_ranges contiguous equal slot ranges (host helper of the C ABI)."""
+    c = _host_i32(counts)
+    out = (ctypes.c_int64 * n_ranges)()
+    _check("moe_range_loads", lib().moe_range_loads(ctypes.cast(c, _P), len(counts), n_ranges,
+                                                    ctypes.cast(out, _P)))
+    return [int(v) for v in out]
+
+
+def moe_logical_counts(counts_P: Sequence[int], p2l: Sequence[int], E: int) -> List[int]:
+    """Tokens per logical expert from tokens per physical slot (host helper of the C ABI)."""
+    if len(p2l) != len(counts_P):
+        raise MoeError("moe_logical_counts", MOE_ERR_INVALID_ARG)
+    c, m = _host_i32(counts_P), _host_i32(p2l)
+    out = (ctypes.c_int64 * E)()
+    _check("moe_logical_counts", lib().moe_logical_counts(ctypes.cast(c, _P), ctypes.cast(m, _P),
+                                                          len(counts_P), E, ctypes.cast(out, _P)))
+    return [int(v) for v in out]
 
 
 # ---------------------------------------------------------------- device calls
@@ -329,6 +354,18 @@ def moe_dispatch_noalloc(x: Optional[torch.Tensor], ids: torch.Tensor, E: int, P
     rows, k = ids.shape
     H = x.shape[1] if x is not None else 0
     dt = dtype_code(x.dtype) if x is not None else MOE_BF16
+    # the kernels write these through plain pointers: refuse other shapes before any launch
+    i32 = lambda t, shape: (t is not None and tuple(t.shape) == shape  # noqa: E731
+                            and t.dtype == torch.int32 and t.is_contiguous())
+    ok = (i32(counts_P, (P,)) and i32(offsets_P, (P + 1,)) and i32(inv, (rows, k))
+          and perm is not None and perm.dtype == torch.int32 and perm.dim() == 1
+          and perm.is_contiguous())
+    if sorted_out is not None:
+        ok = ok and (x is not None and sorted_out.dtype == x.dtype and sorted_out.dim() == 2
+                     and sorted_out.shape[0] == perm.numel() and sorted_out.shape[1] == H
+                     and sorted_out.is_contiguous())
+    if not ok:
+        raise MoeError("moe_dispatch_noalloc", MOE_ERR_INVALID_ARG)
     X = l2p.shape[1] if l2p is not None else 0
     _check("moe_dispatch_noalloc", lib().moe_dispatch_noalloc(
         _ptr(x), _ptr(ids), rows, k, H, dt, E, P, _ptr(l2p), _ptr(nrep), X, align,

@@ -133,6 +133,36 @@ size_t moe_dispatch_ws_bytes(int64_t rows, int k, int E);
  * h[cap, I] in the layer dtype. */
 size_t moe_grouped_ffn_ws_bytes(int64_t cap, int I, int dtype);
 
+/* EPLB load report, [P1] section "不均衡的代价与冗余专家的思路"
+ * (compute_utilization_rate): balancedness of per-rank token loads,
+ * (mean + 1e-5) / (max + 1e-5); 1 is perfect balance, the 1e-5 keeps an
+ * all-idle layer at 1.
+ *   loads  host int64[n], tokens per simulated EP rank (>= 0)
+ * Returns the balancedness in (0, 1], or -1.0 for a null array, n < 1 or a
+ * negative load. */
+double moe_balancedness(const int64_t* loads, int n);
+
+/* Token loads of n_ranges contiguous, equal ranges of n slots (the simulated
+ * EP ranks of [P1] section "逻辑与物理的两套映射": rank r holds slots
+ * [r * n / n_ranges, (r + 1) * n / n_ranges)).
+ *   counts  host int32[n], tokens per slot (>= 0)
+ *   loads   host int64[n_ranges] out
+ * Returns MOE_ERR_INVALID_ARG for null arrays, n_ranges < 1, n not a multiple
+ * of n_ranges or a negative count. */
+moe_status moe_range_loads(const int32_t* counts, int n, int n_ranges, int64_t* loads);
+
+/* Tokens per logical expert from tokens per physical slot: the sum over each
+ * logical expert's replicas ([P1] section "逻辑与物理的两套映射",
+ * physical_to_logical_map; the scatter_add of per-slot counts into logical
+ * counts in section "推理时怎么选副本").
+ *   counts_P  host int32[P], tokens per slot (>= 0)
+ *   p2l       host int32[P], logical expert of each slot, in [0, E)
+ *   counts_E  host int64[E] out
+ * Returns MOE_ERR_INVALID_ARG for null arrays, P < 1, E < 1, a negative count
+ * or a map entry outside [0, E). */
+moe_status moe_logical_counts(const int32_t* counts_P, const int32_t* p2l, int P, int E,
+                              int64_t* counts_E);
+
 /* ========================================================================
  * Device calls
  * ======================================================================== */

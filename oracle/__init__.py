@@ -91,7 +91,7 @@ def _load():
             "orc_quant_blocks": (None, [P, i64, ctypes.c_int, P, P]),
             "orc_expert_ffn_fp8": (None, [P, P, i64, ctypes.c_int, ctypes.c_int, P, P, P, P,
                                           P]),
-            "orc_router_logits": (None, [P, i64, ctypes.c_int, P, ctypes.c_int, P]),
+            "orc_router_logits": (None, [P, i64, ctypes.c_int, P, ctypes.c_int, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -390,13 +390,19 @@ def grouped_ffn_fp8(xq, xe, offsets, wq, slot_lo: int = 0, slot_hi: int | None =
 
 
 # ---------------------------------------------------------------- router GEMM
-def router_logits(x, w) -> np.ndarray:
-    """Gate projection: x [rows, H] f32, w [E, H] f32 -> logits [rows, E] f64."""
+def router_logits(x, w, bias=None) -> np.ndarray:
+    """Gate projection: x [rows, H] f32, w [E, H] f32, optional bias [E] f32
+    -> logits [rows, E] f64 (x . w^T, plus the bias)."""
     x, w = _c(x, np.float32), _c(w, np.float32)
     rows, H = x.shape
     E = w.shape[0]
     assert w.shape == (E, H)
+    b = None
+    if bias is not None:
+        b = _c(bias, np.float32)
+        assert b.shape == (E,)
     out = np.empty((rows, E), np.float64)
     if rows:
-        _load().orc_router_logits(_p(x), rows, H, _p(w), E, _p(out))
+        _load().orc_router_logits(_p(x), rows, H, _p(w), E, None if b is None else _p(b),
+                                  _p(out))
     return out

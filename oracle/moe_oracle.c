@@ -642,16 +642,22 @@ void orc_expert_ffn_fp8(const uint8_t *xq, const uint8_t *xe, int64_t n, int H, 
 /* ------------------------------------------------------------------------ */
 /* Router GEMM.  [P1] section "Two-batch Overlap" lists the MoE operations   */
 /* op_gate then op_select_experts: the gate projects each token's hidden     */
-/* state onto the experts and top-k selection follows.  Reading: a linear    */
-/* gate without bias, logits[g, e] = sum_h x[g, h] * w[e, h] (w [E, H]),     */
-/* h ascending; selection is orc_route_topk on these logits.                */
-/* Parity: pinned (numpy matmul).                                            */
+/* state onto the experts and top-k selection follows; section "推理时怎么    */
+/* “选副本”" hands select_experts the router logits together with a          */
+/* per-expert correction bias.  Reading: a linear gate with an optional      */
+/* per-expert bias, logits[g, e] = sum_h x[g, h] * w[e, h] + b[e]            */
+/* (w [E, H], h ascending, the bias added once after the sum; bias NULL is   */
+/* the gate without bias); selection is orc_route_topk on these logits.     */
+/* Parity: pinned (numpy matmul plus bias; a zero gate returns the bias;     */
+/* a bias that reorders two experts moves the top-1).                        */
 /* ------------------------------------------------------------------------ */
-void orc_router_logits(const float *x, int64_t rows, int H, const float *w, int E, double *logits) {
+void orc_router_logits(const float *x, int64_t rows, int H, const float *w, int E,
+                       const float *bias, double *logits) {
   for (int64_t g = 0; g < rows; ++g)
     for (int e = 0; e < E; ++e) {
       double s = 0.0;
       for (int h = 0; h < H; ++h) s += (double)x[g * H + h] * (double)w[(int64_t)e * H + h];
+      if (bias != NULL) s += (double)bias[e];
       logits[g * E + e] = s;
     }
 }

@@ -64,3 +64,93 @@ def graph_replay_matches_eager(layer, x_loc, lg_loc, out):
     for a, b in zip(out2, eager):
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+
+
+# ------------------------------------------------------------------ hard rows
+def ffn_kernel_of(layer) -> str:
+    """Which grouped-FFN kernel the library runs for this layer: FP8 -> 'fp8' (weights
+    as M, units of up to 64 tokens); bf16 with >= 192 sorted rows per slot on average
+    -> 'pair' (weights as M on SM pairs, units of up to 320 tokens); else 'tc' (tokens
+    as M, 128-row m-tiles)."""
+    if getattr(layer, "fp8", False):
+        return "fp8"
+    return "pair" if layer.cap // max(layer.P, 1) >= 192 else "tc"
+
+
+def _slot_positions(rows: int, kernel: str):
+    """Positions within a slot of `rows` sorted rows where the kernel's tiling changes."""
+    pos = set()
+    if kernel == "pair":
+        # unit = up to 320 tokens; N = tokens rounded up to 16, CTA c of the pair holds
+        # tokens [c*N/2, (c+1)*N/2); the first MMA (N0 = min(N, 256)) reads the first
+        # N0/2 of each CTA's rows, the tail MMA the rest (columns 256-319)
+        for g0 in range(0, rows, 320):
+            nt = min(320, rows - g0)
+            N = (nt + 15) & ~15
+            h, n0 = N // 2, min(N, 256)
+            for p in (0, 31, 32, n0 // 2 - 1, n0 // 2, h - 1, h, h + 31, h + 32,
+                      h + n0 // 2 - 1, h + n0 // 2, N - 1, nt - 1):
+                if 0 <= p < nt:
+                    pos.add(g0 + p)
+    elif kernel == "tc":
+        # 128-row m-tiles; epilogue warps own 32-row lane quarters
+        tiles = list(range(0, rows, 128))
+        for t0 in tiles[:1] + tiles[-1:]:
+            for p in (0, 31, 32, 63, 64, 95, 96, 127):
+                if t0 + p < rows:
+                    pos.add(t0 + p)
+        pos.add(rows - 1)
+    else:  # fp8: units of up to 64 tokens, two epilogue warps of 32 token columns
+        groups = list(range(0, rows, 64))
+        for g0 in groups[:2] + groups[-1:]:
+            for p in (0, 31, 32, 63):
+                if g0 + p < rows:
+                    pos.add(g0 + p)
+        pos.add(rows - 1)
+    return sorted(pos)
+
+
+def hard_rows(offsets, kernel: str, min_rows: int = 64, seed: int = 0):
+    """Sorted-buffer rows d at the grouped-FFN kernel's tiling boundaries: the first and
+    last token of every unit, lane-quarter and 32-column chunk edges, and (pair kernel)
+    both sides of the split between the N <= 256 MMA and the tail MMA of columns
+    256-319.  Slots are taken largest first, then the smallest non-empty one, a slot
+    whose last unit has a tail MMA, then seeded random slots, until at least min_rows
+    rows are chosen."""
+    offsets = np.asarray(offsets, np.int64)
+    counts = np.diff(offsets)
+    nz = np.nonzero(counts > 0)[0]
+    if len(nz) == 0:
+        return []
+    order = [int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])])]
+    tail = [int(s) for s in nz if 256 < (counts[s] - 1) % 320 + 1 <= 320]
+    order += tail[:2]
+    rng = np.random.default_rng(seed)
+    order += [int(s) for s in rng.permutation(nz)]
+    out, seen = [], set()
+    for s in order:
+        if s in seen:
+            continue
+        seen.add(s)
+        out += [int(offsets[s]) + p for p in _slot_positions(int(counts[s]), kernel)]
+        if len(out) >= min_rows and len(seen) >= 4:
+            break
+    return sorted(set(out))
+
+
+def pairs_to_check(layer, o_o, p_o, i_o, real, kk: int, sample):
+    """(token, j) pairs whose expert outputs a layer test compares with the oracle, and
+    the tokens whose combined rows it compares.  sample None: every real token and
+    all its pairs.  Otherwise the pairs at the kernel's hard rows (at least 64; see
+    hard_rows), plus the first two and last two real tokens and `sample` tokens
+    spread over the hard pairs, each with all of its kk pairs."""
+    if sample is None:
+        return [(int(g), j) for g in real for j in range(kk)], real
+    hard = [d for d in hard_rows(o_o, ffn_kernel_of(layer)) if p_o[d] >= 0]
+    hard_pairs = [(int(p_o[d]), int(np.nonzero(i_o[p_o[d]] == d)[0][0])) for d in hard]
+    assert len(hard_pairs) >= 64, len(hard_pairs)
+    picked = np.unique([g for g, _ in hard_pairs])
+    spread = picked[np.linspace(0, len(picked) - 1, min(sample, len(picked))).astype(int)]
+    toks = np.unique(np.concatenate([real[:2], real[-2:], spread])).astype(np.int64)
+    pairs = set(hard_pairs) | {(int(g), j) for g in toks for j in range(kk)}
+    return sorted(pairs), toks

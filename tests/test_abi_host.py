@@ -26,7 +26,7 @@ def md():
 def declared_symbols():
     text = open(HEADER).read()
     return sorted(set(re.findall(
-        r"^\s*(?:moe_status|int|int64_t|size_t|const char\*)\s+(moe_\w+)\s*\(", text, re.M)))
+        r"^\s*(?:moe_status|int|int64_t|size_t|double|const char\*)\s+(moe_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declarations_are_exported(md):
@@ -83,7 +83,36 @@ def test_layout_and_mode_agree_with_oracle_exhaustively(md, orc):
 
 @pytest.mark.parametrize("row", read_golden("balancedness.txt"))
 def test_balancedness_golden(md, row):
-    assert md.utilization_rate(ints(row[0])) == pytest.approx(float(row[1]), rel=1e-15)
+    assert md.moe_balancedness(ints(row[0])) == pytest.approx(float(row[1]), rel=1e-15)
+
+
+def test_balancedness_rejects_bad_loads(md):
+    for bad in ([], [3, -1]):
+        with pytest.raises(md.MoeError):
+            md.moe_balancedness(bad)
+
+
+def test_range_loads_and_logical_counts(md):
+    counts = [3, 0, 5, 7, 1, 1, 0, 2, 9]
+    # three ranges of three slots each: closed-form sums
+    assert md.moe_range_loads(counts, 3) == [8, 9, 11]
+    assert md.moe_range_loads(counts, 1) == [sum(counts)]
+    assert md.moe_range_loads(counts, 9) == counts
+    for bad_n in (2, 4, 0):            # 9 slots do not split into equal ranges of these
+        with pytest.raises(md.MoeError):
+            md.moe_range_loads(counts, bad_n)
+    with pytest.raises(md.MoeError):
+        md.moe_range_loads([1, -2], 1)
+    # slots 0, 4 and 8 replicate logical expert 0; the rest map one to one
+    p2l = [0, 1, 2, 3, 0, 4, 5, 6, 0]
+    got = md.moe_logical_counts(counts, p2l, 7)
+    assert got == [3 + 1 + 9, 0, 5, 7, 1, 0, 2]
+    assert sum(got) == sum(counts)
+    # the identity map returns the counts themselves
+    assert md.moe_logical_counts(counts, list(range(9)), 9) == counts
+    for bad_map in ([0] * 8 + [7], [0] * 8 + [-1]):
+        with pytest.raises(md.MoeError):
+            md.moe_logical_counts(counts, bad_map, 7)
 
 
 def test_sizes(md):

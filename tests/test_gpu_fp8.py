@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from gpu_util import (BF16_ATOL, BF16_RTOL, as_f32, assert_close, graph_replay_matches_eager,
-                      rel_fro, to_np)
+                      pairs_to_check, rel_fro, to_np)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -313,14 +313,13 @@ def _layer_fp8_check(md, orc, spec, sample=None, l2p_np=None, nrep_np=None, p2l=
     assert np.array_equal(to_np(layer.xq[:n]), q_o[p_o[:n]])
     assert np.array_equal(to_np(layer.xq_scales[:n]), s_o[p_o[:n]])
     real = np.nonzero(valid)[0]
-    toks = real if sample is None else np.unique(np.concatenate(
-        [real[:1], real[-1:], np.random.default_rng(0).choice(real, size=min(sample, len(real)),
-                                                             replace=False)]))
+    # every pair of small layers; at full size the kernel's hard rows and a few
+    # tokens' combined rows
+    check, toks = pairs_to_check(layer, o_o, p_o, i_o, real, kk, sample)
     slot_of = np.searchsorted(o_o, np.arange(n), side="right") - 1
     need = {}
-    for g in toks:
-        for j in range(kk):
-            need.setdefault(int(slot_of[i_o[g, j]]), []).append((int(g), j))
+    for g, j in check:
+        need.setdefault(int(slot_of[i_o[g, j]]), []).append((g, j))
     guq, gus, dq, ds = layer.w_fp8
     y_ref = {}
     for s, pairs in need.items():
@@ -333,13 +332,13 @@ def _layer_fp8_check(md, orc, spec, sample=None, l2p_np=None, nrep_np=None, p2l=
         for (g, j), y in zip(pairs, ys_s):
             y_ref[(g, j)] = y
     yg = as_f32(to_np(layer.yg[:rows]))
+    for (g, j), y in y_ref.items():
+        assert_close(as_f32(to_np(layer.ys[int(i_o[g, j])])), y, BF16_ATOL, BF16_RTOL,
+                     f"fp8 expert out row {g} j {j} (sorted row {i_o[g, j]})")
     for g in toks:
         ref = np.zeros(spec.H)
         for j in range(kk):
-            y = y_ref[(int(g), j)]
-            assert_close(as_f32(to_np(layer.ys[int(i_o[g, j])])), y, BF16_ATOL, BF16_RTOL,
-                         f"fp8 expert out row {g} j {j}")
-            ref += w_o[g, j] * y
+            ref += w_o[g, j] * y_ref[(int(g), j)]
         assert_close(yg[g], ref, BF16_ATOL, BF16_RTOL, f"fp8 combined row {g}")
     assert not yg[valid == 0].any()
     got = np.concatenate([as_f32(to_np(t)) for t in out])

@@ -16,7 +16,8 @@ import torch
 import oracle as orc_mod
 from combine_dp_gather_gb300 import synth
 from gpu_util import (BF16_ATOL, BF16_RTOL, F32_ATOL, F32_RTOL, W_ATOL, W_RTOL, as_f32,
-                      assert_close, graph_replay_matches_eager, rel_fro, to_np)
+                      assert_close, graph_replay_matches_eager, pairs_to_check, rel_fro,
+                      to_np)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -601,14 +602,13 @@ def _check_layer(md, orc, spec, layer, out, x_loc, lg_loc, wgu, wd, offs, rows, 
         assert not as_f32(to_np(layer.ys[:n]))[pad].any()
     x_f = as_f32(xg_o)
     real = np.nonzero(valid)[0]
-    toks = real if sample is None else np.unique(np.concatenate(
-        [real[:2], real[-2:], np.random.default_rng(0).choice(real, size=min(sample, len(real)),
-                                                             replace=False)]))
+    # every pair of small layers; at full size the kernel's hard rows and a few
+    # tokens' combined rows
+    check, toks = pairs_to_check(layer, o_o, p_o, i_o, real, kk, sample)
     slot_of = np.searchsorted(o_o, np.arange(n), side="right") - 1
     need = {}
-    for g in toks:
-        for j in range(kk):
-            need.setdefault(int(slot_of[i_o[g, j]]), []).append((int(g), j))
+    for g, j in check:
+        need.setdefault(int(slot_of[i_o[g, j]]), []).append((g, j))
     y_ref = {}
     for s, pairs in need.items():
         wg_s, wd_s = as_f32(to_np(wgu[s])), as_f32(to_np(wd[s]))
@@ -618,13 +618,13 @@ def _check_layer(md, orc, spec, layer, out, x_loc, lg_loc, wgu, wd, offs, rows, 
     ys_gpu = {d: as_f32(to_np(layer.ys[d])) for d in {int(i_o[g, j]) for g, j in y_ref}}
     yg_gpu = as_f32(to_np(layer.yg[:rows]))
     worst = 0.0
+    for (g, j), y in y_ref.items():
+        worst = max(worst, assert_close(ys_gpu[int(i_o[g, j])], y, atol, rtol,
+                                        f"expert out row {g} j {j} (sorted row {i_o[g, j]})"))
     for g in toks:
         ref = np.zeros(spec.H)
         for j in range(kk):
-            y = y_ref[(int(g), j)]
-            worst = max(worst, assert_close(ys_gpu[int(i_o[g, j])], y, atol, rtol,
-                                            f"expert out row {g} j {j}"))
-            ref += w_o[g, j] * y
+            ref += w_o[g, j] * y_ref[(int(g), j)]
         assert_close(yg_gpu[g], ref, atol, rtol, f"combined row {g}")
     assert not yg_gpu[valid == 0].any()                                   # pad rows zero
     # scatter returns exactly the valid rows of the combined buffer (any size)

@@ -60,9 +60,7 @@ def test_route_gemm_topk(md, orc, counts, mode, H, E, k, renorm, n_shared, bias)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     valid = orc.valid_rows(counts, np.array(offs), rows)
-    ref = orc.router_logits(as_f32(to_np(x)), as_f32(to_np(wr)))
-    if bias:
-        ref = ref + to_np(b).astype(np.float64)[None, :]
+    ref = orc.router_logits(as_f32(to_np(x)), as_f32(to_np(wr)), None if b is None else to_np(b))
     got_l = to_np(logits)
     # fp32 sums of H bf16 products (logits ~ N(0, 1)): each addition rounds by about
     # 2^-24 x |partial sum| (~1e-7 here), ~1e-5 over 7168 terms as a random walk and
@@ -104,7 +102,7 @@ def test_layer_with_router_gate(md, orc):
     valid = orc.valid_rows(spec.counts, offs_o, rows_o)
     xg_o = orc.dp_gather([to_np(t) for t in x_loc], spec.counts, offs_o, rows_o)
     assert np.array_equal(to_np(layer.xg[:rows]), xg_o)
-    lg64 = orc.router_logits(as_f32(xg_o), as_f32(to_np(gw))) + to_np(gb)[None, :]
+    lg64 = orc.router_logits(as_f32(xg_o), as_f32(to_np(gw)), to_np(gb))
     ids_o, w_o = orc.route_topk(lg64.astype(np.float32), spec.k, True, valid)
     ids_g, w_g = to_np(layer.ids[:rows]), to_np(layer.w[:rows])
     same = np.array([set(ids_g[r]) == set(ids_o[r]) for r in range(rows)])

@@ -726,3 +726,29 @@ def test_router_logits_match_numpy_and_feed_topk(orc):
     w2[3] = x[0]
     ids, _ = orc.route_topk(orc.router_logits(x[:1], w2), 1, True, np.ones(1, np.uint8))
     assert ids.tolist() == [[3]]
+
+
+def test_router_logits_bias(orc):
+    """The optional per-expert bias is added once to every row's logits."""
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((6, 40)).astype(np.float32)
+    w = rng.standard_normal((9, 40)).astype(np.float32)
+    b = rng.standard_normal(9).astype(np.float32)
+    lg = orc.router_logits(x, w, b)
+    np.testing.assert_allclose(lg, x.astype(np.float64) @ w.astype(np.float64).T
+                               + b.astype(np.float64)[None, :], rtol=1e-12, atol=1e-12)
+    # without a bias it is the plain gate
+    np.testing.assert_array_equal(orc.router_logits(x, w, None), orc.router_logits(x, w))
+    # a zero gate returns the bias itself in every row, exactly
+    z = orc.router_logits(x, np.zeros_like(w), b)
+    np.testing.assert_array_equal(z, np.tile(b.astype(np.float64), (6, 1)))
+    # a bias that lifts expert 2 above expert 3 moves the top-1 there: the gate's row
+    # for expert 3 is the token itself (x . x > 0), expert 2's row is zero
+    w3 = np.zeros((5, 40), np.float32)
+    w3[3] = x[0]
+    gap = float(np.dot(x[0].astype(np.float64), x[0].astype(np.float64)))
+    b3 = np.zeros(5, np.float32)
+    b3[2] = np.float32(gap + 1.0)
+    one = np.ones(1, np.uint8)
+    assert orc.route_topk(orc.router_logits(x[:1], w3), 1, True, one)[0].tolist() == [[3]]
+    assert orc.route_topk(orc.router_logits(x[:1], w3, b3), 1, True, one)[0].tolist() == [[2]]

@@ -46,8 +46,12 @@ def _outputs(md, rows, k, P, H, align, dev="cuda"):
 def test_noalloc_dispatch_matches_dispatch_on_two_calls():
     md = _lib()
     from combine_dp_gather_gb300 import synth
+    # both calls exceed the one-CTA path's 8192 routed pairs, so both keep their
+    # chunk histograms in the shared scratch; the second (12 chunks x 48 experts)
+    # uses fewer entries than the first (24 chunks x 64 experts) left behind, and
+    # must not see them
     cases = [dict(rows=3001, k=8, E=64, H=512, align=1, seed=1, map=False),
-             dict(rows=517, k=4, E=48, H=256, align=4, seed=2, map=True)]
+             dict(rows=1500, k=8, E=48, H=256, align=4, seed=2, map=True)]
     for c in cases:
         ids, x = _case(c["rows"], c["k"], c["E"], c["H"], c["seed"])
         l2p = nrep = None
@@ -82,3 +86,46 @@ def test_noalloc_dispatch_rejects_problems_beyond_its_scratch():
     code = md.lib().moe_dispatch_noalloc(fake, fake, rows, k, 64, 1, E, E, None, None, 0, 1,
                                          rows * k, fake, fake, fake, fake, fake, None, None)
     assert code == md.MOE_ERR_CAPACITY
+
+
+def test_noalloc_dispatch_checks_arguments_before_its_scratch_size():
+    """An invalid call that is also too large for the scratch returns what
+    moe_dispatch returns for the same arguments, not MOE_ERR_CAPACITY."""
+    md = _lib()
+    fake = ctypes.c_void_p(0x1000)
+    rows, E = 40000, 256
+    for k, P, want in ((33, E, md.MOE_ERR_INVALID_ARG),          # k > MOE_MAX_TOPK
+                       (8, E + 1, md.MOE_ERR_INVALID_ARG)):       # P != E without a map
+        code = md.lib().moe_dispatch_noalloc(fake, fake, rows, k, 64, 1, E, P, None, None, 0, 1,
+                                             rows * k, fake, fake, fake, fake, fake, None, None)
+        assert code == want, (k, P, code)
+    # an unsupported dtype with rows to move: the same status as moe_dispatch
+    code = md.lib().moe_dispatch_noalloc(fake, fake, rows, 8, 64, 9, E, E, None, None, 0, 1,
+                                         rows * 8, fake, fake, fake, fake, fake, None, None)
+    assert code == md.MOE_ERR_UNSUPPORTED
+
+
+def test_noalloc_binding_refuses_misshaped_outputs():
+    md = _lib()
+    import torch
+    rows, k, E, H = 8, 2, 4, 64
+    ids = torch.zeros(rows, k, dtype=torch.int32)
+    x = torch.zeros(rows, H, dtype=torch.bfloat16)
+    cap = rows * k
+    good = dict(counts_P=torch.zeros(E, dtype=torch.int32),
+                offsets_P=torch.zeros(E + 1, dtype=torch.int32),
+                perm=torch.zeros(cap, dtype=torch.int32),
+                inv=torch.zeros(rows, k, dtype=torch.int32),
+                sorted_out=torch.zeros(cap, H, dtype=torch.bfloat16))
+    bad = [("counts_P", torch.zeros(E - 1, dtype=torch.int32)),
+           ("offsets_P", torch.zeros(E, dtype=torch.int32)),
+           ("inv", torch.zeros(rows, k + 1, dtype=torch.int32)),
+           ("inv", torch.zeros(rows, k, dtype=torch.int64)),
+           ("sorted_out", torch.zeros(cap, H, dtype=torch.float32)),
+           ("sorted_out", torch.zeros(cap - 1, H, dtype=torch.bfloat16))]
+    for name, t in bad:
+        args = dict(good, **{name: t})
+        with pytest.raises(md.MoeError) as ei:   # refused on the host, before any launch
+            md.moe_dispatch_noalloc(x, ids, E, E, args["counts_P"], args["offsets_P"],
+                                    args["perm"], args["inv"], args["sorted_out"])
+        assert ei.value.code == md.MOE_ERR_INVALID_ARG, name
