@@ -48,22 +48,23 @@ UNIT = "tokens/s"
 L2_NOTE = "inputs larger than L2: every step streams the touched experts' weights from HBM"
 
 def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
-                      fp8: bool = False, router_gemm: bool = False, sms: int = 152) -> int:
+                      fp8: bool = False, router_gemm: bool = False, sms: int = 152,
+                      fused_combine: bool = False) -> int:
     """Kernel launches of one layer step: gather (with given logits it routes the rows
     in the same launch, the fused add + RMSNorm included), dispatch (one CTA-wide kernel for <= 8192 routed pairs whose tables
     fit 48 KB, else histogram + scan + rank; then the row copy; + the alignment pad
     kernel when align > 1, plus the FP8 rows' pad kernel on the FP8 path), grouped FFN
     (MM1+SwiGLU and MM2; one persistent launch for both on FP8), combine with the DP
-    scatter.  With the router gate GEMM the
-    logits gather goes and routing is one fused kernel (>= sms/4 row tiles and k <= 8)
-    or split GEMM + sum + top-k."""
+    scatter (none when the down projection's epilogue combines).  With the router gate
+    GEMM the logits gather goes and routing is one fused kernel (>= sms/4 row tiles and
+    k <= 8) or split GEMM + sum + top-k."""
     small = rows * k <= 8192 and 4 * (33 * E + 3 * P + 1) <= 48 * 1024
     dispatch = (1 if small else 3) + 1 + (1 + (1 if fp8 else 0) if align > 1 else 0)
     gather, route = 1, 0
     if router_gemm:
         gather = 1
         route = 1 if (k <= 8 and 4 * ((rows + 127) // 128) >= sms) else 3
-    return gather + route + dispatch + (1 if fp8 else 2) + 1
+    return gather + route + dispatch + (1 if fp8 else 2) + (0 if fused_combine else 1)
 
 
 def ffn_kernel(cap: int, P: int, fp8: bool = False) -> str:
@@ -126,6 +127,11 @@ def parse():
     ap.add_argument("--exec", default="graph", choices=["graph", "eager"],
                     help="graph: each step is a replay of a CUDA graph of the layer (all its "
                          "kernels; captured before the timed region); eager: stream launches")
+    ap.add_argument("--combine", default="separate", choices=["fused", "separate"],
+                    help="fused: combine + DP scatter through moe_grouped_ffn_combine (in the "
+                         "down projection's epilogue with few rows per slot, else its own "
+                         "launch inside the call); separate: moe_grouped_ffn, then "
+                         "moe_combine_scatter")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 dispatch and grouped FFN (e4m3, UE8M0 scales per 128-token group "
                          "and 128x128 weight block); layer input and output stay bf16")
@@ -287,7 +293,8 @@ def run_native(args, rank, world, local_rank):
         tokens_per_req=spec.tokens_per_req, renormalize=spec.renormalize, align=spec.align,
         l2p=None if l2p_np is None else torch.from_numpy(l2p_np).to(dev),
         nrep=None if nrep_np is None else torch.from_numpy(nrep_np).to(dev),
-        n_shared=spec.n_shared, fp8=args.fp8, router_weight=gate_w, router_bias=gate_b)
+        n_shared=spec.n_shared, fp8=args.fp8, router_weight=gate_w, router_bias=gate_b,
+        fused_combine=(args.combine == "fused" and not args.fp8))
     out = [torch.empty(c, spec.H, device=dev, dtype=wgu.dtype) for c in spec.counts]
     res_loc = None
     if args.boundary == "addnorm":
@@ -353,6 +360,13 @@ def run_native(args, rank, world, local_rank):
             spec.H * (1 + 1 / 128) + 2 * spec.I * (1 + 1 / 128) + 2 * spec.H)
     else:
         ffn_bytes = touched * 3 * spec.I * spec.H * b + routed * (2 * spec.H + 2 * spec.I) * b
+        if layer.fused_combine:
+            # the call's combine: the routed rows read back, T rows written, inv and w
+            kk = spec.k + spec.n_shared
+            ffn_bytes += T * kk * spec.H * b + T * spec.H * b + T * kk * 8
+    # the combine runs inside the grouped-FFN call's down projection (no launch of its own)
+    in_epi = layer.fused_combine and md.moe_grouped_ffn_combine_in_epilogue(
+        layer.cap, layer.P, layer.dtype)
     ffn_flops = synth.flops_ffn(T, spec.k + spec.n_shared, spec.H, spec.I)
     ffn_ms = stage_ms["ffn"]
     pk = peaks()
@@ -374,6 +388,12 @@ def run_native(args, rank, world, local_rank):
     roof.update({"traffic": ffn_traffic(args),
                  "kernel": (f"moe_grouped_ffn_fp8 ({ffn_kernel(layer.cap, layer.P, True)}: "
                             "MM1+SwiGLU and MM2 in one persistent launch)" if args.fp8 else
+                            f"moe_grouped_ffn_combine ({ffn_kernel(layer.cap, layer.P)} "
+                            "MM1+SwiGLU and MM2 launches; combine + DP scatter in MM2's "
+                            "epilogue)" if layer.fused_combine and in_epi else
+                            f"moe_grouped_ffn_combine ({ffn_kernel(layer.cap, layer.P)} "
+                            "MM1+SwiGLU and MM2 launches, then the combine + DP scatter "
+                            "launch)" if layer.fused_combine else
                             f"moe_grouped_ffn ({ffn_kernel(layer.cap, layer.P)} MM1+SwiGLU "
                             "and MM2 launches)"),
                  "tflops": round(tflops, 1),
@@ -387,7 +407,8 @@ def run_native(args, rank, world, local_rank):
                  "algorithmic_bytes": int(ffn_bytes), "algorithmic_flops": int(ffn_flops),
                  "touched_slots": touched, "ffn_ms_per_step": round(ffn_ms, 4),
                  "ffn_samples": len(stage.get("ffn", [])),
-                 "permutes": permute_fractions(spec, rows, stage_ms, pk["hbm_gbs"], args.fp8)})
+                 "permutes": permute_fractions(spec, rows, stage_ms, pk["hbm_gbs"], args.fp8,
+                                               layer.fused_combine)})
 
     # ---- e2e: same calls, inputs from pinned host memory, outputs back to host
     e2e = None
@@ -496,7 +517,8 @@ def run_native(args, rank, world, local_rank):
                 launches=launches_per_step(max(rows, 1), spec.k + spec.n_shared,
                                            spec.E + spec.n_shared, layer.P, layer.cap,
                                            spec.align, args.fp8, args.router == "gemm",
-                                           torch.cuda.get_device_properties(dev).multi_processor_count),
+                                           torch.cuda.get_device_properties(dev).multi_processor_count,
+                                           bool(in_epi)),
                 inputs=(x_loc, lg_loc, wgu, wd, l2p_np, nrep_np), gate=gate_np)
 
 
@@ -508,7 +530,8 @@ def stage_every(args) -> int:
     return max(1, args.steps // 50)
 
 
-def permute_fractions(spec, rows: int, stage_ms: dict, hbm_gbs: float, fp8: bool = False):
+def permute_fractions(spec, rows: int, stage_ms: dict, hbm_gbs: float, fp8: bool = False,
+                      fused_combine: bool = False):
     """Algorithmic bytes of the layer's row-moving stages over their live stage time
     (CUDA events on the launching stream, launch gaps included), against the measured
     HBM copy bandwidth.  T real tokens, `rows` global rows, kk routed slots per token,
@@ -536,6 +559,9 @@ def permute_fractions(spec, rows: int, stage_ms: dict, hbm_gbs: float, fp8: bool
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
                      "achieved_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_gbs, 4)}
+    if fused_combine:
+        out["combine_scatter"] = ("inside the moe_grouped_ffn_combine call (its bytes are "
+                                  "counted in the FFN's)")
     out["target_frac_of_hbm"] = 0.70
     out["peak_gbs"] = hbm_gbs
     return out

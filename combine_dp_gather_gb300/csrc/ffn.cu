@@ -132,3 +132,119 @@ extern "C" moe_status moe_grouped_ffn(const void* d_sorted, const int32_t* d_off
   }
   return launch_ffn_simt_f32(a, s);
 }
+
+// ---------------------------------------------------------------------------
+// Grouped FFN with the combine and the DP scatter in the down projection's
+// epilogue (vLLM chapter 27, figure "MoE 模块化内核的 PrepareAndFinalize 块结构":
+// MM2, then finalize applies the top-k weights; SGLang chapter 17, section
+// "scatter: 把 MoE 的输出还回本副本").  Workspace: h [cap, I] in the layer dtype,
+// then (bf16) one int32 arrival counter per (global row, 256-feature n-tile).
+
+namespace {
+
+size_t fuse_h_bytes(int64_t cap, int I, int eb) {
+  return ((size_t)(cap * (int64_t)I * eb) + 255) & ~(size_t)255;
+}
+
+}  // namespace
+
+extern "C" size_t moe_grouped_ffn_combine_ws_bytes(int64_t cap, int64_t rows, int H, int I,
+                                                   int dtype) {
+  const int eb = dtype_bytes(dtype);
+  if (cap < 0 || rows < 0 || H < 1 || I < 1 || eb == 0) return 0;
+  if (dtype != MOE_BF16) return fuse_h_bytes(cap, I, eb);  // no counters on the float32 path
+  if (H % kFuseBlock != 0) return 0;
+  return fuse_h_bytes(cap, I, eb) + (size_t)rows * (size_t)(H / kFuseBlock) * sizeof(int32_t);
+}
+
+extern "C" int moe_grouped_ffn_combine_in_epilogue(int64_t cap, int P, int dtype) {
+  if (cap < 1 || P < 1 || dtype != MOE_BF16) return 0;
+  FfnArgs a = {};
+  a.cap = cap;
+  a.P = P;
+  return ffn_uses_pair_kernel(a) ? 0 : 1;
+}
+
+extern "C" moe_status moe_grouped_ffn_combine(
+    const void* d_sorted, const int32_t* d_offsets_P, int P, int slot_lo, int slot_hi, int64_t cap,
+    const void* d_w_gate_up, const void* d_w_down, int H, int I, int dtype, void* d_out_sorted,
+    const int32_t* d_perm, const int32_t* d_inv, const float* d_w, int64_t rows, int k,
+    const int32_t* d_counts, const int32_t* d_offsets, int R, void* const* local,
+    void* d_global_out, void* d_ws, size_t ws_bytes, uint32_t* d_status, void* stream) {
+  if (P < 1 || slot_lo < 0 || slot_hi > P || slot_lo > slot_hi || cap < 0 || cap > INT32_MAX ||
+      H < 1 || I < 1 || rows < 0 || rows > INT32_MAX || k < 1 || k > MOE_MAX_TOPK || R < 1 ||
+      R > MOE_MAX_REPLICAS)
+    return MOE_ERR_INVALID_ARG;
+  const int eb = dtype_bytes(dtype);
+  if (eb == 0) return MOE_ERR_UNSUPPORTED;
+  if (((int64_t)H * eb) % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (dtype == MOE_BF16 && (H % kFuseBlock != 0 || I % 128 != 0 || P > MOE_MAX_SLOTS))
+    return MOE_ERR_UNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  if (d_inv == nullptr || d_w == nullptr || d_counts == nullptr || d_offsets == nullptr ||
+      local == nullptr || d_ws == nullptr || (cap > 0 && (d_sorted == nullptr ||
+      d_offsets_P == nullptr || d_w_gate_up == nullptr || d_w_down == nullptr ||
+      d_out_sorted == nullptr || d_perm == nullptr)))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_grouped_ffn_combine_ws_bytes(cap, rows, H, I, dtype)) return MOE_ERR_CAPACITY;
+  if (!aligned16(d_sorted) || !aligned16(d_out_sorted) || !aligned16(d_ws) ||
+      !aligned16(d_w_gate_up) || !aligned16(d_w_down) ||
+      (d_global_out != nullptr && !aligned16(d_global_out)))
+    return MOE_ERR_INVALID_ARG;
+  for (int r = 0; r < R; ++r)
+    if (local[r] != nullptr && !aligned16(local[r])) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  void* h = d_ws;
+  if (dtype != MOE_BF16) {
+    // float32 layers (CUDA-core FFN): the FFN, then the combine + scatter launch
+    if (cap > 0 && slot_lo < slot_hi) {
+      FfnArgs a{d_sorted, d_offsets_P, P, slot_lo, slot_hi, cap, d_w_gate_up, d_w_down,
+                H, I, d_out_sorted, h, d_status};
+      const moe_status st = launch_ffn_simt_f32(a, s);
+      if (st != MOE_OK) return st;
+    }
+    return moe_combine_scatter(d_out_sorted, d_inv, d_w, rows, k, H, dtype, cap, d_counts,
+                               d_offsets, R, local, d_global_out, d_status, stream);
+  }
+  if ((int64_t)P * 2 * I > INT32_MAX || (int64_t)P * H > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  int major = 0, minor = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
+  FuseArgs f = {};
+  f.perm = d_perm;
+  f.inv = d_inv;
+  f.w = d_w;
+  f.cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(d_ws) + fuse_h_bytes(cap, I, eb));
+  f.rows = rows;
+  f.kk = k;
+  f.nblk = H / kFuseBlock;
+  f.H = H;
+  f.R = R;
+  f.counts = d_counts;
+  f.offsets = d_offsets;
+  f.global_out = static_cast<__nv_bfloat16*>(d_global_out);
+  for (int r = 0; r < R; ++r) f.dst.p[r] = local[r];
+  if (cap == 0 || slot_lo == slot_hi) {
+    // no expert rows: every real row's combine is an empty sum
+    return moe_combine_scatter(d_out_sorted, d_inv, d_w, rows, k, H, dtype, cap, d_counts,
+                               d_offsets, R, local, d_global_out, d_status, stream);
+  }
+  FfnArgs a{d_sorted, d_offsets_P, P, slot_lo, slot_hi, cap, d_w_gate_up, d_w_down,
+            H, I, d_out_sorted, h, d_status};
+  if (ffn_uses_pair_kernel(a)) {
+    // Many rows per slot: the pair kernel's down projection already moves its
+    // weights and rows at about 0.8 of the HBM roofline, and a combine in its
+    // epilogue must read the same expert rows back, so it only lengthened the
+    // epilogue (measured: MM2 2.11 ms fused against 1.65 + 0.18 ms for MM2 and
+    // the combine launch at 8192 tokens).  The combine runs as its own launch.
+    const moe_status st = launch_ffn_tc(a, s);
+    if (st != MOE_OK) return st;
+    return moe_combine_scatter(d_out_sorted, d_inv, d_w, rows, k, H, dtype, cap, d_counts,
+                               d_offsets, R, local, d_global_out, d_status, stream);
+  }
+  a.fuse = &f;
+  return launch_ffn_tc(a, s);
+}

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fuse_combine.cuh"
 #include "moe_dp.h"
 
 namespace moe {
@@ -19,10 +20,16 @@ struct FfnArgs {
   void* ys;             // [cap, H]
   void* h;              // [cap, I] workspace
   uint32_t* status;
+  // non-null: the down projection's epilogue also combines each token's rows and
+  // scatters them to the replicas (tokens-as-M kernel only; the pair kernel
+  // ignores it)
+  const FuseArgs* fuse = nullptr;
 };
 
 // bf16 operands on the tcgen05 tensor cores (TMA-fed, TMEM accumulators).
 moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s);
+// True if launch_ffn_tc hands this call to the pair kernel (many rows per slot).
+bool ffn_uses_pair_kernel(const FfnArgs& a);
 // The same with the weights as the MMA's M operand and tokens as N, on pairs
 // of SMs (many tokens per slot).
 moe_status launch_ffn_tc_swap(const FfnArgs& a, cudaStream_t s);

@@ -39,6 +39,15 @@
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel sets
 // MOE_DEV_TIMEOUT, the other roles stop at their next wait, TMEM is freed and
 // the kernel returns.
+//
+// With FUSE (moe_grouped_ffn_combine) the MM2 epilogue also combines: after a
+// thread has stored its row of the n-tile, it counts the row in on the token's
+// counter for that n-tile with one acquire-release atomic (fuse_combine.cuh);
+// the warp then runs the weighted sum of every token whose count its rows
+// completed, one 16-byte vector of the 256 features per lane, straight into the
+// replica rows.  The token of each row is loaded before the accumulator wait and
+// the replica table sits in shared memory, so the combine adds a few memory
+// round trips to the epilogue after the accumulator is handed back.
 #include <mutex>
 
 #include "common.cuh"
@@ -82,6 +91,8 @@ struct SmemLayout {
   int32_t mt[MOE_MAX_SLOTS];        // 128-row m-tiles per slot
   int32_t row_base[MOE_MAX_SLOTS];  // first row of the slot
   int32_t row_end[MOE_MAX_SLOTS];   // one past its last row
+  int32_t r_off[MOE_MAX_REPLICAS + 1];  // FUSE: replica offsets and counts
+  int32_t r_cnt[MOE_MAX_REPLICAS];
 };
 constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemLayout); }
 
@@ -122,10 +133,10 @@ __device__ __forceinline__ Unit decode_unit(const SmemLayout& L, int nslots, int
   return r;
 }
 
-template <bool SWIGLU>
+template <bool SWIGLU, bool FUSE>
 __global__ void __launch_bounds__(THREADS, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const TcParams p) {
+                  const TcParams p, const __grid_constant__ FuseArgs f) {
   grid_dep_wait();    // earlier kernels on the stream are complete
   grid_dep_launch();  // the next kernel may start its launch
   extern __shared__ uint8_t smem_raw[];
@@ -172,6 +183,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) tmem_alloc<1>(smem_u32(&L.tmem_base));  // whole warp
+    if constexpr (FUSE) {
+      for (int i = threadIdx.x; i <= f.R; i += THREADS) {
+        L.r_off[i] = f.offsets[i];
+        if (i < f.R) L.r_cnt[i] = f.counts[i];
+      }
+    }
     __syncthreads();
     int32_t before = 0;
     for (int w = 0; w < warp; ++w) before += L.warp_sums[w];
@@ -279,10 +296,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t row0 = (int64_t)L.row_base[un.slot] + (int64_t)un.mt * BM;
       const int64_t row_end = L.row_end[un.slot];
       const uint32_t acc = local_tile & 1u, acc_ph = (local_tile >> 1) & 1u;
-      if (!wait_bar(smem_u32(&L.tmem_full[acc]), acc_ph, abort_flag, p.status)) break;
-      fence_after();
       const int64_t row = row0 + row_in_tile;
       const bool valid = row < row_end && row < p.cap;
+      int64_t g = -1;  // FUSE: the token of this row, loaded while the MMAs run
+      if constexpr (!SWIGLU && FUSE) {
+        if (valid) g = f.perm[row];
+      }
+      if (!wait_bar(smem_u32(&L.tmem_full[acc]), acc_ph, abort_flag, p.status)) break;
+      fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
       __nv_bfloat16* orow = p.out + row * p.out_ld + (int64_t)un.n * p.out_tile_cols;
       // a warp whose 32 rows all lie past the slot's end has nothing to store
@@ -332,7 +353,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&L.tmem_empty[acc]));
+      if constexpr (!SWIGLU && FUSE) {
+        if (any) {
+          // the arrival releases this thread's row of the tile and acquires the
+          // rows of the token's earlier arrivals
+          const bool own = g >= 0 && g < f.rows && fuse_arrive(f, g, un.n, p.status);
+          const uint32_t owners = __ballot_sync(0xffffffffu, own);
+          __syncwarp();  // the owners' acquires come before every lane's reads
+          for (uint32_t m = owners; m != 0; m &= m - 1) {
+            const int64_t gg = __shfl_sync(0xffffffffu, g, __ffs(m) - 1);
+            fuse_combine_vec(f, p.out, p.cap, gg, un.n * BN + lane * 8, L.r_off, L.r_cnt,
+                             p.status);
+          }
+        }
+      }
     }
+    if constexpr (!SWIGLU && FUSE)
+      fuse_zero_pad_rows(f, L.r_off, L.r_cnt, (int64_t)blockIdx.x * 4 + (warp - 2),
+                         (int64_t)gridDim.x * 4, lane);
   }
 
   fence_before();
@@ -352,18 +390,24 @@ bool device_setup(int* max_ctas) {
   std::lock_guard<std::mutex> lock(mu);
   if (ctas[dev] == 0) {
     const int bytes = (int)smem_bytes();
-    if (cudaFuncSetAttribute(ffn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bytes) != cudaSuccess ||
-        cudaFuncSetAttribute(ffn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(ffn_tc_kernel<true, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(ffn_tc_kernel<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(ffn_tc_kernel<false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
       return false;
-    int b1 = 0, b2 = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, ffn_tc_kernel<true>, THREADS, bytes) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, ffn_tc_kernel<false>, THREADS, bytes) !=
-            cudaSuccess)
+    int b1 = 0, b2 = 0, b3 = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, ffn_tc_kernel<true, false>, THREADS,
+                                                      bytes) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, ffn_tc_kernel<false, false>, THREADS,
+                                                      bytes) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b3, ffn_tc_kernel<false, true>, THREADS,
+                                                      bytes) != cudaSuccess)
       return false;
-    const int n = (b1 < b2 ? b1 : b2) * num_sms();
+    int b = b1 < b2 ? b1 : b2;
+    b = b < b3 ? b : b3;
+    const int n = b * num_sms();
     if (n < 1) return false;
     ctas[dev] = n;
   }
@@ -406,21 +450,28 @@ moe_status run_ffn(const FfnArgs& a, const CUtensorMap& mA, const CUtensorMap& m
   }
   const int64_t bound = m_bound * p.n_tiles;
   const int grid = (int)(bound < max_ctas ? bound : max_ctas);
-  if (gemm1)
-    launch(ffn_tc_kernel<true>, grid, THREADS, smem_bytes(), s, mA, mB, p);
-  else
-    launch(ffn_tc_kernel<false>, grid, THREADS, smem_bytes(), s, mA, mB, p);
+  const FuseArgs none = {};
+  if (gemm1) {
+    launch(ffn_tc_kernel<true, false>, grid, THREADS, smem_bytes(), s, mA, mB, p, none);
+  } else if (a.fuse != nullptr) {
+    launch(ffn_tc_kernel<false, true>, grid, THREADS, smem_bytes(), s, mA, mB, p, *a.fuse);
+  } else {
+    launch(ffn_tc_kernel<false, false>, grid, THREADS, smem_bytes(), s, mA, mB, p, none);
+  }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace
 
+bool ffn_uses_pair_kernel(const FfnArgs& a) {
+  // rows per slot the sorted buffer can hold on average, over the whole layer
+  return a.cap / (a.P > 0 ? a.P : 1) >= kPairRowsPerSlot;
+}
+
 moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   const int nslots = a.slot_hi - a.slot_lo;
   if (nslots <= 0 || a.cap <= 0) return MOE_OK;
-  // rows per slot the sorted buffer can hold on average, over the whole layer
-  const int64_t rows_per_slot = a.cap / (a.P > 0 ? a.P : 1);
-  if (rows_per_slot >= kPairRowsPerSlot) return launch_ffn_tc_swap(a, s);
+  if (ffn_uses_pair_kernel(a)) return launch_ffn_tc_swap(a, s);
   CUtensorMap mA1, mB1, mA2, mB2;
   if (!make_map(&mA1, a.xs, (uint64_t)a.H, (uint64_t)a.cap, 128) ||
       !make_map(&mB1, a.wgu, (uint64_t)a.H, (uint64_t)a.P * 2 * a.I, 128) ||

@@ -77,6 +77,10 @@ _SIGS = {
                                  _P, _SZ, _P, _P]),
     "moe_grouped_ffn_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I64, _P, _P, _P, _P, _I, _I, _P, _P,
                                  _SZ, _P, _P]),
+    "moe_grouped_ffn_combine_ws_bytes": (_SZ, [_I64, _I64, _I, _I, _I]),
+    "moe_grouped_ffn_combine_in_epilogue": (_I, [_I64, _I, _I]),
+    "moe_grouped_ffn_combine": (_I, [_P, _P, _I, _I, _I, _I64, _P, _P, _I, _I, _I, _P, _P, _P, _P,
+                                     _I64, _I, _P, _P, _I, _P, _P, _P, _SZ, _P, _P]),
 }
 MOE_NOALLOC_SCRATCH_BYTES = 256 * 1024
 
@@ -479,6 +483,55 @@ def moe_grouped_ffn(xs: torch.Tensor, offsets_P: torch.Tensor, w_gate_up: torch.
         ws.numel() * ws.element_size(), _ptr(d_status), _stream(stream)))
 
 
+def moe_grouped_ffn_combine_ws_bytes(cap: int, rows: int, H: int, I: int,
+                                     dtype: torch.dtype) -> int:
+    return int(lib().moe_grouped_ffn_combine_ws_bytes(cap, rows, H, I, dtype_code(dtype)))
+
+
+def moe_grouped_ffn_combine_in_epilogue(cap: int, P: int, dtype: torch.dtype) -> bool:
+    """True if moe_grouped_ffn_combine combines in the down projection's epilogue for
+    this buffer (few rows per slot), False if it runs the combine as its own launch."""
+    return bool(lib().moe_grouped_ffn_combine_in_epilogue(cap, P, dtype_code(dtype)))
+
+
+def ffn_combine_workspace(cap: int, rows: int, H: int, I: int, dtype: torch.dtype,
+                          device="cuda") -> torch.Tensor:
+    """A workspace for moe_grouped_ffn_combine: zero-filled, as its arrival counters
+    must be zero before the first call; every call that completes leaves them zero."""
+    n = moe_grouped_ffn_combine_ws_bytes(cap, rows, H, I, dtype)
+    if n == 0:
+        raise MoeError("moe_grouped_ffn_combine_ws_bytes", MOE_ERR_INVALID_ARG)
+    return torch.zeros(n, device=device, dtype=torch.uint8)
+
+
+def moe_grouped_ffn_combine(xs: torch.Tensor, offsets_P: torch.Tensor, w_gate_up: torch.Tensor,
+                            w_down: torch.Tensor, ys: torch.Tensor, perm: torch.Tensor,
+                            inv: torch.Tensor, w: torch.Tensor, d_counts, d_offsets,
+                            local: Sequence[torch.Tensor], ws: torch.Tensor,
+                            global_out: Optional[torch.Tensor] = None, slot_lo: int = 0,
+                            slot_hi: Optional[int] = None, d_status=None, stream=None):
+    """Grouped FFN whose down projection also combines each token's rows (top-k
+    weights, j order) and writes them to the replicas; ws from ffn_combine_workspace."""
+    P = w_gate_up.shape[0]
+    slot_hi = P if slot_hi is None else slot_hi
+    rows, kk = inv.shape
+    H = xs.shape[1]
+    I = w_down.shape[2]
+    ok = (inv.dtype == torch.int32 and inv.is_contiguous() and tuple(w.shape) == (rows, kk)
+          and w.dtype == torch.float32 and w.is_contiguous() and perm.dtype == torch.int32
+          and perm.dim() == 1 and perm.numel() >= xs.shape[0] and tuple(ys.shape) == tuple(xs.shape)
+          and (global_out is None or tuple(global_out.shape) == (rows, H)))
+    if not ok:
+        raise MoeError("moe_grouped_ffn_combine", MOE_ERR_INVALID_ARG)
+    R = len(local)
+    ptrs = (ctypes.c_void_p * R)(*[t.data_ptr() if t.numel() else None for t in local])
+    _check("moe_grouped_ffn_combine", lib().moe_grouped_ffn_combine(
+        _ptr(xs), _ptr(offsets_P), P, slot_lo, slot_hi, xs.shape[0], _ptr(w_gate_up),
+        _ptr(w_down), H, I, dtype_code(xs.dtype), _ptr(ys), _ptr(perm), _ptr(inv), _ptr(w), rows,
+        kk, _ptr(d_counts), _ptr(d_offsets), R, ctypes.cast(ptrs, _P), _ptr(global_out),
+        _ptr(ws), ws.numel() * ws.element_size(), _ptr(d_status), _stream(stream)))
+
+
 def moe_combine(ys: torch.Tensor, inv: torch.Tensor, w: torch.Tensor, out: torch.Tensor,
                 d_status=None, stream=None):
     rows, k = inv.shape
@@ -534,7 +587,8 @@ class MoeLayer:
                  norm_gamma: Optional[torch.Tensor] = None, norm_eps: float = 1e-6,
                  n_shared: int = 0, fp8: bool = False,
                  router_weight: Optional[torch.Tensor] = None,
-                 router_bias: Optional[torch.Tensor] = None, keep_global: bool = False):
+                 router_bias: Optional[torch.Tensor] = None, keep_global: bool = False,
+                 fused_combine: bool = False):
         dev = w_gate_up.device
         # keep_global: also write the combined global buffer (yg, pad rows zero);
         # otherwise the combine writes the replicas' outputs only
@@ -580,10 +634,21 @@ class MoeLayer:
         self.ws_dispatch = torch.empty(max(moe_dispatch_ws_bytes(max_rows, self.kk,
                                                                  E + n_shared), 16),
                                        device=dev, dtype=torch.uint8)
-        ws_ffn = (moe_grouped_ffn_fp8_ws_bytes(self.cap, I) if fp8
-                  else moe_grouped_ffn_ws_bytes(self.cap, I, self.dtype))
-        self.ws_ffn = (fp8_ffn_workspace(self.cap, I, dev) if fp8 else
-                       torch.empty(max(ws_ffn, 16), device=dev, dtype=torch.uint8))
+        # fused_combine: the grouped FFN and the combine + scatter as one call
+        # (moe_grouped_ffn_combine; bf16 layers whose one grouped-FFN call covers every
+        # slot).  Off by default: the separate combine launch measured faster at both
+        # decode and prefill sizes.
+        can_fuse = not fp8 and self.slot_range == (0, self.P)
+        self.fused_combine = bool(fused_combine)
+        if self.fused_combine and not can_fuse:
+            raise ValueError("the fused combine needs a non-FP8 layer over all its slots")
+        if self.fused_combine:
+            self.ws_ffn = ffn_combine_workspace(self.cap, max_rows, H, I, self.dtype, dev)
+        else:
+            ws_ffn = (moe_grouped_ffn_fp8_ws_bytes(self.cap, I) if fp8
+                      else moe_grouped_ffn_ws_bytes(self.cap, I, self.dtype))
+            self.ws_ffn = (fp8_ffn_workspace(self.cap, I, dev) if fp8 else
+                           torch.empty(max(ws_ffn, 16), device=dev, dtype=torch.uint8))
         self.router_weight, self.router_bias = router_weight, router_bias
         if router_weight is not None:
             if router_weight.shape != (E, H) or router_weight.dtype != torch.bfloat16:
@@ -677,6 +742,13 @@ class MoeLayer:
             moe_dispatch(xg, ids, E_all, self.P, self.counts_P, self.offsets_P, self.perm, inv,
                          self.xs, self.ws_dispatch, self.l2p, self.nrep, self.align, st, stream)
             ev("dispatch")
+            if self.fused_combine:  # combine + scatter inside the down projection
+                moe_grouped_ffn_combine(self.xs, self.offsets_P, self.wgu, self.wd, self.ys,
+                                        self.perm, inv, w, self.d_counts, self.d_offsets, out,
+                                        self.ws_ffn, yg if self.keep_global else None,
+                                        self.slot_range[0], self.slot_range[1], st, stream)
+                ev("ffn")
+                return out
             moe_grouped_ffn(self.xs, self.offsets_P, self.wgu, self.wd, self.ys, self.ws_ffn,
                             self.slot_range[0], self.slot_range[1], st, stream)
         ev("ffn")

@@ -393,6 +393,50 @@ moe_status moe_combine_scatter(const void* d_out_sorted, const int32_t* d_inv, c
                                void* const* local, void* d_global_out, uint32_t* d_status,
                                void* stream);
 
+/* The grouped FFN with the combine and the DP scatter after it, as one call:
+ * the result of moe_grouped_ffn followed by moe_combine_scatter.  [P2] figure
+ * "MoE 模块化内核的 PrepareAndFinalize 块结构" (MM2, then finalize applies the
+ * top-k weights to the un-permuted rows); [P1] section "scatter: 把 MoE 的输出
+ * 还回本副本".  With few rows per slot (under 192 on average, the tokens-as-M
+ * kernel: decode) the combine runs in the down projection's epilogue: each MM2
+ * unit still writes its rows of d_out_sorted, then counts itself in on a
+ * per-(token, 256-feature tile) integer counter in the workspace; the unit that
+ * completes a token's count sums the token's rows of the tile in j order in
+ * float32, rounds once and writes the replica row -- the same bits as
+ * moe_combine_scatter, whichever unit wins, and one launch fewer.  With more
+ * rows per slot (the pair kernel: prefill) the combine is its own launch after
+ * the FFN, which measured faster there.
+ * Arguments as moe_grouped_ffn, plus:
+ *   d_perm      device int32[cap] from moe_dispatch (global row of each sorted row)
+ *   d_inv, d_w  device [rows, k] from moe_dispatch / the routing (k = routed slots
+ *               per row, shared experts included)
+ *   d_counts, d_offsets, R, local, d_global_out   as moe_combine_scatter (pad rows
+ *               of d_global_out are written zero)
+ *   d_ws        workspace of moe_grouped_ffn_combine_ws_bytes(cap, rows, H, I, dtype)
+ *               bytes: h [cap, I], then (bf16) rows x H/256 int32 counters.  The
+ *               counters must be zero before the first call (e.g. a zero-filled
+ *               workspace); every call that completes leaves them zero.  A call that
+ *               set MOE_DEV_TIMEOUT may leave them non-zero: zero them again.  A
+ *               counter found above its target sets MOE_DEV_BAD_WORKSPACE.
+ * With slot ranges, a token's rows are combined by whichever call completes
+ * them: the calls of one layer step must together cover every slot that holds
+ * a routed row, and none may run concurrently with another on the same
+ * workspace.  bf16 runs on the tensor-core kernels (H a multiple of 256);
+ * float32 layers run the CUDA-core FFN and then moe_combine_scatter. */
+size_t moe_grouped_ffn_combine_ws_bytes(int64_t cap, int64_t rows, int H, int I, int dtype);
+/* 1 if moe_grouped_ffn_combine on a sorted buffer of cap rows over P slots runs
+ * the combine inside the down projection's epilogue (one launch fewer), 0 if it
+ * runs it as its own launch after the FFN.  Host only, no CUDA call. */
+int moe_grouped_ffn_combine_in_epilogue(int64_t cap, int P, int dtype);
+moe_status moe_grouped_ffn_combine(const void* d_sorted, const int32_t* d_offsets_P, int P,
+                                   int slot_lo, int slot_hi, int64_t cap,
+                                   const void* d_w_gate_up, const void* d_w_down, int H, int I,
+                                   int dtype, void* d_out_sorted, const int32_t* d_perm,
+                                   const int32_t* d_inv, const float* d_w, int64_t rows, int k,
+                                   const int32_t* d_counts, const int32_t* d_offsets, int R,
+                                   void* const* local, void* d_global_out, void* d_ws,
+                                   size_t ws_bytes, uint32_t* d_status, void* stream);
+
 /* Same as moe_dispatch, but allocates nothing and takes no workspace: the
  * per-chunk histograms live in a fixed device array inside the library.
  * The pages have no counterpart; this entry point exists for callers that

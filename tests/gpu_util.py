@@ -110,13 +110,13 @@ def _slot_positions(rows: int, kernel: str):
     return sorted(pos)
 
 
-def hard_rows(offsets, kernel: str, min_rows: int = 64, seed: int = 0):
+def hard_rows(offsets, kernel: str, min_rows: int = 64, seed: int = 0, keep=None):
     """Sorted-buffer rows d at the grouped-FFN kernel's tiling boundaries: the first and
     last token of every unit, lane-quarter and 32-column chunk edges, and (pair kernel)
     both sides of the split between the N <= 256 MMA and the tail MMA of columns
     256-319.  Slots are taken largest first, then the smallest non-empty one, a slot
     whose last unit has a tail MMA, then seeded random slots, until at least min_rows
-    rows are chosen."""
+    rows are chosen; keep (a mask over sorted rows) drops rows such as alignment pads."""
     offsets = np.asarray(offsets, np.int64)
     counts = np.diff(offsets)
     nz = np.nonzero(counts > 0)[0]
@@ -132,8 +132,9 @@ def hard_rows(offsets, kernel: str, min_rows: int = 64, seed: int = 0):
         if s in seen:
             continue
         seen.add(s)
-        out += [int(offsets[s]) + p for p in _slot_positions(int(counts[s]), kernel)]
-        if len(out) >= min_rows and len(seen) >= 4:
+        out += [d for d in (int(offsets[s]) + p for p in _slot_positions(int(counts[s]), kernel))
+                if keep is None or keep[d]]
+        if len(set(out)) >= min_rows and len(seen) >= 4:
             break
     return sorted(set(out))
 
@@ -146,9 +147,13 @@ def pairs_to_check(layer, o_o, p_o, i_o, real, kk: int, sample):
     spread over the hard pairs, each with all of its kk pairs."""
     if sample is None:
         return [(int(g), j) for g in real for j in range(kk)], real
-    hard = [d for d in hard_rows(o_o, ffn_kernel_of(layer)) if p_o[d] >= 0]
+    kernel = ffn_kernel_of(layer)
+    real_d = p_o >= 0                    # sorted rows that hold a token (not an alignment pad)
+    hard = hard_rows(o_o, kernel, keep=real_d)
     hard_pairs = [(int(p_o[d]), int(np.nonzero(i_o[p_o[d]] == d)[0][0])) for d in hard]
-    assert len(hard_pairs) >= 64, len(hard_pairs)
+    # at least 64, unless the layer has fewer boundary rows in all its slots together
+    every = hard_rows(o_o, kernel, min_rows=1 << 30, keep=real_d)
+    assert len(hard_pairs) >= min(64, len(every)), (len(hard_pairs), len(every))
     picked = np.unique([g for g, _ in hard_pairs])
     spread = picked[np.linspace(0, len(picked) - 1, min(sample, len(picked))).astype(int)]
     toks = np.unique(np.concatenate([real[:2], real[-2:], spread])).astype(np.int64)

@@ -191,6 +191,46 @@ def test_gather2_and_combine_scatter_reject_bad_args(md):
     assert c(a3=0) == md.MOE_OK
 
 
+def test_grouped_ffn_combine_rejects_bad_args(md):
+    """moe_grouped_ffn_combine refuses bad sizes, pointers and workspaces before any
+    launch (and before looking for a device)."""
+    L = md.lib()
+    two = _ptrs(0x2000, 0x3000)
+    E_ARG, E_UNS, E_CAP = md.MOE_ERR_INVALID_ARG, md.MOE_ERR_UNSUPPORTED, md.MOE_ERR_CAPACITY
+    cap, rows, H, I, k = 64, 16, 256, 128, 4
+    import torch
+    ws = md.moe_grouped_ffn_combine_ws_bytes(cap, rows, H, I, torch.bfloat16)
+    assert ws == cap * I * 2 + rows * (H // 256) * 4     # h, then one counter per 256 features
+    assert md.moe_grouped_ffn_combine_ws_bytes(cap, rows, 384, I, torch.bfloat16) == 0
+    assert md.moe_grouped_ffn_combine_ws_bytes(cap, rows, 96, I, torch.float32) == cap * I * 4
+    ok = (FAKE, FAKE, 8, 0, 8, cap, FAKE, FAKE, H, I, 1, FAKE, FAKE, FAKE, FAKE, rows, k,
+          FAKE, FAKE, 2, two, NULL, FAKE, ws, NULL, NULL)
+
+    def f(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return L.moe_grouped_ffn_combine(*a)
+    assert f(a2=0) == E_ARG                          # P = 0
+    assert f(a3=5, a4=2) == E_ARG                    # slot_lo > slot_hi
+    assert f(a4=9) == E_ARG                          # slot_hi > P
+    assert f(a16=0) == E_ARG and f(a16=33) == E_ARG  # k outside 1..32
+    assert f(a19=0) == E_ARG and f(a19=300) == E_ARG
+    assert f(a8=4) == E_ARG                          # 8-byte rows
+    assert f(a8=384) == E_UNS                        # bf16 tensor cores need H % 256 == 0
+    assert f(a10=3) == E_UNS
+    assert f(a12=NULL) == E_ARG                      # no perm
+    assert f(a13=NULL) == E_ARG and f(a14=NULL) == E_ARG
+    assert f(a17=NULL) == E_ARG and f(a18=NULL) == E_ARG
+    assert f(a20=NULL) == E_ARG                      # no replica table
+    assert f(a20=_ptrs(0x2008, 0x3000)) == E_ARG     # misaligned replica row
+    assert f(a21=MISAL) == E_ARG                     # misaligned optional global buffer
+    assert f(a22=NULL) == E_ARG                      # no workspace
+    assert f(a23=ws - 1) == E_CAP                    # workspace one byte short
+    assert f(a0=MISAL) == E_ARG
+    assert f(a15=0) == md.MOE_OK                     # no rows: nothing to do
+
+
 def test_routing_gather_bindings_check_output_shapes(md):
     """The bindings refuse ids / w / gathered-logit tensors the kernels would write past."""
     import torch

@@ -75,3 +75,6 @@ def test_launch_counts_match_the_measured_steps():
     assert bench.launches_per_step(440, 8, 256, 256, 3584, 1, router_gemm=True) == 9
     # prefill: 8192 rows x 8 pairs take the chunked dispatch (histogram, scan, rank, copy)
     assert bench.launches_per_step(8192, 8, 256, 256, 65600, 1) == 8
+    # the combine in the down projection's epilogue takes one launch off either step
+    assert bench.launches_per_step(440, 8, 256, 256, 3584, 1, fused_combine=True) == 5
+    assert bench.launches_per_step(8192, 8, 256, 256, 65600, 1, fused_combine=True) == 7
