@@ -49,7 +49,7 @@ L2_NOTE = "inputs larger than L2: every step streams the touched experts' weight
 
 def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
                       fp8: bool = False, router_gemm: bool = False, sms: int = 152,
-                      fused_combine: bool = False) -> int:
+                      fused_combine: bool = False, ffn_split: bool = False) -> int:
     """Kernel launches of one layer step: gather (with given logits it routes the rows
     in the same launch, the fused add + RMSNorm included), dispatch (one CTA-wide kernel for <= 8192 routed pairs whose tables
     fit 48 KB, else histogram + scan + rank; then the row copy; + the alignment pad
@@ -64,7 +64,8 @@ def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
     if router_gemm:
         gather = 1
         route = 1 if (k <= 8 and 4 * ((rows + 127) // 128) >= sms) else 3
-    return gather + route + dispatch + (1 if fp8 else 2) + (0 if fused_combine else 1)
+    ffn = 1 if fp8 else (4 if ffn_split else 2)   # the split: two launches per stream
+    return gather + route + dispatch + ffn + (0 if fused_combine else 1)
 
 
 def ffn_kernel(cap: int, P: int, fp8: bool = False) -> str:
@@ -132,6 +133,10 @@ def parse():
                          "down projection's epilogue with few rows per slot, else its own "
                          "launch inside the call); separate: moe_grouped_ffn, then "
                          "moe_combine_scatter")
+    ap.add_argument("--ffn-split", default=None,
+                    help="HOT_ROWS:HOT_SMS: the grouped FFN split by slot over two streams "
+                         "(slots with >= HOT_ROWS rows on the pair kernel on HOT_SMS SMs, the "
+                         "rest on the single-SM kernel beside it); 'none' for one kernel")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 dispatch and grouped FFN (e4m3, UE8M0 scales per 128-token group "
                          "and 128x128 weight block); layer input and output stay bf16")
@@ -294,7 +299,8 @@ def run_native(args, rank, world, local_rank):
         l2p=None if l2p_np is None else torch.from_numpy(l2p_np).to(dev),
         nrep=None if nrep_np is None else torch.from_numpy(nrep_np).to(dev),
         n_shared=spec.n_shared, fp8=args.fp8, router_weight=gate_w, router_bias=gate_b,
-        fused_combine=(args.combine == "fused" and not args.fp8))
+        fused_combine=(args.combine == "fused" and not args.fp8),
+        ffn_split=ffn_split_of(args))
     out = [torch.empty(c, spec.H, device=dev, dtype=wgu.dtype) for c in spec.counts]
     res_loc = None
     if args.boundary == "addnorm":
@@ -394,6 +400,10 @@ def run_native(args, rank, world, local_rank):
                             f"moe_grouped_ffn_combine ({ffn_kernel(layer.cap, layer.P)} "
                             "MM1+SwiGLU and MM2 launches, then the combine + DP scatter "
                             "launch)" if layer.fused_combine else
+                            "moe_grouped_ffn_split (slots with >= {} rows: ffn_swap_kernel on "
+                            "{} SMs of a second stream; the rest: ffn_tc_kernel beside it; "
+                            "MM1+SwiGLU and MM2 launches each)".format(*layer.ffn_split)
+                            if layer.ffn_split else
                             f"moe_grouped_ffn ({ffn_kernel(layer.cap, layer.P)} MM1+SwiGLU "
                             "and MM2 launches)"),
                  "tflops": round(tflops, 1),
@@ -518,8 +528,16 @@ def run_native(args, rank, world, local_rank):
                                            spec.E + spec.n_shared, layer.P, layer.cap,
                                            spec.align, args.fp8, args.router == "gemm",
                                            torch.cuda.get_device_properties(dev).multi_processor_count,
-                                           bool(in_epi)),
+                                           bool(in_epi), bool(layer.ffn_split)),
                 inputs=(x_loc, lg_loc, wgu, wd, l2p_np, nrep_np), gate=gate_np)
+
+
+def ffn_split_of(args):
+    """(hot_rows, hot_sms) of --ffn-split, or None."""
+    if not args.ffn_split or args.ffn_split == "none" or args.fp8:
+        return None
+    a, b = args.ffn_split.split(":")
+    return int(a), int(b)
 
 
 def stage_every(args) -> int:
@@ -739,6 +757,8 @@ def main():
             "scaling": "weak", "vs_baseline": None,
             "dtype": "fp8-e4m3" if args.fp8 else spec.dtype, "data": "synthetic",
             "config": dict(synth.describe(spec), global_rows=r["rows"], l2=L2_NOTE, **r["extra"],
+                           ffn_split=("slots with >= %d rows on %d SMs of a second stream"
+                                      % ffn_split_of(args) if ffn_split_of(args) else None),
                            boundary=args.boundary, shared_experts=spec.n_shared,
                            router=("gate GEMM fused ahead of top-k, W_r N(0, 1/H) plus the Zipf "
                                    "bias" if args.router == "gemm" else "given logits"),

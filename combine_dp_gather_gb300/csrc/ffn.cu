@@ -3,6 +3,8 @@
 // The float32 path serves fp32 layers (small, latency-bound shapes): one thread
 // per output element, float32 accumulation in index order.  bf16 layers go to
 // the tcgen05 kernel in ffn_tc.cu.
+#include <mutex>
+
 #include "common.cuh"
 #include "ffn_internal.h"
 
@@ -247,4 +249,107 @@ extern "C" moe_status moe_grouped_ffn_combine(
   }
   a.fuse = &f;
   return launch_ffn_tc(a, s);
+}
+
+// ---------------------------------------------------------------------------
+// Grouped FFN of a skewed layer split by slot over two streams: the slots with
+// at least hot_rows rows run on the pair kernel (weights as M) on hot_sms SMs
+// of stream_hot, the others on the single-SM kernel (tokens as M) on the rest
+// of the SMs of `stream`, at the same time.  SGLang chapter 17, section
+// "Two-batch Overlap" and vLLM chapter 27 (Dual Batch Overlap, its SM control):
+// two streams keep different kinds of work in flight together; here it is the
+// hot slots' tensor-bound GEMMs beside the cold slots' weight stream, and every
+// weight tile is still read once.
+
+namespace {
+
+// Fork and join events of the split FFN, created once per device on first use
+// (never inside a call that is being captured, if the first call on the device
+// runs eagerly).  The mutex keeps each record + wait pair together when several
+// host threads call on one device.
+struct SplitEvents {
+  std::mutex mu;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+SplitEvents* split_events(int dev) {
+  static std::mutex mu;
+  static SplitEvents* cache[64] = {nullptr};
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == nullptr) {
+    SplitEvents* e = new SplitEvents();
+    if (cudaEventCreateWithFlags(&e->fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&e->join, cudaEventDisableTiming) != cudaSuccess) {
+      delete e;
+      return nullptr;
+    }
+    cache[dev] = e;
+  }
+  return cache[dev];
+}
+
+}  // namespace
+
+extern "C" moe_status moe_grouped_ffn_split(const void* d_sorted, const int32_t* d_offsets_P,
+                                            int P, int slot_lo, int slot_hi, int64_t cap,
+                                            const void* d_w_gate_up, const void* d_w_down, int H,
+                                            int I, int dtype, void* d_out_sorted, void* d_ws,
+                                            size_t ws_bytes, int hot_rows, int hot_sms,
+                                            uint32_t* d_status, void* stream, void* stream_hot) {
+  if (P < 1 || slot_lo < 0 || slot_hi > P || slot_lo > slot_hi || cap < 0 || cap > INT32_MAX ||
+      H < 1 || I < 1 || hot_rows < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (H % 256 != 0 || I % 128 != 0 || P > MOE_MAX_SLOTS) return MOE_ERR_UNSUPPORTED;
+  if (cap == 0 || slot_lo == slot_hi) return MOE_OK;
+  if (d_sorted == nullptr || d_offsets_P == nullptr || d_w_gate_up == nullptr ||
+      d_w_down == nullptr || d_out_sorted == nullptr || d_ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_grouped_ffn_ws_bytes(cap, I, dtype)) return MOE_ERR_CAPACITY;
+  if (!aligned16(d_sorted) || !aligned16(d_out_sorted) || !aligned16(d_ws) ||
+      !aligned16(d_w_gate_up) || !aligned16(d_w_down))
+    return MOE_ERR_INVALID_ARG;
+  if ((int64_t)P * 2 * I > INT32_MAX || (int64_t)P * H > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  int major = 0, minor = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
+  const int sms = num_sms();
+  if (hot_sms < 2 || hot_sms % 2 != 0 || hot_sms > sms - 2) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  cudaStream_t sh = stream_hot != nullptr ? as_stream(stream_hot) : s;
+  FfnArgs hot{d_sorted, d_offsets_P, P, slot_lo, slot_hi, cap, d_w_gate_up, d_w_down,
+              H, I, d_out_sorted, d_ws, d_status};
+  FfnArgs cold = hot;
+  hot.min_slot_rows = hot_rows;
+  hot.sm_budget = hot_sms;
+  cold.max_slot_rows = hot_rows - 1;
+  cold.sm_budget = sms - hot_sms;
+  if (sh == s) {  // one stream: the two parts one after the other
+    const moe_status st = launch_ffn_tc_swap(hot, s);
+    return st != MOE_OK ? st : launch_ffn_tc_single(cold, s);
+  }
+  // fork: stream_hot starts after everything already on `stream`; join: `stream`
+  // continues after both parts
+  SplitEvents* ev = split_events(dev);
+  if (ev == nullptr) return MOE_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(ev->mu);
+    if (cudaEventRecord(ev->fork, s) != cudaSuccess ||
+        cudaStreamWaitEvent(sh, ev->fork, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  moe_status st = launch_ffn_tc_swap(hot, sh);
+  const moe_status st2 = launch_ffn_tc_single(cold, s);
+  if (st == MOE_OK) st = st2;
+  // the join is recorded whatever happened, so `stream` never runs ahead of work
+  // already queued on stream_hot
+  std::lock_guard<std::mutex> lock(ev->mu);
+  if (cudaEventRecord(ev->join, sh) != cudaSuccess ||
+      cudaStreamWaitEvent(s, ev->join, 0) != cudaSuccess)
+    st = MOE_ERR_CUDA;
+  return st;
 }

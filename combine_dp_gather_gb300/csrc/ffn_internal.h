@@ -24,12 +24,21 @@ struct FfnArgs {
   // scatters them to the replicas (tokens-as-M kernel only; the pair kernel
   // ignores it)
   const FuseArgs* fuse = nullptr;
+  // slot filter by rows (device-side counts): the kernel serves only the slots
+  // with min_slot_rows <= rows <= max_slot_rows
+  int32_t min_slot_rows = 0;
+  int32_t max_slot_rows = INT32_MAX;
+  // SMs the persistent grid may use (0: every resident CTA)
+  int sm_budget = 0;
 };
 
 // bf16 operands on the tcgen05 tensor cores (TMA-fed, TMEM accumulators).
 moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s);
 // True if launch_ffn_tc hands this call to the pair kernel (many rows per slot).
 bool ffn_uses_pair_kernel(const FfnArgs& a);
+// The two kernels directly, whatever the rows per slot (slot filter and SM
+// budget from the args): tokens as M on single SMs, weights as M on pairs.
+moe_status launch_ffn_tc_single(const FfnArgs& a, cudaStream_t s);
 // The same with the weights as the MMA's M operand and tokens as N, on pairs
 // of SMs (many tokens per slot).
 moe_status launch_ffn_tc_swap(const FfnArgs& a, cudaStream_t s);

@@ -99,6 +99,7 @@ constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * STAGE_BYTES + siz
 struct TcParams {
   const int32_t* offsets;
   int slot_lo, nslots;
+  int32_t min_slot_rows, max_slot_rows;  // slots outside [min, max] rows get no units
   int64_t cap;
   int num_kb;
   int n_tiles;
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (s < p.nslots) {
         const int64_t o0 = p.offsets[p.slot_lo + s];
         int64_t rows = (int64_t)p.offsets[p.slot_lo + s + 1] - o0;
-        if (rows < 0) rows = 0;
+        if (rows < 0 || rows < p.min_slot_rows || rows > p.max_slot_rows) rows = 0;
         const int32_t mt = (int32_t)((rows + BM - 1) / BM);
         L.mt[s] = mt;
         L.row_base[s] = (int32_t)o0;
@@ -427,6 +428,9 @@ moe_status run_ffn(const FfnArgs& a, const CUtensorMap& mA, const CUtensorMap& m
   p.offsets = a.offsets;
   p.slot_lo = a.slot_lo;
   p.nslots = nslots;
+  p.min_slot_rows = a.min_slot_rows;
+  p.max_slot_rows = a.max_slot_rows;
+  if (a.sm_budget > 0 && a.sm_budget < max_ctas) max_ctas = a.sm_budget;
   p.cap = a.cap;
   p.status = a.status;
   if (gemm1) {
@@ -472,6 +476,12 @@ moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
   const int nslots = a.slot_hi - a.slot_lo;
   if (nslots <= 0 || a.cap <= 0) return MOE_OK;
   if (ffn_uses_pair_kernel(a)) return launch_ffn_tc_swap(a, s);
+  return launch_ffn_tc_single(a, s);
+}
+
+moe_status launch_ffn_tc_single(const FfnArgs& a, cudaStream_t s) {
+  const int nslots = a.slot_hi - a.slot_lo;
+  if (nslots <= 0 || a.cap <= 0) return MOE_OK;
   CUtensorMap mA1, mB1, mA2, mB2;
   if (!make_map(&mA1, a.xs, (uint64_t)a.H, (uint64_t)a.cap, 128) ||
       !make_map(&mB1, a.wgu, (uint64_t)a.H, (uint64_t)a.P * 2 * a.I, 128) ||

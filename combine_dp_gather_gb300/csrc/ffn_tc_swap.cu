@@ -88,6 +88,7 @@ struct Maps {
 struct SwapParams {
   const int32_t* offsets;
   int slot_lo, nslots;
+  int32_t min_slot_rows, max_slot_rows;  // slots outside [min, max] rows get no units
   int64_t cap;
   int num_kb;
   int n_tiles;          // weight tiles per slot
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (s < p.nslots) {
         const int32_t o0 = p.offsets[p.slot_lo + s];
         int32_t rows = p.offsets[p.slot_lo + s + 1] - o0;
-        if (rows < 0) rows = 0;
+        if (rows < 0 || rows < p.min_slot_rows || rows > p.max_slot_rows) rows = 0;
         L.row0[s] = o0;
         L.rows[s] = rows;
         local += token_groups(rows) * p.n_tiles;
@@ -521,10 +522,14 @@ bool device_setup(int* max_clusters) {
 moe_status run_swap(const FfnArgs& a, const Maps& m, bool gemm1, cudaStream_t s) {
   int max_clusters = 0;
   if (!device_setup(&max_clusters)) return MOE_ERR_CUDA;
+  if (a.sm_budget > 0 && a.sm_budget / 2 < max_clusters) max_clusters = a.sm_budget / 2;
+  if (max_clusters < 1) return MOE_ERR_INVALID_ARG;
   SwapParams p;
   p.offsets = a.offsets;
   p.slot_lo = a.slot_lo;
   p.nslots = a.slot_hi - a.slot_lo;
+  p.min_slot_rows = a.min_slot_rows;
+  p.max_slot_rows = a.max_slot_rows;
   p.cap = a.cap;
   p.status = a.status;
   p.gemm1 = gemm1 ? 1 : 0;

@@ -77,6 +77,8 @@ _SIGS = {
                                  _P, _SZ, _P, _P]),
     "moe_grouped_ffn_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I64, _P, _P, _P, _P, _I, _I, _P, _P,
                                  _SZ, _P, _P]),
+    "moe_grouped_ffn_split": (_I, [_P, _P, _I, _I, _I, _I64, _P, _P, _I, _I, _I, _P, _P, _SZ,
+                                   _I, _I, _P, _P, _P]),
     "moe_grouped_ffn_combine_ws_bytes": (_SZ, [_I64, _I64, _I, _I, _I]),
     "moe_grouped_ffn_combine_in_epilogue": (_I, [_I64, _I, _I]),
     "moe_grouped_ffn_combine": (_I, [_P, _P, _I, _I, _I, _I64, _P, _P, _I, _I, _I, _P, _P, _P, _P,
@@ -483,6 +485,23 @@ def moe_grouped_ffn(xs: torch.Tensor, offsets_P: torch.Tensor, w_gate_up: torch.
         ws.numel() * ws.element_size(), _ptr(d_status), _stream(stream)))
 
 
+def moe_grouped_ffn_split(xs: torch.Tensor, offsets_P: torch.Tensor, w_gate_up: torch.Tensor,
+                          w_down: torch.Tensor, ys: torch.Tensor, ws: torch.Tensor,
+                          hot_rows: int, hot_sms: int, stream_hot=None, slot_lo: int = 0,
+                          slot_hi: Optional[int] = None, d_status=None, stream=None):
+    """Grouped FFN split by slot over two streams: slots with >= hot_rows rows on the
+    pair kernel (hot_sms SMs, stream_hot), the rest on the single-SM kernel."""
+    P = w_gate_up.shape[0]
+    slot_hi = P if slot_hi is None else slot_hi
+    H = xs.shape[1]
+    I = w_down.shape[2]
+    sh = None if stream_hot is None else ctypes.c_void_p(stream_hot.cuda_stream)
+    _check("moe_grouped_ffn_split", lib().moe_grouped_ffn_split(
+        _ptr(xs), _ptr(offsets_P), P, slot_lo, slot_hi, xs.shape[0], _ptr(w_gate_up),
+        _ptr(w_down), H, I, dtype_code(xs.dtype), _ptr(ys), _ptr(ws),
+        ws.numel() * ws.element_size(), hot_rows, hot_sms, _ptr(d_status), _stream(stream), sh))
+
+
 def moe_grouped_ffn_combine_ws_bytes(cap: int, rows: int, H: int, I: int,
                                      dtype: torch.dtype) -> int:
     return int(lib().moe_grouped_ffn_combine_ws_bytes(cap, rows, H, I, dtype_code(dtype)))
@@ -588,7 +607,7 @@ class MoeLayer:
                  n_shared: int = 0, fp8: bool = False,
                  router_weight: Optional[torch.Tensor] = None,
                  router_bias: Optional[torch.Tensor] = None, keep_global: bool = False,
-                 fused_combine: bool = False):
+                 fused_combine: bool = False, ffn_split=None):
         dev = w_gate_up.device
         # keep_global: also write the combined global buffer (yg, pad rows zero);
         # otherwise the combine writes the replicas' outputs only
@@ -640,6 +659,14 @@ class MoeLayer:
         # decode and prefill sizes.
         can_fuse = not fp8 and self.slot_range == (0, self.P)
         self.fused_combine = bool(fused_combine)
+        # ffn_split = (hot_rows, hot_sms): the grouped FFN split by slot over two
+        # streams (moe_grouped_ffn_split), for skewed layers; bf16 only
+        self.ffn_split = tuple(ffn_split) if ffn_split else None
+        self.stream_hot = None
+        if self.ffn_split:
+            if fp8 or self.fused_combine:
+                raise ValueError("ffn_split takes a bf16 layer with the separate combine")
+            self.stream_hot = torch.cuda.Stream(device=dev)
         if self.fused_combine and not can_fuse:
             raise ValueError("the fused combine needs a non-FP8 layer over all its slots")
         if self.fused_combine:
@@ -749,8 +776,14 @@ class MoeLayer:
                                         self.slot_range[0], self.slot_range[1], st, stream)
                 ev("ffn")
                 return out
-            moe_grouped_ffn(self.xs, self.offsets_P, self.wgu, self.wd, self.ys, self.ws_ffn,
-                            self.slot_range[0], self.slot_range[1], st, stream)
+            if self.ffn_split:
+                moe_grouped_ffn_split(self.xs, self.offsets_P, self.wgu, self.wd, self.ys,
+                                      self.ws_ffn, self.ffn_split[0], self.ffn_split[1],
+                                      self.stream_hot, self.slot_range[0], self.slot_range[1],
+                                      st, stream)
+            else:
+                moe_grouped_ffn(self.xs, self.offsets_P, self.wgu, self.wd, self.ys, self.ws_ffn,
+                                self.slot_range[0], self.slot_range[1], st, stream)
         ev("ffn")
         moe_combine_scatter(self.ys, inv, w, self.d_counts, self.d_offsets, out,
                             yg if self.keep_global else None, st, stream)

@@ -360,6 +360,33 @@ moe_status moe_grouped_ffn(const void* d_sorted, const int32_t* d_offsets_P, int
                            const void* d_w_down, int H, int I, int dtype, void* d_out_sorted,
                            void* d_ws, size_t ws_bytes, uint32_t* d_status, void* stream);
 
+/* The grouped FFN of a skewed layer, split by slot over two streams with an SM
+ * budget: slots with at least hot_rows rows run on the pair kernel (expert
+ * weights as the MMA's M operand on two-SM pairs, each weight tile read once
+ * per 320 tokens) on hot_sms SMs of stream_hot, all other slots on the
+ * single-SM kernel (tokens as M) on the remaining SMs of `stream`, at the same
+ * time; the result is what moe_grouped_ffn computes.  [P1] section "Two-batch
+ * Overlap" and [P2] (Dual Batch Overlap, its SM control): two streams keep
+ * different work in flight together -- here the hot slots' tensor-bound GEMMs
+ * beside the cold slots' weight stream, with every weight tile still read once.
+ * Arguments as moe_grouped_ffn (bf16 only), plus:
+ *   hot_rows    >= 1: a slot with at least this many rows is hot
+ *   hot_sms     SMs of the hot part: even, 2 .. (SM count - 2)
+ *   stream_hot  second stream (void* cudaStream_t); it waits for the work queued
+ *               on `stream` before the call, and `stream` waits for it after.
+ *               NULL or equal to `stream`: the two parts run one after the other.
+ * The fork and join use two events the library creates on the first call on a
+ * device and keeps until exit (make that first call outside stream capture);
+ * the call can then be captured into a CUDA graph, where the fork and join
+ * become graph edges.
+ * The rounding order of a slot's sums can differ between the two kernels, so
+ * the output equals moe_grouped_ffn within the bf16 tolerance, not bit for bit. */
+moe_status moe_grouped_ffn_split(const void* d_sorted, const int32_t* d_offsets_P, int P,
+                                 int slot_lo, int slot_hi, int64_t cap, const void* d_w_gate_up,
+                                 const void* d_w_down, int H, int I, int dtype,
+                                 void* d_out_sorted, void* d_ws, size_t ws_bytes, int hot_rows,
+                                 int hot_sms, uint32_t* d_status, void* stream, void* stream_hot);
+
 /* Combine: un-permute and apply the top-k weights.
  * [P2] figure "MoE 模块化内核的 PrepareAndFinalize 块结构" (finalize applies
  * the top-k weights): out[row] = sum_{j<k} w[row, j] * y[inv[row, j]],

@@ -67,13 +67,17 @@ def graph_replay_matches_eager(layer, x_loc, lg_loc, out):
 
 
 # ------------------------------------------------------------------ hard rows
-def ffn_kernel_of(layer) -> str:
+def ffn_kernel_of(layer):
     """Which grouped-FFN kernel the library runs for this layer: FP8 -> 'fp8' (weights
     as M, units of up to 64 tokens); bf16 with >= 192 sorted rows per slot on average
     -> 'pair' (weights as M on SM pairs, units of up to 320 tokens); else 'tc' (tokens
-    as M, 128-row m-tiles)."""
+    as M, 128-row m-tiles).  With the split FFN, a function of the slot's rows: 'pair'
+    from the hot threshold, else 'tc'."""
     if getattr(layer, "fp8", False):
         return "fp8"
+    split = getattr(layer, "ffn_split", None)
+    if split:
+        return lambda rows: "pair" if rows >= split[0] else "tc"
     return "pair" if layer.cap // max(layer.P, 1) >= 192 else "tc"
 
 
@@ -123,6 +127,11 @@ def hard_rows(offsets, kernel: str, min_rows: int = 64, seed: int = 0, keep=None
     if len(nz) == 0:
         return []
     order = [int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])])]
+    if callable(kernel):   # the hottest and coldest slot of each kernel first
+        for kern in ("pair", "tc"):
+            mine = [int(x) for x in nz if kernel(int(counts[x])) == kern]
+            if mine:
+                order += [max(mine, key=lambda x: counts[x]), min(mine, key=lambda x: counts[x])]
     tail = [int(s) for s in nz if 256 < (counts[s] - 1) % 320 + 1 <= 320]
     order += tail[:2]
     rng = np.random.default_rng(seed)
@@ -132,7 +141,8 @@ def hard_rows(offsets, kernel: str, min_rows: int = 64, seed: int = 0, keep=None
         if s in seen:
             continue
         seen.add(s)
-        out += [d for d in (int(offsets[s]) + p for p in _slot_positions(int(counts[s]), kernel))
+        kern = kernel(int(counts[s])) if callable(kernel) else kernel
+        out += [d for d in (int(offsets[s]) + p for p in _slot_positions(int(counts[s]), kern))
                 if keep is None or keep[d]]
         if len(set(out)) >= min_rows and len(seen) >= 4:
             break

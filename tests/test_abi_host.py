@@ -231,6 +231,29 @@ def test_grouped_ffn_combine_rejects_bad_args(md):
     assert f(a15=0) == md.MOE_OK                     # no rows: nothing to do
 
 
+def test_grouped_ffn_split_rejects_bad_args(md):
+    L = md.lib()
+    E_ARG, E_UNS, E_CAP = md.MOE_ERR_INVALID_ARG, md.MOE_ERR_UNSUPPORTED, md.MOE_ERR_CAPACITY
+    cap, H, I = 64, 256, 128
+    ws = cap * I * 2
+    ok = (FAKE, FAKE, 8, 0, 8, cap, FAKE, FAKE, H, I, 1, FAKE, FAKE, ws, 192, 32, NULL, NULL,
+          NULL)
+
+    def f(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return L.moe_grouped_ffn_split(*a)
+    assert f(a14=0) == E_ARG                         # hot_rows < 1
+    assert f(a10=0) == E_UNS                         # float32: the split is bf16 only
+    assert f(a8=384) == E_UNS                        # H % 256 != 0
+    assert f(a2=0) == E_ARG and f(a4=9) == E_ARG
+    assert f(a0=NULL) == E_ARG and f(a12=NULL) == E_ARG
+    assert f(a13=ws - 1) == E_CAP
+    assert f(a11=MISAL) == E_ARG
+    assert f(a5=0) == md.MOE_OK                      # nothing to compute
+
+
 def test_routing_gather_bindings_check_output_shapes(md):
     """The bindings refuse ids / w / gathered-logit tensors the kernels would write past."""
     import torch
