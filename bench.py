@@ -78,14 +78,15 @@ def ffn_kernel(cap: int, P: int, fp8: bool = False) -> str:
 
 # dram__bytes_read.sum + dram__bytes_write.sum of the grouped-FFN launches (two in bf16,
 # one on FP8) of one step of the workload (ncu, --clock-control none), valid while the kernel's
-# sources hash to the recorded SHA-256 prefix; any other source reports traffic null.
+# sources hash to the recorded SHA-256 prefix; any other source reports traffic null.  The bf16
+# records come from shrunk cases of the same kernels (32-expert prefill, 64-expert decode) and
+# are scaled to the workload by the units processed (traffic per slot and per routed row is
+# the same); the FP8 decode record is a capture of the full workload.
 FFN_TRAFFIC = {
-    "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "10e862941fb51ca1",
-               "bytes": 5582041088},
-    "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "205258ea68ec00af",
-                "bytes": 25761555200},
-    "eplb": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "10e862941fb51ca1",
-             "bytes": 12737062656},
+    "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "e25e9afc9231a9d9",
+                "bytes": 25142339584},
+    "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "ec94ad3d0984b261",
+               "bytes": 5580442771},
     "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
                    "sha256_16": "b18d85061d74668d", "bytes": 2789277440},
 }
@@ -263,6 +264,8 @@ class StepEvents:
 def ffn_traffic(args):
     if args.experts is not None or args.tokens is not None or args.seed != 0:
         return None  # recorded for the default workload only
+    if args.combine == "fused" or ffn_split_of(args):
+        return None  # recorded for the grouped FFN's own launches
     rec = FFN_TRAFFIC.get(args.config + ("_fp8" if args.fp8 else ""))
     if not rec or rec["bytes"] is None:
         return None
