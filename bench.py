@@ -85,8 +85,8 @@ def ffn_kernel(cap: int, P: int, fp8: bool = False) -> str:
 FFN_TRAFFIC = {
     "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "e25e9afc9231a9d9",
                 "bytes": 25142339584},
-    "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "caca0ba381278ae4",
-               "bytes": 5598301426},
+    "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "ec94ad3d0984b261",
+               "bytes": 5580442771},
     "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
                    "sha256_16": "b18d85061d74668d", "bytes": 2789277440},
 }

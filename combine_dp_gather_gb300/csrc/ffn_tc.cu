@@ -15,13 +15,7 @@
 // Work units are (slot, n-tile, m-tile) with the m-tiles of one slot and
 // n-tile adjacent, so units running at the same time share the weight tile
 // through L2; unit counts come from the device-side slot offsets, so the host
-// never synchronises after dispatch.  Units of slots with one m-tile stream
-// their weight tile from HBM alone; units of slots with several share it and
-// are bound by the tensor cores instead.  The two kinds are interleaved evenly
-// over the unit order (each in slot order), so every round of the persistent
-// grid keeps the HBM stream and the tensor cores busy together instead of
-// alternating between rounds of one kind (a skewed EPLB layer's few hot slots
-// hold most of its rows).  A unit's rows start at the slot's first
+// never synchronises after dispatch.  A unit's rows start at the slot's first
 // row (no alignment needed); rows past the slot's end are computed from
 // whatever follows and never stored.
 //
@@ -92,12 +86,8 @@ struct SmemLayout {
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t total_units;
-  int32_t total_shared;             // units of slots with several m-tiles
-  int32_t warp_sums[2][THREADS / 32];
-  // unit prefixes over the slot range: of slots with several m-tiles (shared
-  // weight tiles) and of slots with one (each slot counts in its own kind only)
-  int32_t pref_s[MOE_MAX_SLOTS + 1];
-  int32_t pref_1[MOE_MAX_SLOTS + 1];
+  int32_t warp_sums[THREADS / 32];
+  int32_t pref[MOE_MAX_SLOTS + 1];  // unit prefix over the slot range
   int32_t mt[MOE_MAX_SLOTS];        // 128-row m-tiles per slot
   int32_t row_base[MOE_MAX_SLOTS];  // first row of the slot
   int32_t row_end[MOE_MAX_SLOTS];   // one past its last row
@@ -105,7 +95,6 @@ struct SmemLayout {
   int32_t r_cnt[MOE_MAX_REPLICAS];
 };
 constexpr size_t smem_bytes() { return 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemLayout); }
-static_assert(smem_bytes() <= 232448, "shared memory per CTA");
 
 struct TcParams {
   const int32_t* offsets;
@@ -123,38 +112,20 @@ struct TcParams {
   uint32_t* status;
 };
 
-// Row tiles move as one TMA box of 16, 32, 64 or 128 rows: the smallest that
-// holds the unit's rows (a slot's last m-tile is often short, and at decode
-// most slots have a few rows).  The MMA still reads all 128 rows of the tile;
-// the rows past the box hold whatever an earlier stage left there, and their
-// accumulator rows are never stored.
-constexpr int A_BOXES = 4;
-struct AMaps {
-  CUtensorMap m[A_BOXES];  // box 64 x (16 << i) rows
-};
-
-// Work unit u -> (slot, m-tile, n-tile).  Of the first u units, floor(u * S / U)
-// are of the S shared-tile units (U in all), so unit u is the shared-tile unit
-// of that index when the count grows at u + 1, else the one-tile unit of index
-// u minus it; the kind's prefix over the slot range then gives the slot.
+// Work unit u -> (slot, m-tile, n-tile) through the prefix over the slot range.
 struct Unit {
   int slot, mt, n;
 };
 __device__ __forceinline__ Unit decode_unit(const SmemLayout& L, int nslots, int u) {
-  const int64_t S = L.total_shared, U = L.total_units;
-  const int32_t a0 = (int32_t)((int64_t)u * S / U), a1 = (int32_t)((int64_t)(u + 1) * S / U);
-  const bool shared = a1 > a0;
-  const int32_t* pref = shared ? L.pref_s : L.pref_1;
-  const int32_t idx = shared ? a0 : u - a0;
   int lo = 0, hi = nslots - 1;
-  while (lo < hi) {  // largest s with pref[s] <= idx: a slot of this kind
+  while (lo < hi) {  // largest s with pref[s] <= u
     int mid = (lo + hi + 1) >> 1;
-    if (pref[mid] <= idx)
+    if (L.pref[mid] <= u)
       lo = mid;
     else
       hi = mid - 1;
   }
-  const int local = idx - pref[lo];
+  const int local = u - L.pref[lo];
   const int tiles = L.mt[lo];
   Unit r;
   r.slot = lo;
@@ -165,7 +136,7 @@ __device__ __forceinline__ Unit decode_unit(const SmemLayout& L, int nslots, int
 
 template <bool SWIGLU, bool FUSE>
 __global__ void __launch_bounds__(THREADS, 1)
-    ffn_tc_kernel(const __grid_constant__ AMaps tmA, const __grid_constant__ CUtensorMap tmB,
+    ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const TcParams p, const __grid_constant__ FuseArgs f) {
   grid_dep_wait();    // earlier kernels on the stream are complete
   grid_dep_launch();  // the next kernel may start its launch
@@ -175,11 +146,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   SmemLayout& L = *reinterpret_cast<SmemLayout*>(stage_base + (size_t)STAGES * STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- unit table: m-tiles per slot, exclusive prefixes of both kinds' units
+  // ---- unit table: m-tiles per slot, exclusive prefix of units
   {
     const int per = (p.nslots + THREADS - 1) / THREADS;
     const int s0 = threadIdx.x * per;
-    int32_t local[2] = {0, 0};  // [0]: shared-tile units, [1]: one-tile units
+    int32_t local = 0;
     for (int i = 0; i < per; ++i) {
       int s = s0 + i;
       if (s < p.nslots) {
@@ -190,22 +161,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         L.mt[s] = mt;
         L.row_base[s] = (int32_t)o0;
         L.row_end[s] = (int32_t)(o0 + rows);
-        local[mt > 1 ? 0 : 1] += mt * p.n_tiles;
+        local += mt * p.n_tiles;
       }
     }
-    int32_t x[2] = {local[0], local[1]};
+    int32_t x = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        int32_t y = __shfl_up_sync(0xffffffffu, x[k], off);
-        if (lane >= off) x[k] += y;
-      }
+      int32_t y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
     }
-    if (lane == 31) {
-      L.warp_sums[0][warp] = x[0];
-      L.warp_sums[1][warp] = x[1];
-    }
+    if (lane == 31) L.warp_sums[warp] = x;
     if (threadIdx.x == 0) {
       L.abort_flag = 0;
       for (int i = 0; i < STAGES; ++i) {
@@ -226,31 +191,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     __syncthreads();
-    int32_t run[2];  // exclusive prefixes of this thread's group
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      int32_t before = 0;
-      for (int w = 0; w < warp; ++w) before += L.warp_sums[k][w];
-      run[k] = before + x[k] - local[k];
-    }
+    int32_t before = 0;
+    for (int w = 0; w < warp; ++w) before += L.warp_sums[w];
+    int32_t run = before + x - local;  // exclusive prefix of this thread's group
     for (int i = 0; i < per; ++i) {
       int s = s0 + i;
       if (s < p.nslots) {
-        L.pref_s[s] = run[0];
-        L.pref_1[s] = run[1];
-        run[L.mt[s] > 1 ? 0 : 1] += L.mt[s] * p.n_tiles;
+        L.pref[s] = run;
+        run += L.mt[s] * p.n_tiles;
       }
     }
     if (threadIdx.x == THREADS - 1) {
-      int32_t tot[2] = {0, 0};
-      for (int w = 0; w < THREADS / 32; ++w) {
-        tot[0] += L.warp_sums[0][w];
-        tot[1] += L.warp_sums[1][w];
-      }
-      L.pref_s[p.nslots] = tot[0];
-      L.pref_1[p.nslots] = tot[1];
-      L.total_shared = tot[0];
-      L.total_units = tot[0] + tot[1];
+      int32_t tot = 0;
+      for (int w = 0; w < THREADS / 32; ++w) tot += L.warp_sums[w];
+      L.pref[p.nslots] = tot;
+      L.total_units = tot;
     }
     fence_before();
     __syncthreads();
@@ -265,9 +220,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint64_t pol_act = policy_evict_last();
     const uint64_t pol_w = policy_evict_first();
     if (lane == 0) {
-      for (int i = 0; i < A_BOXES; ++i)
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA.m[i]))
-                     : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
     }
     uint32_t it = 0;
@@ -277,10 +230,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int32_t row0 = L.row_base[un.slot] + un.mt * BM;
       const int32_t brow1 = slot * p.b_rows_per_slot + un.n * p.b_tile_step;
       const int32_t brow2 = brow1 + p.b_second;
-      const int32_t nrows = L.row_end[un.slot] - row0;  // >= 1 for a unit's m-tile
-      const int bi = nrows <= 16 ? 0 : (nrows <= 32 ? 1 : (nrows <= 64 ? 2 : 3));
-      const CUtensorMap* amap = &tmA.m[bi];
-      const uint32_t tx = (uint32_t)((16 << bi) * BK * 2 + B_BYTES);
       bool ok = true;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
@@ -292,8 +241,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t full = smem_u32(&L.full[st]);
           const uint32_t sa = smem_u32(stage_base + (size_t)st * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
-          mbar_arrive_expect_tx(full, tx);
-          tma_load_2d<1>(sa, amap, kb * BK, row0, full, pol_act);
+          mbar_arrive_expect_tx(full, STAGE_BYTES);
+          tma_load_2d<1>(sa, &tmA, kb * BK, row0, full, pol_act);
           tma_load_2d<1>(sb, &tmB, kb * BK, brow1, full, pol_w);
           tma_load_2d<1>(sb + B_BOX_BYTES, &tmB, kb * BK, brow2, full, pol_w);
         }
@@ -468,7 +417,7 @@ bool device_setup(int* max_ctas) {
 }
 
 // One launch of MM1 + SwiGLU (gemm1) or MM2.
-moe_status run_ffn(const FfnArgs& a, const AMaps& mA, const CUtensorMap& mB, bool gemm1,
+moe_status run_ffn(const FfnArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, bool gemm1,
                    cudaStream_t s) {
   const int nslots = a.slot_hi - a.slot_lo;
   int max_ctas = 0;
@@ -533,14 +482,12 @@ moe_status launch_ffn_tc(const FfnArgs& a, cudaStream_t s) {
 moe_status launch_ffn_tc_single(const FfnArgs& a, cudaStream_t s) {
   const int nslots = a.slot_hi - a.slot_lo;
   if (nslots <= 0 || a.cap <= 0) return MOE_OK;
-  AMaps mA1, mA2;
-  CUtensorMap mB1, mB2;
-  bool ok = make_map(&mB1, a.wgu, (uint64_t)a.H, (uint64_t)a.P * 2 * a.I, 128) &&
-            make_map(&mB2, a.wd, (uint64_t)a.I, (uint64_t)a.P * a.H, 128);
-  for (int i = 0; i < A_BOXES && ok; ++i)
-    ok = make_map(&mA1.m[i], a.xs, (uint64_t)a.H, (uint64_t)a.cap, 16u << i) &&
-         make_map(&mA2.m[i], a.h, (uint64_t)a.I, (uint64_t)a.cap, 16u << i);
-  if (!ok) return MOE_ERR_CUDA;
+  CUtensorMap mA1, mB1, mA2, mB2;
+  if (!make_map(&mA1, a.xs, (uint64_t)a.H, (uint64_t)a.cap, 128) ||
+      !make_map(&mB1, a.wgu, (uint64_t)a.H, (uint64_t)a.P * 2 * a.I, 128) ||
+      !make_map(&mA2, a.h, (uint64_t)a.I, (uint64_t)a.cap, 128) ||
+      !make_map(&mB2, a.wd, (uint64_t)a.I, (uint64_t)a.P * a.H, 128))
+    return MOE_ERR_CUDA;
   moe_status st = run_ffn(a, mA1, mB1, true, s);
   if (st != MOE_OK) return st;
   return run_ffn(a, mA2, mB2, false, s);
