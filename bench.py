@@ -49,12 +49,14 @@ L2_NOTE = "inputs larger than L2: every step streams the touched experts' weight
 
 def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
                       fp8: bool = False, router_gemm: bool = False, sms: int = 152,
-                      fused_combine: bool = False, ffn_split: bool = False) -> int:
+                      fused_combine: bool = False, ffn_split: bool = False,
+                      fp8_pair: bool = False) -> int:
     """Kernel launches of one layer step: gather (with given logits it routes the rows
     in the same launch, the fused add + RMSNorm included), dispatch (one CTA-wide kernel for <= 8192 routed pairs whose tables
     fit 48 KB, else histogram + scan + rank; then the row copy; + the alignment pad
     kernel when align > 1, plus the FP8 rows' pad kernel on the FP8 path), grouped FFN
-    (MM1+SwiGLU and MM2; one persistent launch for both on FP8), combine with the DP
+    (MM1+SwiGLU and MM2; one persistent launch for both on FP8 with few rows per
+    slot, MM1 + the quantisation of h + MM2 with many), combine with the DP
     scatter (none when the down projection's epilogue combines).  With the router gate
     GEMM the logits gather goes and routing is one fused kernel (>= sms/4 row tiles and
     k <= 8) or split GEMM + sum + top-k."""
@@ -64,31 +66,40 @@ def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
     if router_gemm:
         gather = 1
         route = 1 if (k <= 8 and 4 * ((rows + 127) // 128) >= sms) else 3
-    ffn = 1 if fp8 else (4 if ffn_split else 2)   # the split: two launches per stream
+    ffn = (3 if fp8_pair else 1) if fp8 else (4 if ffn_split else 2)   # split: 2 per stream
     return gather + route + dispatch + ffn + (0 if fused_combine else 1)
 
 
-def ffn_kernel(cap: int, P: int, fp8: bool = False) -> str:
-    """The grouped-FFN kernel the library picks: on FP8 operands the weights-as-M
-    single-SM kernel; in bf16 weights as M on SM pairs from 192 sorted rows per slot
-    on average, else tokens as M on single SMs."""
+def fp8_pair(cap: int, P: int, H: int, I: int) -> bool:
+    """True if the FP8 grouped FFN runs on SM pairs with block-scaled MMAs (192 or
+    more sorted rows per slot on average, H and I multiples of 512)."""
+    return cap // max(P, 1) >= 192 and H % 512 == 0 and I % 512 == 0
+
+
+def ffn_kernel(cap: int, P: int, fp8: bool = False, H: int = 0, I: int = 0) -> str:
+    """The grouped-FFN kernel the library picks: on FP8 operands the block-scaled
+    pair kernel with many rows per slot, else the weights-as-M single-SM kernel; in
+    bf16 weights as M on SM pairs from 192 sorted rows per slot on average, else
+    tokens as M on single SMs."""
     if fp8:
-        return "ffn_fp8_kernel"
+        return "ffn_f8swap_kernel" if fp8_pair(cap, P, H, I) else "ffn_fp8_kernel"
     return "ffn_swap_kernel" if cap // max(P, 1) >= 192 else "ffn_tc_kernel"
 
-# dram__bytes_read.sum + dram__bytes_write.sum of the grouped-FFN launches (two in bf16,
-# one on FP8) of one step of the workload (ncu, --clock-control none), valid while the kernel's
-# sources hash to the recorded SHA-256 prefix; any other source reports traffic null.  The bf16
-# records come from shrunk cases of the same kernels (32-expert prefill, 64-expert decode) and
-# are scaled to the workload by the units processed (traffic per slot and per routed row is
-# the same); the FP8 decode record is a capture of the full workload.
+# dram__bytes_read.sum + dram__bytes_write.sum of the grouped-FFN launches (two in bf16; on
+# FP8 one with few rows per slot, three with many: MM1, the quantisation of h, MM2) of one step
+# of the workload (ncu, --clock-control none), valid while the kernel's sources hash to the
+# recorded SHA-256 prefix; any other source reports traffic null.  The records come from shrunk
+# cases of the same kernels (32-expert prefill, 64-expert decode) and are scaled to the workload
+# by the units processed (traffic per slot and per routed row is the same).
 FFN_TRAFFIC = {
     "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "e25e9afc9231a9d9",
                 "bytes": 25142339584},
     "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "ec94ad3d0984b261",
                "bytes": 5580442771},
     "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
-                   "sha256_16": "b18d85061d74668d", "bytes": 2789277440},
+                   "sha256_16": "5c89e5373772b8fd", "bytes": 2791012496},
+    "prefill_fp8": {"sources": ["ffn_fp8_swap.cu", "ffn_fp8.cu", "fp8.cu", "tc_ptx.cuh"],
+                    "sha256_16": "29482dbcecfb0245", "bytes": 13580828672},
 }
 
 
@@ -367,6 +378,9 @@ def run_native(args, rank, world, local_rank):
         # and scales, h written and read back (codes + scales), bf16 output row
         ffn_bytes = touched * 3 * spec.I * spec.H * (1 + 1 / 16384) + routed * (
             spec.H * (1 + 1 / 128) + 2 * spec.I * (1 + 1 / 128) + 2 * spec.H)
+        if fp8_pair(layer.cap, layer.P, spec.H, spec.I):
+            # h also goes through HBM in fp32: written by MM1, read by its quantisation
+            ffn_bytes += routed * 8 * spec.I
     else:
         ffn_bytes = touched * 3 * spec.I * spec.H * b + routed * (2 * spec.H + 2 * spec.I) * b
         if layer.fused_combine:
@@ -395,8 +409,12 @@ def run_native(args, rank, world, local_rank):
     # attainable at this intensity: min(tensor peak, intensity x HBM bandwidth)
     attainable = min(tc_peak, intensity * pk["hbm_gbs"] / 1e3)
     roof.update({"traffic": ffn_traffic(args),
-                 "kernel": (f"moe_grouped_ffn_fp8 ({ffn_kernel(layer.cap, layer.P, True)}: "
-                            "MM1+SwiGLU and MM2 in one persistent launch)" if args.fp8 else
+                 "kernel": ((f"moe_grouped_ffn_fp8 ({ffn_kernel(layer.cap, layer.P, True, spec.H, spec.I)} "
+                             "MM1+SwiGLU and MM2 launches with block-scaled MMAs, h quantised "
+                             "by its own launch between them)"
+                             if fp8_pair(layer.cap, layer.P, spec.H, spec.I) else
+                             f"moe_grouped_ffn_fp8 ({ffn_kernel(layer.cap, layer.P, True)}: "
+                             "MM1+SwiGLU and MM2 in one persistent launch)") if args.fp8 else
                             f"moe_grouped_ffn_combine ({ffn_kernel(layer.cap, layer.P)} "
                             "MM1+SwiGLU and MM2 launches; combine + DP scatter in MM2's "
                             "epilogue)" if layer.fused_combine and in_epi else
@@ -531,7 +549,8 @@ def run_native(args, rank, world, local_rank):
                                            spec.E + spec.n_shared, layer.P, layer.cap,
                                            spec.align, args.fp8, args.router == "gemm",
                                            torch.cuda.get_device_properties(dev).multi_processor_count,
-                                           bool(in_epi), bool(layer.ffn_split)),
+                                           bool(in_epi), bool(layer.ffn_split),
+                                           fp8_pair(layer.cap, layer.P, spec.H, spec.I)),
                 inputs=(x_loc, lg_loc, wgu, wd, l2p_np, nrep_np), gate=gate_np)
 
 

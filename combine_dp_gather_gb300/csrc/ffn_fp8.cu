@@ -59,6 +59,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "ffn_internal.h"
 #include "fp8.cuh"
 #include "tc_ptx.cuh"
 
@@ -737,9 +738,14 @@ moe_status run_f8(const F8Args& a, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Workspace: h codes [cap, I], h scale bytes [cap, I/128], then (the pair
+// kernel's path) h in fp32 [cap, I], then the scheduler's words.
 size_t hscale_offset(int64_t cap, int I) { return ((size_t)cap * I + 255) & ~(size_t)255; }
-size_t sync_offset(int64_t cap, int I) {
+size_t h32_offset(int64_t cap, int I) {
   return (hscale_offset(cap, I) + (size_t)cap * (I / 128) + 255) & ~(size_t)255;
+}
+size_t sync_offset(int64_t cap, int I) {
+  return (h32_offset(cap, I) + (size_t)cap * I * sizeof(float) + 255) & ~(size_t)255;
 }
 
 }  // namespace
@@ -780,6 +786,32 @@ extern "C" moe_status moe_grouped_ffn_fp8(const uint8_t* d_sorted_q,
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
+  auto aligned4 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 3u) == 0; };
+  if (ffn_fp8_uses_pair_kernel(cap, P, H, I) && aligned4(d_sorted_scales) &&
+      aligned4(d_w_gate_up_scales) && aligned4(d_w_down_scales)) {
+    // many rows per slot: weights as M on SM pairs, block-scaled MMAs
+    uint8_t* ws = static_cast<uint8_t*>(d_ws);
+    F8SwapArgs f;
+    f.xq = d_sorted_q;
+    f.xs = d_sorted_scales;
+    f.offsets = d_offsets_P;
+    f.P = P;
+    f.slot_lo = slot_lo;
+    f.slot_hi = slot_hi;
+    f.cap = cap;
+    f.wguq = d_w_gate_up_q;
+    f.wgus = d_w_gate_up_scales;
+    f.wdq = d_w_down_q;
+    f.wds = d_w_down_scales;
+    f.H = H;
+    f.I = I;
+    f.h32 = reinterpret_cast<float*>(ws + h32_offset(cap, I));
+    f.hq = ws;
+    f.hs = ws + hscale_offset(cap, I);
+    f.y = static_cast<__nv_bfloat16*>(d_out_sorted);
+    f.status = d_status;
+    return launch_ffn_fp8_swap(f, as_stream(stream));
+  }
   F8Args a;
   a.xq = d_sorted_q;
   a.xscale = d_sorted_scales;

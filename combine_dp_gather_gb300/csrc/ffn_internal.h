@@ -45,4 +45,30 @@ moe_status launch_ffn_tc_swap(const FfnArgs& a, cudaStream_t s);
 // float32 on the CUDA cores.
 moe_status launch_ffn_simt_f32(const FfnArgs& a, cudaStream_t s);
 
+// FP8 operands on SM pairs with the weights as M and block-scaled MMAs (many
+// rows per slot): MM1 + SwiGLU into float h32, its per-token-group
+// quantisation into hq / hs, MM2 into bf16 y.
+struct F8SwapArgs {
+  const uint8_t* xq;     // [cap, H] e4m3 rows, sorted by slot
+  const uint8_t* xs;     // [cap, H/128] their scale bytes
+  const int32_t* offsets;  // [P + 1]
+  int P, slot_lo, slot_hi;
+  int64_t cap;
+  const uint8_t* wguq;   // [P, 2I, H] e4m3
+  const uint8_t* wgus;   // [P, 2I/128, H/128]
+  const uint8_t* wdq;    // [P, H, I] e4m3
+  const uint8_t* wds;    // [P, H/128, I/128]
+  int H, I;
+  float* h32;            // [cap, I] workspace
+  uint8_t* hq;           // [cap, I] workspace
+  uint8_t* hs;           // [cap, I/128] workspace
+  __nv_bfloat16* y;      // [cap, H]
+  uint32_t* status;
+};
+// True for many rows per slot with H and I multiples of 512 (the scale words
+// of four k-blocks are then 4-byte aligned); the caller also checks that the
+// scale arrays are.
+bool ffn_fp8_uses_pair_kernel(int64_t cap, int P, int H, int I);
+moe_status launch_ffn_fp8_swap(const F8SwapArgs& a, cudaStream_t s);
+
 }  // namespace moe

@@ -529,7 +529,8 @@ moe_status moe_dispatch_fp8(const void* d_global, const int32_t* d_ids, int64_t 
                             void* d_ws, size_t ws_bytes, uint32_t* d_status, void* stream);
 
 /* Workspace of moe_grouped_ffn_fp8: the FP8 SwiGLU activation (codes and
- * scale bytes) of cap rows, then the scheduler's words: the last
+ * scale bytes) of cap rows, the fp32 activation of cap rows (the path for many
+ * rows per slot), then the scheduler's words: the last
  * 4 * (3 + MOE_MAX_SLOTS) bytes.  They must be zero before the first call on a
  * workspace (e.g. a zero-filled allocation); every call leaves them zero.  A
  * call that finds them otherwise sets MOE_DEV_BAD_WORKSPACE (its output is then
@@ -546,9 +547,15 @@ size_t moe_grouped_ffn_fp8_ws_bytes(int64_t cap, int I);
  *   d_w_down_q [P, H, I], d_w_down_scales [P, H/128, I/128]
  *   d_out_sorted  device bf16 [cap, H] out (rows of the slot range)
  * H a multiple of 256, I a multiple of 128; sm_103 only (else
- * MOE_ERR_UNSUPPORTED).  Both GEMMs run in one launch: CTAs claim the MM1 units
- * and then the MM2 units in order, and an MM2 unit waits (bounded, else
- * MOE_DEV_TIMEOUT) until its slot's h is written. */
+ * MOE_ERR_UNSUPPORTED).  With few rows per slot both GEMMs run in one launch:
+ * CTAs claim the MM1 units and then the MM2 units in order, and an MM2 unit
+ * waits (bounded, else MOE_DEV_TIMEOUT) until its slot's h is written.  With
+ * 192 or more rows per slot on average (cap / P), H and I multiples of 512 and
+ * 4-byte aligned scale arrays, the GEMMs run on SM pairs with the weights as the
+ * MMA's M operand and block-scaled MMAs (the scales applied by the tensor cores,
+ * accumulators in tensor memory for a whole unit of up to 320 tokens): MM1 +
+ * SwiGLU writes h in fp32 to the workspace, one launch quantises it per token
+ * (groups of 128 features, as moe_quantize_fp8_groups), MM2 follows. */
 moe_status moe_grouped_ffn_fp8(const uint8_t* d_sorted_q, const uint8_t* d_sorted_scales,
                                const int32_t* d_offsets_P, int P, int slot_lo, int slot_hi,
                                int64_t cap, const uint8_t* d_w_gate_up_q,

@@ -69,11 +69,17 @@ def graph_replay_matches_eager(layer, x_loc, lg_loc, out):
 # ------------------------------------------------------------------ hard rows
 def ffn_kernel_of(layer):
     """Which grouped-FFN kernel the library runs for this layer: FP8 -> 'fp8' (weights
-    as M, units of up to 64 tokens); bf16 with >= 192 sorted rows per slot on average
+    as M, units of up to 64 tokens), or with >= 192 sorted rows per slot on average and
+    H, I multiples of 512 'pair8' (the pair kernel's units on FP8, the first MMA up to
+    224 tokens); bf16 with >= 192 sorted rows per slot on average
     -> 'pair' (weights as M on SM pairs, units of up to 320 tokens); else 'tc' (tokens
     as M, 128-row m-tiles).  With the split FFN, a function of the slot's rows: 'pair'
     from the hot threshold, else 'tc'."""
     if getattr(layer, "fp8", False):
+        # many rows per slot (and H, I multiples of 512): the FP8 pair kernel
+        if (layer.cap // max(layer.P, 1) >= 192 and layer.H % 512 == 0
+                and layer.I % 512 == 0):
+            return "pair8"
         return "fp8"
     split = getattr(layer, "ffn_split", None)
     if split:
@@ -84,14 +90,14 @@ def ffn_kernel_of(layer):
 def _slot_positions(rows: int, kernel: str):
     """Positions within a slot of `rows` sorted rows where the kernel's tiling changes."""
     pos = set()
-    if kernel == "pair":
+    if kernel in ("pair", "pair8"):
         # unit = up to 320 tokens; N = tokens rounded up to 16, CTA c of the pair holds
-        # tokens [c*N/2, (c+1)*N/2); the first MMA (N0 = min(N, 256)) reads the first
-        # N0/2 of each CTA's rows, the tail MMA the rest (columns 256-319)
+        # tokens [c*N/2, (c+1)*N/2); the first MMA (N0 = min(N, 256), FP8: 224) reads
+        # the first N0/2 of each CTA's rows, the tail MMA the rest
         for g0 in range(0, rows, 320):
             nt = min(320, rows - g0)
             N = (nt + 15) & ~15
-            h, n0 = N // 2, min(N, 256)
+            h, n0 = N // 2, min(N, 256 if kernel == "pair" else 224)
             for p in (0, 31, 32, n0 // 2 - 1, n0 // 2, h - 1, h, h + 31, h + 32,
                       h + n0 // 2 - 1, h + n0 // 2, N - 1, nt - 1):
                 if 0 <= p < nt:

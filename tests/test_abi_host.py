@@ -482,11 +482,12 @@ def test_fp8_entries_reject_bad_args(md):
     assert ffn(wsb=16) == E_CAP
     assert ffn(cap=0) == md.MOE_OK             # nothing to do
     assert L.moe_grouped_ffn_fp8_ws_bytes(64, 100) == 0
-    # layout: h codes [cap, I], scale bytes [cap, I/128] (each from a 256-byte boundary),
-    # then the scheduler's 3 + MOE_MAX_SLOTS int32 words, last
+    # layout: h codes [cap, I], scale bytes [cap, I/128], h in fp32 [cap, I] (the pair
+    # kernel's path; each from a 256-byte boundary), then the scheduler's
+    # 3 + MOE_MAX_SLOTS int32 words, last
     up = lambda n: (n + 255) // 256 * 256
     for cap, I in [(64, 256), (1, 128), (1000, 2048), (65600, 2048)]:
-        words = up(up(cap * I) + cap * (I // 128))
+        words = up(up(up(cap * I) + cap * (I // 128)) + 4 * cap * I)
         assert L.moe_grouped_ffn_fp8_ws_bytes(cap, I) == words + 4 * (3 + 1024)
         assert md.fp8_ffn_workspace(cap, I, "cpu").numel() == words + 4 * (3 + 1024)
     assert not md.fp8_ffn_workspace(64, 256, "cpu").any()      # zero-filled

@@ -72,6 +72,10 @@ def test_launch_counts_match_the_measured_steps():
     # decode: 440 global rows, top-8, 256 experts / slots, cap 3520 + 64
     assert bench.launches_per_step(440, 8, 256, 256, 3584, 1) == 6
     assert bench.launches_per_step(440, 8, 256, 256, 3584, 1, fp8=True) == 5
+    # FP8 with many rows per slot: MM1, the quantisation of h, MM2
+    assert bench.launches_per_step(8192, 8, 256, 256, 65600, 1, fp8=True, fp8_pair=True) == 9
+    assert bench.fp8_pair(65600, 256, 7168, 2048) and not bench.fp8_pair(3584, 256, 7168, 2048)
+    assert not bench.fp8_pair(65600, 256, 7168, 2304)
     assert bench.launches_per_step(440, 8, 256, 256, 3584, 1, router_gemm=True) == 9
     # prefill: 8192 rows x 8 pairs take the chunked dispatch (histogram, scan, rank, copy)
     assert bench.launches_per_step(8192, 8, 256, 256, 65600, 1) == 8

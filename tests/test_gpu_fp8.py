@@ -114,7 +114,7 @@ def test_dispatch_fp8_bitexact(md, orc, rows, E, align):
     assert (to_np(xq)[n:] == 0x55).all()                                  # past the last slot
 
 
-def _fp8_inputs(orc, counts, H, I, seed, extra_rows=40):
+def _fp8_inputs(orc, counts, H, I, seed, extra_rows=40, w_std=0.05):
     P = len(counts)
     offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     cap = int(offsets[-1]) + extra_rows
@@ -124,7 +124,7 @@ def _fp8_inputs(orc, counts, H, I, seed, extra_rows=40):
     # per-block weight magnitudes differ, so a misread block scale shows
     def blocks(R, K):
         m = 2.0 ** rng.integers(-3, 4, (R // 128, K // 128))
-        return (rng.standard_normal((R, K)) * 0.05 * m.repeat(128, 0).repeat(128, 1))
+        return (rng.standard_normal((R, K)) * w_std * m.repeat(128, 0).repeat(128, 1))
     wgu = [orc.quant_blocks(blocks(2 * I, H)) for _ in range(P)]
     wd = [orc.quant_blocks(blocks(H, I)) for _ in range(P)]
     return offsets, cap, xq, xe, wgu, wd
@@ -160,6 +160,46 @@ def test_grouped_ffn_fp8(md, orc, counts, lo, hi, H, I):
     assert_close(got[a:b], ref[a:b], BF16_ATOL, BF16_RTOL, "grouped FFN fp8")
     assert rel_fro(got[a:b], ref[a:b]) < 1e-2
     assert (got[:a] == sentinel).all() and (got[b:] == sentinel).all()
+
+
+@pytest.mark.parametrize("counts,lo,hi,H,I", [
+    ([0, 1, 15, 16, 17, 100, 223, 224, 225, 240, 256, 300, 320, 321, 700, 1000], 0, 16,
+     1024, 512),
+    ([250, 0, 333, 96, 260, 640, 5, 255], 1, 7, 1536, 1024)])
+def test_grouped_ffn_fp8_pair(md, orc, counts, lo, hi, H, I):
+    """Many rows per slot: the FP8 pair kernel (weights as M on SM pairs, scales applied
+    by the block-scaled MMA, units of up to 320 tokens split 224 + 96).  Ragged groups,
+    tails of 1-96 tokens, several groups per slot, empty slots, slot ranges; rows
+    outside the range untouched; K / 128 = 8 and 4 (first case), 12 and 8 k-blocks.
+    The weights are small enough that every gate value goes through a sigmoid that is
+    not 1 in fp32: with large gates the activation is an exact product of e4m3 values
+    and lands on e4m3 rounding ties, where the kernel's fp32 and the oracle's fp64 round
+    to neighbouring codes (both correct)."""
+    offsets, cap, xq, xe, wgu, wd = _fp8_inputs(orc, counts, H, I, seed=sum(counts) + lo,
+                                                w_std=0.01)
+    P = len(counts)
+    assert cap // P >= 192                           # the pair kernel's shape
+    w_fp8 = (_dev_u8(np.stack([w[0] for w in wgu])), _dev_u8(np.stack([w[1] for w in wgu])),
+             _dev_u8(np.stack([w[0] for w in wd])), _dev_u8(np.stack([w[1] for w in wd])))
+    sentinel = 1232.0
+    ys = torch.full((cap, H), sentinel, device=DEV, dtype=torch.bfloat16)
+    ws = md.fp8_ffn_workspace(cap, I, DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    md.moe_grouped_ffn_fp8(_dev_u8(xq), _dev_u8(xe), torch.from_numpy(offsets).to(DEV), w_fp8, ys,
+                           ws, lo, hi, d_status=st)
+    assert _status(st) == 0
+    a, b = int(offsets[lo]), int(offsets[hi])
+    ref = orc.grouped_ffn_fp8(xq, xe, offsets, lambda s: (*wgu[s], *wd[s]), lo, hi)
+    got = as_f32(to_np(ys)).astype(np.float64)
+    assert_close(got[a:b], ref[a:b], BF16_ATOL, BF16_RTOL, "grouped FFN fp8, pair kernel")
+    assert rel_fro(got[a:b], ref[a:b]) < 1e-2
+    assert (got[:a] == sentinel).all() and (got[b:] == sentinel).all()
+    # a second call on the same workspace gives the same bits
+    ys2 = torch.full((cap, H), sentinel, device=DEV, dtype=torch.bfloat16)
+    md.moe_grouped_ffn_fp8(_dev_u8(xq), _dev_u8(xe), torch.from_numpy(offsets).to(DEV), w_fp8,
+                           ys2, ws, lo, hi, d_status=st)
+    assert _status(st) == 0
+    assert torch.equal(ys.view(torch.int16), ys2.view(torch.int16))
 
 
 def test_grouped_ffn_fp8_dsv3_width(md, orc):
