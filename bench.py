@@ -99,7 +99,7 @@ FFN_TRAFFIC = {
     "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
                    "sha256_16": "5c89e5373772b8fd", "bytes": 2791012496},
     "prefill_fp8": {"sources": ["ffn_fp8_swap.cu", "ffn_fp8.cu", "fp8.cu", "tc_ptx.cuh"],
-                    "sha256_16": "29482dbcecfb0245", "bytes": 13580828672},
+                    "sha256_16": "4f4867ec8b900465", "bytes": 13580828672},
 }
 
 

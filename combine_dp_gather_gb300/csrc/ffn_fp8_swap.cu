@@ -40,9 +40,9 @@
 //
 //   MM1 + SwiGLU: as the bf16 kernel; h is written in fp32 and quantised per
 //                 token over groups of 128 features by its own launch
-//                 (moe_quantize_fp8_groups), so its e4m3 codes round from
-//                 fp32 values as the reference quantisation rounds from exact
-//                 ones.
+//                 (moe_quantize_fp8_groups): its e4m3 codes are those of the
+//                 exact activations except where one lies within fp32 rounding
+//                 of a rounding tie (a bf16 copy of h would move many more).
 //   MM2:          bf16 output rows, as the bf16 kernel.
 //
 // Roles (448 threads, one CTA per SM, clusters of two):
