@@ -50,7 +50,7 @@ L2_NOTE = "inputs larger than L2: every step streams the touched experts' weight
 def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
                       fp8: bool = False, router_gemm: bool = False, sms: int = 152,
                       fused_combine: bool = False, ffn_split: bool = False,
-                      fp8_pair: bool = False) -> int:
+                      fp8_pair: bool = False, fp8_split: bool = False) -> int:
     """Kernel launches of one layer step: gather (with given logits it routes the rows
     in the same launch, the fused add + RMSNorm included), dispatch (one CTA-wide kernel for <= 8192 routed pairs whose tables
     fit 48 KB, else histogram + scan + rank; then the row copy; + the alignment pad
@@ -66,7 +66,8 @@ def launches_per_step(rows: int, k: int, E: int, P: int, cap: int, align: int,
     if router_gemm:
         gather = 1
         route = 1 if (k <= 8 and 4 * ((rows + 127) // 128) >= sms) else 3
-    ffn = (3 if fp8_pair else 1) if fp8 else (4 if ffn_split else 2)   # split: 2 per stream
+    ffn = ((3 if fp8_pair else (4 if fp8_split else 1)) if fp8
+           else (4 if ffn_split else 2))   # bf16 split: 2 per stream
     return gather + route + dispatch + ffn + (0 if fused_combine else 1)
 
 
@@ -76,12 +77,21 @@ def fp8_pair(cap: int, P: int, H: int, I: int) -> bool:
     return cap // max(P, 1) >= 192 and H % 512 == 0 and I % 512 == 0
 
 
+def fp8_split(cap: int, P: int, H: int, I: int) -> bool:
+    """True if the FP8 grouped FFN sends its slots of 192 or more rows to the pair
+    kernel and the rest to the one-launch kernel (32-191 rows per slot on average)."""
+    return (32 <= cap // max(P, 1) < 192 and cap >= 192 and H % 512 == 0
+            and I % 512 == 0)
+
+
 def ffn_kernel(cap: int, P: int, fp8: bool = False, H: int = 0, I: int = 0) -> str:
     """The grouped-FFN kernel the library picks: on FP8 operands the block-scaled
     pair kernel with many rows per slot, else the weights-as-M single-SM kernel; in
     bf16 weights as M on SM pairs from 192 sorted rows per slot on average, else
     tokens as M on single SMs."""
     if fp8:
+        if fp8_split(cap, P, H, I):
+            return "ffn_f8swap_kernel for slots of >= 192 rows, ffn_fp8_kernel for the rest"
         return "ffn_f8swap_kernel" if fp8_pair(cap, P, H, I) else "ffn_fp8_kernel"
     return "ffn_swap_kernel" if cap // max(P, 1) >= 192 else "ffn_tc_kernel"
 
@@ -413,6 +423,9 @@ def run_native(args, rank, world, local_rank):
                              "MM1+SwiGLU and MM2 launches with block-scaled MMAs, h quantised "
                              "by its own launch between them)"
                              if fp8_pair(layer.cap, layer.P, spec.H, spec.I) else
+                             (f"moe_grouped_ffn_fp8 ({ffn_kernel(layer.cap, layer.P, True, spec.H, spec.I)}: "
+                              "pair launches with h quantised between them, then one launch)")
+                             if fp8_split(layer.cap, layer.P, spec.H, spec.I) else
                              f"moe_grouped_ffn_fp8 ({ffn_kernel(layer.cap, layer.P, True)}: "
                              "MM1+SwiGLU and MM2 in one persistent launch)") if args.fp8 else
                             f"moe_grouped_ffn_combine ({ffn_kernel(layer.cap, layer.P)} "
@@ -550,7 +563,8 @@ def run_native(args, rank, world, local_rank):
                                            spec.align, args.fp8, args.router == "gemm",
                                            torch.cuda.get_device_properties(dev).multi_processor_count,
                                            bool(in_epi), bool(layer.ffn_split),
-                                           fp8_pair(layer.cap, layer.P, spec.H, spec.I)),
+                                           fp8_pair(layer.cap, layer.P, spec.H, spec.I),
+                                           fp8_split(layer.cap, layer.P, spec.H, spec.I)),
                 inputs=(x_loc, lg_loc, wgu, wd, l2p_np, nrep_np), gate=gate_np)
 
 

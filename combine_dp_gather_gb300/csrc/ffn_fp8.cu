@@ -157,6 +157,7 @@ struct F8Phase {
 struct F8Params {
   const int32_t* offsets;
   int slot_lo, nslots;
+  int32_t max_slot_rows;   // slots with more rows get no units (another kernel's)
   int64_t cap;
   int H;
   F8Phase ph[2];
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (s < p.nslots) {
         const int32_t o0 = p.offsets[p.slot_lo + s];
         int32_t rows = p.offsets[p.slot_lo + s + 1] - o0;
-        if (rows < 0) rows = 0;
+        if (rows < 0 || rows > p.max_slot_rows) rows = 0;
         L.row0[s] = o0;
         L.rows[s] = rows;
         local += token_groups(rows);
@@ -689,6 +690,7 @@ struct F8Args {
   __nv_bfloat16* y;
   int32_t* sync;
   uint32_t* status;
+  int32_t max_slot_rows;
 };
 
 moe_status run_f8(const F8Args& a, cudaStream_t s) {
@@ -706,6 +708,7 @@ moe_status run_f8(const F8Args& a, cudaStream_t s) {
   p.offsets = a.offsets;
   p.slot_lo = a.slot_lo;
   p.nslots = a.slot_hi - a.slot_lo;
+  p.max_slot_rows = a.max_slot_rows;
   p.cap = a.cap;
   p.H = a.H;
   F8Phase& m1 = p.ph[0];
@@ -787,9 +790,14 @@ extern "C" moe_status moe_grouped_ffn_fp8(const uint8_t* d_sorted_q,
     return MOE_ERR_CUDA;
   if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
   auto aligned4 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 3u) == 0; };
-  if (ffn_fp8_uses_pair_kernel(cap, P, H, I) && aligned4(d_sorted_scales) &&
-      aligned4(d_w_gate_up_scales) && aligned4(d_w_down_scales)) {
-    // many rows per slot: weights as M on SM pairs, block-scaled MMAs
+  const bool pair_ok = H % 512 == 0 && I % 512 == 0 && aligned4(d_sorted_scales) &&
+                       aligned4(d_w_gate_up_scales) && aligned4(d_w_down_scales);
+  // many rows per slot: every slot on SM pairs with block-scaled MMAs; a
+  // skewed layer (fewer rows per slot on average, EPLB): its slots of 192 or
+  // more rows there, the others on the single-SM kernel after them
+  const bool all_pair = pair_ok && ffn_fp8_uses_pair_kernel(cap, P, H, I);
+  const bool split = pair_ok && !all_pair && ffn_fp8_splits_slots(cap, P, H, I);
+  if (all_pair || split) {
     uint8_t* ws = static_cast<uint8_t*>(d_ws);
     F8SwapArgs f;
     f.xq = d_sorted_q;
@@ -810,7 +818,9 @@ extern "C" moe_status moe_grouped_ffn_fp8(const uint8_t* d_sorted_q,
     f.hs = ws + hscale_offset(cap, I);
     f.y = static_cast<__nv_bfloat16*>(d_out_sorted);
     f.status = d_status;
-    return launch_ffn_fp8_swap(f, as_stream(stream));
+    f.min_slot_rows = split ? kFp8PairRows : 0;
+    const moe_status st = launch_ffn_fp8_swap(f, as_stream(stream));
+    if (st != MOE_OK || !split) return st;
   }
   F8Args a;
   a.xq = d_sorted_q;
@@ -831,5 +841,6 @@ extern "C" moe_status moe_grouped_ffn_fp8(const uint8_t* d_sorted_q,
   a.y = static_cast<__nv_bfloat16*>(d_out_sorted);
   a.sync = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(d_ws) + sync_offset(cap, I));
   a.status = d_status;
+  a.max_slot_rows = split ? kFp8PairRows - 1 : INT32_MAX;
   return run_f8(a, as_stream(stream));
 }

@@ -716,7 +716,7 @@ moe_status run_f8swap(const F8SwapArgs& a, const Maps& m, bool gemm1, cudaStream
   p.offsets = a.offsets;
   p.slot_lo = a.slot_lo;
   p.nslots = a.slot_hi - a.slot_lo;
-  p.min_slot_rows = 0;
+  p.min_slot_rows = a.min_slot_rows;
   p.max_slot_rows = INT32_MAX;
   p.cap = a.cap;
   p.status = a.status;
@@ -761,7 +761,11 @@ moe_status run_f8swap(const F8SwapArgs& a, const Maps& m, bool gemm1, cudaStream
 
 bool ffn_fp8_uses_pair_kernel(int64_t cap, int P, int H, int I) {
   // many rows per slot, and the scale words of four k-blocks 4-byte aligned
-  return P > 0 && cap / P >= 192 && H % 512 == 0 && I % 512 == 0;
+  return P > 0 && cap / P >= kFp8PairRows && H % 512 == 0 && I % 512 == 0;
+}
+bool ffn_fp8_splits_slots(int64_t cap, int P, int H, int I) {
+  return P > 0 && cap / P >= 32 && cap / P < kFp8PairRows && cap >= kFp8PairRows &&
+         H % 512 == 0 && I % 512 == 0;
 }
 
 moe_status launch_ffn_fp8_swap(const F8SwapArgs& a, cudaStream_t s) {

@@ -64,11 +64,18 @@ struct F8SwapArgs {
   uint8_t* hs;           // [cap, I/128] workspace
   __nv_bfloat16* y;      // [cap, H]
   uint32_t* status;
+  int32_t min_slot_rows = 0;  // slots with fewer rows get no units
 };
-// True for many rows per slot with H and I multiples of 512 (the scale words
-// of four k-blocks are then 4-byte aligned); the caller also checks that the
-// scale arrays are.
+// Rows per slot from which a slot goes to the FP8 pair kernel.
+constexpr int32_t kFp8PairRows = 192;
+// True for many rows per slot (kFp8PairRows on average) with H and I multiples
+// of 512 (the scale words of four k-blocks are then 4-byte aligned); the caller
+// also checks that the scale arrays are.
 bool ffn_fp8_uses_pair_kernel(int64_t cap, int P, int H, int I);
+// True for a layer with fewer rows per slot on average but enough (32) that
+// some slots may hold kFp8PairRows or more: those run on the pair kernel, the
+// rest on the single-SM FP8 kernel.
+bool ffn_fp8_splits_slots(int64_t cap, int P, int H, int I);
 moe_status launch_ffn_fp8_swap(const F8SwapArgs& a, cudaStream_t s);
 
 }  // namespace moe

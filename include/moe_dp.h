@@ -555,7 +555,9 @@ size_t moe_grouped_ffn_fp8_ws_bytes(int64_t cap, int I);
  * MMA's M operand and block-scaled MMAs (the scales applied by the tensor cores,
  * accumulators in tensor memory for a whole unit of up to 320 tokens): MM1 +
  * SwiGLU writes h in fp32 to the workspace, one launch quantises it per token
- * (groups of 128 features, as moe_quantize_fp8_groups), MM2 follows. */
+ * (groups of 128 features, as moe_quantize_fp8_groups), MM2 follows.  With 32 to
+ * 191 rows per slot on average (a skewed layer, e.g. EPLB) the slots of 192 or
+ * more rows take that path and the others the one-launch kernel after it. */
 moe_status moe_grouped_ffn_fp8(const uint8_t* d_sorted_q, const uint8_t* d_sorted_scales,
                                const int32_t* d_offsets_P, int P, int slot_lo, int slot_hi,
                                int64_t cap, const uint8_t* d_w_gate_up_q,

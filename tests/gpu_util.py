@@ -76,10 +76,14 @@ def ffn_kernel_of(layer):
     as M, 128-row m-tiles).  With the split FFN, a function of the slot's rows: 'pair'
     from the hot threshold, else 'tc'."""
     if getattr(layer, "fp8", False):
-        # many rows per slot (and H, I multiples of 512): the FP8 pair kernel
-        if (layer.cap // max(layer.P, 1) >= 192 and layer.H % 512 == 0
-                and layer.I % 512 == 0):
-            return "pair8"
+        # many rows per slot (and H, I multiples of 512): the FP8 pair kernel; 32-191
+        # rows per slot on average: the pair kernel for slots of 192 or more rows
+        per = layer.cap // max(layer.P, 1)
+        if layer.H % 512 == 0 and layer.I % 512 == 0:
+            if per >= 192:
+                return "pair8"
+            if per >= 32 and layer.cap >= 192:
+                return lambda rows: "pair8" if rows >= 192 else "fp8"
         return "fp8"
     split = getattr(layer, "ffn_split", None)
     if split:

@@ -76,6 +76,9 @@ def test_launch_counts_match_the_measured_steps():
     assert bench.launches_per_step(8192, 8, 256, 256, 65600, 1, fp8=True, fp8_pair=True) == 9
     assert bench.fp8_pair(65600, 256, 7168, 2048) and not bench.fp8_pair(3584, 256, 7168, 2048)
     assert not bench.fp8_pair(65600, 256, 7168, 2304)
+    # a skewed FP8 layer (EPLB: 57 rows per slot): pair launches, then the one-launch kernel
+    assert bench.fp8_split(16384, 288, 7168, 2048) and not bench.fp8_split(3584, 256, 7168, 2048)
+    assert bench.launches_per_step(2048, 8, 256, 288, 16384, 1, fp8=True, fp8_split=True) == 10
     assert bench.launches_per_step(440, 8, 256, 256, 3584, 1, router_gemm=True) == 9
     # prefill: 8192 rows x 8 pairs take the chunked dispatch (histogram, scan, rank, copy)
     assert bench.launches_per_step(8192, 8, 256, 256, 65600, 1) == 8
