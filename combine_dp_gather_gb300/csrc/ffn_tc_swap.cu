@@ -10,7 +10,8 @@
 // The products are computed transposed, D^T = W . X^T: the weight rows fill
 // the MMA's M = 256 (128 per SM of the pair) and a slot's tokens are its N.
 // One work unit is (slot, weight tile, token group) and covers up to 320 of
-// the slot's tokens with one or two MMAs per K step (N <= 256, then the rest),
+// the slot's tokens with one or two MMAs per K step (N <= 256: one; above, the
+// last 64 tokens in a second MMA so that no MMA is narrower than 64 columns),
 // so every weight tile crosses HBM once per slot however many tokens the slot
 // has, and a ragged token count costs N rounded up to 16 columns rather than
 // a second weight pass.  (With tokens as M, a slot of 256 + t rows needs a
@@ -34,7 +35,7 @@
 //
 // TMEM (512 fp32 columns per SM) is two halves of 256 columns, each a "head"
 // (its first 64 columns) and a "rest".  Units alternate halves: unit s puts
-// its first N0 <= 256 tokens in half s % 2 and its tail (N1 <= 64 tokens) in
+// its first N0 <= 256 tokens in half s % 2 and its tail (N1 = 64 tokens) in
 // the head of the other half.  The epilogue reads the tail, then the main
 // part from its first column, and hands each of the three regions back as
 // soon as its warps have loaded their last chunk of it; the next unit needs
@@ -128,7 +129,7 @@ struct SUnit {
   int slot, tile;
   int32_t tok0;  // first sorted row of the token group
   int32_t ntok;  // tokens in the group (1..NMAX)
-  int N0, N1;    // MMA widths: tokens rounded up to 16, split at 256
+  int N0, N1;    // MMA widths: tokens rounded up to 16; above 256, N1 = 64
 };
 // Unit u -> (slot, tile, token group).  The token groups of one (slot, tile)
 // are adjacent, then the tiles of one slot, so units running at the same time
@@ -153,8 +154,11 @@ __device__ __forceinline__ SUnit decode_unit(const SmemLayout& L, int nslots, in
   const int32_t left = T - grp * NMAX;
   r.ntok = left < NMAX ? left : NMAX;
   const int N = (r.ntok + 15) & ~15;
-  r.N0 = N < N_INSTR ? N : N_INSTR;
-  r.N1 = N - r.N0;
+  // A tail MMA rereads all 128 weight rows from shared memory whatever its
+  // width, so a 16-column tail costs nearly what a 64-column one does: give
+  // the tail the whole head.
+  r.N1 = N > N_INSTR ? HEAD_COLS : 0;
+  r.N0 = N - r.N1;
   return r;
 }
 

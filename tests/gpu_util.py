@@ -96,12 +96,17 @@ def _slot_positions(rows: int, kernel: str):
     pos = set()
     if kernel in ("pair", "pair8"):
         # unit = up to 320 tokens; N = tokens rounded up to 16, CTA c of the pair holds
-        # tokens [c*N/2, (c+1)*N/2); the first MMA (N0 = min(N, 256), FP8: 224) reads
-        # the first N0/2 of each CTA's rows, the tail MMA the rest
+        # tokens [c*N/2, (c+1)*N/2); the first MMA reads the first N0/2 of each CTA's
+        # rows, the tail MMA the rest: bf16 N0 = N up to 256, else N - 64 (the tail
+        # takes the last 64 columns); FP8 N0 = min(N, 224)
         for g0 in range(0, rows, 320):
             nt = min(320, rows - g0)
             N = (nt + 15) & ~15
-            h, n0 = N // 2, min(N, 256 if kernel == "pair" else 224)
+            if kernel == "pair":
+                n0 = N if N <= 256 else N - 64
+            else:
+                n0 = min(N, 224)
+            h = N // 2
             for p in (0, 31, 32, n0 // 2 - 1, n0 // 2, h - 1, h, h + 31, h + 32,
                       h + n0 // 2 - 1, h + n0 // 2, N - 1, nt - 1):
                 if 0 <= p < nt:
