@@ -102,8 +102,8 @@ def ffn_kernel(cap: int, P: int, fp8: bool = False, H: int = 0, I: int = 0) -> s
 # cases of the same kernels (32-expert prefill, 64-expert decode) and are scaled to the workload
 # by the units processed (traffic per slot and per routed row is the same).
 FFN_TRAFFIC = {
-    "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "0cf8deaf8c3db061",
-                "bytes": 25091414016},
+    "prefill": {"sources": ["ffn_tc_swap.cu", "tc_ptx.cuh"], "sha256_16": "2e18b47c963aca57",
+                "bytes": 25088589824},
     "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "ec94ad3d0984b261",
                "bytes": 5580442771},
     "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
