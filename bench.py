@@ -107,9 +107,9 @@ FFN_TRAFFIC = {
     "decode": {"sources": ["ffn_tc.cu", "tc_ptx.cuh"], "sha256_16": "ec94ad3d0984b261",
                "bytes": 5580442771},
     "decode_fp8": {"sources": ["ffn_fp8.cu", "tc_ptx.cuh", "fp8.cuh"],
-                   "sha256_16": "5c89e5373772b8fd", "bytes": 2791012496},
+                   "sha256_16": "1c554e5f6c0387c9", "bytes": 2790912240},
     "prefill_fp8": {"sources": ["ffn_fp8_swap.cu", "ffn_fp8.cu", "fp8.cu", "tc_ptx.cuh"],
-                    "sha256_16": "4f4867ec8b900465", "bytes": 13580828672},
+                    "sha256_16": "de840ae3f400969f", "bytes": 13571117056},
 }
 
 
